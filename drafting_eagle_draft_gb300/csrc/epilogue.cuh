@@ -1,0 +1,174 @@
+// Fused GEMM epilogues of the draft pass.
+//
+// Every projection of the pass is Y[r, m] = sum_k X[r, k] W[m, k] (nn.Linear) over a
+// handful of rows r (batch x K) and a long output dimension m.  The epilogue turns a
+// finished 128-feature tile of Y (fp32, indexable as src[r * ld + (m - m0)]) into
+// the pass's next tensor, so that Y itself never reaches HBM:
+//   STORE      fp32 copy (fc projection; fc(h_shared) at create time)
+//   QKV_ROPE   RoPE (rotate-half pairs i, i+hd/2) on q and k, then q -> Q [R, nq, hd],
+//              k, v -> the drafter KV cache slot of each row (decode) or to per-row
+//              K/V arrays (training-style forward)
+//   RESID      residual stream += Y (o-proj, down-proj)
+//   SWIGLU     act = silu(gate) * up, with gate/up rows interleaved in 64-row blocks
+//   LMHEAD     optional fp32 logits + per-row argmax folded into a 64-bit atomicMax key
+// A tile never splits a head (hd in {64, 128}, tiles start at multiples of 128) nor a
+// gate/up block, so each epilogue only needs its own tile.
+#pragma once
+
+#include "common.cuh"
+
+namespace peagle {
+
+enum EpiKind : int { EPI_STORE = 0, EPI_QKV_ROPE = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_LMHEAD = 4 };
+
+struct EpiArgs {
+  int kind;
+  int R;     // valid rows
+  int Nout;  // valid output features
+  // STORE
+  float* out_f32;
+  int out_ld;
+  // RESID: fp32 residual [R, ld_res]
+  float* resid;
+  int ld_res;
+  // QKV_ROPE
+  void* q_out;            // [R, nq*hd]
+  void* k_dst;            // decode: cache layer base [B][nkv][cap][hd]; rows: [R][nkv][hd]
+  void* v_dst;
+  void* k1_dst;           // rows mode: depth-1 copy [n][nkv][hd] (may be null)
+  void* v1_dst;
+  const int* seq_lens;    // decode: [B]
+  const int* row_pos;     // rows mode: RoPE position of each row
+  const int* row_depth;   // rows mode: depth of each row (1-based)
+  int n_seq;              // rows mode: sequence length (depth-1 copy bound)
+  int decode;             // 1: decode (cache slot = seq_lens[b] + j), 0: rows
+  int K;                  // decode: draft depth (rows per request)
+  int nq, nkv, hd, cap;
+  const float2* rope;     // [max_positions][hd/2] (cos, sin)
+  int max_pos;
+  // SWIGLU
+  void* act_out;          // [R, I]
+  int I;
+  // LMHEAD
+  float* logits;          // [R, Nout] or null
+  unsigned long long* keys;  // [R]
+  unsigned* err;
+};
+
+template <typename T>
+__device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src, int ld, int m0,
+                                              int tid, int nthr) {
+  const int R = a.R;
+  const int mcount = min(128, a.Nout - m0);
+  switch (a.kind) {
+    case EPI_STORE: {
+      for (int idx = tid; idx < R * 128; idx += nthr) {
+        int r = idx >> 7, ml = idx & 127;
+        if (ml < mcount) a.out_f32[(size_t)r * a.out_ld + m0 + ml] = src[(size_t)r * ld + ml];
+      }
+    } break;
+    case EPI_RESID: {
+      for (int idx = tid; idx < R * 128; idx += nthr) {
+        int r = idx >> 7, ml = idx & 127;
+        if (ml < mcount) a.resid[(size_t)r * a.ld_res + m0 + ml] += src[(size_t)r * ld + ml];
+      }
+    } break;
+    case EPI_SWIGLU: {
+      // tile rows [0,64) = gate, [64,128) = up of intermediate features m0/2 + i
+      T* act = (T*)a.act_out;
+      for (int idx = tid; idx < R * 64; idx += nthr) {
+        int r = idx >> 6, i = idx & 63;
+        float g = src[(size_t)r * ld + i];
+        float u = src[(size_t)r * ld + 64 + i];
+        float s = g / (1.f + expf(-g));
+        act[(size_t)r * a.I + (m0 >> 1) + i] = from_f32<T>(s * u);
+      }
+    } break;
+    case EPI_QKV_ROPE: {
+      const int hd = a.hd, half = hd >> 1;
+      const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
+      for (int idx = tid; idx < R * 128; idx += nthr) {
+        int r = idx >> 7, ml = idx & 127;
+        int m = m0 + ml;
+        if (ml >= mcount) continue;
+        int i = m % hd;
+        int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
+        int pos;
+        int b = 0, j = 0;
+        if (a.decode) {
+          b = r / a.K;
+          j = r - b * a.K;
+          pos = a.seq_lens[b] + j;
+        } else {
+          pos = a.row_pos[r];
+        }
+        bool pos_ok = pos >= 0 && pos < a.max_pos;
+        if (a.decode && (pos < 0 || pos >= a.cap)) {
+          if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
+          if (sec != 0) continue;  // no cache slot for this row
+        }
+        float v0 = src[(size_t)r * ld + ml];
+        float out0, out1 = 0.f;
+        int mm = m;
+        if (sec == 2) {
+          out0 = v0;
+        } else {
+          if (i >= half) continue;  // handled together with its pair partner
+          float v1 = src[(size_t)r * ld + ml + half];
+          float2 cs = pos_ok ? a.rope[(size_t)pos * half + i] : make_float2(1.f, 0.f);
+          out0 = v0 * cs.x - v1 * cs.y;
+          out1 = v1 * cs.x + v0 * cs.y;
+        }
+        if (sec == 0) {
+          T* q = (T*)a.q_out + (size_t)r * a.nq * hd + mm;
+          q[0] = from_f32<T>(out0);
+          q[half] = from_f32<T>(out1);
+        } else {
+          int g = (mm - (sec == 1 ? qend : kend)) / hd;
+          T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
+          size_t off;
+          if (a.decode)
+            off = (((size_t)b * a.nkv + g) * a.cap + pos) * hd + i;
+          else
+            off = ((size_t)r * a.nkv + g) * hd + i;
+          dst[off] = from_f32<T>(out0);
+          if (sec == 1) dst[off + half] = from_f32<T>(out1);
+          if (!a.decode && a.row_depth && a.row_depth[r] == 1 && pos >= 0 && pos < a.n_seq) {
+            T* d1 = (T*)(sec == 1 ? a.k1_dst : a.v1_dst);
+            if (d1) {
+              size_t o1 = ((size_t)pos * a.nkv + g) * hd + i;
+              d1[o1] = from_f32<T>(out0);
+              if (sec == 1) d1[o1 + half] = from_f32<T>(out1);
+            }
+          }
+        }
+      }
+    } break;
+    case EPI_LMHEAD: {
+      if (a.logits) {
+        for (int idx = tid; idx < R * 128; idx += nthr) {
+          int r = idx >> 7, ml = idx & 127;
+          if (ml < mcount) a.logits[(size_t)r * a.Nout + m0 + ml] = src[(size_t)r * ld + ml];
+        }
+      }
+      // per row: best (value, index) over the tile -> one atomicMax per warp and row
+      const int lane = tid & 31;
+      const int nw = nthr >> 5;
+      for (int r = tid >> 5; r < R; r += nw) {
+        unsigned long long best = 0ull;
+        for (int ml = lane; ml < mcount; ml += 32) {
+          unsigned long long k = argmax_key(src[(size_t)r * ld + ml], m0 + ml);
+          best = k > best ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+          best = other > best ? other : best;
+        }
+        if (lane == 0) atomicMax(a.keys + r, best);
+      }
+    } break;
+  }
+}
+
+}  // namespace peagle

@@ -1,0 +1,71 @@
+// Internal launchers of the P-EAGLE GB300 library (host side, C++).  Not part of the
+// C ABI: peagle_api.cu composes them into the calls declared in include/peagle.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epilogue.cuh"
+
+namespace peagle {
+
+struct AttnArgs {
+  const void* q;          // [R, nq*hd]
+  const void* kc;         // layer cache base [B][nkv][cap][hd]
+  const void* vc;
+  const int* seq_lens;    // [B]
+  void* o;                // [R, nq*hd]
+  float* part;            // split-KV partials
+  unsigned* counters;     // [B * nkv], zero between launches
+  int B, K, nq, nkv, hd, cap, chunk, nchunk;
+  float scale;
+  unsigned* err;
+};
+
+struct MaskedAttnArgs {
+  const void* q;          // [M, nq*hd]
+  const void* k;          // [M, nkv, hd]   all rows
+  const void* v;
+  const void* k1;         // [n, nkv, hd]   depth-1 rows by position
+  const void* v1;
+  const int* row_p;       // [M]
+  const int* row_d;       // [M]
+  const int* row_index;   // [n * (Kmax + 1)] row of (p, d), -1 if absent
+  void* o;                // [M, nq*hd]
+  int M, n, Kmax, nq, nkv, hd;
+  float scale;
+};
+
+// fp32-accumulating FFMA GEMM: Y[r, m] = sum_k X[r, k] W[m, k]; then the fused epilogue.
+void launch_gemm_simt(bool bf16, const void* W, const void* X, int ldx, float* Y, int ldy,
+                      int Nout, int Kd, int R, const EpiArgs& epi, cudaStream_t s);
+
+void launch_input_fusion(bool bf16, int mode, int R, int K, int n_src, int H, const void* embed,
+                         int Vt,
+                         const void* emb_mask, const float* F, const float* f_shared,
+                         const int* tokens, const int* row_p, const int* row_d,
+                         const void* g_in, const void* g_hid, float eps, void* X0, float* res,
+                         unsigned long long* keys, unsigned* err, cudaStream_t s);
+
+void launch_rmsnorm(bool bf16, int R, int H, const float* res, const void* gamma, float eps,
+                    void* out, cudaStream_t s);
+
+void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);
+
+void launch_masked_attention(bool bf16, const MaskedAttnArgs& a, cudaStream_t s);
+
+void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* out_tokens,
+                          cudaStream_t s);
+
+void launch_verify(int B, int K, const int* draft, const int* tgt, int* acc, int* bonus,
+                   cudaStream_t s);
+
+void launch_append_kv(bool bf16, int B, int N, int nkv, int hd, int cap, void* kc, void* vc,
+                      int* seq_lens, const int* n_commit, const void* k_rows,
+                      const void* v_rows, int n_max, int batch_slots, unsigned* err,
+                      cudaStream_t s);
+
+void launch_rows_prepare(int M, int n, int K, int Kmax, const int* row_p, const int* row_d,
+                         int* row_index, unsigned* err, cudaStream_t s);
+
+}  // namespace peagle

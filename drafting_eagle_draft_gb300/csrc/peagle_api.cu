@@ -1,0 +1,575 @@
+// C ABI of the P-EAGLE GB300 library (declared in include/peagle.h): argument
+// validation, the drafter context (weights + workspaces, allocated once in
+// peagle_create), and the kernel sequences of the draft pass, verification, KV commit
+// and the training-style forward.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "gemm_tc.h"
+#include "kernels.h"
+
+using namespace peagle;
+
+struct peagle_ctx {
+  peagle_dims d;
+  bool bf;          // bf16 storage
+  size_t es;        // element size
+  int device;
+  int num_sms;
+  // weights (library-owned device memory)
+  void *embed, *emb_mask, *h_shared, *fc, *input_norm, *hidden_norm, *final_norm, *lm_head;
+  int* d2t;
+  std::vector<void*> qkv, o, attn_norm, post_norm, gate_up, down;
+  float2* rope;
+  float* f_shared;  // fc(h_shared) [H]
+  // workspaces
+  int rows_max;     // max(max_batch * max_K, max_rows)
+  float* F;         // [max(max_batch, max_seq), H]
+  void* X0;         // [rows_max, 2H]
+  float* res;       // [rows_max, H]
+  void* Xn;         // [rows_max, H]
+  void* Q;          // [rows_max, nq*hd]
+  void* O;          // [rows_max, nq*hd]
+  void* act;        // [rows_max, I]
+  float* Y;         // fp32 GEMM output (FFMA path) [rows_max, max_out]
+  int ldY;
+  unsigned long long* keys;  // [rows_max]
+  float* att_part;
+  unsigned* att_cnt;
+  int att_chunks_max;
+  // training-style forward
+  void *Kr, *Vr, *K1, *V1;
+  int* row_index;
+  unsigned* err;
+  unsigned last_err_bits;
+  TcGemmPlan* tc;   // tensor-core GEMM state (bf16 only)
+  std::vector<void*> allocs;
+};
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    fprintf(stderr, "peagle: %s: %s\n", what, cudaGetErrorString(e));
+    return PEAGLE_ERR_CUDA;
+  }
+  return PEAGLE_OK;
+}
+#define CK(x)                                        \
+  do {                                               \
+    int _r = cuda_fail((x), #x);                     \
+    if (_r != PEAGLE_OK) return _r;                  \
+  } while (0)
+
+static int dalloc(peagle_ctx* c, void** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  c->allocs.push_back(*p);
+  return cudaMemset(*p, 0, bytes) == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+}
+
+static int copy_in(peagle_ctx* c, void** dst, const void* src, size_t bytes) {
+  if (!src) return PEAGLE_ERR_INVALID;
+  int r = dalloc(c, dst, bytes);
+  if (r) return r;
+  CK(cudaMemcpy(*dst, src, bytes, cudaMemcpyDefault));
+  return PEAGLE_OK;
+}
+
+static void free_ctx(peagle_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  for (void* p : c->allocs) cudaFree(p);
+  if (c->tc) tc_destroy(c->tc);
+  delete c;
+}
+
+static int validate_dims(const peagle_dims* d) {
+  if (!d) return PEAGLE_ERR_INVALID;
+  if (d->hidden <= 0 || d->n_layers <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 ||
+      d->head_dim <= 0 || d->intermediate <= 0 || d->draft_vocab <= 0 || d->target_vocab <= 0 ||
+      d->max_batch <= 0 || d->max_K <= 0 || d->max_positions <= 0 || d->max_rows < 0 ||
+      d->max_seq < 0 || !(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f))
+    return PEAGLE_ERR_INVALID;
+  if (d->dtype != PEAGLE_F32 && d->dtype != PEAGLE_BF16) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->n_q_heads % d->n_kv_heads) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->hidden % 64 || d->intermediate % 64) return PEAGLE_ERR_UNSUPPORTED;
+  if (((d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim) % 128) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->max_K > 16 || d->max_batch * d->max_K > 256) return PEAGLE_ERR_CAPACITY;
+  if (d->max_K * (d->n_q_heads / d->n_kv_heads) > 128) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->max_rows > 0 && d->max_seq <= 0) return PEAGLE_ERR_INVALID;
+  return PEAGLE_OK;
+}
+
+// ---- GEMM dispatch: tensor cores for bf16, FFMA for fp32 --------------------------------
+static void gemm(peagle_ctx* c, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
+                 const EpiArgs& epi, cudaStream_t s) {
+  if (c->bf && c->tc)
+    tc_gemm(c->tc, W, X, ldx, Nout, Kd, R, epi, s);
+  else
+    launch_gemm_simt(c->bf, W, X, ldx, c->Y, c->ldY, Nout, Kd, R, epi, s);
+}
+
+static EpiArgs epi_base(peagle_ctx* c, int kind, int R, int Nout) {
+  EpiArgs e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.R = R;
+  e.Nout = Nout;
+  e.err = c->err;
+  e.nq = c->d.n_q_heads;
+  e.nkv = c->d.n_kv_heads;
+  e.hd = c->d.head_dim;
+  e.rope = c->rope;
+  e.max_pos = c->d.max_positions;
+  e.I = c->d.intermediate;
+  e.ld_res = c->d.hidden;
+  return e;
+}
+
+extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, peagle_ctx** out) {
+  if (!out) return PEAGLE_ERR_INVALID;
+  *out = nullptr;
+  int r = validate_dims(dims);
+  if (r) return r;
+  if (!w || !w->embed || !w->emb_mask || !w->h_shared || !w->fc || !w->input_norm ||
+      !w->hidden_norm || !w->qkv || !w->o || !w->post_norm || !w->gate || !w->up || !w->down ||
+      !w->final_norm || !w->lm_head || !w->d2t)
+    return PEAGLE_ERR_INVALID;
+  const peagle_dims& d = *dims;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!w->qkv[l] || !w->o[l] || !w->post_norm[l] || !w->gate[l] || !w->up[l] || !w->down[l] ||
+        (l > 0 && (!w->attn_norm || !w->attn_norm[l])))
+      return PEAGLE_ERR_INVALID;
+
+  peagle_ctx* c = new peagle_ctx();
+  c->d = d;
+  c->bf = d.dtype == PEAGLE_BF16;
+  c->es = c->bf ? 2 : 4;
+  c->tc = nullptr;
+  c->last_err_bits = 0;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return PEAGLE_ERR_CUDA;
+  }
+  const size_t es = c->es;
+  const int H = d.hidden, I = d.intermediate, nq = d.n_q_heads, nkv = d.n_kv_heads,
+            hd = d.head_dim;
+  const int qkv_out = (nq + 2 * nkv) * hd;
+#define TRY(x)            \
+  do {                    \
+    int _r = (x);         \
+    if (_r) {             \
+      free_ctx(c);        \
+      return _r;          \
+    }                     \
+  } while (0)
+  TRY(copy_in(c, &c->embed, w->embed, (size_t)d.target_vocab * H * es));
+  TRY(copy_in(c, &c->emb_mask, w->emb_mask, (size_t)H * es));
+  TRY(copy_in(c, &c->h_shared, w->h_shared, (size_t)3 * H * es));
+  TRY(copy_in(c, &c->fc, w->fc, (size_t)H * 3 * H * es));
+  TRY(copy_in(c, &c->input_norm, w->input_norm, (size_t)H * es));
+  TRY(copy_in(c, &c->hidden_norm, w->hidden_norm, (size_t)H * es));
+  TRY(copy_in(c, &c->final_norm, w->final_norm, (size_t)H * es));
+  TRY(copy_in(c, &c->lm_head, w->lm_head, (size_t)d.draft_vocab * H * es));
+  TRY(copy_in(c, (void**)&c->d2t, w->d2t, (size_t)d.draft_vocab * 4));
+  c->qkv.resize(d.n_layers);
+  c->o.resize(d.n_layers);
+  c->attn_norm.assign(d.n_layers, nullptr);
+  c->post_norm.resize(d.n_layers);
+  c->gate_up.resize(d.n_layers);
+  c->down.resize(d.n_layers);
+  for (int l = 0; l < d.n_layers; ++l) {
+    const int din = l == 0 ? 2 * H : H;
+    TRY(copy_in(c, &c->qkv[l], w->qkv[l], (size_t)qkv_out * din * es));
+    TRY(copy_in(c, &c->o[l], w->o[l], (size_t)H * nq * hd * es));
+    if (l > 0) TRY(copy_in(c, &c->attn_norm[l], w->attn_norm[l], (size_t)H * es));
+    TRY(copy_in(c, &c->post_norm[l], w->post_norm[l], (size_t)H * es));
+    TRY(copy_in(c, &c->down[l], w->down[l], (size_t)H * I * es));
+    // gate/up interleaved in 64-row blocks: [gate 64 rows | up 64 rows] per block
+    TRY(dalloc(c, &c->gate_up[l], (size_t)2 * I * H * es));
+    const size_t blk = (size_t)64 * H * es;
+    if (cudaMemcpy2D(c->gate_up[l], 2 * blk, w->gate[l], blk, blk, I / 64, cudaMemcpyDefault) ||
+        cudaMemcpy2D((char*)c->gate_up[l] + blk, 2 * blk, w->up[l], blk, blk, I / 64,
+                     cudaMemcpyDefault)) {
+      free_ctx(c);
+      return PEAGLE_ERR_CUDA;
+    }
+  }
+  // RoPE table (cos, sin) for positions [0, max_positions), angles in double
+  {
+    const int half = hd / 2;
+    std::vector<float2> tab((size_t)d.max_positions * half);
+    for (int p = 0; p < d.max_positions; ++p)
+      for (int i = 0; i < half; ++i) {
+        double inv = pow((double)d.rope_theta, -2.0 * i / hd);
+        double ang = (double)p * inv;
+        tab[(size_t)p * half + i] = make_float2((float)cos(ang), (float)sin(ang));
+      }
+    TRY(copy_in(c, (void**)&c->rope, tab.data(), tab.size() * sizeof(float2)));
+  }
+  // workspaces
+  c->rows_max = d.max_batch * d.max_K;
+  if (d.max_rows > c->rows_max) c->rows_max = d.max_rows;
+  const int R = c->rows_max;
+  const int fr = d.max_batch > d.max_seq ? d.max_batch : d.max_seq;
+  TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 4));
+  TRY(dalloc(c, (void**)&c->f_shared, (size_t)H * 4));
+  TRY(dalloc(c, &c->X0, (size_t)R * 2 * H * es));
+  TRY(dalloc(c, (void**)&c->res, (size_t)R * H * 4));
+  TRY(dalloc(c, &c->Xn, (size_t)R * H * es));
+  TRY(dalloc(c, &c->Q, (size_t)R * nq * hd * es));
+  TRY(dalloc(c, &c->O, (size_t)R * nq * hd * es));
+  TRY(dalloc(c, &c->act, (size_t)R * I * es));
+  TRY(dalloc(c, (void**)&c->keys, (size_t)R * 8));
+  TRY(dalloc(c, (void**)&c->err, 64));
+  int max_out = qkv_out;
+  if (2 * I > max_out) max_out = 2 * I;
+  if (H > max_out) max_out = H;
+  if (d.draft_vocab > max_out) max_out = d.draft_vocab;
+  c->ldY = (max_out + 127) / 128 * 128;
+  if (!c->bf) TRY(dalloc(c, (void**)&c->Y, (size_t)R * c->ldY * 4));
+  {
+    const int G = nq / nkv;
+    c->att_chunks_max = 64;
+    TRY(dalloc(c, (void**)&c->att_part, (size_t)d.max_batch * nkv * c->att_chunks_max *
+                                            (d.max_K * G) * (hd + 2) * 4));
+    TRY(dalloc(c, (void**)&c->att_cnt, (size_t)d.max_batch * nkv * 4));
+  }
+  if (d.max_rows > 0) {
+    TRY(dalloc(c, &c->Kr, (size_t)d.max_rows * nkv * hd * es));
+    TRY(dalloc(c, &c->Vr, (size_t)d.max_rows * nkv * hd * es));
+    TRY(dalloc(c, &c->K1, (size_t)d.max_seq * nkv * hd * es));
+    TRY(dalloc(c, &c->V1, (size_t)d.max_seq * nkv * hd * es));
+    TRY(dalloc(c, (void**)&c->row_index, (size_t)d.max_seq * 17 * 4));
+  }
+  if (c->bf) {
+    int rr = tc_create(&c->tc, c->num_sms, R, max_out > 3 * H ? max_out : 3 * H);
+    if (rr) {
+      free_ctx(c);
+      return rr;
+    }
+  }
+  if (c->bf && !c->tc) {
+    // the bf16 path runs its projections on the FFMA GEMM until tensor-core tiles exist
+    TRY(dalloc(c, (void**)&c->Y, (size_t)R * c->ldY * 4));
+  }
+  // fc(h_shared): constant for every MTP row, computed once with the pass's own GEMM
+  {
+    EpiArgs e = epi_base(c, EPI_STORE, 1, H);
+    e.out_f32 = c->f_shared;
+    e.out_ld = H;
+    gemm(c, c->fc, c->h_shared, 3 * H, H, 3 * H, 1, e, 0);
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+      free_ctx(c);
+      return PEAGLE_ERR_CUDA;
+    }
+  }
+#undef TRY
+  *out = c;
+  return PEAGLE_OK;
+}
+
+static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchunk) {
+  const int target = 2 * c->num_sms;
+  const int pairs = B * c->d.n_kv_heads;
+  int want = (target + pairs - 1) / pairs;
+  if (want < 1) want = 1;
+  if (want > c->att_chunks_max) want = c->att_chunks_max;
+  int ch = (cap + want - 1) / want;
+  ch = (ch + 63) / 64 * 64;
+  if (ch < 64) ch = 64;
+  *chunk = ch;
+  *nchunk = (cap + ch - 1) / ch;
+}
+
+extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
+                            const int32_t* seq_lens, const void* target_hidden,
+                            const int32_t* new_token, int32_t K, int32_t* out_draft_tokens,
+                            float* out_logits, void* stream) {
+  if (!c || !kv || !kv->k || !kv->v || !seq_lens || !target_hidden || !new_token ||
+      !out_draft_tokens)
+    return PEAGLE_ERR_INVALID;
+  const peagle_dims& d = c->d;
+  if (batch < 1 || K < 1) return PEAGLE_ERR_INVALID;
+  if (batch > d.max_batch || K > d.max_K || batch > kv->batch) return PEAGLE_ERR_CAPACITY;
+  if (kv->capacity < K || kv->capacity > d.max_positions) return PEAGLE_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
+  const int qkv_out = (nq + 2 * nkv) * hd;
+  const int R = batch * K;
+  const size_t es = c->es;
+  const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
+
+  // S1: fc over the NTP rows' target hidden states, then the fused input rows
+  {
+    EpiArgs e = epi_base(c, EPI_STORE, batch, H);
+    e.out_f32 = c->F;
+    e.out_ld = H;
+    gemm(c, c->fc, target_hidden, 3 * H, H, 3 * H, batch, e, s);
+  }
+  launch_input_fusion(c->bf, 0, R, K, batch, H, c->embed, d.target_vocab, c->emb_mask, c->F,
+                      c->f_shared, new_token, nullptr, nullptr, c->input_norm, c->hidden_norm,
+                      d.rms_eps, c->X0, c->res, c->keys, c->err, s);
+  int chunk, nchunk;
+  attention_plan(c, batch, kv->capacity, &chunk, &nchunk);
+  for (int l = 0; l < d.n_layers; ++l) {
+    const void* a_in = c->X0;
+    int din = 2 * H;
+    if (l > 0) {
+      launch_rmsnorm(c->bf, R, H, c->res, c->attn_norm[l], d.rms_eps, c->Xn, s);
+      a_in = c->Xn;
+      din = H;
+    }
+    // S2: QKV projection + RoPE; k/v of row j go to cache slot seq_lens[b] + j
+    {
+      EpiArgs e = epi_base(c, EPI_QKV_ROPE, R, qkv_out);
+      e.q_out = c->Q;
+      e.k_dst = (char*)kv->k + l * layer_stride;
+      e.v_dst = (char*)kv->v + l * layer_stride;
+      e.seq_lens = seq_lens;
+      e.decode = 1;
+      e.K = K;
+      e.cap = kv->capacity;
+      gemm(c, c->qkv[l], a_in, din, qkv_out, din, R, e, s);
+    }
+    // S3: split-KV attention over the cache + causal draft block
+    {
+      AttnArgs a;
+      a.q = c->Q;
+      a.kc = (char*)kv->k + l * layer_stride;
+      a.vc = (char*)kv->v + l * layer_stride;
+      a.seq_lens = seq_lens;
+      a.o = c->O;
+      a.part = c->att_part;
+      a.counters = c->att_cnt;
+      a.B = batch;
+      a.K = K;
+      a.nq = nq;
+      a.nkv = nkv;
+      a.hd = hd;
+      a.cap = kv->capacity;
+      a.chunk = chunk;
+      a.nchunk = nchunk;
+      a.scale = 1.f / sqrtf((float)hd);
+      a.err = c->err;
+      launch_attention_decode(c->bf, a, s);
+    }
+    // S4: o-proj + residual
+    {
+      EpiArgs e = epi_base(c, EPI_RESID, R, H);
+      e.resid = c->res;
+      gemm(c, c->o[l], c->O, nq * hd, H, nq * hd, R, e, s);
+    }
+    // S5: SwiGLU MLP
+    launch_rmsnorm(c->bf, R, H, c->res, c->post_norm[l], d.rms_eps, c->Xn, s);
+    {
+      EpiArgs e = epi_base(c, EPI_SWIGLU, R, 2 * d.intermediate);
+      e.act_out = c->act;
+      gemm(c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, R, e, s);
+    }
+    {
+      EpiArgs e = epi_base(c, EPI_RESID, R, H);
+      e.resid = c->res;
+      gemm(c, c->down[l], c->act, d.intermediate, H, d.intermediate, R, e, s);
+    }
+  }
+  // S6: final norm, LM head with fused argmax, d2t remap
+  launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, c->Xn, s);
+  {
+    EpiArgs e = epi_base(c, EPI_LMHEAD, R, d.draft_vocab);
+    e.logits = out_logits;
+    e.keys = c->keys;
+    gemm(c, c->lm_head, c->Xn, H, d.draft_vocab, H, R, e, s);
+  }
+  launch_argmax_decode(R, c->keys, c->d2t, out_draft_tokens, s);
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_draft launch");
+}
+
+extern "C" int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* draft_tokens,
+                                    const int32_t* target_argmax, int32_t* out_accept_len,
+                                    int32_t* out_bonus, void* stream) {
+  if (batch < 1 || K < 1 || K > 64 || !draft_tokens || !target_argmax || !out_accept_len ||
+      !out_bonus)
+    return PEAGLE_ERR_INVALID;
+  launch_verify(batch, K, draft_tokens, target_argmax, out_accept_len, out_bonus,
+                (cudaStream_t)stream);
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_verify_greedy launch");
+}
+
+extern "C" int peagle_append_kv(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
+                                int32_t* seq_lens, const int32_t* n_commit, const void* k_rows,
+                                const void* v_rows, int32_t n_max, void* stream) {
+  if (!c || !kv || !kv->k || !kv->v || !seq_lens || !n_commit) return PEAGLE_ERR_INVALID;
+  if (batch < 1 || n_max < 0 || (k_rows == nullptr) != (v_rows == nullptr))
+    return PEAGLE_ERR_INVALID;
+  if (batch > kv->batch) return PEAGLE_ERR_CAPACITY;
+  const peagle_dims& d = c->d;
+  launch_append_kv(c->bf, batch, d.n_layers, d.n_kv_heads, d.head_dim, kv->capacity, kv->k,
+                   kv->v, seq_lens, n_commit, k_rows, v_rows, n_max, kv->batch, c->err,
+                   (cudaStream_t)stream);
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_append_kv launch");
+}
+
+extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, const int32_t* tokens,
+                                       const void* hidden, const int32_t* row_p,
+                                       const int32_t* row_d, int32_t M, int32_t* out_argmax,
+                                       float* out_logits, void* stream) {
+  if (!c || !tokens || !hidden || !row_p || !row_d || !out_argmax) return PEAGLE_ERR_INVALID;
+  const peagle_dims& d = c->d;
+  if (n < 1 || K < 1 || M < 1) return PEAGLE_ERR_INVALID;
+  if (d.max_rows <= 0 || M > d.max_rows || n > d.max_seq || K > 16) return PEAGLE_ERR_CAPACITY;
+  if (n > d.max_positions) return PEAGLE_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
+  const int qkv_out = (nq + 2 * nkv) * hd;
+  const int Kmax = 16;
+  launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s);
+  {
+    EpiArgs e = epi_base(c, EPI_STORE, n, H);
+    e.out_f32 = c->F;
+    e.out_ld = H;
+    gemm(c, c->fc, hidden, 3 * H, H, 3 * H, n, e, s);
+  }
+  launch_input_fusion(c->bf, 1, M, K, n, H, c->embed, d.target_vocab, c->emb_mask, c->F,
+                      c->f_shared, tokens, row_p, row_d, c->input_norm, c->hidden_norm,
+                      d.rms_eps, c->X0, c->res, c->keys, c->err, s);
+  for (int l = 0; l < d.n_layers; ++l) {
+    const void* a_in = c->X0;
+    int din = 2 * H;
+    if (l > 0) {
+      launch_rmsnorm(c->bf, M, H, c->res, c->attn_norm[l], d.rms_eps, c->Xn, s);
+      a_in = c->Xn;
+      din = H;
+    }
+    {
+      EpiArgs e = epi_base(c, EPI_QKV_ROPE, M, qkv_out);
+      e.q_out = c->Q;
+      e.k_dst = c->Kr;
+      e.v_dst = c->Vr;
+      e.k1_dst = c->K1;
+      e.v1_dst = c->V1;
+      e.row_pos = row_p;
+      e.row_depth = row_d;
+      e.n_seq = n;
+      e.decode = 0;
+      gemm(c, c->qkv[l], a_in, din, qkv_out, din, M, e, s);
+    }
+    {
+      MaskedAttnArgs a;
+      a.q = c->Q;
+      a.k = c->Kr;
+      a.v = c->Vr;
+      a.k1 = c->K1;
+      a.v1 = c->V1;
+      a.row_p = row_p;
+      a.row_d = row_d;
+      a.row_index = c->row_index;
+      a.o = c->O;
+      a.M = M;
+      a.n = n;
+      a.Kmax = Kmax;
+      a.nq = nq;
+      a.nkv = nkv;
+      a.hd = hd;
+      a.scale = 1.f / sqrtf((float)hd);
+      launch_masked_attention(c->bf, a, s);
+    }
+    {
+      EpiArgs e = epi_base(c, EPI_RESID, M, H);
+      e.resid = c->res;
+      gemm(c, c->o[l], c->O, nq * hd, H, nq * hd, M, e, s);
+    }
+    launch_rmsnorm(c->bf, M, H, c->res, c->post_norm[l], d.rms_eps, c->Xn, s);
+    {
+      EpiArgs e = epi_base(c, EPI_SWIGLU, M, 2 * d.intermediate);
+      e.act_out = c->act;
+      gemm(c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, M, e, s);
+    }
+    {
+      EpiArgs e = epi_base(c, EPI_RESID, M, H);
+      e.resid = c->res;
+      gemm(c, c->down[l], c->act, d.intermediate, H, d.intermediate, M, e, s);
+    }
+  }
+  launch_rmsnorm(c->bf, M, H, c->res, c->final_norm, d.rms_eps, c->Xn, s);
+  {
+    EpiArgs e = epi_base(c, EPI_LMHEAD, M, d.draft_vocab);
+    e.logits = out_logits;
+    e.keys = c->keys;
+    gemm(c, c->lm_head, c->Xn, H, d.draft_vocab, H, M, e, s);
+  }
+  launch_argmax_decode(M, c->keys, nullptr, out_argmax, s);
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_forward_parallel launch");
+}
+
+extern "C" int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double* uniforms,
+                               int32_t* out_p, int32_t* out_d, int32_t max_out) {
+  if (n < 0 || K < 1 || K > 16 || !uniforms || !out_p || !out_d || max_out < 0)
+    return PEAGLE_ERR_INVALID;
+  // kept[d] for the previous position; depth 1 always kept
+  std::vector<char> prev(K + 1, 0), cur(K + 1, 0);
+  int count = 0;
+  for (int p = 0; p < n; ++p) {
+    for (int d = 1; d <= K; ++d) {
+      bool keep;
+      if (d == 1)
+        keep = true;
+      else if (p - d + 1 < 0)
+        keep = false;
+      else
+        keep = prev[d - 1] && uniforms[(size_t)p * K + (d - 1)] < ratio;
+      cur[d] = keep;
+      if (keep) {
+        if (count >= max_out) return PEAGLE_ERR_CAPACITY;
+        out_p[count] = p;
+        out_d[count] = d;
+        ++count;
+      }
+    }
+    prev.swap(cur);
+  }
+  return count;
+}
+
+extern "C" int peagle_status(peagle_ctx* c) {
+  if (!c) return PEAGLE_ERR_INVALID;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "peagle_status");
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, c->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return PEAGLE_ERR_CUDA;
+  c->last_err_bits = bits;
+  if (bits) {
+    cudaMemset(c->err, 0, 4);
+    return PEAGLE_ERR_DEVICE;
+  }
+  return PEAGLE_OK;
+}
+
+extern "C" int32_t peagle_device_error_bits(const peagle_ctx* c) {
+  return c ? (int32_t)c->last_err_bits : 0;
+}
+
+extern "C" const char* peagle_strerror(int code) {
+  switch (code) {
+    case PEAGLE_OK: return "ok";
+    case PEAGLE_ERR_INVALID: return "invalid argument";
+    case PEAGLE_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case PEAGLE_ERR_CAPACITY: return "capacity exceeded";
+    case PEAGLE_ERR_CUDA: return "CUDA error";
+    case PEAGLE_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown error";
+  }
+}
+
+extern "C" void peagle_destroy(peagle_ctx* c) { free_ctx(c); }

@@ -1,0 +1,206 @@
+/*
+ * peagle.h -- C ABI of the GB300 (sm_103a) P-EAGLE parallel draft pass.
+ *
+ * One library call runs one step of the speculative round described in
+ *   "P-EAGLE: A Technical Deep Dive into Parallel Speculative Decoding",
+ *   section "2. The P-EAGLE Parallel Drafter", and
+ *   "P-EAGLE: Parallel-Drafting EAGLE with Scalable Training", A2 section 2:
+ * from the target's captured hidden states and the newly generated token, ONE forward
+ * pass of an N-layer Llama-3 drafter produces all K draft tokens; the target then
+ * verifies them and keeps the longest agreeing prefix plus a bonus token
+ * ("EAGLE-4", section "EAGLE-4 overview").
+ *
+ * Conventions shared by every call
+ *   - Sizes are int32; pointers are plain pointers.  "device" means a CUDA device
+ *     pointer on the current device; "host or device" means any pointer that
+ *     cudaMemcpy with cudaMemcpyDefault accepts (pageable/pinned host or device).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every call except peagle_create, peagle_status and peagle_destroy is
+ *     asynchronous on `stream`, performs no allocation and no host synchronisation,
+ *     and may be captured into a CUDA graph.
+ *   - Return value: PEAGLE_OK or a negative error code.  Host-detectable argument
+ *     errors are returned immediately and nothing is launched.  Errors that depend on
+ *     device-resident values (token ids, seq_lens) are latched in the context's
+ *     device error word by the kernels, which then skip the offending access; the
+ *     next peagle_status() reports them.  No call aborts, exits or traps.
+ *   - dtype: PEAGLE_F32 keeps every tensor (weights, caches, activations) in fp32
+ *     and computes with fp32 FMA; PEAGLE_BF16 stores weights, caches and
+ *     activations in bf16 and accumulates in fp32 on the tensor cores.
+ */
+#ifndef PEAGLE_H
+#define PEAGLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PEAGLE_OK 0
+#define PEAGLE_ERR_INVALID (-1)      /* bad pointer / size / argument combination  */
+#define PEAGLE_ERR_UNSUPPORTED (-2)  /* dims outside what the kernels implement     */
+#define PEAGLE_ERR_CAPACITY (-3)     /* batch, K, rows or KV capacity beyond limits */
+#define PEAGLE_ERR_CUDA (-4)         /* a CUDA runtime/driver call failed           */
+#define PEAGLE_ERR_DEVICE (-5)       /* a device-side check tripped (see status)    */
+
+/* Device error word bits (peagle_status() returns PEAGLE_ERR_DEVICE if any is set;
+ * peagle_device_error_bits() returns the raw bits of the last status call). */
+#define PEAGLE_DEV_BAD_TOKEN 0x1     /* token id outside [0, target_vocab)          */
+#define PEAGLE_DEV_KV_OVERFLOW 0x2   /* seq_lens[b] + K (or + n_commit) > capacity  */
+#define PEAGLE_DEV_BAD_COMMIT 0x4    /* n_commit[b] outside [0, n_max]              */
+#define PEAGLE_DEV_BAD_ROW 0x8       /* forward_parallel row (p, d) invalid         */
+#define PEAGLE_DEV_TIMEOUT 0x10      /* a bounded on-chip wait gave up              */
+
+typedef enum { PEAGLE_F32 = 0, PEAGLE_BF16 = 1 } peagle_dtype;
+
+typedef struct peagle_ctx peagle_ctx;
+
+/* Drafter dimensions.  Constraints (else PEAGLE_ERR_UNSUPPORTED):
+ *   head_dim in {64, 128}; n_q_heads % n_kv_heads == 0; hidden % 64 == 0;
+ *   intermediate % 64 == 0; (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0;
+ *   max_batch * max_K <= 256; max_K <= 16. */
+typedef struct peagle_dims {
+  int32_t hidden;        /* H                                                     */
+  int32_t n_layers;      /* N decoder layers                                      */
+  int32_t n_q_heads;     /* nq                                                    */
+  int32_t n_kv_heads;    /* nkv (GQA: q head h reads kv head h / (nq / nkv))       */
+  int32_t head_dim;      /* hd                                                    */
+  int32_t intermediate;  /* I (SwiGLU)                                            */
+  int32_t draft_vocab;   /* Vd rows of the LM head                                */
+  int32_t target_vocab;  /* Vt rows of the embedding table; d2t maps into it      */
+  int32_t max_batch;     /* largest `batch` any draft call will use               */
+  int32_t max_K;         /* largest K any draft call will use                     */
+  int32_t max_rows;      /* largest M of peagle_forward_parallel (0: not used)    */
+  int32_t max_seq;       /* largest n of peagle_forward_parallel (0: not used)    */
+  int32_t max_positions; /* RoPE table size: every position used must be below it */
+  int32_t dtype;         /* peagle_dtype                                          */
+  float rope_theta;      /* RoPE base                                             */
+  float rms_eps;         /* RMSNorm epsilon                                       */
+} peagle_dims;
+
+/* Drafter weights (host or device pointers; dtype = dims.dtype for every float
+ * tensor).  nn.Linear layout [out, in], row-major.  Per-layer entries are host
+ * arrays of n_layers pointers.  peagle_create copies (and repacks) everything into
+ * library-owned device memory, so the caller may free these buffers afterwards. */
+typedef struct peagle_weights {
+  const void* embed;             /* [Vt, H] token embeddings                        */
+  const void* emb_mask;          /* [H]     learnable emb(mask)                     */
+  const void* h_shared;          /* [3H]    learnable shared hidden state           */
+  const void* fc;                /* [H, 3H] projection of the 3 target states       */
+  const void* input_norm;        /* [H]     RMSNorm gain of the embedding half      */
+  const void* hidden_norm;       /* [H]     RMSNorm gain of the fc half             */
+  const void* const* qkv;        /* N x [(nq+2nkv)hd, 2H (layer 0) | H]             */
+  const void* const* o;          /* N x [H, nq hd]                                  */
+  const void* const* attn_norm;  /* N x [H] (entry 0 unused, may be NULL)           */
+  const void* const* post_norm;  /* N x [H]                                         */
+  const void* const* gate;       /* N x [I, H]                                      */
+  const void* const* up;         /* N x [I, H]                                      */
+  const void* const* down;       /* N x [H, I]                                      */
+  const void* final_norm;        /* [H]                                             */
+  const void* lm_head;           /* [Vd, H]                                         */
+  const int32_t* d2t;            /* [Vd] draft->target offsets: id = i + d2t[i]     */
+} peagle_weights;
+
+/* Caller-owned drafter KV cache (device).  Layout of k and v:
+ *   [n_layers][batch][n_kv_heads][capacity][head_dim], dtype = dims.dtype.
+ * Keys are stored after RoPE.  Request b's committed entries are slots
+ * 0 .. seq_lens[b]-1. */
+typedef struct peagle_kv {
+  void* k;
+  void* v;
+  int32_t capacity; /* slots per (layer, request, kv head)                          */
+  int32_t batch;    /* request slots in the buffers (>= the call's batch)           */
+} peagle_kv;
+
+/* Create a drafter context: validates dims, allocates all device memory the other
+ * calls need (weights, workspaces sized for max_batch x max_K rows and max_rows),
+ * copies and repacks the weights, precomputes fc(h_shared) and the RoPE table,
+ * and synchronises.  The only allocating call.  *out is NULL on failure. */
+int peagle_create(const peagle_weights* w, const peagle_dims* dims, peagle_ctx** out);
+
+/* One parallel draft pass ("2. The P-EAGLE Parallel Drafter").
+ *   batch            requests, 1 .. max_batch (and <= kv->batch)
+ *   kv               drafter cache; the pass WRITES row j's key/value of every layer
+ *                    into slot seq_lens[b] + j (uncommitted until peagle_append_kv)
+ *   seq_lens         device int32 [batch]: committed KV length of each request
+ *   target_hidden    device [batch, 3H] (dims dtype): the target's three captured
+ *                    hidden states, concatenated early | mid | late
+ *   new_token        device int32 [batch]: the newly generated token (target vocab)
+ *   K                draft depth, 1 .. max_K; rows r = b*K + j, j = 0 is the NTP row
+ *   out_draft_tokens device int32 [batch, K]: argmax over the draft vocabulary
+ *                    (lowest index on ties) mapped to the target vocabulary by d2t
+ *   out_logits       device fp32 [batch, K, Vd], or NULL to skip writing logits
+ * Device checks: new_token in range (else BAD_TOKEN, row treated as token 0);
+ * seq_lens[b] + K <= capacity (else KV_OVERFLOW, out-of-range slots skipped). */
+int peagle_draft(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv, const int32_t* seq_lens,
+                 const void* target_hidden, const int32_t* new_token, int32_t K,
+                 int32_t* out_draft_tokens, float* out_logits, void* stream);
+
+/* Greedy verification ("EAGLE-4 overview"): for each request, the longest prefix of
+ * draft_tokens[b, :] equal to target_argmax[b, :], plus one bonus token.
+ *   draft_tokens   device int32 [batch, K]
+ *   target_argmax  device int32 [batch, K+1]: the target's greedy choice after each
+ *                  draft prefix (position K = after all K drafts)
+ *   out_accept_len device int32 [batch]: m in 0..K (tokens emitted = m + 1)
+ *   out_bonus      device int32 [batch]: target_argmax[b, m]
+ * Needs no context; 1 <= K <= 64. */
+int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* draft_tokens,
+                         const int32_t* target_argmax, int32_t* out_accept_len,
+                         int32_t* out_bonus, void* stream);
+
+/* Commit accepted rows to the KV cache and advance seq_lens (device, in place):
+ *   n_commit device int32 [batch], each in 0..n_max.
+ *   k_rows/v_rows NULL: the first n_commit[b] draft-block rows already sit in slots
+ *     seq_lens[b] .. (written by peagle_draft); only seq_lens advances.
+ *   otherwise device [n_layers][batch][n_max][n_kv_heads][head_dim] (dims dtype)
+ *     rows copied into slots seq_lens[b] + i, i < n_commit[b].
+ * Device checks: n_commit range (BAD_COMMIT), capacity (KV_OVERFLOW); a request
+ * that fails a check is left unchanged. */
+int peagle_append_kv(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv, int32_t* seq_lens,
+                     const int32_t* n_commit, const void* k_rows, const void* v_rows,
+                     int32_t n_max, void* stream);
+
+/* Training-style parallel-prediction forward ("P-EAGLE: Parallel-Drafting EAGLE with
+ * Scalable Training", sections 3.1-3.2; "Speeding LLM inference with P-EAGLE in
+ * vLLM/Speculators", section "Flex-attention mask") over M retained rows (p, d),
+ * depths 1-based, sorted p-major (by p, then d).  Row (p, 1) takes
+ * embed[tokens[p]] and fc(hidden[p]); row (p, d >= 2) takes emb(mask) and
+ * fc(h_shared).  RoPE position p.  Row (p, d) attends depth-1 rows p' <= p - d + 1,
+ * its chain (p - j, d - j), j = 1 .. d-1, and itself; every chain row must be in the
+ * set (COD sampling guarantees it).
+ *   n, K      sequence length (<= max_seq) and depth (<= 16)
+ *   tokens    device int32 [n]; hidden device [n, 3H] (dims dtype)
+ *   row_p, row_d device int32 [M]; M <= max_rows
+ *   out_argmax device int32 [M] draft-vocab argmax (no d2t); out_logits fp32 [M, Vd]
+ *   or NULL.  Device checks: BAD_ROW for rows outside the contract. */
+int peagle_forward_parallel(peagle_ctx* ctx, int32_t n, int32_t K, const int32_t* tokens,
+                            const void* hidden, const int32_t* row_p, const int32_t* row_d,
+                            int32_t M, int32_t* out_argmax, float* out_logits, void* stream);
+
+/* Host-side COD sampling ("COD sampling"; 3.2): depth 1 keeps every position; row
+ * (p, d >= 2) exists when p - d + 1 >= 0 and is kept when its dependency (p-1, d-1)
+ * was kept and uniforms[p*K + d-1] < ratio.  Writes the retained rows p-major into
+ * out_p/out_d (host int32, capacity max_out) and returns their count, or a negative
+ * error (PEAGLE_ERR_CAPACITY if max_out is too small). */
+int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double* uniforms,
+                    int32_t* out_p, int32_t* out_d, int32_t max_out);
+
+/* Synchronise the context's device work and return PEAGLE_OK, PEAGLE_ERR_DEVICE if
+ * the device error word is non-zero (the word is then cleared), or PEAGLE_ERR_CUDA
+ * if a sticky CUDA error is pending. */
+int peagle_status(peagle_ctx* ctx);
+
+/* Raw device error bits observed by the last peagle_status call. */
+int32_t peagle_device_error_bits(const peagle_ctx* ctx);
+
+/* Static description of an error code. */
+const char* peagle_strerror(int code);
+
+/* Free all device memory of the context (synchronises). NULL is ignored. */
+void peagle_destroy(peagle_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PEAGLE_H */

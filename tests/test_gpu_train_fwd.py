@@ -1,0 +1,111 @@
+"""GPU parity of the training-style parallel-prediction forward (COD-sampled rows, the
+flex-attention mask rules) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import peagle_oracle as O
+from pe_helpers import LOGIT_TOL, MARGIN, make_ctx, pk
+
+pytestmark = pytest.mark.gpu
+
+SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_dim=64,
+                        intermediate=320, draft_vocab=1000, target_vocab=1500,
+                        rope_theta=10000.0, rms_eps=1e-5, dtype="bf16", d2t="monotone")
+SMALL_HD128 = synth.Dims(hidden=256, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                         intermediate=384, draft_vocab=777, target_vocab=777,
+                         rope_theta=500000.0, rms_eps=1e-5, dtype="bf16", d2t="identity")
+
+
+def _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K, logits=True):
+    m = pk()
+    M = len(rp)
+    am = torch.full((M,), -3, dtype=torch.int32, device="cuda")
+    lg = torch.full((M, dims.draft_vocab), float("nan"), device="cuda") if logits else None
+    m.peagle_forward_parallel(ctx, n, K, torch.from_numpy(tokens).cuda(), hidden.cuda(),
+                              torch.from_numpy(rp).cuda(), torch.from_numpy(rd).cuda(), M, am, lg)
+    assert m.peagle_status(ctx) == m.PEAGLE_OK
+    return am.cpu().numpy(), (lg.cpu().numpy() if logits else None)
+
+
+def _compare(dims, ref_logits, ref_am, ref_margin, am, lg, what):
+    tol = LOGIT_TOL[dims.dtype]
+    err = float(np.max(np.abs(lg - ref_logits)))
+    assert err <= tol, f"{what}: logits max abs err {err:.3e}"
+    ok = ref_margin > MARGIN
+    assert np.array_equal(am[ok], ref_am[ok]), what
+    assert np.array_equal(am, np.argmax(lg, axis=-1)), what
+    return err
+
+
+@pytest.mark.parametrize("dims,n,K,r", [
+    (synth.DIMS_TINY, 24, 4, 0.8),
+    (SMALL_BF16, 40, 8, 0.8),
+    (SMALL_HD128, 30, 3, 0.7),
+    (SMALL_BF16, 1, 4, 0.8),
+])
+def test_forward_parallel_small(dims, n, K, r):
+    m = pk()
+    w = synth.make_weights(dims, 17 + n)
+    tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
+    hidden = synth.normal((n, 3 * dims.hidden), 4, 1.0, dims.torch_dtype)
+    u = synth.cod_uniforms(n, K, seed=5)
+    rp, rd = m.peagle_cod_rows(n, K, r, u)
+    rows = O.cod_retained(n, K, r, u)
+    assert np.array_equal(np.stack([rp, rd], 1), rows)
+    ctx = make_ctx(dims, w, 1, K, max(n, 8), max_rows=len(rp), max_seq=n)
+    am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
+    ctx.close()
+    W = O.Weights64.from_synth(w)
+    ref_logits, ref_am, ref_margin = O.forward_parallel(W, dims, tokens, hidden, rows)
+    _compare(dims, ref_logits, ref_am, ref_margin, am, lg, f"fwd n={n} K={K}")
+
+
+def test_forward_parallel_rejects_bad_rows():
+    m = pk()
+    dims = synth.DIMS_TINY
+    w = synth.make_weights(dims, 2)
+    n, K = 8, 4
+    tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
+    hidden = synth.normal((n, 3 * dims.hidden), 4)
+    rp = np.array([0, 1, 1, 2, 2], np.int32)
+    rd = np.array([1, 1, 3, 1, 2], np.int32)  # (1,3): anchor -1, and its parent is absent
+    ctx = make_ctx(dims, w, 1, K, 16, max_rows=16, max_seq=n)
+    M = len(rp)
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    m.peagle_forward_parallel(ctx, n, K, torch.from_numpy(tokens).cuda(), hidden.cuda(),
+                              torch.from_numpy(rp).cuda(), torch.from_numpy(rd).cuda(), M, am)
+    assert m.peagle_status(ctx) == m.PEAGLE_ERR_DEVICE
+    assert m.peagle_device_error_bits(ctx) & m.PEAGLE_DEV_BAD_ROW
+    ctx.close()
+
+
+def test_train_fwd_full_prefix_and_tail():
+    """The full n=2048, K=8 forward (about 8.5K rows) on the GPU.  The oracle checks (a)
+    every row with p < 96 and (b) the last rows of the sequence through their
+    dependency closure (all depth-1 rows up to their anchors plus their chains): the
+    mask makes both subsets closed, so the oracle's outputs on them are exact."""
+    m = pk()
+    wl = synth.WORKLOADS["train_fwd"]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    ti = synth.make_train_inputs(wl, 21)
+    n, K = wl.n_seq, wl.K
+    rp, rd = m.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
+    rows = np.stack([rp, rd], 1).astype(np.int64)
+    M = len(rp)
+    assert abs(M - O.cod_expected_rows(n, K, wl.cod_ratio)) < 400
+    ctx = make_ctx(dims, w, 1, K, n, max_rows=M, max_seq=n)
+    am, lg = _run_fwd(ctx, dims, ti["tokens"], ti["hidden"], rp, rd, n, K)
+    ctx.close()
+    W = O.Weights64.from_synth(w, lazy=True)
+    pre = rows[rows[:, 0] < 96]
+    rl, ra, rm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], pre)
+    _compare(dims, rl, ra, rm, am[: len(pre)], lg[: len(pre)], "train_fwd prefix")
+    tail = rows[-3:]
+    clo = O.dependency_closure(rows, tail)
+    cl, ca, cm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], clo)
+    idx = {(int(p), int(d)): i for i, (p, d) in enumerate(clo)}
+    sel = [idx[(int(p), int(d))] for p, d in tail]
+    _compare(dims, cl[sel], ca[sel], cm[sel], am[-3:], lg[-3:], "train_fwd tail")
