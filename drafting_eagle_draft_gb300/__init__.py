@@ -32,7 +32,9 @@ PEAGLE_BF16 = 1
 # every entry point declared in include/peagle.h
 EXPORTS = ("peagle_create", "peagle_draft", "peagle_verify_greedy", "peagle_append_kv",
            "peagle_forward_parallel", "peagle_cod_rows", "peagle_status",
+           "peagle_set_timing", "peagle_read_timing",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
+STAGES = ("fc", "qkv", "attn", "oproj", "gate_up", "down", "lm_head", "norm", "small")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -81,12 +83,14 @@ def lib():
         L.peagle_draft.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _vp, _i32,
                                    _vp, _vp, _vp]
         L.peagle_verify_greedy.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
-        L.peagle_append_kv.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _vp, _vp,
-                                       _i32, _vp]
+        L.peagle_append_kv.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _i32,
+                                       _vp, _vp, _i32, _vp]
         L.peagle_forward_parallel.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp,
                                               _vp, _vp]
         L.peagle_cod_rows.argtypes = [_i32, _i32, ctypes.c_double, _vp, _vp, _vp, _i32]
         L.peagle_status.argtypes = [_vp]
+        L.peagle_set_timing.argtypes = [_vp, _i32]
+        L.peagle_read_timing.argtypes = [_vp, _vp, _vp]
         L.peagle_device_error_bits.argtypes = [_vp]
         L.peagle_device_error_bits.restype = _i32
         L.peagle_strerror.argtypes = [ctypes.c_int]
@@ -210,10 +214,10 @@ def peagle_verify_greedy(batch, K, draft_tokens, target_argmax, out_accept_len, 
 
 
 def peagle_append_kv(ctx: Context, batch, kv: PeagleKV, seq_lens, n_commit, k_rows=None,
-                     v_rows=None, n_max=0, stream=None):
+                     v_rows=None, n_max=0, stream=None, n_extra=0):
     _check(lib().peagle_append_kv(ctx.handle, int(batch), ctypes.byref(kv), _ptr(seq_lens),
-                                  _ptr(n_commit), _ptr(k_rows), _ptr(v_rows), int(n_max),
-                                  _stream_ptr(stream)),
+                                  _ptr(n_commit), int(n_extra), _ptr(k_rows), _ptr(v_rows),
+                                  int(n_max), _stream_ptr(stream)),
            "peagle_append_kv")
 
 
@@ -243,6 +247,19 @@ def peagle_cod_rows(n, K, ratio, uniforms):
 def peagle_status(ctx: Context) -> int:
     """Synchronises; returns PEAGLE_OK or PEAGLE_ERR_DEVICE (device error bits cleared)."""
     return lib().peagle_status(ctx.handle)
+
+
+def peagle_set_timing(ctx: Context, enable: bool):
+    _check(lib().peagle_set_timing(ctx.handle, 1 if enable else 0), "peagle_set_timing")
+
+
+def peagle_read_timing(ctx: Context) -> dict:
+    """{stage: (milliseconds, launches)} since the previous read (synchronises)."""
+    ms = np.zeros(len(STAGES), np.float32)
+    n = np.zeros(len(STAGES), np.int32)
+    _check(lib().peagle_read_timing(ctx.handle, ms.ctypes.data, n.ctypes.data),
+           "peagle_read_timing")
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(STAGES)}
 
 
 def peagle_device_error_bits(ctx: Context) -> int:

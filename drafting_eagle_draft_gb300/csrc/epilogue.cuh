@@ -2,8 +2,8 @@
 //
 // Every projection of the pass is Y[r, m] = sum_k X[r, k] W[m, k] (nn.Linear) over a
 // handful of rows r (batch x K) and a long output dimension m.  The epilogue turns a
-// finished 128-feature tile of Y (fp32, indexable as src[r * ld + (m - m0)]) into
-// the pass's next tensor, so that Y itself never reaches HBM:
+// finished 128-feature tile of Y (fp32) into the pass's next tensor, so that Y itself
+// never reaches HBM:
 //   STORE      fp32 copy (fc projection; fc(h_shared) at create time)
 //   QKV_ROPE   RoPE (rotate-half pairs i, i+hd/2) on q and k, then q -> Q [R, nq, hd],
 //              k, v -> the drafter KV cache slot of each row (decode) or to per-row
@@ -23,8 +23,11 @@ enum EpiKind : int { EPI_STORE = 0, EPI_QKV_ROPE = 1, EPI_RESID = 2, EPI_SWIGLU 
 
 struct EpiArgs {
   int kind;
-  int R;     // valid rows
+  int R;     // valid (logical) rows
   int Nout;  // valid output features
+  int in_split;   // the GEMM's activation operand holds rows [0,R) = bf16 hi parts and
+                  // [R,2R) = bf16 lo parts; the epilogue adds the two partial products
+  int out_split;  // activation outputs (SWIGLU) are written as hi rows [0,R), lo [R,2R)
   // STORE
   float* out_f32;
   int out_ld;
@@ -32,7 +35,8 @@ struct EpiArgs {
   float* resid;
   int ld_res;
   // QKV_ROPE
-  void* q_out;            // [R, nq*hd]
+  void* q_out;            // [R, nq*hd]; fp32 when q_f32, else the activation dtype
+  int q_f32;
   void* k_dst;            // decode: cache layer base [B][nkv][cap][hd]; rows: [R][nkv][hd]
   void* v_dst;
   void* k1_dst;           // rows mode: depth-1 copy [n][nkv][hd] (may be null)
@@ -47,7 +51,7 @@ struct EpiArgs {
   const float2* rope;     // [max_positions][hd/2] (cos, sin)
   int max_pos;
   // SWIGLU
-  void* act_out;          // [R, I]
+  void* act_out;          // [R, I] (or [2R, I] when out_split)
   int I;
   // LMHEAD
   float* logits;          // [R, Nout] or null
@@ -55,40 +59,59 @@ struct EpiArgs {
   unsigned* err;
 };
 
+// Store an activation that feeds the next projection: a single value, or its bf16
+// hi part at row r and the bf16 rounding of the remainder at row r + R.
 template <typename T>
-__device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src, int ld, int m0,
-                                              int tid, int nthr) {
-  const int R = a.R;
+__device__ __forceinline__ void store_act(T* base, size_t row_stride, int r, int R, int split,
+                                          int col, float v) {
+  T hi = from_f32<T>(v);
+  base[(size_t)r * row_stride + col] = hi;
+  if (split) base[(size_t)(r + R) * row_stride + col] = from_f32<T>(v - to_f32(hi));
+}
+
+// Apply the epilogue to rows r0 .. r0+rcount-1 of a 128-feature tile starting at m0.
+// The tile value of row r0+i, feature m0+ml is src[i*ld + ml], plus src[(i+lo_off)*ld + ml]
+// when lo_off >= 0 (the lo-part product of a split activation operand).
+template <typename T>
+__device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src, int ld,
+                                              int lo_off, int m0, int r0, int rcount, int tid,
+                                              int nthr) {
   const int mcount = min(128, a.Nout - m0);
+  auto val = [&](int i, int ml) -> float {
+    float v = src[(size_t)i * ld + ml];
+    if (lo_off >= 0) v += src[(size_t)(i + lo_off) * ld + ml];
+    return v;
+  };
   switch (a.kind) {
     case EPI_STORE: {
-      for (int idx = tid; idx < R * 128; idx += nthr) {
-        int r = idx >> 7, ml = idx & 127;
-        if (ml < mcount) a.out_f32[(size_t)r * a.out_ld + m0 + ml] = src[(size_t)r * ld + ml];
+      for (int idx = tid; idx < rcount * 128; idx += nthr) {
+        int i = idx >> 7, ml = idx & 127;
+        if (ml < mcount) a.out_f32[(size_t)(r0 + i) * a.out_ld + m0 + ml] = val(i, ml);
       }
     } break;
     case EPI_RESID: {
-      for (int idx = tid; idx < R * 128; idx += nthr) {
-        int r = idx >> 7, ml = idx & 127;
-        if (ml < mcount) a.resid[(size_t)r * a.ld_res + m0 + ml] += src[(size_t)r * ld + ml];
+      for (int idx = tid; idx < rcount * 128; idx += nthr) {
+        int i = idx >> 7, ml = idx & 127;
+        if (ml < mcount) a.resid[(size_t)(r0 + i) * a.ld_res + m0 + ml] += val(i, ml);
       }
     } break;
     case EPI_SWIGLU: {
-      // tile rows [0,64) = gate, [64,128) = up of intermediate features m0/2 + i
+      // tile rows [0,64) = gate, [64,128) = up of intermediate features m0/2 + f
       T* act = (T*)a.act_out;
-      for (int idx = tid; idx < R * 64; idx += nthr) {
-        int r = idx >> 6, i = idx & 63;
-        float g = src[(size_t)r * ld + i];
-        float u = src[(size_t)r * ld + 64 + i];
+      for (int idx = tid; idx < rcount * 64; idx += nthr) {
+        int i = idx >> 6, f = idx & 63;
+        float g = val(i, f);
+        float u = val(i, 64 + f);
         float s = g / (1.f + expf(-g));
-        act[(size_t)r * a.I + (m0 >> 1) + i] = from_f32<T>(s * u);
+        store_act<T>(act, a.I, r0 + i, a.R, a.out_split, (m0 >> 1) + f, s * u);
       }
     } break;
     case EPI_QKV_ROPE: {
       const int hd = a.hd, half = hd >> 1;
       const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
-      for (int idx = tid; idx < R * 128; idx += nthr) {
-        int r = idx >> 7, ml = idx & 127;
+      for (int idx = tid; idx < rcount * 128; idx += nthr) {
+        int ti = idx >> 7, ml = idx & 127;
+        int r = r0 + ti;
         int m = m0 + ml;
         if (ml >= mcount) continue;
         int i = m % hd;
@@ -107,24 +130,29 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
           if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
           if (sec != 0) continue;  // no cache slot for this row
         }
-        float v0 = src[(size_t)r * ld + ml];
+        float v0 = val(ti, ml);
         float out0, out1 = 0.f;
-        int mm = m;
         if (sec == 2) {
           out0 = v0;
         } else {
           if (i >= half) continue;  // handled together with its pair partner
-          float v1 = src[(size_t)r * ld + ml + half];
+          float v1 = val(ti, ml + half);
           float2 cs = pos_ok ? a.rope[(size_t)pos * half + i] : make_float2(1.f, 0.f);
           out0 = v0 * cs.x - v1 * cs.y;
           out1 = v1 * cs.x + v0 * cs.y;
         }
         if (sec == 0) {
-          T* q = (T*)a.q_out + (size_t)r * a.nq * hd + mm;
-          q[0] = from_f32<T>(out0);
-          q[half] = from_f32<T>(out1);
+          if (a.q_f32) {
+            float* q = (float*)a.q_out + (size_t)r * a.nq * hd + m;
+            q[0] = out0;
+            q[half] = out1;
+          } else {
+            T* q = (T*)a.q_out + (size_t)r * a.nq * hd + m;
+            q[0] = from_f32<T>(out0);
+            q[half] = from_f32<T>(out1);
+          }
         } else {
-          int g = (mm - (sec == 1 ? qend : kend)) / hd;
+          int g = (m - (sec == 1 ? qend : kend)) / hd;
           T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
           size_t off;
           if (a.decode)
@@ -146,18 +174,18 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
     } break;
     case EPI_LMHEAD: {
       if (a.logits) {
-        for (int idx = tid; idx < R * 128; idx += nthr) {
-          int r = idx >> 7, ml = idx & 127;
-          if (ml < mcount) a.logits[(size_t)r * a.Nout + m0 + ml] = src[(size_t)r * ld + ml];
+        for (int idx = tid; idx < rcount * 128; idx += nthr) {
+          int i = idx >> 7, ml = idx & 127;
+          if (ml < mcount) a.logits[(size_t)(r0 + i) * a.Nout + m0 + ml] = val(i, ml);
         }
       }
       // per row: best (value, index) over the tile -> one atomicMax per warp and row
       const int lane = tid & 31;
       const int nw = nthr >> 5;
-      for (int r = tid >> 5; r < R; r += nw) {
+      for (int i = tid >> 5; i < rcount; i += nw) {
         unsigned long long best = 0ull;
         for (int ml = lane; ml < mcount; ml += 32) {
-          unsigned long long k = argmax_key(src[(size_t)r * ld + ml], m0 + ml);
+          unsigned long long k = argmax_key(val(i, ml), m0 + ml);
           best = k > best ? k : best;
         }
 #pragma unroll
@@ -165,7 +193,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
           unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
           best = other > best ? other : best;
         }
-        if (lane == 0) atomicMax(a.keys + r, best);
+        if (lane == 0) atomicMax(a.keys + r0 + i, best);
       }
     } break;
   }

@@ -1,8 +1,504 @@
+// Tensor-core GEMM of the bf16 draft pass on sm_103a: tcgen05.mma with the accumulator
+// in tensor memory, operands streamed by TMA into a shared-memory ring, stream-K work
+// split, and the pass's fused epilogues.
+//
+// Y^T = W X^T with W [Nout, Kd] (weights, the MMA's M=128 operand, "swap-AB") and
+// X [rows, Kd] (activations, the MMA's N operand).  The decode pass has only batch x K
+// rows, so the weight stream is the whole cost: the flattened (tile, k-block) space is
+// cut into one equal contiguous range per CTA (stream-K), every SM streams the same
+// number of weight bytes, and a tile shared by several CTAs is finished by whichever
+// contributor arrives last (atomic counter, no waiting), which adds the fp32 partials in
+// contributor order and applies the epilogue.
+//
+// Split activations: an operand row may be carried as a bf16 hi part and a bf16 lo part
+// (x = hi + lo to about 16 significant bits).  Both parts go through the same MMA as
+// extra N columns and the epilogue adds their products, so the weights are read once.
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 issues
+// tcgen05.mma (and warp 1 owns the TMEM allocation), warps 2-5 drain the accumulator
+// (tcgen05.ld), exchange partials and run the epilogue.  Two TMEM accumulators let the
+// epilogue of one segment overlap the MMAs of the next.
+//
+// Programmatic dependent launch: weight tiles do not depend on the previous kernel, so
+// the producer issues the first ring's weight loads before griddepcontrol.wait and the
+// activation loads after it.
+#include <cuda.h>
+#include <stdio.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "gemm_tc.h"
+#include "tc_ptx.cuh"
 
 namespace peagle {
-struct TcGemmPlan {};
-int tc_create(TcGemmPlan** out, int, int, int) { *out = nullptr; return 0; }
-void tc_gemm(TcGemmPlan*, const void*, const void*, int, int, int, int, const EpiArgs&, cudaStream_t) {}
-void tc_destroy(TcGemmPlan*) {}
+
+constexpr int TC_THREADS = 192;
+constexpr int A_BYTES = 128 * 128;  // one 128 x 64 bf16 weight tile
+constexpr int STAGE_F_BYTES = 32 * 128 * 4;
+
+struct TcParams {
+  int Nout, Kd;
+  int R;        // logical rows
+  int split;    // X rows [0,R) hi parts, [R,2R) lo parts
+  int BN;       // MMA N = operand rows per tile
+  int rpt;      // logical rows per tile
+  int lo_col;   // split: TMEM column of the lo part of tile row 0
+  int two_box;  // split with several tiles: hi and lo rows come from two 128-row boxes
+  int n_tiles;  // row tiles
+  int KB;       // k-blocks of 64
+  long long total;  // tiles * KB
+  int G;        // CTAs
+  int stages;
+  uint32_t tmem_cols;
+  float* ws;          // partial slots [2G][BN][128]
+  unsigned* counters; // per tile, zero between launches
+  unsigned* err;
+};
+
+__device__ __forceinline__ long long range_begin(long long c, const TcParams& p) {
+  return c * p.total / p.G;
+}
+// CTA whose stream-K range contains iteration `it`
+__device__ __forceinline__ int owner_of(long long it, const TcParams& p) {
+  long long c = it * p.G / p.total;
+  while (c + 1 < p.G && range_begin(c + 1, p) <= it) ++c;
+  while (c > 0 && range_begin(c, p) > it) --c;
+  return (int)c;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Activation operand of k-block kb for row tile nt: one box of BN rows, or (split over
+// several tiles) the tile's 128 hi rows followed by its 128 lo rows.
+__device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* m, int kb, int nt,
+                                       uint64_t* bar, uint64_t pol, const TcParams& p) {
+  if (p.two_box) {
+    tc::tma_load_2d(dst, m, kb * 64, nt * 128, bar, pol);
+    tc::tma_load_2d(dst + 128 * 128, m, kb * 64, p.R + nt * 128, bar, pol);
+  } else {
+    tc::tma_load_2d(dst, m, kb * 64, nt * p.BN, bar, pol);
+  }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const TcParams p, const EpiArgs epi) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int S = p.stages;
+  const int B_BYTES = p.BN * 128;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + (size_t)S * A_BYTES;
+  float* stg = (float*)(sB + (size_t)S * B_BYTES);  // [32][128] fp32 epilogue staging
+  uint64_t* full = (uint64_t*)((uint8_t*)stg + STAGE_F_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint64_t* acce = accf + 2;
+  uint32_t* s_tmem = (uint32_t*)(acce + 2);
+  volatile int* s_flag = (volatile int*)(s_tmem + 1);
+  volatile int* s_abort = s_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&accf[i], 1);
+      tc::mbar_init(&acce[i], 128);
+    }
+    *s_abort = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(s_tmem, p.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  tc::pdl_launch_dependents();
+
+  const long long beg = range_begin(c, p), end = range_begin(c + 1, p);
+  const int KB = p.KB;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = tc::policy_evict_first();
+      const uint64_t pol_x = tc::policy_evict_last();
+      const uint32_t bytes = A_BYTES + B_BYTES;
+      const long long n_it = end - beg;
+      const int npre = (int)(n_it < S ? n_it : S);
+      for (int i = 0; i < npre; ++i) {
+        const long long it = beg + i;
+        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
+        tc::mbar_expect_tx(&full[i], bytes);
+        tc::tma_load_2d(sA + (size_t)i * A_BYTES, &tmW, kb * 64, (tile / p.n_tiles) * 128, &full[i],
+                        pol_w);
+      }
+      tc::pdl_wait();
+      for (int i = 0; i < npre; ++i) {
+        const long long it = beg + i;
+        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
+        load_b(sB + (size_t)i * B_BYTES, &tmX, kb, tile % p.n_tiles, &full[i], pol_x, p);
+      }
+      int stage = npre % S;
+      uint32_t ph = (npre == S) ? 1u : 0u;
+      for (long long it = beg + npre; it < end; ++it) {
+        if (!tc::mbar_wait(&empty[stage], ph ^ 1u, s_abort)) {
+          raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
+        tc::mbar_expect_tx(&full[stage], bytes);
+        tc::tma_load_2d(sA + (size_t)stage * A_BYTES, &tmW, kb * 64, (tile / p.n_tiles) * 128,
+                        &full[stage], pol_w);
+        load_b(sB + (size_t)stage * B_BYTES, &tmX, kb, tile % p.n_tiles, &full[stage], pol_x, p);
+        if (++stage == S) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, p.BN);
+      int stage = 0;
+      uint32_t ph = 0;
+      int seg = 0;
+      bool ok = true;
+      for (long long it = beg; it < end && ok;) {
+        const int tile = (int)(it / KB);
+        long long seg_end = (long long)(tile + 1) * KB;
+        if (seg_end > end) seg_end = end;
+        const int buf = seg & 1;
+        const uint32_t use = (uint32_t)(seg >> 1);
+        if (!tc::mbar_wait(&acce[buf], (use & 1u) ^ 1u, s_abort)) {
+          raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(buf * p.BN);
+        const long long seg_beg = it;
+        for (; it < seg_end; ++it) {
+          if (!tc::mbar_wait(&full[stage], ph, s_abort)) {
+            raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)stage * A_BYTES));
+          const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (it != seg_beg || k > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        tc::mma_commit(&accf[buf]);
+        ++seg;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int et = threadIdx.x - 64;      // 0 .. 127
+    const int quarter = warp & 3;         // TMEM lane quarter this warp may access
+    const int ml = quarter * 32 + lane;   // tile feature = TMEM lane
+    const int R = p.R;
+    int seg = 0;
+    for (long long it = beg; it < end;) {
+      const int tile = (int)(it / KB);
+      long long seg_end = (long long)(tile + 1) * KB;
+      if (seg_end > end) seg_end = end;
+      it = seg_end;
+      const int buf = seg & 1;
+      const uint32_t use = (uint32_t)(seg >> 1);
+      ++seg;
+      // one thread observes the accumulator barrier; the named barrier publishes the
+      // outcome so the four warps stay in lock-step even if the wait gives up
+      if (et == 0 && !tc::mbar_wait(&accf[buf], use & 1u, s_abort)) {
+        raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+        *s_abort = 1;
+      }
+      epi_bar();
+      if (*s_abort) break;
+      tc::fence_after_sync();
+      const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+      const int m0 = mt * 128;
+      const int row0 = nt * p.rpt;               // first logical row of this tile
+      const int lrows = min(p.rpt, R - row0);    // logical rows in this tile
+      const long long t_beg = (long long)tile * KB;
+      const int cf = owner_of(t_beg, p), cl = owner_of(t_beg + KB - 1, p);
+      const uint32_t tb = tmem + (uint32_t)(buf * p.BN) + ((uint32_t)(quarter * 32) << 16);
+      // chunking: split tiles take 16 logical rows per chunk (hi + lo columns), others 32
+      const int step = p.split ? 16 : 32;
+      const int nch = (lrows + step - 1) / step;
+      if (cf == cl) {
+        // ---- sole owner: TMEM -> staging -> epilogue
+        for (int ch = 0; ch < nch; ++ch) {
+          const int i0 = ch * step;
+          float v[16], w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[j] = 0.f;
+          tc::tmem_ld16(tb + i0, v);
+          if (p.split) {
+            tc::tmem_ld16(tb + p.lo_col + i0, w);
+          } else if (i0 + 16 < p.BN) {
+            tc::tmem_ld16(tb + i0 + 16, w);
+          }
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            stg[j * 128 + ml] = v[j];
+            stg[(16 + j) * 128 + ml] = w[j];
+          }
+          if (ch == nch - 1) {
+            tc::fence_before_sync();
+            tc::mbar_arrive(&acce[buf]);
+          }
+          epi_bar();
+          epilogue_tile<bf16>(epi, stg, 128, p.split ? 16 : -1, m0, row0 + i0,
+                              min(step, lrows - i0), et, 128);
+          epi_bar();
+        }
+      } else {
+        // ---- shared tile: write this CTA's partial, the last contributor reduces
+        const int slot = (range_begin(c, p) >= t_beg) ? 2 * c : 2 * c + 1;
+        float* wsl = p.ws + (size_t)slot * p.BN * 128;
+        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(tb + c0, v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) wsl[(size_t)(c0 + j) * 128 + ml] = v[j];
+        }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&acce[buf]);
+        __threadfence();
+        epi_bar();
+        if (et == 0) {
+          const unsigned prev = atomicAdd(p.counters + tile, 1u);
+          *s_flag = (prev == (unsigned)(cl - cf)) ? 1 : 0;
+        }
+        epi_bar();
+        if (*s_flag) {
+          __threadfence();
+          for (int ch = 0; ch < nch; ++ch) {
+            const int i0 = ch * step;
+            for (int j = 0; j < 32; ++j) {
+              int col;
+              bool valid;
+              if (p.split) {
+                const int ii = i0 + (j & 15);
+                col = (j < 16) ? ii : p.lo_col + ii;
+                valid = ii < lrows;
+              } else {
+                col = i0 + j;
+                valid = col < lrows;
+              }
+              float acc = 0.f;
+              if (valid) {
+                for (int cc = cf; cc <= cl; ++cc) {
+                  const int sl = (range_begin(cc, p) >= t_beg) ? 2 * cc : 2 * cc + 1;
+                  acc += __ldcg(p.ws + ((size_t)sl * p.BN + col) * 128 + ml);
+                }
+              }
+              stg[j * 128 + ml] = acc;
+            }
+            epi_bar();
+            epilogue_tile<bf16>(epi, stg, 128, p.split ? 16 : -1, m0, row0 + i0,
+                                min(step, lrows - i0), et, 128);
+            epi_bar();
+          }
+          if (et == 0) p.counters[tile] = 0u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// =====================================================================================
+// host side
+// =====================================================================================
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct TcGemmPlan {
+  int num_sms;
+  int max_bn;
+  float* ws;
+  unsigned* counters;
+  int max_tiles;
+  unsigned* err;
+  EncodeTiledFn encode;
+  std::mutex mu;
+  std::map<std::tuple<const void*, int, int, int, int>, CUtensorMap> maps;
+};
+
+static bool encode_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
+                       int ld, int box_rows) {
+  auto key = std::make_tuple(base, rows, cols, ld, box_rows);
+  {
+    std::lock_guard<std::mutex> g(p->mu);
+    auto itr = p->maps.find(key);
+    if (itr != p->maps.end()) {
+      *out = itr->second;
+      return true;
+    }
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = p->encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "peagle: cuTensorMapEncodeTiled failed (%d) rows=%d cols=%d ld=%d box=%d\n",
+            (int)r, rows, cols, ld, box_rows);
+    return false;
+  }
+  std::lock_guard<std::mutex> g(p->mu);
+  if (p->maps.size() > 4096) p->maps.clear();
+  p->maps[key] = *out;
+  return true;
+}
+
+static size_t smem_bytes(int stages, int bn) {
+  return 1024 /*align slack*/ + (size_t)stages * (A_BYTES + bn * 128) + STAGE_F_BYTES +
+         (size_t)(2 * stages + 4) * 8 + 16;
+}
+
+void tc_destroy(TcGemmPlan* p) {
+  if (!p) return;
+  if (p->ws) cudaFree(p->ws);
+  if (p->counters) cudaFree(p->counters);
+  delete p;
+}
+
+int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned* err) {
+  *out = nullptr;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return PEAGLE_ERR_CUDA;
+  TcGemmPlan* p = new TcGemmPlan();
+  p->num_sms = num_sms;
+  p->encode = (EncodeTiledFn)fn;
+  p->err = err;
+  p->max_bn = 256;
+  p->ws = nullptr;
+  p->counters = nullptr;
+  const int n_tiles_max = (rows_max + 15) / 16 + 1;
+  p->max_tiles = ((max_dim + 127) / 128 + 1) * n_tiles_max;
+  if (cudaMalloc(&p->ws, (size_t)2 * num_sms * p->max_bn * 128 * 4) != cudaSuccess ||
+      cudaMalloc(&p->counters, (size_t)p->max_tiles * 4) != cudaSuccess ||
+      cudaMemset(p->counters, 0, (size_t)p->max_tiles * 4) != cudaSuccess) {
+    tc_destroy(p);
+    return PEAGLE_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           227 * 1024) != cudaSuccess) {
+    tc_destroy(p);
+    return PEAGLE_ERR_CUDA;
+  }
+  *out = p;
+  return PEAGLE_OK;
+}
+
+static uint32_t pow2_at_least(uint32_t v) {
+  uint32_t r = 32;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
+            const EpiArgs& epi, cudaStream_t s) {
+  TcParams p;
+  p.Nout = Nout;
+  p.Kd = Kd;
+  p.R = R;
+  p.split = epi.in_split ? 1 : 0;
+  const int xrows = p.split ? 2 * R : R;
+  p.two_box = 0;
+  if (p.split && 2 * R <= 240) {
+    // one tile: a single box of BN rows holds the hi rows [0,R) and the lo rows [R,2R)
+    p.BN = (2 * R + 15) / 16 * 16;
+    p.rpt = R;
+    p.lo_col = R;
+    p.n_tiles = 1;
+  } else if (p.split) {
+    // 128 logical rows per tile: hi rows in TMEM columns [0,128), lo rows in [128,256)
+    p.BN = 256;
+    p.rpt = 128;
+    p.lo_col = 128;
+    p.two_box = 1;
+    p.n_tiles = (R + 127) / 128;
+  } else {
+    p.BN = R <= 256 ? (R + 15) / 16 * 16 : 256;
+    p.rpt = p.BN;
+    p.lo_col = 0;
+    p.n_tiles = (R + p.BN - 1) / p.BN;
+  }
+  p.KB = Kd / 64;
+  const int m_tiles = (Nout + 127) / 128;
+  const long long tiles = (long long)m_tiles * p.n_tiles;
+  if (tiles > pl->max_tiles || Kd % 64) return PEAGLE_ERR_CAPACITY;
+  p.total = tiles * p.KB;
+  p.G = (int)(p.total < pl->num_sms ? p.total : pl->num_sms);
+  // shared memory ring: decode-sized tiles keep ~110 KB so a second CTA (the next
+  // kernel's, under programmatic dependent launch) fits on the SM; large tiles take more
+  const size_t budget = p.BN <= 64 ? 112 * 1024 : 220 * 1024;
+  int stages = 2;
+  while (stages < 12 && smem_bytes(stages + 1, p.BN) <= budget) ++stages;
+  p.stages = stages;
+  // single-tile split reads 16-column groups starting at column R + i0, which may run
+  // up to 15 columns past the second accumulator: keep that slack allocated
+  p.tmem_cols = pow2_at_least((uint32_t)(2 * p.BN + ((p.split && !p.two_box) ? 16 : 0)));
+  if (p.tmem_cols > 512) return PEAGLE_ERR_CAPACITY;
+  p.ws = pl->ws;
+  p.counters = pl->counters;
+  p.err = pl->err;
+  CUtensorMap mw, mx;
+  if (!encode_map(pl, &mw, W, Nout, Kd, Kd, 128)) return PEAGLE_ERR_CUDA;
+  if (!encode_map(pl, &mx, X, xrows, Kd, ldx, p.two_box ? 128 : p.BN)) return PEAGLE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes(stages, p.BN);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, mw, mx, p, epi);
+  return e == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+}
+
 }  // namespace peagle

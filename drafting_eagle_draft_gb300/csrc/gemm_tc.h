@@ -9,12 +9,16 @@ namespace peagle {
 
 struct TcGemmPlan;
 
-// Allocates the GEMM's workspace for up to rows_max activation rows and output /
-// reduction dimensions up to max_dim.  *out stays NULL when the tensor-core path is
-// not available in this build (the caller then uses the FFMA GEMM).
-int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim);
-void tc_gemm(TcGemmPlan* p, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
-             const EpiArgs& epi, cudaStream_t s);
+// Allocates the GEMM's workspace (stream-K partial slots and tile counters) for up to
+// rows_max activation rows and output dimensions up to max_dim; device-side timeouts are
+// reported in *err.
+int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned* err);
+// Launches Y^T = W X^T with the fused epilogue `epi` on stream s (asynchronous).
+//   W [Nout, Kd] bf16 row-major (device), X [rows, Kd] bf16 with row stride ldx elements;
+//   rows = R, or 2R when epi.in_split (hi rows then lo rows).  Kd % 64 == 0.
+// Returns PEAGLE_OK or a negative PEAGLE_ERR_* code (nothing launched on error).
+int tc_gemm(TcGemmPlan* p, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
+            const EpiArgs& epi, cudaStream_t s);
 void tc_destroy(TcGemmPlan* p);
 
 }  // namespace peagle

@@ -65,21 +65,16 @@ template <typename T>
 __global__ void __launch_bounds__(256) epilogue_kernel(const float* __restrict__ Y, int ldy,
                                                        EpiArgs a) {
   const int m0 = blockIdx.x * 128;
-  epilogue_tile<T>(a, Y + m0, ldy, m0, threadIdx.x, blockDim.x);
+  epilogue_tile<T>(a, Y + m0, ldy, a.in_split ? a.R : -1, m0, 0, a.R, threadIdx.x, blockDim.x);
 }
 
 void launch_gemm_simt(bool bf16m, const void* W, const void* X, int ldx, float* Y, int ldy,
                       int Nout, int Kd, int R, const EpiArgs& epi, cudaStream_t s) {
+  (void)bf16m;  // fp32 drafters only: bf16 projections run on the tensor cores
   dim3 g(cdiv(Nout, 8));
-  if (bf16m)
-    gemm_simt_kernel<bf16><<<g, 256, 0, s>>>((const bf16*)W, (const bf16*)X, ldx, Y, ldy, Nout, Kd, R);
-  else
-    gemm_simt_kernel<float><<<g, 256, 0, s>>>((const float*)W, (const float*)X, ldx, Y, ldy, Nout, Kd, R);
+  gemm_simt_kernel<float><<<g, 256, 0, s>>>((const float*)W, (const float*)X, ldx, Y, ldy, Nout, Kd, R);
   dim3 ge(cdiv(Nout, 128));
-  if (bf16m)
-    epilogue_kernel<bf16><<<ge, 256, 0, s>>>(Y, ldy, epi);
-  else
-    epilogue_kernel<float><<<ge, 256, 0, s>>>(Y, ldy, epi);
+  epilogue_kernel<float><<<ge, 256, 0, s>>>(Y, ldy, epi);
 }
 
 // =====================================================================================
@@ -96,10 +91,11 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
     const T* __restrict__ emb_mask,
     const float* __restrict__ F, const float* __restrict__ f_shared, const int* __restrict__ tokens,
     const int* __restrict__ row_p, const int* __restrict__ row_d, const T* __restrict__ g_in,
-    const T* __restrict__ g_hid, float eps, T* __restrict__ X0, float* __restrict__ res,
-    unsigned long long* __restrict__ keys, unsigned* err) {
+    const T* __restrict__ g_hid, float eps, int split, T* __restrict__ X0,
+    float* __restrict__ res, unsigned long long* __restrict__ keys, unsigned* err) {
   __shared__ float red[32];
   const int r = blockIdx.x;
+  const int R = gridDim.x;
   bool ntp;
   int src;  // request (mode 0) or position (mode 1)
   if (mode == 0) {
@@ -137,12 +133,11 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
   __syncthreads();
   sf = block_sum(sf, red);
   const float ie = rsqrtf(se / H + eps), ifv = rsqrtf(sf / H + eps);
-  T* x = X0 + (size_t)r * 2 * H;
   float* rs = res + (size_t)r * H;
   for (int i = threadIdx.x; i < H; i += blockDim.x) {
     float fv = f[i];
-    x[i] = from_f32<T>(ld(e + i) * ie * ld(g_in + i));
-    x[H + i] = from_f32<T>(fv * ifv * ld(g_hid + i));
+    store_act<T>(X0, 2 * H, r, R, split, i, ld(e + i) * ie * ld(g_in + i));
+    store_act<T>(X0, 2 * H, r, R, split, H + i, fv * ifv * ld(g_hid + i));
     rs[i] = fv;
   }
   if (threadIdx.x == 0 && keys) keys[r] = 0ull;
@@ -152,16 +147,16 @@ void launch_input_fusion(bool bf16m, int mode, int R, int K, int n_src, int H, c
                          int Vt,
                          const void* emb_mask, const float* F, const float* f_shared,
                          const int* tokens, const int* row_p, const int* row_d,
-                         const void* g_in, const void* g_hid, float eps, void* X0, float* res,
-                         unsigned long long* keys, unsigned* err, cudaStream_t s) {
+                         const void* g_in, const void* g_hid, float eps, int split, void* X0,
+                         float* res, unsigned long long* keys, unsigned* err, cudaStream_t s) {
   if (bf16m)
     input_fusion_kernel<bf16><<<R, 256, 0, s>>>(mode, K, n_src, H, (const bf16*)embed, Vt,
         (const bf16*)emb_mask, F, f_shared, tokens, row_p, row_d, (const bf16*)g_in,
-        (const bf16*)g_hid, eps, (bf16*)X0, res, keys, err);
+        (const bf16*)g_hid, eps, split, (bf16*)X0, res, keys, err);
   else
     input_fusion_kernel<float><<<R, 256, 0, s>>>(mode, K, n_src, H, (const float*)embed, Vt,
         (const float*)emb_mask, F, f_shared, tokens, row_p, row_d, (const float*)g_in,
-        (const float*)g_hid, eps, (float*)X0, res, keys, err);
+        (const float*)g_hid, eps, 0, (float*)X0, res, keys, err);
 }
 
 // =====================================================================================
@@ -170,7 +165,7 @@ void launch_input_fusion(bool bf16m, int mode, int R, int K, int n_src, int H, c
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(int H, const float* __restrict__ res,
                                                       const T* __restrict__ gamma, float eps,
-                                                      T* __restrict__ out) {
+                                                      int split, T* __restrict__ out) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float* x = res + (size_t)r * H;
@@ -179,15 +174,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(int H, const float* __rest
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / H + eps);
   for (int i = threadIdx.x; i < H; i += blockDim.x)
-    out[(size_t)r * H + i] = from_f32<T>(x[i] * inv * ld(gamma + i));
+    store_act<T>(out, H, r, gridDim.x, split, i, x[i] * inv * ld(gamma + i));
 }
 
 void launch_rmsnorm(bool bf16m, int R, int H, const float* res, const void* gamma, float eps,
-                    void* out, cudaStream_t s) {
+                    int split, void* out, cudaStream_t s) {
   if (bf16m)
-    rmsnorm_kernel<bf16><<<R, 256, 0, s>>>(H, res, (const bf16*)gamma, eps, (bf16*)out);
+    rmsnorm_kernel<bf16><<<R, 256, 0, s>>>(H, res, (const bf16*)gamma, eps, split, (bf16*)out);
   else
-    rmsnorm_kernel<float><<<R, 256, 0, s>>>(H, res, (const float*)gamma, eps, (float*)out);
+    rmsnorm_kernel<float><<<R, 256, 0, s>>>(H, res, (const float*)gamma, eps, 0, (float*)out);
 }
 
 // =====================================================================================
@@ -219,11 +214,11 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
   float* vs = ks + 32 * (HD + 1);         // [32][HD]
   __shared__ int s_last;
 
-  const T* qg = (const T*)a.q;
+  const float* qg = (const float*)a.q;
   for (int idx = threadIdx.x; idx < rows * HD; idx += blockDim.x) {
     int rr = idx / HD, d = idx - rr * HD;
     int j = rr / G, h = g * G + (rr - j * G);
-    qs[idx] = ld(qg + ((size_t)(b * a.K + j) * a.nq + h) * HD + d) * a.scale;
+    qs[idx] = qg[((size_t)(b * a.K + j) * a.nq + h) * HD + d] * a.scale;
   }
   const size_t head_off = ((size_t)b * a.nkv + g) * a.cap * HD;
   const T* kc = (const T*)a.kc + head_off;
@@ -327,7 +322,8 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
     const float inv = 1.f / Ls;
 #pragma unroll
     for (int e = 0; e < E; ++e)
-      st(og + ((size_t)(b * a.K + j) * a.nq + h) * HD + lane + 32 * e, acc[e] * inv);
+      store_act<T>(og, (size_t)a.nq * HD, b * a.K + j, a.B * a.K, a.split, h * HD + lane + 32 * e,
+                   acc[e] * inv);
   }
   if (threadIdx.x == 0) a.counters[b * a.nkv + g] = 0u;
 }
@@ -371,12 +367,12 @@ __global__ void __launch_bounds__(256) masked_attn_kernel(MaskedAttnArgs a) {
   const int p = a.row_p[i], d = a.row_d[i];
   const int anchor = p - d + 1;
   if (p < 0 || p >= a.n || d < 1 || d > a.Kmax || anchor < 0) {
-    T* og = (T*)a.o + ((size_t)i * a.nq + h) * HD;
-    for (int t = lane; t < HD; t += 32) st(og + t, 0.f);
+    for (int t = lane; t < HD; t += 32)
+      store_act<T>((T*)a.o, (size_t)a.nq * HD, i, a.M, a.split, h * HD + t, 0.f);
     return;  // outside the contract (reported as BAD_ROW by the row check)
   }
-  const T* q = (const T*)a.q + ((size_t)i * a.nq + h) * HD;
-  for (int t = lane; t < HD; t += 32) qs[warp][t] = ld(q + t) * a.scale;
+  const float* q = (const float*)a.q + ((size_t)i * a.nq + h) * HD;
+  for (int t = lane; t < HD; t += 32) qs[warp][t] = q[t] * a.scale;
   __syncwarp();
   const int n_base = (anchor >= 0) ? anchor + 1 : 0;
   const int n_keys = n_base + max(d - 1, 0);
@@ -432,10 +428,10 @@ __global__ void __launch_bounds__(256) masked_attn_kernel(MaskedAttnArgs a) {
     }
     m = m_new;
   }
-  T* og = (T*)a.o + ((size_t)i * a.nq + h) * HD;
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) st(og + lane + 32 * e, o[e] * inv);
+  for (int e = 0; e < E; ++e)
+    store_act<T>((T*)a.o, (size_t)a.nq * HD, i, a.M, a.split, h * HD + lane + 32 * e, o[e] * inv);
 }
 
 void launch_masked_attention(bool bf16m, const MaskedAttnArgs& a, cudaStream_t s) {
@@ -533,11 +529,12 @@ template <typename T>
 __global__ void __launch_bounds__(256) append_kv_kernel(int N, int nkv, int hd, int cap,
                                                         int batch_slots, T* kc, T* vc,
                                                         int* seq_lens, const int* n_commit,
-                                                        const T* k_rows, const T* v_rows,
-                                                        int n_max, int B, unsigned* err) {
+                                                        int n_extra, const T* k_rows,
+                                                        const T* v_rows, int n_max, int B,
+                                                        unsigned* err) {
   const int b = blockIdx.x;
   const int L = seq_lens[b];
-  const int n = n_commit[b];
+  const int n = n_commit[b] + n_extra;
   if (n < 0 || n > n_max) {
     if (threadIdx.x == 0) raise_error(err, PEAGLE_DEV_BAD_COMMIT);
     return;
@@ -566,15 +563,15 @@ __global__ void __launch_bounds__(256) append_kv_kernel(int N, int nkv, int hd, 
 }
 
 void launch_append_kv(bool bf16m, int B, int N, int nkv, int hd, int cap, void* kc, void* vc,
-                      int* seq_lens, const int* n_commit, const void* k_rows,
+                      int* seq_lens, const int* n_commit, int n_extra, const void* k_rows,
                       const void* v_rows, int n_max, int batch_slots, unsigned* err,
                       cudaStream_t s) {
   if (bf16m)
     append_kv_kernel<bf16><<<B, 256, 0, s>>>(N, nkv, hd, cap, batch_slots, (bf16*)kc, (bf16*)vc,
-        seq_lens, n_commit, (const bf16*)k_rows, (const bf16*)v_rows, n_max, B, err);
+        seq_lens, n_commit, n_extra, (const bf16*)k_rows, (const bf16*)v_rows, n_max, B, err);
   else
     append_kv_kernel<float><<<B, 256, 0, s>>>(N, nkv, hd, cap, batch_slots, (float*)kc, (float*)vc,
-        seq_lens, n_commit, (const float*)k_rows, (const float*)v_rows, n_max, B, err);
+        seq_lens, n_commit, n_extra, (const float*)k_rows, (const float*)v_rows, n_max, B, err);
 }
 
 }  // namespace peagle

@@ -10,11 +10,12 @@
 namespace peagle {
 
 struct AttnArgs {
-  const void* q;          // [R, nq*hd]
+  const void* q;          // [R, nq*hd] fp32 (post-RoPE)
   const void* kc;         // layer cache base [B][nkv][cap][hd]
   const void* vc;
   const int* seq_lens;    // [B]
-  void* o;                // [R, nq*hd]
+  void* o;                // [R, nq*hd] (hi rows, then lo rows when split)
+  int split;
   float* part;            // split-KV partials
   unsigned* counters;     // [B * nkv], zero between launches
   int B, K, nq, nkv, hd, cap, chunk, nchunk;
@@ -23,7 +24,7 @@ struct AttnArgs {
 };
 
 struct MaskedAttnArgs {
-  const void* q;          // [M, nq*hd]
+  const void* q;          // [M, nq*hd] fp32 (post-RoPE)
   const void* k;          // [M, nkv, hd]   all rows
   const void* v;
   const void* k1;         // [n, nkv, hd]   depth-1 rows by position
@@ -31,7 +32,8 @@ struct MaskedAttnArgs {
   const int* row_p;       // [M]
   const int* row_d;       // [M]
   const int* row_index;   // [n * (Kmax + 1)] row of (p, d), -1 if absent
-  void* o;                // [M, nq*hd]
+  void* o;                // [M, nq*hd] (hi rows, then lo rows when split)
+  int split;
   int M, n, Kmax, nq, nkv, hd;
   float scale;
 };
@@ -44,11 +46,11 @@ void launch_input_fusion(bool bf16, int mode, int R, int K, int n_src, int H, co
                          int Vt,
                          const void* emb_mask, const float* F, const float* f_shared,
                          const int* tokens, const int* row_p, const int* row_d,
-                         const void* g_in, const void* g_hid, float eps, void* X0, float* res,
-                         unsigned long long* keys, unsigned* err, cudaStream_t s);
+                         const void* g_in, const void* g_hid, float eps, int split, void* X0,
+                         float* res, unsigned long long* keys, unsigned* err, cudaStream_t s);
 
 void launch_rmsnorm(bool bf16, int R, int H, const float* res, const void* gamma, float eps,
-                    void* out, cudaStream_t s);
+                    int split, void* out, cudaStream_t s);
 
 void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);
 
@@ -61,7 +63,7 @@ void launch_verify(int B, int K, const int* draft, const int* tgt, int* acc, int
                    cudaStream_t s);
 
 void launch_append_kv(bool bf16, int B, int N, int nkv, int hd, int cap, void* kc, void* vc,
-                      int* seq_lens, const int* n_commit, const void* k_rows,
+                      int* seq_lens, const int* n_commit, int n_extra, const void* k_rows,
                       const void* v_rows, int n_max, int batch_slots, unsigned* err,
                       cudaStream_t s);
 

@@ -27,12 +27,12 @@ struct peagle_ctx {
   float2* rope;
   float* f_shared;  // fc(h_shared) [H]
   // workspaces
-  int rows_max;     // max(max_batch * max_K, max_rows)
+  int rows_max;     // activation operand rows: 2 * max(max_batch * max_K, max_rows)
   float* F;         // [max(max_batch, max_seq), H]
   void* X0;         // [rows_max, 2H]
   float* res;       // [rows_max, H]
   void* Xn;         // [rows_max, H]
-  void* Q;          // [rows_max, nq*hd]
+  float* Qf;        // [max(max_batch*max_K, max_rows), nq*hd] fp32 post-RoPE queries
   void* O;          // [rows_max, nq*hd]
   void* act;        // [rows_max, I]
   float* Y;         // fp32 GEMM output (FFMA path) [rows_max, max_out]
@@ -48,7 +48,36 @@ struct peagle_ctx {
   unsigned last_err_bits;
   TcGemmPlan* tc;   // tensor-core GEMM state (bf16 only)
   std::vector<void*> allocs;
+  // optional per-stage timing: CUDA events recorded around each launch on its stream
+  bool timing;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> ev_stage;
+  size_t ev_used;
+  int pending_stage;
 };
+
+// ---- per-stage timing ------------------------------------------------------------------
+static void t_begin(peagle_ctx* c, int stage, cudaStream_t s) {
+  if (!c->timing || c->ev_used + 2 > c->ev.size()) {
+    c->pending_stage = -1;
+    return;
+  }
+  cudaEventRecord(c->ev[c->ev_used], s);
+  c->ev_stage[c->ev_used / 2] = stage;
+  c->pending_stage = stage;
+}
+static void t_end(peagle_ctx* c, cudaStream_t s) {
+  if (c->pending_stage < 0) return;
+  cudaEventRecord(c->ev[c->ev_used + 1], s);
+  c->ev_used += 2;
+  c->pending_stage = -1;
+}
+#define TIMED(stage, call)      \
+  do {                          \
+    t_begin(c, (stage), s);     \
+    call;                       \
+    t_end(c, s);                \
+  } while (0)
 
 static int cuda_fail(cudaError_t e, const char* what) {
   if (e != cudaSuccess) {
@@ -83,6 +112,7 @@ static int copy_in(peagle_ctx* c, void** dst, const void* src, size_t bytes) {
 static void free_ctx(peagle_ctx* c) {
   if (!c) return;
   cudaDeviceSynchronize();
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->tc) tc_destroy(c->tc);
   delete c;
@@ -107,13 +137,24 @@ static int validate_dims(const peagle_dims* d) {
 }
 
 // ---- GEMM dispatch: tensor cores for bf16, FFMA for fp32 --------------------------------
-static void gemm(peagle_ctx* c, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
-                 const EpiArgs& epi, cudaStream_t s) {
-  if (c->bf && c->tc)
-    tc_gemm(c->tc, W, X, ldx, Nout, Kd, R, epi, s);
-  else
-    launch_gemm_simt(c->bf, W, X, ldx, c->Y, c->ldY, Nout, Kd, R, epi, s);
+static int gemm(peagle_ctx* c, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
+                const EpiArgs& epi, cudaStream_t s) {
+  if (c->bf) return tc_gemm(c->tc, W, X, ldx, Nout, Kd, R, epi, s);
+  launch_gemm_simt(false, W, X, ldx, c->Y, c->ldY, Nout, Kd, R, epi, s);
+  return PEAGLE_OK;
 }
+#define GEMM(stage, ...)              \
+  do {                                \
+    t_begin(c, (stage), s);           \
+    int _g = gemm(__VA_ARGS__);       \
+    t_end(c, s);                      \
+    if (_g != PEAGLE_OK) return _g;   \
+  } while (0)
+
+// The bf16 path carries every projection input as a bf16 hi + lo pair (2R operand rows):
+// the weights are streamed once either way, and rounding then happens only where a value
+// is stored in the bf16 KV cache.
+static int use_split(const peagle_ctx* c) { return c->bf ? 1 : 0; }
 
 static EpiArgs epi_base(peagle_ctx* c, int kind, int R, int Nout) {
   EpiArgs e;
@@ -153,6 +194,9 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   c->es = c->bf ? 2 : 4;
   c->tc = nullptr;
   c->last_err_bits = 0;
+  c->timing = false;
+  c->ev_used = 0;
+  c->pending_stage = -1;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     delete c;
@@ -215,8 +259,8 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     TRY(copy_in(c, (void**)&c->rope, tab.data(), tab.size() * sizeof(float2)));
   }
   // workspaces
-  c->rows_max = d.max_batch * d.max_K;
-  if (d.max_rows > c->rows_max) c->rows_max = d.max_rows;
+  const int logical_rows = d.max_batch * d.max_K > d.max_rows ? d.max_batch * d.max_K : d.max_rows;
+  c->rows_max = 2 * logical_rows;
   const int R = c->rows_max;
   const int fr = d.max_batch > d.max_seq ? d.max_batch : d.max_seq;
   TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 4));
@@ -224,7 +268,7 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   TRY(dalloc(c, &c->X0, (size_t)R * 2 * H * es));
   TRY(dalloc(c, (void**)&c->res, (size_t)R * H * 4));
   TRY(dalloc(c, &c->Xn, (size_t)R * H * es));
-  TRY(dalloc(c, &c->Q, (size_t)R * nq * hd * es));
+  TRY(dalloc(c, (void**)&c->Qf, (size_t)logical_rows * nq * hd * 4));
   TRY(dalloc(c, &c->O, (size_t)R * nq * hd * es));
   TRY(dalloc(c, &c->act, (size_t)R * I * es));
   TRY(dalloc(c, (void**)&c->keys, (size_t)R * 8));
@@ -249,24 +293,14 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     TRY(dalloc(c, &c->V1, (size_t)d.max_seq * nkv * hd * es));
     TRY(dalloc(c, (void**)&c->row_index, (size_t)d.max_seq * 17 * 4));
   }
-  if (c->bf) {
-    int rr = tc_create(&c->tc, c->num_sms, R, max_out > 3 * H ? max_out : 3 * H);
-    if (rr) {
-      free_ctx(c);
-      return rr;
-    }
-  }
-  if (c->bf && !c->tc) {
-    // the bf16 path runs its projections on the FFMA GEMM until tensor-core tiles exist
-    TRY(dalloc(c, (void**)&c->Y, (size_t)R * c->ldY * 4));
-  }
+  if (c->bf) TRY(tc_create(&c->tc, c->num_sms, R, max_out > 3 * H ? max_out : 3 * H, c->err));
   // fc(h_shared): constant for every MTP row, computed once with the pass's own GEMM
   {
     EpiArgs e = epi_base(c, EPI_STORE, 1, H);
     e.out_f32 = c->f_shared;
     e.out_ld = H;
-    gemm(c, c->fc, c->h_shared, 3 * H, H, 3 * H, 1, e, 0);
-    if (cudaDeviceSynchronize() != cudaSuccess) {
+    int g = gemm(c, c->fc, c->h_shared, 3 * H, H, 3 * H, 1, e, 0);
+    if (g != PEAGLE_OK || cudaDeviceSynchronize() != cudaSuccess) {
       free_ctx(c);
       return PEAGLE_ERR_CUDA;
     }
@@ -304,6 +338,7 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
   const int qkv_out = (nq + 2 * nkv) * hd;
   const int R = batch * K;
+  const int split = use_split(c);
   const size_t es = c->es;
   const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
 
@@ -312,37 +347,42 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
     EpiArgs e = epi_base(c, EPI_STORE, batch, H);
     e.out_f32 = c->F;
     e.out_ld = H;
-    gemm(c, c->fc, target_hidden, 3 * H, H, 3 * H, batch, e, s);
+    GEMM(PEAGLE_STAGE_FC, c, c->fc, target_hidden, 3 * H, H, 3 * H, batch, e, s);
   }
-  launch_input_fusion(c->bf, 0, R, K, batch, H, c->embed, d.target_vocab, c->emb_mask, c->F,
-                      c->f_shared, new_token, nullptr, nullptr, c->input_norm, c->hidden_norm,
-                      d.rms_eps, c->X0, c->res, c->keys, c->err, s);
+  TIMED(PEAGLE_STAGE_NORM,
+        launch_input_fusion(c->bf, 0, R, K, batch, H, c->embed, d.target_vocab, c->emb_mask,
+                            c->F, c->f_shared, new_token, nullptr, nullptr, c->input_norm,
+                            c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, c->err, s));
   int chunk, nchunk;
   attention_plan(c, batch, kv->capacity, &chunk, &nchunk);
   for (int l = 0; l < d.n_layers; ++l) {
     const void* a_in = c->X0;
     int din = 2 * H;
     if (l > 0) {
-      launch_rmsnorm(c->bf, R, H, c->res, c->attn_norm[l], d.rms_eps, c->Xn, s);
+      TIMED(PEAGLE_STAGE_NORM,
+            launch_rmsnorm(c->bf, R, H, c->res, c->attn_norm[l], d.rms_eps, split, c->Xn, s));
       a_in = c->Xn;
       din = H;
     }
     // S2: QKV projection + RoPE; k/v of row j go to cache slot seq_lens[b] + j
     {
       EpiArgs e = epi_base(c, EPI_QKV_ROPE, R, qkv_out);
-      e.q_out = c->Q;
+      e.in_split = split;
+      e.q_out = c->Qf;
+      e.q_f32 = 1;
       e.k_dst = (char*)kv->k + l * layer_stride;
       e.v_dst = (char*)kv->v + l * layer_stride;
       e.seq_lens = seq_lens;
       e.decode = 1;
       e.K = K;
       e.cap = kv->capacity;
-      gemm(c, c->qkv[l], a_in, din, qkv_out, din, R, e, s);
+      GEMM(PEAGLE_STAGE_QKV, c, c->qkv[l], a_in, din, qkv_out, din, R, e, s);
     }
     // S3: split-KV attention over the cache + causal draft block
     {
       AttnArgs a;
-      a.q = c->Q;
+      a.q = c->Qf;
+      a.split = split;
       a.kc = (char*)kv->k + l * layer_stride;
       a.vc = (char*)kv->v + l * layer_stride;
       a.seq_lens = seq_lens;
@@ -359,36 +399,43 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       a.nchunk = nchunk;
       a.scale = 1.f / sqrtf((float)hd);
       a.err = c->err;
-      launch_attention_decode(c->bf, a, s);
+      TIMED(PEAGLE_STAGE_ATTN, launch_attention_decode(c->bf, a, s));
     }
     // S4: o-proj + residual
     {
       EpiArgs e = epi_base(c, EPI_RESID, R, H);
+      e.in_split = split;
       e.resid = c->res;
-      gemm(c, c->o[l], c->O, nq * hd, H, nq * hd, R, e, s);
+      GEMM(PEAGLE_STAGE_OPROJ, c, c->o[l], c->O, nq * hd, H, nq * hd, R, e, s);
     }
     // S5: SwiGLU MLP
-    launch_rmsnorm(c->bf, R, H, c->res, c->post_norm[l], d.rms_eps, c->Xn, s);
+    TIMED(PEAGLE_STAGE_NORM,
+          launch_rmsnorm(c->bf, R, H, c->res, c->post_norm[l], d.rms_eps, split, c->Xn, s));
     {
       EpiArgs e = epi_base(c, EPI_SWIGLU, R, 2 * d.intermediate);
+      e.in_split = split;
+      e.out_split = split;
       e.act_out = c->act;
-      gemm(c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, R, e, s);
+      GEMM(PEAGLE_STAGE_GATEUP, c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, R, e, s);
     }
     {
       EpiArgs e = epi_base(c, EPI_RESID, R, H);
+      e.in_split = split;
       e.resid = c->res;
-      gemm(c, c->down[l], c->act, d.intermediate, H, d.intermediate, R, e, s);
+      GEMM(PEAGLE_STAGE_DOWN, c, c->down[l], c->act, d.intermediate, H, d.intermediate, R, e, s);
     }
   }
   // S6: final norm, LM head with fused argmax, d2t remap
-  launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, c->Xn, s);
+  TIMED(PEAGLE_STAGE_NORM,
+        launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, split, c->Xn, s));
   {
     EpiArgs e = epi_base(c, EPI_LMHEAD, R, d.draft_vocab);
+    e.in_split = split;
     e.logits = out_logits;
     e.keys = c->keys;
-    gemm(c, c->lm_head, c->Xn, H, d.draft_vocab, H, R, e, s);
+    GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_head, c->Xn, H, d.draft_vocab, H, R, e, s);
   }
-  launch_argmax_decode(R, c->keys, c->d2t, out_draft_tokens, s);
+  TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, out_draft_tokens, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_draft launch");
 }
@@ -406,16 +453,21 @@ extern "C" int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* dra
 }
 
 extern "C" int peagle_append_kv(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
-                                int32_t* seq_lens, const int32_t* n_commit, const void* k_rows,
-                                const void* v_rows, int32_t n_max, void* stream) {
+                                int32_t* seq_lens, const int32_t* n_commit, int32_t n_extra,
+                                const void* k_rows, const void* v_rows, int32_t n_max,
+                                void* stream) {
   if (!c || !kv || !kv->k || !kv->v || !seq_lens || !n_commit) return PEAGLE_ERR_INVALID;
   if (batch < 1 || n_max < 0 || (k_rows == nullptr) != (v_rows == nullptr))
     return PEAGLE_ERR_INVALID;
   if (batch > kv->batch) return PEAGLE_ERR_CAPACITY;
   const peagle_dims& d = c->d;
-  launch_append_kv(c->bf, batch, d.n_layers, d.n_kv_heads, d.head_dim, kv->capacity, kv->k,
-                   kv->v, seq_lens, n_commit, k_rows, v_rows, n_max, kv->batch, c->err,
-                   (cudaStream_t)stream);
+  // in-place commits are bounded by the draft block (max_K rows); copies by n_max
+  const int bound = k_rows ? n_max : d.max_K;
+  cudaStream_t s = (cudaStream_t)stream;
+  TIMED(PEAGLE_STAGE_SMALL,
+        launch_append_kv(c->bf, batch, d.n_layers, d.n_kv_heads, d.head_dim, kv->capacity,
+                         kv->k, kv->v, seq_lens, n_commit, n_extra, k_rows, v_rows, bound,
+                         kv->batch, c->err, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_append_kv launch");
 }
@@ -433,27 +485,33 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
   const int qkv_out = (nq + 2 * nkv) * hd;
   const int Kmax = 16;
-  launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s);
+  const int split = use_split(c);
+  TIMED(PEAGLE_STAGE_SMALL,
+        launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s));
   {
     EpiArgs e = epi_base(c, EPI_STORE, n, H);
     e.out_f32 = c->F;
     e.out_ld = H;
-    gemm(c, c->fc, hidden, 3 * H, H, 3 * H, n, e, s);
+    GEMM(PEAGLE_STAGE_FC, c, c->fc, hidden, 3 * H, H, 3 * H, n, e, s);
   }
-  launch_input_fusion(c->bf, 1, M, K, n, H, c->embed, d.target_vocab, c->emb_mask, c->F,
-                      c->f_shared, tokens, row_p, row_d, c->input_norm, c->hidden_norm,
-                      d.rms_eps, c->X0, c->res, c->keys, c->err, s);
+  TIMED(PEAGLE_STAGE_NORM,
+        launch_input_fusion(c->bf, 1, M, K, n, H, c->embed, d.target_vocab, c->emb_mask, c->F,
+                            c->f_shared, tokens, row_p, row_d, c->input_norm, c->hidden_norm,
+                            d.rms_eps, split, c->X0, c->res, c->keys, c->err, s));
   for (int l = 0; l < d.n_layers; ++l) {
     const void* a_in = c->X0;
     int din = 2 * H;
     if (l > 0) {
-      launch_rmsnorm(c->bf, M, H, c->res, c->attn_norm[l], d.rms_eps, c->Xn, s);
+      TIMED(PEAGLE_STAGE_NORM,
+            launch_rmsnorm(c->bf, M, H, c->res, c->attn_norm[l], d.rms_eps, split, c->Xn, s));
       a_in = c->Xn;
       din = H;
     }
     {
       EpiArgs e = epi_base(c, EPI_QKV_ROPE, M, qkv_out);
-      e.q_out = c->Q;
+      e.in_split = split;
+      e.q_out = c->Qf;
+      e.q_f32 = 1;
       e.k_dst = c->Kr;
       e.v_dst = c->Vr;
       e.k1_dst = c->K1;
@@ -462,11 +520,12 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       e.row_depth = row_d;
       e.n_seq = n;
       e.decode = 0;
-      gemm(c, c->qkv[l], a_in, din, qkv_out, din, M, e, s);
+      GEMM(PEAGLE_STAGE_QKV, c, c->qkv[l], a_in, din, qkv_out, din, M, e, s);
     }
     {
       MaskedAttnArgs a;
-      a.q = c->Q;
+      a.q = c->Qf;
+      a.split = split;
       a.k = c->Kr;
       a.v = c->Vr;
       a.k1 = c->K1;
@@ -482,33 +541,40 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       a.nkv = nkv;
       a.hd = hd;
       a.scale = 1.f / sqrtf((float)hd);
-      launch_masked_attention(c->bf, a, s);
+      TIMED(PEAGLE_STAGE_ATTN, launch_masked_attention(c->bf, a, s));
     }
     {
       EpiArgs e = epi_base(c, EPI_RESID, M, H);
+      e.in_split = split;
       e.resid = c->res;
-      gemm(c, c->o[l], c->O, nq * hd, H, nq * hd, M, e, s);
+      GEMM(PEAGLE_STAGE_OPROJ, c, c->o[l], c->O, nq * hd, H, nq * hd, M, e, s);
     }
-    launch_rmsnorm(c->bf, M, H, c->res, c->post_norm[l], d.rms_eps, c->Xn, s);
+    TIMED(PEAGLE_STAGE_NORM,
+          launch_rmsnorm(c->bf, M, H, c->res, c->post_norm[l], d.rms_eps, split, c->Xn, s));
     {
       EpiArgs e = epi_base(c, EPI_SWIGLU, M, 2 * d.intermediate);
+      e.in_split = split;
+      e.out_split = split;
       e.act_out = c->act;
-      gemm(c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, M, e, s);
+      GEMM(PEAGLE_STAGE_GATEUP, c, c->gate_up[l], c->Xn, H, 2 * d.intermediate, H, M, e, s);
     }
     {
       EpiArgs e = epi_base(c, EPI_RESID, M, H);
+      e.in_split = split;
       e.resid = c->res;
-      gemm(c, c->down[l], c->act, d.intermediate, H, d.intermediate, M, e, s);
+      GEMM(PEAGLE_STAGE_DOWN, c, c->down[l], c->act, d.intermediate, H, d.intermediate, M, e, s);
     }
   }
-  launch_rmsnorm(c->bf, M, H, c->res, c->final_norm, d.rms_eps, c->Xn, s);
+  TIMED(PEAGLE_STAGE_NORM,
+        launch_rmsnorm(c->bf, M, H, c->res, c->final_norm, d.rms_eps, split, c->Xn, s));
   {
     EpiArgs e = epi_base(c, EPI_LMHEAD, M, d.draft_vocab);
+    e.in_split = split;
     e.logits = out_logits;
     e.keys = c->keys;
-    gemm(c, c->lm_head, c->Xn, H, d.draft_vocab, H, M, e, s);
+    GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_head, c->Xn, H, d.draft_vocab, H, M, e, s);
   }
-  launch_argmax_decode(M, c->keys, nullptr, out_argmax, s);
+  TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(M, c->keys, nullptr, out_argmax, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_forward_parallel launch");
 }
@@ -553,6 +619,38 @@ extern "C" int peagle_status(peagle_ctx* c) {
     cudaMemset(c->err, 0, 4);
     return PEAGLE_ERR_DEVICE;
   }
+  return PEAGLE_OK;
+}
+
+extern "C" int peagle_set_timing(peagle_ctx* c, int32_t enable) {
+  if (!c) return PEAGLE_ERR_INVALID;
+  if (enable && c->ev.empty()) {
+    c->ev.resize(1024);
+    c->ev_stage.assign(512, 0);
+    for (auto& e : c->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return PEAGLE_ERR_CUDA;
+  }
+  c->timing = enable != 0;
+  c->ev_used = 0;
+  return PEAGLE_OK;
+}
+
+extern "C" int peagle_read_timing(peagle_ctx* c, float* stage_ms, int32_t* stage_launches) {
+  if (!c || !stage_ms || !stage_launches) return PEAGLE_ERR_INVALID;
+  for (int i = 0; i < PEAGLE_NUM_STAGES; ++i) {
+    stage_ms[i] = 0.f;
+    stage_launches[i] = 0;
+  }
+  for (size_t k = 0; k + 1 < c->ev_used; k += 2) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(c->ev[k + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, c->ev[k], c->ev[k + 1]) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    const int st = c->ev_stage[k / 2];
+    stage_ms[st] += ms;
+    stage_launches[st] += 1;
+  }
+  c->ev_used = 0;
   return PEAGLE_OK;
 }
 

@@ -149,16 +149,18 @@ int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* draft_tokens,
                          int32_t* out_bonus, void* stream);
 
 /* Commit accepted rows to the KV cache and advance seq_lens (device, in place):
- *   n_commit device int32 [batch], each in 0..n_max.
- *   k_rows/v_rows NULL: the first n_commit[b] draft-block rows already sit in slots
- *     seq_lens[b] .. (written by peagle_draft); only seq_lens advances.
+ *   n_commit device int32 [batch]; request b commits n = n_commit[b] + n_extra rows
+ *     (e.g. out_accept_len of peagle_verify_greedy with n_extra = 1: the NTP row and
+ *     the accepted drafts, without a round trip to the host).
+ *   k_rows/v_rows NULL: the first n (0..max_K) draft-block rows already sit in slots
+ *     seq_lens[b] .. (written by peagle_draft); only seq_lens advances, n_max ignored.
  *   otherwise device [n_layers][batch][n_max][n_kv_heads][head_dim] (dims dtype)
- *     rows copied into slots seq_lens[b] + i, i < n_commit[b].
+ *     rows copied into slots seq_lens[b] + i, i < n (0..n_max).
  * Device checks: n_commit range (BAD_COMMIT), capacity (KV_OVERFLOW); a request
  * that fails a check is left unchanged. */
 int peagle_append_kv(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv, int32_t* seq_lens,
-                     const int32_t* n_commit, const void* k_rows, const void* v_rows,
-                     int32_t n_max, void* stream);
+                     const int32_t* n_commit, int32_t n_extra, const void* k_rows,
+                     const void* v_rows, int32_t n_max, void* stream);
 
 /* Training-style parallel-prediction forward ("P-EAGLE: Parallel-Drafting EAGLE with
  * Scalable Training", sections 3.1-3.2; "Speeding LLM inference with P-EAGLE in
@@ -189,6 +191,29 @@ int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double* uniforms,
  * the device error word is non-zero (the word is then cleared), or PEAGLE_ERR_CUDA
  * if a sticky CUDA error is pending. */
 int peagle_status(peagle_ctx* ctx);
+
+/* Per-stage timing (diagnostics).  Stages of the pass: */
+#define PEAGLE_STAGE_FC 0      /* fc projection of the target hidden states       */
+#define PEAGLE_STAGE_QKV 1     /* QKV projection + RoPE + KV write                */
+#define PEAGLE_STAGE_ATTN 2    /* attention (split-KV decode or masked)           */
+#define PEAGLE_STAGE_OPROJ 3   /* o-projection + residual                         */
+#define PEAGLE_STAGE_GATEUP 4  /* gate/up projection + SwiGLU                     */
+#define PEAGLE_STAGE_DOWN 5    /* down projection + residual                      */
+#define PEAGLE_STAGE_LMHEAD 6  /* LM head + argmax                                */
+#define PEAGLE_STAGE_NORM 7    /* input fusion and RMSNorms                       */
+#define PEAGLE_STAGE_SMALL 8   /* argmax decode, KV commit, row table             */
+#define PEAGLE_NUM_STAGES 9
+
+/* Enable (1) or disable (0) timing: while enabled, every kernel launch of peagle_draft,
+ * peagle_append_kv and peagle_forward_parallel is bracketed by CUDA events recorded on
+ * the call's stream (which serialises launches that would otherwise overlap).  The first
+ * enable creates the event pool (up to 512 launches between reads); call it outside
+ * stream capture. */
+int peagle_set_timing(peagle_ctx* ctx, int32_t enable);
+
+/* Wait for the recorded events, write the summed milliseconds and launch counts per
+ * stage (arrays of PEAGLE_NUM_STAGES) since the previous read, and reset them. */
+int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches);
 
 /* Raw device error bits observed by the last peagle_status call. */
 int32_t peagle_device_error_bits(const peagle_ctx* ctx);

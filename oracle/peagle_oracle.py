@@ -24,14 +24,15 @@ Sources (page title, then section):
 Readings where the pages are silent or ambiguous are listed with the design notes;
 the ones this file depends on are repeated at the function that applies them.
 
-Two modes of arithmetic:
-  * exact (``bf16=False``): every value is widened exactly to float64 and the whole
-    pass is evaluated in float64;
-  * cast-emulating (``bf16=True``): values are rounded to the nearest bf16 (ties to
-    even) at the points where the bf16 GPU path stores bf16: the 2H first-layer input,
-    the normalised inputs of every projection, q/k/v after RoPE, the attention output
-    and the SwiGLU product.  Accumulations, the residual stream, norms, RoPE and
-    softmax stay float64 here (fp32 on the GPU).
+Modes of arithmetic (argument ``bf16``):
+  * exact (False): every value is widened exactly to float64 and the whole pass is
+    evaluated in float64;
+  * cast-emulating (a set of point names from CAST_POINTS, or True for all of them):
+    values are rounded to the nearest bf16 (ties to even) at the named storage points
+    (x0: the 2H first-layer input, xn: normalised projection inputs, q, kv: keys and
+    values, o: attention output, act: SwiGLU product, y: LM-head input).  The bf16 GPU
+    path stores bf16 only in the KV cache (DRAFT_BF16_CASTS); the default for bf16 dims.
+    Accumulations, the residual stream, norms, RoPE and softmax stay float64 here.
 
 Parity status of each function (what pins it, besides this file) is tested in
 tests/test_oracle_pins.py.  Logit VALUES of the full pass are not printed anywhere in
@@ -207,6 +208,26 @@ def input_rows(W: Weights64, dims, target_hidden, new_token, K):
     return E, Hin
 
 
+CAST_POINTS = ("x0", "xn", "q", "kv", "o", "act", "y")
+# Rounding profile of the bf16 GPU path (draft pass and training-style forward):
+# activations travel as bf16 hi + lo pairs (about 16 significant bits) and queries in
+# fp32, so the only bf16 rounding left is the one the KV storage format imposes on keys
+# and values.
+DRAFT_BF16_CASTS = frozenset({"kv"})
+# Every storage point rounded to bf16 (a plain all-bf16 pipeline); kept for comparisons.
+ALL_BF16_CASTS = frozenset(CAST_POINTS)
+
+
+def _cast_fn(bf16, point):
+    """Rounding applied at a cast point: bf16 is True (every point), False (none) or a
+    collection of point names from CAST_POINTS."""
+    if bf16 is True:
+        return bf16_round
+    if not bf16:
+        return lambda v: v
+    return bf16_round if point in bf16 else (lambda v: v)
+
+
 def first_layer_input(W: Weights64, dims, E, Hin, bf16):
     """fc projection 3H -> H and the 2H first-layer input.
 
@@ -214,7 +235,7 @@ def first_layer_input(W: Weights64, dims, E, Hin, bf16):
     itself, before any norm (reading of the --no-norm-before-residual flag in
     [RH] "Train your own in 4 steps").  Returns (x0 [R,2H], res [R,H]).
     """
-    cast = bf16_round if bf16 else (lambda v: v)
+    cast = _cast_fn(bf16, "x0")
     f = linear(Hin, W.fc)
     x0 = np.concatenate([rmsnorm(E, W.input_norm, dims.rms_eps),
                          rmsnorm(f, W.hidden_norm, dims.rms_eps)], axis=-1)
@@ -230,7 +251,8 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
     q head h reading kv head h // (nq/nkv), scale 1/sqrt(hd).
     Returns (res_out, k_draft [B,K,nkv,hd], v_draft).
     """
-    cast = bf16_round if bf16 else (lambda v: v)
+    cq, ckv, co = _cast_fn(bf16, "q"), _cast_fn(bf16, "kv"), _cast_fn(bf16, "o")
+    cx, ca = _cast_fn(bf16, "xn"), _cast_fn(bf16, "act")
     nq, nkv, hd = dims.n_q_heads, dims.n_kv_heads, dims.head_dim
     G = nq // nkv
     R = a.shape[0]
@@ -239,9 +261,9 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
     q = qkv[:, : nq * hd].reshape(R, nq, hd)
     k = qkv[:, nq * hd: (nq + nkv) * hd].reshape(R, nkv, hd)
     v = qkv[:, (nq + nkv) * hd:].reshape(R, nkv, hd)
-    q = cast(rope(q, pos[:, None], dims.rope_theta))
-    k = cast(rope(k, pos[:, None], dims.rope_theta))
-    v = cast(v)
+    q = cq(rope(q, pos[:, None], dims.rope_theta))
+    k = ckv(rope(k, pos[:, None], dims.rope_theta))
+    v = ckv(v)
     scale = 1.0 / math.sqrt(hd)
     o = np.empty((R, nq, hd))
     kd = k.reshape(B, K, nkv, hd)
@@ -255,10 +277,10 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
                 n_vis = Lb + j + 1
                 for h in range(g * G, (g + 1) * G):
                     o[b * K + j, h] = attend(q[b * K + j, h], keys[:n_vis], vals[:n_vis], scale)
-    o = cast(o.reshape(R, nq * hd))
+    o = co(o.reshape(R, nq * hd))
     res = res + linear(o, L["o"])
-    u = cast(rmsnorm(res, L["post_norm"], dims.rms_eps))
-    act = cast(silu(linear(u, L["gate"])) * linear(u, L["up"]))
+    u = cx(rmsnorm(res, L["post_norm"], dims.rms_eps))
+    act = ca(silu(linear(u, L["gate"])) * linear(u, L["up"]))
     res = res + linear(act, L["down"])
     return res, kd, vd
 
@@ -269,7 +291,7 @@ def lm_head_argmax(W: Weights64, dims, res, bf16):
     d2t is not on the pages; the reading is an offset table (target = i + d2t[i]).
     Returns (logits [R,Vd], argmax [R], tokens [R], margin [R]).
     """
-    cast = bf16_round if bf16 else (lambda v: v)
+    cast = _cast_fn(bf16, "y")
     y = cast(rmsnorm(res, W.final_norm, dims.rms_eps))
     logits = linear(y, W.lm_head)
     am = np.argmax(logits, axis=-1)  # first occurrence = lowest index on ties
@@ -289,8 +311,8 @@ def draft_pass(W: Weights64, dims, cache_k, cache_v, seq_lens, target_hidden, ne
     decoder layers and the LM head in a single execution; [PE] A2 section 2.)
     """
     if bf16 is None:
-        bf16 = dims.dtype == "bf16"
-    cast = bf16_round if bf16 else (lambda v: v)
+        bf16 = DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    cast = _cast_fn(bf16, "xn")
     seq_lens = np.asarray(seq_lens, np.int64)
     B = len(seq_lens)
     E, Hin = input_rows(W, dims, target_hidden, new_token, K)
@@ -455,8 +477,9 @@ def forward_parallel(W: Weights64, dims, tokens, hidden, rows, bf16=None):
     Returns (logits [M, Vd], argmax [M], margin [M]).
     """
     if bf16 is None:
-        bf16 = dims.dtype == "bf16"
-    cast = bf16_round if bf16 else (lambda v: v)
+        bf16 = DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    cx0, cxn, cq, ckv = (_cast_fn(bf16, k) for k in ("x0", "xn", "q", "kv"))
+    co, cact = _cast_fn(bf16, "o"), _cast_fn(bf16, "act")
     rows = np.asarray(rows, np.int64)
     M = rows.shape[0]
     H = dims.hidden
@@ -480,12 +503,12 @@ def forward_parallel(W: Weights64, dims, tokens, hidden, rows, bf16=None):
         ((P[None, :] - D[None, :]) == (P - D)[:, None]) & (D[None, :] <= D[:, None]))
     scale = 1.0 / math.sqrt(hd)
     for li, L in enumerate(W.layers):
-        a = x0 if li == 0 else cast(rmsnorm(res, L["attn_norm"], dims.rms_eps))
+        a = x0 if li == 0 else cxn(rmsnorm(res, L["attn_norm"], dims.rms_eps))
         qkv = linear(a, L["qkv"])
-        q = cast(rope(qkv[:, : nq * hd].reshape(M, nq, hd), pos[:, None], dims.rope_theta))
-        k = cast(rope(qkv[:, nq * hd: (nq + nkv) * hd].reshape(M, nkv, hd), pos[:, None],
-                      dims.rope_theta))
-        v = cast(qkv[:, (nq + nkv) * hd:].reshape(M, nkv, hd))
+        q = cq(rope(qkv[:, : nq * hd].reshape(M, nq, hd), pos[:, None], dims.rope_theta))
+        k = ckv(rope(qkv[:, nq * hd: (nq + nkv) * hd].reshape(M, nkv, hd), pos[:, None],
+                     dims.rope_theta))
+        v = ckv(qkv[:, (nq + nkv) * hd:].reshape(M, nkv, hd))
         o = np.empty((M, nq, hd))
         for h in range(nq):
             g = h // G
@@ -495,10 +518,10 @@ def forward_parallel(W: Weights64, dims, tokens, hidden, rows, bf16=None):
             pr = np.exp(s)
             pr /= pr.sum(axis=1, keepdims=True)
             o[:, h] = pr @ v[:, g]
-        o = cast(o.reshape(M, nq * hd))
+        o = co(o.reshape(M, nq * hd))
         res = res + linear(o, L["o"])
-        u = cast(rmsnorm(res, L["post_norm"], dims.rms_eps))
-        act = cast(silu(linear(u, L["gate"])) * linear(u, L["up"]))
+        u = cxn(rmsnorm(res, L["post_norm"], dims.rms_eps))
+        act = cact(silu(linear(u, L["gate"])) * linear(u, L["up"]))
         res = res + linear(act, L["down"])
     logits, am, _, margin = lm_head_argmax(W, dims, res, bf16)
     return logits, am, margin

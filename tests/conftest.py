@@ -25,3 +25,17 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the parity errors the GPU tests observed to $PEAGLE_PARITY_LOG (JSON)."""
+    path = os.environ.get("PEAGLE_PARITY_LOG")
+    if not path:
+        return
+    try:
+        from pe_helpers import RECORD
+    except Exception:  # pragma: no cover
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(RECORD, f, indent=1)

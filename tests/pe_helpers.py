@@ -8,6 +8,7 @@ from oracle import peagle_oracle as O
 
 LOGIT_TOL = {"f32": 1e-4, "bf16": 2e-2}
 MARGIN = 1e-2  # draft ids must match the oracle wherever its top-1 margin exceeds this
+RECORD = []  # (case, max abs logit error, tolerance, compared logits, rows with clear margin)
 
 
 def pk():
@@ -50,14 +51,16 @@ def run_draft(ctx, dims, inp, K, d=None, logits=True):
 
 
 def oracle_draft(dims, w, inp, K, idx=None, W=None):
+    """Oracle draft pass with the bf16 path's rounding profile (KV-cache stores only)."""
     W = W or O.Weights64.from_synth(w, lazy=True)
+    casts = O.DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
     if idx is None:
         return O.draft_pass(W, dims, inp["cache_k"], inp["cache_v"], inp["seq_lens"],
-                            inp["target_hidden"], inp["new_token"], K)
+                            inp["target_hidden"], inp["new_token"], K, bf16=casts)
     idx = list(idx)
     return O.draft_pass(W, dims, inp["cache_k"][:, idx], inp["cache_v"][:, idx],
                         np.asarray(inp["seq_lens"])[idx], inp["target_hidden"][idx],
-                        np.asarray(inp["new_token"])[idx], K)
+                        np.asarray(inp["new_token"])[idx], K, bf16=casts)
 
 
 def check_tokens_vs_own_logits(tokens, logits, d2t):
@@ -73,5 +76,7 @@ def compare(dims, ref, tokens, logits, what=""):
     ok = ref.margin > MARGIN
     assert ok.mean() > 0.5, f"{what}: too few rows with a clear margin"
     bad = np.argwhere(ok & (tokens != ref.tokens))
+    RECORD.append({"case": what, "max_abs_err": err, "tol": tol, "logits": int(logits.size),
+                   "id_rows_checked": int(ok.sum()), "id_rows": int(ok.size)})
     assert len(bad) == 0, f"{what}: draft ids differ at {bad[:5].tolist()}"
     return err

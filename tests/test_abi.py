@@ -58,7 +58,8 @@ def test_host_argument_errors(pk):
     assert L.peagle_verify_greedy(1, 4, None, 1, 1, 1, None) == pk.PEAGLE_ERR_INVALID
     kv = pk.PeagleKV(1, 1, 16, 1)
     assert L.peagle_draft(None, 1, ctypes.byref(kv), 1, 1, 1, 4, 1, None, None) == pk.PEAGLE_ERR_INVALID
-    assert L.peagle_append_kv(None, 1, ctypes.byref(kv), 1, 1, None, None, 0, None) == pk.PEAGLE_ERR_INVALID
+    assert L.peagle_append_kv(None, 1, ctypes.byref(kv), 1, 1, 0, None, None, 0, None) == pk.PEAGLE_ERR_INVALID
+    assert L.peagle_set_timing(None, 1) == pk.PEAGLE_ERR_INVALID
     assert L.peagle_forward_parallel(None, 8, 4, 1, 1, 1, 1, 4, 1, None, None) == pk.PEAGLE_ERR_INVALID
     assert L.peagle_status(None) == pk.PEAGLE_ERR_INVALID
     L.peagle_destroy(None)

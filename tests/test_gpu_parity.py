@@ -36,8 +36,8 @@ def _small_case(dims, lens, K, seed, cap=None):
 def tiny():
     wl = synth.WORKLOADS["tiny_f32"]
     w = synth.make_weights(wl.dims, 1234)
-    inp = synth.make_decode_inputs(wl, 99)
-    ctx = make_ctx(wl.dims, w, wl.batch, 16, inp["capacity"] + 16)
+    inp = synth.make_decode_inputs(wl, 99, capacity=int(wl.seq_lens[0]) + 16)
+    ctx = make_ctx(wl.dims, w, wl.batch, 16, inp["capacity"])
     yield wl, w, inp, ctx
     ctx.close()
 
@@ -245,10 +245,11 @@ def test_round_draft_commit_draft():
     bonus = torch.empty(2, dtype=torch.int32, device="cuda")
     m.peagle_verify_greedy(2, K, torch.from_numpy(toks).cuda(), torch.from_numpy(tgt).cuda(), acc,
                            bonus)
-    # commit the NTP row plus the accepted drafts' rows, as written by the draft pass
-    n_commit = torch.clamp(acc + 1, max=K).to(torch.int32)
+    # commit the NTP row plus the accepted drafts' rows (accept_len + 1), as written by
+    # the draft pass; a fully accepted block commits all K rows
+    acc = torch.clamp(acc, max=K - 1).to(torch.int32)
     kv = m.kv_struct(d["ck"], d["cv"], 48, 2)
-    m.peagle_append_kv(ctx, 2, kv, d["sl"], n_commit)
+    m.peagle_append_kv(ctx, 2, kv, d["sl"], acc, n_extra=1)
     assert m.peagle_status(ctx) == m.PEAGLE_OK
     inp2 = dict(inp)
     inp2["cache_k"] = d["ck"].cpu()

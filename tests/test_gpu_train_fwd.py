@@ -6,7 +6,7 @@ import torch
 
 import synth
 from oracle import peagle_oracle as O
-from pe_helpers import LOGIT_TOL, MARGIN, make_ctx, pk
+from pe_helpers import LOGIT_TOL, MARGIN, RECORD, make_ctx, pk
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +34,8 @@ def _compare(dims, ref_logits, ref_am, ref_margin, am, lg, what):
     err = float(np.max(np.abs(lg - ref_logits)))
     assert err <= tol, f"{what}: logits max abs err {err:.3e}"
     ok = ref_margin > MARGIN
+    RECORD.append({"case": what, "max_abs_err": err, "tol": tol, "logits": int(lg.size),
+                   "id_rows_checked": int(ok.sum()), "id_rows": int(ok.size)})
     assert np.array_equal(am[ok], ref_am[ok]), what
     assert np.array_equal(am, np.argmax(lg, axis=-1)), what
     return err
@@ -58,7 +60,8 @@ def test_forward_parallel_small(dims, n, K, r):
     am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
     ctx.close()
     W = O.Weights64.from_synth(w)
-    ref_logits, ref_am, ref_margin = O.forward_parallel(W, dims, tokens, hidden, rows)
+    casts = O.DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    ref_logits, ref_am, ref_margin = O.forward_parallel(W, dims, tokens, hidden, rows, bf16=casts)
     _compare(dims, ref_logits, ref_am, ref_margin, am, lg, f"fwd n={n} K={K}")
 
 
@@ -101,11 +104,13 @@ def test_train_fwd_full_prefix_and_tail():
     ctx.close()
     W = O.Weights64.from_synth(w, lazy=True)
     pre = rows[rows[:, 0] < 96]
-    rl, ra, rm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], pre)
+    rl, ra, rm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], pre,
+                                    bf16=O.DRAFT_BF16_CASTS)
     _compare(dims, rl, ra, rm, am[: len(pre)], lg[: len(pre)], "train_fwd prefix")
     tail = rows[-3:]
     clo = O.dependency_closure(rows, tail)
-    cl, ca, cm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], clo)
+    cl, ca, cm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], clo,
+                                    bf16=O.DRAFT_BF16_CASTS)
     idx = {(int(p), int(d)): i for i, (p, d) in enumerate(clo)}
     sel = [idx[(int(p), int(d))] for p, d in tail]
     _compare(dims, cl[sel], ca[sel], cm[sel], am[-3:], lg[-3:], "train_fwd tail")
