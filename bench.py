@@ -1,0 +1,428 @@
+"""Throughput of the P-EAGLE parallel draft pass on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  draft (fc + input fusion, N decoder layers, LM head + argmax + d2t; peagle_draft),
+  greedy verification (peagle_verify_greedy), KV commit of the NTP row plus the accepted
+  drafts (peagle_append_kv), and a reset of seq_lens so every step drafts from the same
+  committed context.  The metric is draft tokens per second (batch x K per step) for the
+  decode-shaped bf16 drafter: H=2880, 4 layers, 64/8 heads of 64, I=7680, Vd=32000 ->
+  Vt=201088, batch 1, 4096 cached positions, K=8.  The step is captured in a CUDA graph
+  and replayed; each replay streams 1.04 GB (weights + KV), far more than the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode_b1|decode_b2|ragged_b16]
+
+--impl reference times the fp64 oracle on the host cores instead (a deliberately slow
+plain program; see the cpu_baseline object).  Under torchrun each rank runs an
+independent replica on its own GPU (the pass shards by request: no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_b1"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=["decode_b1", "decode_b2", "ragged_b16"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.5)  # let the sampler start before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gemm_weight_bytes(dims) -> int:
+    """Weight bytes one draft pass streams through the projections."""
+    H, I, Vd = dims.hidden, dims.intermediate, dims.draft_vocab
+    qkv = dims.qkv_out
+    p = H * 3 * H + Vd * H
+    for layer in range(dims.n_layers):
+        din = 2 * H if layer == 0 else H
+        p += qkv * din + H * dims.n_q_heads * dims.head_dim + 2 * I * H + H * I
+    return p * 2
+
+
+def kv_bytes(dims, lens, K) -> int:
+    """KV-cache bytes the attention reads per pass (committed context + draft block)."""
+    per_pos = dims.n_layers * dims.n_kv_heads * dims.head_dim * 2 * 2
+    return int(sum(int(L) + K for L in lens)) * per_pos
+
+
+# ---------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import drafting_eagle_draft_gb300 as pk
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    inp = synth.make_decode_inputs(wl, 99)
+    B, K, cap = wl.batch, wl.K, inp["capacity"]
+    R = B * K
+    ctx = pk.peagle_create(w, pk.make_dims(dims, B, K, cap))
+    del w
+    ck = inp["cache_k"].to(dev)
+    cv = inp["cache_v"].to(dev)
+    kv = pk.kv_struct(ck, cv, cap, B)
+    sl0 = torch.from_numpy(inp["seq_lens"]).to(dev)
+    sl = sl0.clone()
+    th = inp["target_hidden"].to(dev)
+    nt = torch.from_numpy(inp["new_token"]).to(dev)
+    toks = torch.zeros(B, K, dtype=torch.int32, device=dev)
+    acc = torch.zeros(B, dtype=torch.int32, device=dev)
+    bonus = torch.zeros(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # target argmax agreeing with the drafts on a geometric(0.7) prefix
+    with torch.cuda.stream(stream):
+        pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
+    stream.synchronize()
+    tgt_np, _ = synth.geometric_target_argmax(toks.cpu().numpy(), dims.target_vocab, 0.7, 6)
+    tgt = torch.from_numpy(tgt_np).to(dev)
+
+    def step():
+        sl.copy_(sl0)
+        pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
+        pk.peagle_verify_greedy(B, K, toks, tgt, acc, bonus, stream)
+        pk.peagle_append_kv(ctx, B, kv, sl, acc, stream=stream, n_extra=1)
+
+    # warm-up (eager), then capture one step in a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms_step = ms / args.steps
+    assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+
+    # per-stage CUDA-event timing of the same step (launches serialised by the events)
+    pk.peagle_set_timing(ctx, True)
+    stage_ms = {k: 0.0 for k in pk.STAGES}
+    stage_n = {k: 0 for k in pk.STAGES}
+    reps = 5
+    with torch.cuda.stream(stream):
+        step()
+        pk.peagle_read_timing(ctx)
+        for _ in range(reps):
+            step()
+            t = pk.peagle_read_timing(ctx)
+            for k, (m_, n_) in t.items():
+                stage_ms[k] += m_ / reps
+                stage_n[k] = n_
+    pk.peagle_set_timing(ctx, False)
+    launches_per_step = sum(stage_n.values()) + 1  # + verify (context-free)
+
+    # end to end through the public API with host buffers (pinned), copies in the region
+    th_h = inp["target_hidden"].pin_memory()
+    nt_h = torch.from_numpy(inp["new_token"]).pin_memory()
+    sl_h = torch.from_numpy(inp["seq_lens"]).pin_memory()
+    toks_h = torch.empty(B, K, dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    bonus_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = th_h.numel() * th_h.element_size() + nt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = toks_h.numel() * 4 + acc_h.numel() * 4 + bonus_h.numel() * 4
+
+    def e2e_step():
+        th.copy_(th_h, non_blocking=True)
+        nt.copy_(nt_h, non_blocking=True)
+        sl.copy_(sl_h, non_blocking=True)
+        pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
+        pk.peagle_verify_greedy(B, K, toks, tgt, acc, bonus, stream)
+        pk.peagle_append_kv(ctx, B, kv, sl, acc, stream=stream, n_extra=1)
+        toks_h.copy_(toks, non_blocking=True)
+        acc_h.copy_(acc, non_blocking=True)
+        bonus_h.copy_(bonus, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        t1 = time.perf_counter()
+    e2e_ms = (t1 - t0) * 1e3 / args.e2e_steps
+
+    # roofline of the dominant kernel: the tensor-core projection GEMM (all its launches)
+    gemm_stages = ("fc", "qkv", "oproj", "gate_up", "down", "lm_head")
+    gemm_ms = sum(stage_ms[k] for k in gemm_stages)
+    gemm_launches = sum(stage_n[k] for k in gemm_stages)
+    wbytes = gemm_weight_bytes(dims)
+    pk_ = peaks()
+    achieved = wbytes / (gemm_ms * 1e-3) / 1e9
+    lens = inp["seq_lens"]
+    total_bytes = wbytes + kv_bytes(dims, lens, K)
+    roofline_us = total_bytes / (pk_["hbm_gbs"] * 1e9) * 1e6
+
+    # whole job: tokens of all ranks / max time over ranks
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    else:
+        ms_max = ms_step
+    total_tok_s = world * R / (ms_max * 1e-3)
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(wl, inp, budget_s=12.0)
+        out = {
+            "metric": "draft tokens/s", "value": round(total_tok_s, 2), "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 5), "us_per_pass": round(ms_max * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": wl.name, "batch": B, "K": K, "kv_len": [int(x) for x in lens],
+                       "hidden": dims.hidden, "layers": dims.n_layers,
+                       "heads": [dims.n_q_heads, dims.n_kv_heads, dims.head_dim],
+                       "intermediate": dims.intermediate,
+                       "vocab": [dims.draft_vocab, dims.target_vocab],
+                       "l2": "inputs larger than L2: %.2f GB streamed per step vs 129 MB L2"
+                             % (total_bytes / 1e9),
+                       "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
+            "roofline": {"bound": "hbm", "kernel": "tc_gemm_kernel (all projection launches)",
+                         "achieved": round(achieved, 1), "peak": pk_["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk_["hbm_gbs"], 4), "traffic": None,
+                         "bytes_per_step": wbytes, "launches_per_step": gemm_launches,
+                         "kernel_ms_per_step": round(gemm_ms, 4),
+                         "peak_source": pk_["source"],
+                         "pass_roofline_us": round(roofline_us, 2),
+                         "pass_frac": round(roofline_us / (ms_max * 1e3), 4)},
+            "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "e2e": {"value": round(R / (e2e_ms * 1e-3), 2), "unit": "tok/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches_per_step * args.steps),
+            "clocks": clk,
+        }
+        if cpu:
+            out["cpu_baseline"] = cpu
+    ctx.close()
+    return out
+
+
+# ---------------------------------------------------------------------------- oracle arm
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """The fp64 oracle (as it stands) on the host cores: full draft passes of the same
+    workload until about budget_s seconds of work have run."""
+    from oracle import peagle_oracle as O
+
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    W = O.Weights64.from_synth(w, lazy=True)
+    K = wl.K
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        O.draft_pass(W, dims, inp["cache_k"], inp["cache_v"], inp["seq_lens"],
+                     inp["target_hidden"], inp["new_token"], K, bf16=O.DRAFT_BF16_CASTS)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(wl.batch * K / dt, 3), "unit": "tok/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} full fp64 draft passes of {wl.name} (all rows, all layers), "
+                      f"{dt:.2f} s each; numpy BLAS threads over {cores} cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from oracle import peagle_oracle as O
+
+    wl = synth.WORKLOADS[args.workload]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    W = O.Weights64.from_synth(w, lazy=True)
+    inp = synth.make_decode_inputs(wl, 99)
+    K = wl.K
+
+    def step():
+        r = O.draft_pass(W, dims, inp["cache_k"], inp["cache_v"], inp["seq_lens"],
+                         inp["target_hidden"], inp["new_token"], K, bf16=O.DRAFT_BF16_CASTS)
+        tgt, _ = synth.geometric_target_argmax(r.tokens, dims.target_vocab, 0.7, 6)
+        acc, _ = O.verify_greedy(r.tokens, tgt)
+        return acc
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    v = wl.batch * K / dt
+    return {"impl": "reference", "metric": "draft tokens/s", "value": round(v, 3), "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": wl.name, "batch": wl.batch, "K": K,
+                       "kv_len": [int(x) for x in inp["seq_lens"]]},
+            "cpu_baseline": {"value": round(v, 3), "unit": "tok/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"each step one full fp64 oracle draft pass of {wl.name} "
+                                       "plus greedy verification"},
+            "e2e": {"value": round(v, 3), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------- main
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    dist = None
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+            dist = tdist
+        out = run_ours(args, rank, world, dist)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -298,28 +298,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         epi_bar();
         if (*s_flag) {
           __threadfence();
+          // contributor cf's share of this tile is its last segment unless its range starts
+          // exactly at the tile; every later contributor's share is its first segment
+          const int slot_f = (range_begin(cf, p) == t_beg) ? 2 * cf : 2 * cf + 1;
           for (int ch = 0; ch < nch; ++ch) {
             const int i0 = ch * step;
+            int col[32];
+            float acc[32];
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
-              int col;
-              bool valid;
               if (p.split) {
                 const int ii = i0 + (j & 15);
-                col = (j < 16) ? ii : p.lo_col + ii;
-                valid = ii < lrows;
+                col[j] = min((j < 16) ? ii : p.lo_col + ii, p.BN - 1);
               } else {
-                col = i0 + j;
-                valid = col < lrows;
+                col[j] = min(i0 + j, p.BN - 1);
               }
-              float acc = 0.f;
-              if (valid) {
-                for (int cc = cf; cc <= cl; ++cc) {
-                  const int sl = (range_begin(cc, p) >= t_beg) ? 2 * cc : 2 * cc + 1;
-                  acc += __ldcg(p.ws + ((size_t)sl * p.BN + col) * 128 + ml);
-                }
-              }
-              stg[j * 128 + ml] = acc;
+              acc[j] = 0.f;
             }
+            for (int cc = cf; cc <= cl; ++cc) {
+              const float* src = p.ws + (size_t)(cc == cf ? slot_f : 2 * cc) * p.BN * 128 + ml;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] += __ldcg(src + (size_t)col[j] * 128);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[j * 128 + ml] = acc[j];
             epi_bar();
             epilogue_tile<bf16>(epi, stg, 128, p.split ? 16 : -1, m0, row0 + i0,
                                 min(step, lrows - i0), et, 128);

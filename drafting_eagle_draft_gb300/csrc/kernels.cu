@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
     const T* __restrict__ g_hid, float eps, int split, T* __restrict__ X0,
     float* __restrict__ res, unsigned long long* __restrict__ keys, unsigned* err) {
   __shared__ float red[32];
+  pdl_enter();
   const int r = blockIdx.x;
   const int R = gridDim.x;
   bool ntp;
@@ -150,9 +151,9 @@ void launch_input_fusion(bool bf16m, int mode, int R, int K, int n_src, int H, c
                          const void* g_in, const void* g_hid, float eps, int split, void* X0,
                          float* res, unsigned long long* keys, unsigned* err, cudaStream_t s) {
   if (bf16m)
-    input_fusion_kernel<bf16><<<R, 256, 0, s>>>(mode, K, n_src, H, (const bf16*)embed, Vt,
-        (const bf16*)emb_mask, F, f_shared, tokens, row_p, row_d, (const bf16*)g_in,
-        (const bf16*)g_hid, eps, split, (bf16*)X0, res, keys, err);
+    launch_pdl(input_fusion_kernel<bf16>, dim3(R), dim3(256), 0, s, mode, K, n_src, H,
+               (const bf16*)embed, Vt, (const bf16*)emb_mask, F, f_shared, tokens, row_p, row_d,
+               (const bf16*)g_in, (const bf16*)g_hid, eps, split, (bf16*)X0, res, keys, err);
   else
     input_fusion_kernel<float><<<R, 256, 0, s>>>(mode, K, n_src, H, (const float*)embed, Vt,
         (const float*)emb_mask, F, f_shared, tokens, row_p, row_d, (const float*)g_in,
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(int H, const float* __rest
                                                       const T* __restrict__ gamma, float eps,
                                                       int split, T* __restrict__ out) {
   __shared__ float red[32];
+  pdl_enter();
   const int r = blockIdx.x;
   const float* x = res + (size_t)r * H;
   float ss = 0.f;
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(int H, const float* __rest
 void launch_rmsnorm(bool bf16m, int R, int H, const float* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s) {
   if (bf16m)
-    rmsnorm_kernel<bf16><<<R, 256, 0, s>>>(H, res, (const bf16*)gamma, eps, split, (bf16*)out);
+    launch_pdl(rmsnorm_kernel<bf16>, dim3(R), dim3(256), 0, s, H, res, (const bf16*)gamma, eps,
+               split, (bf16*)out);
   else
     rmsnorm_kernel<float><<<R, 256, 0, s>>>(H, res, (const float*)gamma, eps, 0, (float*)out);
 }
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
   constexpr int E = HD / 32;          // output dims per lane
   constexpr int RPW = ATT_MAX_ROWS / 8;  // max rows per warp
   extern __shared__ float smem[];
+  pdl_enter();
   const int b = blockIdx.z, g = blockIdx.y, c = blockIdx.x;
   const int G = a.nq / a.nkv;
   const int rows = a.K * G;
@@ -303,20 +307,32 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
   const float* pbase = a.part + ((size_t)b * a.nkv + g) * a.nchunk * rows * (HD + 2);
   T* og = (T*)a.o;
   for (int rr = warp; rr < rows; rr += 8) {
-    float M = -INFINITY;
-    for (int cc = 0; cc < nvalid; ++cc)
-      M = fmaxf(M, __ldcg(pbase + ((size_t)cc * rows + rr) * (HD + 2) + HD));
-    float Ls = 0.f, acc[E];
+    // chunk statistics in parallel: lane c holds chunks c and c + 32 (nchunk <= 64)
+    float mc[2], lc[2], wc[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int cc = lane + 32 * t;
+      mc[t] = -INFINITY;
+      lc[t] = 0.f;
+      if (cc < nvalid) {
+        const float* pr = pbase + ((size_t)cc * rows + rr) * (HD + 2);
+        mc[t] = __ldcg(pr + HD);
+        lc[t] = __ldcg(pr + HD + 1);
+      }
+    }
+    const float M = warp_max(fmaxf(mc[0], mc[1]));
+#pragma unroll
+    for (int t = 0; t < 2; ++t) wc[t] = (mc[t] == -INFINITY) ? 0.f : expf(mc[t] - M);
+    const float Ls = warp_sum(lc[0] * wc[0] + lc[1] * wc[1]);
+    float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
     for (int cc = 0; cc < nvalid; ++cc) {
+      const float w = __shfl_sync(0xffffffffu, cc < 32 ? wc[0] : wc[1], cc & 31);
       const float* pr = pbase + ((size_t)cc * rows + rr) * (HD + 2);
-      const float mc = __ldcg(pr + HD);
-      if (mc == -INFINITY) continue;
-      const float w = expf(mc - M);
-      Ls += __ldcg(pr + HD + 1) * w;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += __ldcg(pr + lane + 32 * e) * w;
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(__ldcg(pr + lane + 32 * e), w, acc[e]);
     }
     const int j = rr / G, h = g * G + (rr - j * G);
     const float inv = 1.f / Ls;
@@ -339,7 +355,7 @@ static void attn_launch(const AttnArgs& a, cudaStream_t s) {
     attr_set = true;
   }
   dim3 grid(a.nchunk, a.nkv, a.B);
-  attn_decode_kernel<T, HD><<<grid, 256, sm, s>>>(a);
+  launch_pdl(attn_decode_kernel<T, HD>, grid, dim3(256), sm, s, a);
 }
 
 void launch_attention_decode(bool bf16m, const AttnArgs& a, cudaStream_t s) {
@@ -359,6 +375,7 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(256) masked_attn_kernel(MaskedAttnArgs a) {
   constexpr int E = HD / 32;
   __shared__ float qs[8][HD];
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long gw = (long)blockIdx.x * 8 + warp;
   if (gw >= (long)a.M * a.nq) return;
@@ -438,8 +455,8 @@ void launch_masked_attention(bool bf16m, const MaskedAttnArgs& a, cudaStream_t s
   const long warps = (long)a.M * a.nq;
   dim3 grid((unsigned)((warps + 7) / 8));
   if (bf16m) {
-    if (a.hd == 64) masked_attn_kernel<bf16, 64><<<grid, 256, 0, s>>>(a);
-    else masked_attn_kernel<bf16, 128><<<grid, 256, 0, s>>>(a);
+    if (a.hd == 64) launch_pdl(masked_attn_kernel<bf16, 64>, grid, dim3(256), 0, s, a);
+    else launch_pdl(masked_attn_kernel<bf16, 128>, grid, dim3(256), 0, s, a);
   } else {
     if (a.hd == 64) masked_attn_kernel<float, 64><<<grid, 256, 0, s>>>(a);
     else masked_attn_kernel<float, 128><<<grid, 256, 0, s>>>(a);
@@ -488,6 +505,7 @@ void launch_rows_prepare(int M, int n, int K, int Kmax, const int* row_p, const 
 // Argmax decode: key -> draft index -> target id via d2t; resets the key.
 // =====================================================================================
 __global__ void argmax_decode_kernel(int R, unsigned long long* keys, const int* d2t, int* out) {
+  pdl_enter();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
   const int idx = argmax_key_index(keys[r]);
@@ -497,7 +515,7 @@ __global__ void argmax_decode_kernel(int R, unsigned long long* keys, const int*
 
 void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* out,
                           cudaStream_t s) {
-  argmax_decode_kernel<<<cdiv(R, 128), 128, 0, s>>>(R, keys, d2t, out);
+  launch_pdl(argmax_decode_kernel, dim3(cdiv(R, 128)), dim3(128), 0, s, R, keys, d2t, out);
 }
 
 // =====================================================================================
@@ -506,6 +524,7 @@ void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* 
 __global__ void verify_kernel(int B, int K, const int* __restrict__ draft,
                               const int* __restrict__ tgt, int* __restrict__ acc,
                               int* __restrict__ bonus) {
+  pdl_enter();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int* d = draft + (size_t)b * K;
@@ -518,7 +537,7 @@ __global__ void verify_kernel(int B, int K, const int* __restrict__ draft,
 
 void launch_verify(int B, int K, const int* draft, const int* tgt, int* acc, int* bonus,
                    cudaStream_t s) {
-  verify_kernel<<<cdiv(B, 128), 128, 0, s>>>(B, K, draft, tgt, acc, bonus);
+  launch_pdl(verify_kernel, dim3(cdiv(B, 128)), dim3(128), 0, s, B, K, draft, tgt, acc, bonus);
 }
 
 // =====================================================================================
@@ -532,6 +551,7 @@ __global__ void __launch_bounds__(256) append_kv_kernel(int N, int nkv, int hd, 
                                                         int n_extra, const T* k_rows,
                                                         const T* v_rows, int n_max, int B,
                                                         unsigned* err) {
+  pdl_enter();
   const int b = blockIdx.x;
   const int L = seq_lens[b];
   const int n = n_commit[b] + n_extra;
@@ -567,8 +587,9 @@ void launch_append_kv(bool bf16m, int B, int N, int nkv, int hd, int cap, void* 
                       const void* v_rows, int n_max, int batch_slots, unsigned* err,
                       cudaStream_t s) {
   if (bf16m)
-    append_kv_kernel<bf16><<<B, 256, 0, s>>>(N, nkv, hd, cap, batch_slots, (bf16*)kc, (bf16*)vc,
-        seq_lens, n_commit, n_extra, (const bf16*)k_rows, (const bf16*)v_rows, n_max, B, err);
+    launch_pdl(append_kv_kernel<bf16>, dim3(B), dim3(256), 0, s, N, nkv, hd, cap, batch_slots,
+               (bf16*)kc, (bf16*)vc, seq_lens, n_commit, n_extra, (const bf16*)k_rows,
+               (const bf16*)v_rows, n_max, B, err);
   else
     append_kv_kernel<float><<<B, 256, 0, s>>>(N, nkv, hd, cap, batch_slots, (float*)kc, (float*)vc,
         seq_lens, n_commit, n_extra, (const float*)k_rows, (const float*)v_rows, n_max, B, err);
