@@ -29,9 +29,35 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// ---- fixed-point accumulators ---------------------------------------------------------
+// The residual stream and the fc output are kept as signed 64-bit fixed point with 32
+// fractional bits.  Split-K contributions are added with integer atomics, which are
+// associative: the sum is the same for any order of arrival (deterministic) and its
+// resolution (2^-32) is finer than fp32's at the magnitudes of the pass.
+typedef long long fx_t;
+// fp32 <-> fixed point without double arithmetic: scaling by 2^32 is exact in fp32, and
+// the conversions round to nearest (an fp32 input keeps all its 24 significant bits).
+__device__ __forceinline__ fx_t to_fx(float v) { return __float2ll_rn(v * 4294967296.0f); }
+__device__ __forceinline__ float from_fx(fx_t v) { return __ll2float_rn(v) * 2.3283064365386963e-10f; }
+__device__ __forceinline__ void red_add_fx(fx_t* p, fx_t v) {
+  asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"((unsigned long long)v) : "memory");
+}
+
 // ---- error word ---------------------------------------------------------------------
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
+}
+
+// Counter increment with acquire-release semantics at GPU scope.  After a CTA barrier,
+// one thread's release publishes every write the CTA made before the barrier; the thread
+// that observes the final count acquires all of them (no separate fences needed).
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 // ---- reductions ---------------------------------------------------------------------

@@ -4,15 +4,17 @@
 // handful of rows r (batch x K) and a long output dimension m.  The epilogue turns a
 // finished 128-feature tile of Y (fp32) into the pass's next tensor, so that Y itself
 // never reaches HBM:
-//   STORE      fp32 copy (fc projection; fc(h_shared) at create time)
+//   STORE      fixed-point accumulation (fc projection; fc(h_shared) at create time)
 //   QKV_ROPE   RoPE (rotate-half pairs i, i+hd/2) on q and k, then q -> Q [R, nq, hd],
 //              k, v -> the drafter KV cache slot of each row (decode) or to per-row
 //              K/V arrays (training-style forward)
-//   RESID      residual stream += Y (o-proj, down-proj)
+//   RESID      residual stream += Y (o-proj, down-proj), fixed point
 //   SWIGLU     act = silu(gate) * up, with gate/up rows interleaved in 64-row blocks
 //   LMHEAD     optional fp32 logits + per-row argmax folded into a 64-bit atomicMax key
 // A tile never splits a head (hd in {64, 128}, tiles start at multiples of 128) nor a
-// gate/up block, so each epilogue only needs its own tile.
+// gate/up block, so each epilogue only needs its own tile.  STORE and RESID are additive:
+// every split-K contributor adds its own partial with integer atomics (see fx_t), so they
+// need no cross-CTA reduction.
 #pragma once
 
 #include "common.cuh"
@@ -28,11 +30,11 @@ struct EpiArgs {
   int in_split;   // the GEMM's activation operand holds rows [0,R) = bf16 hi parts and
                   // [R,2R) = bf16 lo parts; the epilogue adds the two partial products
   int out_split;  // activation outputs (SWIGLU) are written as hi rows [0,R), lo [R,2R)
-  // STORE
-  float* out_f32;
+  // STORE: fixed-point destination [R, out_ld] (accumulated, zero beforehand)
+  fx_t* out_fx;
   int out_ld;
-  // RESID: fp32 residual [R, ld_res]
-  float* resid;
+  // RESID: fixed-point residual [R, ld_res]
+  fx_t* resid;
   int ld_res;
   // QKV_ROPE
   void* q_out;            // [R, nq*hd]; fp32 when q_f32, else the activation dtype
@@ -41,8 +43,8 @@ struct EpiArgs {
   void* v_dst;
   void* k1_dst;           // rows mode: depth-1 copy [n][nkv][hd] (may be null)
   void* v1_dst;
-  const int* seq_lens;    // decode: [B]
-  const int* row_pos;     // rows mode: RoPE position of each row
+  const int* row_pos;     // RoPE position of each row (decode: seq_lens[b] + j, written by
+                          // the input-fusion kernel; rows mode: p)
   const int* row_depth;   // rows mode: depth of each row (1-based)
   int n_seq;              // rows mode: sequence length (depth-1 copy bound)
   int decode;             // 1: decode (cache slot = seq_lens[b] + j), 0: rows
@@ -83,16 +85,13 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
     return v;
   };
   switch (a.kind) {
-    case EPI_STORE: {
-      for (int idx = tid; idx < rcount * 128; idx += nthr) {
-        int i = idx >> 7, ml = idx & 127;
-        if (ml < mcount) a.out_f32[(size_t)(r0 + i) * a.out_ld + m0 + ml] = val(i, ml);
-      }
-    } break;
+    case EPI_STORE:
     case EPI_RESID: {
+      fx_t* dst = a.kind == EPI_STORE ? a.out_fx : a.resid;
+      const int ldd = a.kind == EPI_STORE ? a.out_ld : a.ld_res;
       for (int idx = tid; idx < rcount * 128; idx += nthr) {
         int i = idx >> 7, ml = idx & 127;
-        if (ml < mcount) a.resid[(size_t)(r0 + i) * a.ld_res + m0 + ml] += val(i, ml);
+        if (ml < mcount) red_add_fx(dst + (size_t)(r0 + i) * ldd + m0 + ml, to_fx(val(i, ml)));
       }
     } break;
     case EPI_SWIGLU: {
@@ -109,23 +108,38 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
     case EPI_QKV_ROPE: {
       const int hd = a.hd, half = hd >> 1;
       const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
-      for (int idx = tid; idx < rcount * 128; idx += nthr) {
+      constexpr int U = 8;
+      for (int base = tid; base < rcount * 128; base += nthr * U) {
+      // positions and RoPE factors of U elements are fetched before any is used
+      int pos_u[U];
+      float2 cs_u[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * nthr;
+        pos_u[u] = idx < rcount * 128 ? __ldg(a.row_pos + r0 + (idx >> 7)) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * nthr;
+        const int m = m0 + (idx & 127);
+        const int i = m % hd;
+        const bool need = idx < rcount * 128 && m < kend && i < half && pos_u[u] >= 0 &&
+                          pos_u[u] < a.max_pos;
+        cs_u[u] = need ? __ldg(a.rope + (size_t)pos_u[u] * half + i) : make_float2(1.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * nthr;
+        if (idx >= rcount * 128) continue;
         int ti = idx >> 7, ml = idx & 127;
         int r = r0 + ti;
         int m = m0 + ml;
         if (ml >= mcount) continue;
         int i = m % hd;
         int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
-        int pos;
-        int b = 0, j = 0;
-        if (a.decode) {
-          b = r / a.K;
-          j = r - b * a.K;
-          pos = a.seq_lens[b] + j;
-        } else {
-          pos = a.row_pos[r];
-        }
-        bool pos_ok = pos >= 0 && pos < a.max_pos;
+        const int pos = pos_u[u];
+        int b = 0;
+        if (a.decode) b = r / a.K;
         if (a.decode && (pos < 0 || pos >= a.cap)) {
           if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
           if (sec != 0) continue;  // no cache slot for this row
@@ -137,7 +151,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
         } else {
           if (i >= half) continue;  // handled together with its pair partner
           float v1 = val(ti, ml + half);
-          float2 cs = pos_ok ? a.rope[(size_t)pos * half + i] : make_float2(1.f, 0.f);
+          const float2 cs = cs_u[u];
           out0 = v0 * cs.x - v1 * cs.y;
           out1 = v1 * cs.x + v0 * cs.y;
         }
@@ -170,6 +184,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
             }
           }
         }
+      }
       }
     } break;
     case EPI_LMHEAD: {

@@ -42,6 +42,7 @@ struct TcParams {
   int Nout, Kd;
   int R;        // logical rows
   int split;    // X rows [0,R) hi parts, [R,2R) lo parts
+  int additive; // epilogue adds into its destination: no cross-CTA reduction
   int BN;       // MMA N = operand rows per tile
   int rpt;      // logical rows per tile
   int lo_col;   // split: TMEM column of the lo part of tile row 0
@@ -248,8 +249,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // chunking: split tiles take 16 logical rows per chunk (hi + lo columns), others 32
       const int step = p.split ? 16 : 32;
       const int nch = (lrows + step - 1) / step;
-      if (cf == cl) {
-        // ---- sole owner: TMEM -> staging -> epilogue
+      if (cf == cl || p.additive) {
+        // ---- sole owner, or an additive epilogue (each contributor adds its own partial):
+        //      TMEM -> staging -> epilogue
         for (int ch = 0; ch < nch; ++ch) {
           const int i0 = ch * step;
           float v[16], w[16];
@@ -289,20 +291,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&acce[buf]);
-        __threadfence();
         epi_bar();
         if (et == 0) {
-          const unsigned prev = atomicAdd(p.counters + tile, 1u);
+          const unsigned prev = atom_add_acq_rel(p.counters + tile, 1u);
           *s_flag = (prev == (unsigned)(cl - cf)) ? 1 : 0;
         }
         epi_bar();
         if (*s_flag) {
-          __threadfence();
           // contributor cf's share of this tile is its last segment unless its range starts
           // exactly at the tile; every later contributor's share is its first segment
           const int slot_f = (range_begin(cf, p) == t_beg) ? 2 * cf : 2 * cf + 1;
           for (int ch = 0; ch < nch; ++ch) {
             const int i0 = ch * step;
+            // staging rows [0,16) / [16,32): hi / lo parts (split) or rows i0.. (plain)
             int col[32];
             float acc[32];
 #pragma unroll
@@ -446,6 +447,7 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   p.Kd = Kd;
   p.R = R;
   p.split = epi.in_split ? 1 : 0;
+  p.additive = (epi.kind == EPI_STORE || epi.kind == EPI_RESID) ? 1 : 0;
   const int xrows = p.split ? 2 * R : R;
   p.two_box = 0;
   if (p.split && 2 * R <= 240) {
@@ -479,6 +481,7 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   int stages = 2;
   while (stages < 12 && smem_bytes(stages + 1, p.BN) <= budget) ++stages;
   p.stages = stages;
+
   // single-tile split reads 16-column groups starting at column R + i0, which may run
   // up to 15 columns past the second accumulator: keep that slack allocated
   p.tmem_cols = pow2_at_least((uint32_t)(2 * p.BN + ((p.split && !p.two_box) ? 16 : 0)));

@@ -44,12 +44,13 @@ void launch_gemm_simt(bool bf16, const void* W, const void* X, int ldx, float* Y
 
 void launch_input_fusion(bool bf16, int mode, int R, int K, int n_src, int H, const void* embed,
                          int Vt,
-                         const void* emb_mask, const float* F, const float* f_shared,
+                         const void* emb_mask, fx_t* F, const fx_t* f_shared,
                          const int* tokens, const int* row_p, const int* row_d,
                          const void* g_in, const void* g_hid, float eps, int split, void* X0,
-                         float* res, unsigned long long* keys, unsigned* err, cudaStream_t s);
+                         fx_t* res, unsigned long long* keys, const int* seq_lens, int* row_pos,
+                         unsigned* err, cudaStream_t s);
 
-void launch_rmsnorm(bool bf16, int R, int H, const float* res, const void* gamma, float eps,
+void launch_rmsnorm(bool bf16, int R, int H, const fx_t* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s);
 
 void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);

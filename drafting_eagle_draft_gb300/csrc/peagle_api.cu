@@ -25,12 +25,12 @@ struct peagle_ctx {
   int* d2t;
   std::vector<void*> qkv, o, attn_norm, post_norm, gate_up, down;
   float2* rope;
-  float* f_shared;  // fc(h_shared) [H]
+  fx_t* f_shared;   // fc(h_shared) [H], fixed point
   // workspaces
   int rows_max;     // activation operand rows: 2 * max(max_batch * max_K, max_rows)
-  float* F;         // [max(max_batch, max_seq), H]
+  fx_t* F;          // fc outputs [max(max_batch, max_seq), H], fixed point, zero between uses
   void* X0;         // [rows_max, 2H]
-  float* res;       // [rows_max, H]
+  fx_t* res;        // residual stream [rows_max, H], fixed point
   void* Xn;         // [rows_max, H]
   float* Qf;        // [max(max_batch*max_K, max_rows), nq*hd] fp32 post-RoPE queries
   void* O;          // [rows_max, nq*hd]
@@ -38,6 +38,7 @@ struct peagle_ctx {
   float* Y;         // fp32 GEMM output (FFMA path) [rows_max, max_out]
   int ldY;
   unsigned long long* keys;  // [rows_max]
+  int* row_pos;     // [max_batch * max_K] RoPE position / cache slot of each draft row
   float* att_part;
   unsigned* att_cnt;
   int att_chunks_max;
@@ -263,15 +264,16 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   c->rows_max = 2 * logical_rows;
   const int R = c->rows_max;
   const int fr = d.max_batch > d.max_seq ? d.max_batch : d.max_seq;
-  TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 4));
-  TRY(dalloc(c, (void**)&c->f_shared, (size_t)H * 4));
+  TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 8));
+  TRY(dalloc(c, (void**)&c->f_shared, (size_t)H * 8));
   TRY(dalloc(c, &c->X0, (size_t)R * 2 * H * es));
-  TRY(dalloc(c, (void**)&c->res, (size_t)R * H * 4));
+  TRY(dalloc(c, (void**)&c->res, (size_t)R * H * 8));
   TRY(dalloc(c, &c->Xn, (size_t)R * H * es));
   TRY(dalloc(c, (void**)&c->Qf, (size_t)logical_rows * nq * hd * 4));
   TRY(dalloc(c, &c->O, (size_t)R * nq * hd * es));
   TRY(dalloc(c, &c->act, (size_t)R * I * es));
   TRY(dalloc(c, (void**)&c->keys, (size_t)R * 8));
+  TRY(dalloc(c, (void**)&c->row_pos, (size_t)d.max_batch * d.max_K * 4));
   TRY(dalloc(c, (void**)&c->err, 64));
   int max_out = qkv_out;
   if (2 * I > max_out) max_out = 2 * I;
@@ -297,7 +299,7 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   // fc(h_shared): constant for every MTP row, computed once with the pass's own GEMM
   {
     EpiArgs e = epi_base(c, EPI_STORE, 1, H);
-    e.out_f32 = c->f_shared;
+    e.out_fx = c->f_shared;
     e.out_ld = H;
     int g = gemm(c, c->fc, c->h_shared, 3 * H, H, 3 * H, 1, e, 0);
     if (g != PEAGLE_OK || cudaDeviceSynchronize() != cudaSuccess) {
@@ -345,14 +347,15 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   // S1: fc over the NTP rows' target hidden states, then the fused input rows
   {
     EpiArgs e = epi_base(c, EPI_STORE, batch, H);
-    e.out_f32 = c->F;
+    e.out_fx = c->F;
     e.out_ld = H;
     GEMM(PEAGLE_STAGE_FC, c, c->fc, target_hidden, 3 * H, H, 3 * H, batch, e, s);
   }
   TIMED(PEAGLE_STAGE_NORM,
         launch_input_fusion(c->bf, 0, R, K, batch, H, c->embed, d.target_vocab, c->emb_mask,
                             c->F, c->f_shared, new_token, nullptr, nullptr, c->input_norm,
-                            c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, c->err, s));
+                            c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, seq_lens,
+                            c->row_pos, c->err, s));
   int chunk, nchunk;
   attention_plan(c, batch, kv->capacity, &chunk, &nchunk);
   for (int l = 0; l < d.n_layers; ++l) {
@@ -372,7 +375,7 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       e.q_f32 = 1;
       e.k_dst = (char*)kv->k + l * layer_stride;
       e.v_dst = (char*)kv->v + l * layer_stride;
-      e.seq_lens = seq_lens;
+      e.row_pos = c->row_pos;
       e.decode = 1;
       e.K = K;
       e.cap = kv->capacity;
@@ -488,16 +491,21 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   const int split = use_split(c);
   TIMED(PEAGLE_STAGE_SMALL,
         launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s));
+  // the fc projection accumulates into F; clear every row of this sequence first (a row
+  // list that skips a depth-1 position would otherwise leave it uncleared)
+  if (cudaMemsetAsync(c->F, 0, (size_t)n * H * sizeof(fx_t), s) != cudaSuccess)
+    return PEAGLE_ERR_CUDA;
   {
     EpiArgs e = epi_base(c, EPI_STORE, n, H);
-    e.out_f32 = c->F;
+    e.out_fx = c->F;
     e.out_ld = H;
     GEMM(PEAGLE_STAGE_FC, c, c->fc, hidden, 3 * H, H, 3 * H, n, e, s);
   }
   TIMED(PEAGLE_STAGE_NORM,
         launch_input_fusion(c->bf, 1, M, K, n, H, c->embed, d.target_vocab, c->emb_mask, c->F,
                             c->f_shared, tokens, row_p, row_d, c->input_norm, c->hidden_norm,
-                            d.rms_eps, split, c->X0, c->res, c->keys, c->err, s));
+                            d.rms_eps, split, c->X0, c->res, c->keys, nullptr, nullptr, c->err,
+                            s));
   for (int l = 0; l < d.n_layers; ++l) {
     const void* a_in = c->X0;
     int din = 2 * H;
