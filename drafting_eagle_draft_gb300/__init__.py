@@ -32,7 +32,7 @@ PEAGLE_BF16 = 1
 # every entry point declared in include/peagle.h
 EXPORTS = ("peagle_create", "peagle_draft", "peagle_verify_greedy", "peagle_append_kv",
            "peagle_forward_parallel", "peagle_cod_rows", "peagle_status",
-           "peagle_set_timing", "peagle_read_timing",
+           "peagle_set_timing", "peagle_read_timing", "peagle_decode_attention_static",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
 STAGES = ("fc", "qkv", "attn", "oproj", "gate_up", "down", "lm_head", "norm", "small")
 
@@ -90,6 +90,8 @@ def lib():
         L.peagle_cod_rows.argtypes = [_i32, _i32, ctypes.c_double, _vp, _vp, _vp, _i32]
         L.peagle_status.argtypes = [_vp]
         L.peagle_set_timing.argtypes = [_vp, _i32]
+        L.peagle_decode_attention_static.argtypes = [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                                     _i32, _vp, _vp, _vp]
         L.peagle_read_timing.argtypes = [_vp, _vp, _vp]
         L.peagle_device_error_bits.argtypes = [_vp]
         L.peagle_device_error_bits.restype = _i32
@@ -260,6 +262,16 @@ def peagle_read_timing(ctx: Context) -> dict:
     _check(lib().peagle_read_timing(ctx.handle, ms.ctypes.data, n.ctypes.data),
            "peagle_read_timing")
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(STAGES)}
+
+
+def peagle_decode_attention_static(batch, K, n_q_heads, n_kv_heads, head_dim, q, k_cache,
+                                   v_cache, capacity, seq_lens, out, stream=None):
+    """Decode attention with no device allocation (see include/peagle.h)."""
+    _check(lib().peagle_decode_attention_static(int(batch), int(K), int(n_q_heads),
+                                                int(n_kv_heads), int(head_dim), _ptr(q),
+                                                _ptr(k_cache), _ptr(v_cache), int(capacity),
+                                                _ptr(seq_lens), _ptr(out), _stream_ptr(stream)),
+           "peagle_decode_attention_static")
 
 
 def peagle_device_error_bits(ctx: Context) -> int:

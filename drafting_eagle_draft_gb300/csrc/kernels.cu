@@ -2,6 +2,12 @@
 // attention with the causal draft block, the training-style masked attention, greedy
 // verification, KV commit, argmax decode, and the fp32 FFMA GEMM used by the fp32
 // drafter (whose 1e-4 logit tolerance rules out TF32 tensor cores).
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "kernels.h"
 
 namespace peagle {
@@ -916,3 +922,134 @@ void launch_append_kv(bool bf16m, int B, int N, int nkv, int hd, int cap, void* 
 }
 
 }  // namespace peagle
+
+// =====================================================================================
+// peagle_decode_attention_static: the split-KV decode attention for callers that cannot
+// allocate device memory.  Its split-KV partial results live in the file-scope array
+// below (PEAGLE_STATIC_ATTN_SCRATCH_BYTES, held by every GPU that loads the library until
+// the process exits) instead of a context workspace.
+// =====================================================================================
+namespace peagle {
+
+static __device__ __align__(256) float g_static_attn_scratch[PEAGLE_STATIC_ATTN_SCRATCH_BYTES /
+                                                             sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+float* g_static_ptr[kMaxDevices] = {};   // device address of the array, per device
+bool g_static_attr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per device:
+// in host code the array's name is only a host-side stand-in).
+int static_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PEAGLE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_attn_scratch);
+    if (e != cudaSuccess || !p) {
+      fprintf(stderr, "peagle: cudaGetSymbolAddress(static attention scratch) failed: %s\n",
+              cudaGetErrorString(e));
+      return PEAGLE_ERR_CUDA;
+    }
+    g_static_ptr[dev] = (float*)p;
+  }
+  if (!g_static_attr[dev]) {
+    if (cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             100 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             100 * 1024) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    g_static_attr[dev] = true;
+  }
+  *out = g_static_ptr[dev];
+  return PEAGLE_OK;
+}
+
+template <int HD>
+cudaError_t static_attn_launch(const AttnArgs& a, cudaStream_t s) {
+  const int rows = a.K * (a.nq / a.nkv);
+  const int warps = (rows + 15) / 16;
+  const size_t sm = (size_t)4 * MMA_KT * HD * 2;
+  cudaError_t e = launch_pdl(attn_mma_kernel<HD>, dim3(a.nchunk, a.nkv, a.B), dim3(32 * warps),
+                             sm, s, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_merge_kernel<float, HD>, dim3(cdiv(rows, 4), a.nkv, a.B), dim3(128), 0,
+                    s, a);
+}
+}  // namespace
+
+}  // namespace peagle
+
+extern "C" int peagle_decode_attention_static(int32_t batch, int32_t K, int32_t n_q_heads,
+                                              int32_t n_kv_heads, int32_t head_dim,
+                                              const float* q, const void* k_cache,
+                                              const void* v_cache, int32_t capacity,
+                                              const int32_t* seq_lens, float* out, void* stream) {
+  using namespace peagle;
+  if (batch < 1 || K < 1 || n_q_heads < 1 || n_kv_heads < 1 || capacity < K || !q || !k_cache ||
+      !v_cache || !seq_lens || !out)
+    return PEAGLE_ERR_INVALID;
+  if ((head_dim != 64 && head_dim != 128) || n_q_heads % n_kv_heads) return PEAGLE_ERR_UNSUPPORTED;
+  const int G = n_q_heads / n_kv_heads;
+  const int rows = K * G;
+  if (rows > ATT_MAX_ROWS) return PEAGLE_ERR_UNSUPPORTED;
+  int num_sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PEAGLE_ERR_CUDA;
+  // split plan: about two CTAs per SM, chunks of whole 64-key tiles, at most 64 chunks;
+  // fewer, longer chunks if the partials would not fit the static array
+  const size_t per_chunk = (size_t)batch * n_kv_heads * rows * (head_dim + 2) * sizeof(float);
+  const size_t max_chunks = PEAGLE_STATIC_ATTN_SCRATCH_BYTES / per_chunk;
+  if (max_chunks < 1) {
+    fprintf(stderr,
+            "peagle_decode_attention_static: batch %d x kv heads %d x rows %d needs %zu bytes "
+            "of scratch per chunk, more than the %u-byte static array\n",
+            batch, n_kv_heads, rows, per_chunk, (unsigned)PEAGLE_STATIC_ATTN_SCRATCH_BYTES);
+    return PEAGLE_ERR_CAPACITY;
+  }
+  int want = (2 * num_sms + batch * n_kv_heads - 1) / (batch * n_kv_heads);
+  if (want < 1) want = 1;
+  if (want > 64) want = 64;
+  if ((size_t)want > max_chunks) want = (int)max_chunks;
+  int chunk = (capacity + want - 1) / want;
+  chunk = (chunk + 63) / 64 * 64;
+  int nchunk = (capacity + chunk - 1) / chunk;
+  while ((size_t)nchunk > max_chunks || nchunk > 64) {
+    chunk += 64;
+    nchunk = (capacity + chunk - 1) / chunk;
+  }
+  float* scratch = nullptr;
+  int r = static_scratch(&scratch);
+  if (r != PEAGLE_OK) return r;
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.seq_lens = seq_lens;
+  a.o = out;
+  a.split = 0;
+  a.part = scratch;  // every element read by the merge is written first: no clearing needed
+  a.counters = nullptr;
+  a.B = batch;
+  a.K = K;
+  a.nq = n_q_heads;
+  a.nkv = n_kv_heads;
+  a.hd = head_dim;
+  a.cap = capacity;
+  a.chunk = chunk;
+  a.nchunk = nchunk;
+  a.scale = 1.f / sqrtf((float)head_dim);
+  a.err = nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = head_dim == 64 ? static_attn_launch<64>(a, s) : static_attn_launch<128>(a, s);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "peagle_decode_attention_static: launch failed: %s\n", cudaGetErrorString(e));
+    return PEAGLE_ERR_CUDA;
+  }
+  return PEAGLE_OK;
+}

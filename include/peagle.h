@@ -215,6 +215,38 @@ int peagle_set_timing(peagle_ctx* ctx, int32_t enable);
  * stage (arrays of PEAGLE_NUM_STAGES) since the previous read, and reset them. */
 int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches);
 
+/* Size of the library's static scratch array used by peagle_decode_attention_static. */
+#define PEAGLE_STATIC_ATTN_SCRATCH_BYTES (8u << 20)
+
+/* Decode attention for callers that cannot allocate device memory.  The pages have no
+ * counterpart for this call: it exists for users of the library whose code may not call
+ * cudaMalloc -- for example a process whose device memory is entirely handed out by its
+ * own arena allocator, or code that may not make allocating CUDA calls at the point where
+ * attention runs -- and who therefore cannot hold a peagle_ctx and its workspaces.
+ *
+ * It computes the draft pass's attention step for one layer: for request b, query row j
+ * (rows b*K + j) and query head h, softmax(q . k / sqrt(head_dim)) . v over the cached
+ * keys/values of kv head h / (n_q_heads / n_kv_heads) at slots 0 .. seq_lens[b] + j.
+ *   q        device fp32 [batch*K][n_q_heads][head_dim] (keys are not rotated here: q and
+ *            the cache are taken as already RoPE-rotated)
+ *   k_cache, v_cache  device bf16 [batch][n_kv_heads][capacity][head_dim] (one layer)
+ *   seq_lens device int32 [batch]; keys at slots >= min(seq_lens[b] + K, capacity) unused
+ *   out      device fp32 [batch*K][n_q_heads][head_dim]
+ * Limits: head_dim 64 or 128; K * n_q_heads / n_kv_heads <= 128; the split-KV partials,
+ * batch * n_kv_heads * chunks * K * (n_q_heads/n_kv_heads) * (head_dim + 2) floats, must fit
+ * PEAGLE_STATIC_ATTN_SCRATCH_BYTES (fewer, longer chunks are used when needed; a batch
+ * too large for even one chunk is rejected with PEAGLE_ERR_CAPACITY and a message on
+ * stderr).  No allocation and no host synchronisation.
+ * The scratch is one array per GPU, shared by every call and keeping the last call's
+ * contents (nothing in it needs to start at zero); calls that overlap on the GPU (other
+ * streams, other threads) race on it, so order them on one stream.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and sets kernel
+ * attributes: make that first call before any stream capture. */
+int peagle_decode_attention_static(int32_t batch, int32_t K, int32_t n_q_heads,
+                                   int32_t n_kv_heads, int32_t head_dim, const float* q,
+                                   const void* k_cache, const void* v_cache, int32_t capacity,
+                                   const int32_t* seq_lens, float* out, void* stream);
+
 /* Raw device error bits observed by the last peagle_status call. */
 int32_t peagle_device_error_bits(const peagle_ctx* ctx);
 
