@@ -46,6 +46,8 @@ def parse():
                     choices=["decode_b1", "decode_b2", "ragged_b16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-train-fwd", action="store_true",
+                    help="skip the training-style masked forward measurement")
     return ap.parse_args()
 
 
@@ -326,7 +328,70 @@ def run_ours(args, rank, world, dist):
         if cpu:
             out["cpu_baseline"] = cpu
     ctx.close()
+    if rank == 0 and world == 1 and not args.no_train_fwd:
+        out["train_fwd"] = train_fwd_measure(dev)
     return out
+
+
+def train_fwd_measure(dev, reps=3):
+    """Training-style masked forward of the decode drafter (n=2048, K=8, COD 0.8): time per
+    forward with CUDA events, and the tensor-core roofline of its algorithmic FLOPs
+    (projections 2*M*params + masked attention 4*nq*hd*(allowed pairs)).  The projections
+    execute twice the algorithmic MMA work (bf16 hi + lo activation operands)."""
+    import torch
+
+    import drafting_eagle_draft_gb300 as pk
+
+    wl = synth.WORKLOADS["train_fwd"]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    ti = synth.make_train_inputs(wl, 21)
+    n, K = wl.n_seq, wl.K
+    rp, rd = pk.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
+    M = len(rp)
+    ctx = pk.peagle_create(w, pk.make_dims(dims, 1, K, n, max_rows=M, max_seq=n))
+    del w
+    tok = torch.from_numpy(ti["tokens"]).to(dev)
+    hid = ti["hidden"].to(dev)
+    rpd = torch.from_numpy(rp).to(dev)
+    rdd = torch.from_numpy(rd).to(dev)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def fwd():
+        pk.peagle_forward_parallel(ctx, n, K, tok, hid, rpd, rdd, M, am, None, s)
+
+    with torch.cuda.stream(s):
+        fwd()
+    s.synchronize()
+    assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            fwd()
+        e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    pk.peagle_set_timing(ctx, True)
+    with torch.cuda.stream(s):
+        fwd()
+    st = pk.peagle_read_timing(ctx)
+    ctx.close()
+    params = gemm_weight_bytes(dims) // 2
+    p_np, d_np = rp.astype("int64"), rd.astype("int64")
+    # allowed (query, key) pairs of the mask: depth-1 keys up to the anchor + own chain
+    pairs = int(((p_np - d_np + 1) + 1).sum() + (d_np - 1).sum())
+    gemm_flops = 2.0 * M * params
+    attn_flops = 4.0 * dims.n_q_heads * dims.head_dim * pairs
+    pk_ = peaks()
+    tflops = (gemm_flops + attn_flops) / (ms * 1e-3) / 1e12
+    return {"workload": wl.name, "rows": M, "ms": round(ms, 3),
+            "tflops": round(tflops, 1), "peak_tflops": pk_["bf16_tflops_sustained"],
+            "frac": round(tflops / pk_["bf16_tflops_sustained"], 4),
+            "algorithmic_tflop": round((gemm_flops + attn_flops) / 1e12, 3),
+            "stages_ms": {k: round(v[0], 3) for k, v in st.items()}}
 
 
 # ---------------------------------------------------------------------------- oracle arm

@@ -83,7 +83,9 @@ __device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* m, int k
   }
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// two CTAs per SM: under programmatic dependent launch the next projection's CTA starts
+// (and prefetches its weights) beside this one
+__global__ void __launch_bounds__(TC_THREADS, 2)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const TcParams p, const EpiArgs epi) {
   extern __shared__ uint8_t smem_raw[];

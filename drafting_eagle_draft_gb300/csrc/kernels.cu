@@ -93,8 +93,10 @@ void launch_gemm_simt(bool bf16m, const void* W, const void* X, int ldx, float* 
 // F (the fc output, fixed point) is cleared after use so the next fc launch can
 // accumulate into it; each F row is read by exactly one CTA.
 // =====================================================================================
-template <typename T>
-__global__ void __launch_bounds__(256) input_fusion_kernel(
+constexpr int ROW_THREADS = 512;  // one CTA per row; each thread keeps NPT row elements
+
+template <typename T, int NPT>
+__global__ void __launch_bounds__(ROW_THREADS) input_fusion_kernel(
     int mode, int K, int n_src, int H, const T* __restrict__ embed, int Vt,
     const T* __restrict__ emb_mask,
     fx_t* __restrict__ F, const fx_t* __restrict__ f_shared, const int* __restrict__ tokens,
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
     }
   }
   const T* e;
-  const fx_t* f;
+  fx_t* f;
   if (ntp) {
     int tok = tokens[src];
     if (tok < 0 || tok >= Vt) {
@@ -131,12 +133,25 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
     f = F + (size_t)src * H;
   } else {
     e = emb_mask;
-    f = f_shared;
+    f = const_cast<fx_t*>(f_shared);
+  }
+  // the whole row in registers: every load of the row is issued in one round
+  float ev[NPT], gi[NPT], gh[NPT];
+  fx_t fq[NPT];
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    const bool ok = i < H;
+    ev[k] = ok ? ld(e + i) : 0.f;
+    fq[k] = ok ? f[i] : 0;
+    gi[k] = ok ? ld(g_in + i) : 0.f;
+    gh[k] = ok ? ld(g_hid + i) : 0.f;
   }
   float se = 0.f, sf = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    float ev = ld(e + i), fv = from_fx(f[i]);
-    se += ev * ev;
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    const float fv = from_fx(fq[k]);
+    se += ev[k] * ev[k];
     sf += fv * fv;
   }
   se = block_sum(se, red);
@@ -144,20 +159,50 @@ __global__ void __launch_bounds__(256) input_fusion_kernel(
   sf = block_sum(sf, red);
   const float ie = rsqrtf(se / H + eps), ifv = rsqrtf(sf / H + eps);
   fx_t* rs = res + (size_t)r * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const fx_t fq = f[i];
-    const float fv = from_fx(fq);
-    store_act<T>(X0, 2 * H, r, R, split, i, ld(e + i) * ie * ld(g_in + i));
-    store_act<T>(X0, 2 * H, r, R, split, H + i, fv * ifv * ld(g_hid + i));
-    rs[i] = fq;
-  }
-  if (ntp) {  // clear this F row for the next fc accumulation (read above by this CTA only)
-    __syncthreads();
-    fx_t* fw = F + (size_t)src * H;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) fw[i] = 0;
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i >= H) continue;
+    store_act<T>(X0, 2 * H, r, R, split, i, ev[k] * ie * gi[k]);
+    store_act<T>(X0, 2 * H, r, R, split, H + i, from_fx(fq[k]) * ifv * gh[k]);
+    rs[i] = fq[k];
+    // the fc output row of an NTP row is read only here: clear it for the next
+    // accumulation (this thread's own elements, already loaded)
+    if (ntp) f[i] = 0;
   }
   if (threadIdx.x == 0 && keys) keys[r] = 0ull;
   if (threadIdx.x == 0 && mode == 0 && row_pos_out) row_pos_out[r] = seq_lens[src] + (r - src * K);
+}
+
+template <typename T>
+static void input_fusion_dispatch(int npt, dim3 g, cudaStream_t s, int mode, int K, int n_src,
+                                  int H, const T* embed, int Vt, const T* emb_mask, fx_t* F,
+                                  const fx_t* f_shared, const int* tokens, const int* row_p,
+                                  const int* row_d, const T* g_in, const T* g_hid, float eps,
+                                  int split, T* X0, fx_t* res, unsigned long long* keys,
+                                  const int* seq_lens, int* row_pos, unsigned* err) {
+#define PEAGLE_IF_CASE(N)                                                                     \
+  case N:                                                                                     \
+    launch_pdl(input_fusion_kernel<T, N>, g, dim3(ROW_THREADS), 0, s, mode, K, n_src, H, embed, \
+               Vt, emb_mask, F, f_shared, tokens, row_p, row_d, g_in, g_hid, eps, split, X0,  \
+               res, keys, seq_lens, row_pos, err);                                            \
+    break;
+  switch (npt) {
+    PEAGLE_IF_CASE(1)
+    PEAGLE_IF_CASE(2)
+    PEAGLE_IF_CASE(4)
+    PEAGLE_IF_CASE(8)
+    PEAGLE_IF_CASE(16)
+    default:
+      PEAGLE_IF_CASE(32)
+  }
+#undef PEAGLE_IF_CASE
+}
+
+static int row_npt(int H) {
+  int npt = 1;
+  while (npt * ROW_THREADS < H) npt <<= 1;
+  return npt;
 }
 
 void launch_input_fusion(bool bf16m, int mode, int R, int K, int n_src, int H, const void* embed,
@@ -167,46 +212,72 @@ void launch_input_fusion(bool bf16m, int mode, int R, int K, int n_src, int H, c
                          const void* g_in, const void* g_hid, float eps, int split, void* X0,
                          fx_t* res, unsigned long long* keys, const int* seq_lens, int* row_pos,
                          unsigned* err, cudaStream_t s) {
+  const int npt = row_npt(H);
   if (bf16m)
-    launch_pdl(input_fusion_kernel<bf16>, dim3(R), dim3(256), 0, s, mode, K, n_src, H,
-               (const bf16*)embed, Vt, (const bf16*)emb_mask, F, f_shared, tokens, row_p, row_d,
-               (const bf16*)g_in, (const bf16*)g_hid, eps, split, (bf16*)X0, res, keys, seq_lens,
-               row_pos, err);
+    input_fusion_dispatch<bf16>(npt, dim3(R), s, mode, K, n_src, H, (const bf16*)embed, Vt,
+                                (const bf16*)emb_mask, F, f_shared, tokens, row_p, row_d,
+                                (const bf16*)g_in, (const bf16*)g_hid, eps, split, (bf16*)X0, res,
+                                keys, seq_lens, row_pos, err);
   else
-    input_fusion_kernel<float><<<R, 256, 0, s>>>(mode, K, n_src, H, (const float*)embed, Vt,
-        (const float*)emb_mask, F, f_shared, tokens, row_p, row_d, (const float*)g_in,
-        (const float*)g_hid, eps, 0, (float*)X0, res, keys, seq_lens, row_pos, err);
+    input_fusion_dispatch<float>(npt, dim3(R), s, mode, K, n_src, H, (const float*)embed, Vt,
+                                 (const float*)emb_mask, F, f_shared, tokens, row_p, row_d,
+                                 (const float*)g_in, (const float*)g_hid, eps, 0, (float*)X0, res,
+                                 keys, seq_lens, row_pos, err);
 }
 
 // =====================================================================================
 // RMSNorm of the fp32 residual stream into the next projection's input dtype.
 // =====================================================================================
-template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(int H, const fx_t* __restrict__ res,
-                                                      const T* __restrict__ gamma, float eps,
-                                                      int split, T* __restrict__ out) {
+template <typename T, int NPT>
+__global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(int H, const fx_t* __restrict__ res,
+                                                              const T* __restrict__ gamma,
+                                                              float eps, int split,
+                                                              T* __restrict__ out) {
   __shared__ float red[32];
   pdl_enter();
   const int r = blockIdx.x;
   const fx_t* x = res + (size_t)r * H;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const float v = from_fx(x[i]);
-    ss += v * v;
+  float v[NPT], g[NPT];
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    v[k] = i < H ? from_fx(x[i]) : 0.f;
+    g[k] = i < H ? ld(gamma + i) : 0.f;
   }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) ss += v[k] * v[k];
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / H + eps);
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    store_act<T>(out, H, r, gridDim.x, split, i, from_fx(x[i]) * inv * ld(gamma + i));
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < H) store_act<T>(out, H, r, gridDim.x, split, i, v[k] * inv * g[k]);
+  }
 }
 
 void launch_rmsnorm(bool bf16m, int R, int H, const fx_t* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s) {
-  if (bf16m)
-    launch_pdl(rmsnorm_kernel<bf16>, dim3(R), dim3(256), 0, s, H, res, (const bf16*)gamma, eps,
-               split, (bf16*)out);
-  else
-    rmsnorm_kernel<float><<<R, 256, 0, s>>>(H, res, (const float*)gamma, eps, 0, (float*)out);
+  const int npt = row_npt(H);
+#define PEAGLE_RMS_CASE(N)                                                                 \
+  case N:                                                                                  \
+    if (bf16m)                                                                             \
+      launch_pdl(rmsnorm_kernel<bf16, N>, dim3(R), dim3(ROW_THREADS), 0, s, H, res,         \
+                 (const bf16*)gamma, eps, split, (bf16*)out);                              \
+    else                                                                                   \
+      rmsnorm_kernel<float, N><<<R, ROW_THREADS, 0, s>>>(H, res, (const float*)gamma, eps, \
+                                                         0, (float*)out);                  \
+    break;
+  switch (npt) {
+    PEAGLE_RMS_CASE(1)
+    PEAGLE_RMS_CASE(2)
+    PEAGLE_RMS_CASE(4)
+    PEAGLE_RMS_CASE(8)
+    PEAGLE_RMS_CASE(16)
+    default:
+      PEAGLE_RMS_CASE(32)
+  }
+#undef PEAGLE_RMS_CASE
 }
 
 // =====================================================================================
@@ -469,6 +540,7 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(AttnArgs a) {
     }
     cp_async_commit();
   };
+  load_tile(0, kbeg);  // the first K/V tile is in flight while the queries load
   // query fragments of this warp's 16 rows, pre-scaled for exp2, split hi / lo
   const float qscale = a.scale * 1.4426950408889634f;
   const int r0 = warp * 16 + gq, r1 = r0 + 8;
@@ -500,7 +572,6 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(AttnArgs a) {
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const bool active = warp * 16 < rows;
   const int ntile = (kend - kbeg + MMA_KT - 1) / MMA_KT;
-  load_tile(0, kbeg);
   for (int it = 0; it < ntile; ++it) {
     const int buf = it & 1;
     const int t0 = kbeg + it * MMA_KT;

@@ -130,6 +130,7 @@ static int validate_dims(const peagle_dims* d) {
   if (d->head_dim != 64 && d->head_dim != 128) return PEAGLE_ERR_UNSUPPORTED;
   if (d->n_q_heads % d->n_kv_heads) return PEAGLE_ERR_UNSUPPORTED;
   if (d->hidden % 64 || d->intermediate % 64) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->hidden > 16384) return PEAGLE_ERR_UNSUPPORTED;
   if (((d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim) % 128) return PEAGLE_ERR_UNSUPPORTED;
   if (d->max_K > 16 || d->max_batch * d->max_K > 256) return PEAGLE_ERR_CAPACITY;
   if (d->max_K * (d->n_q_heads / d->n_kv_heads) > 128) return PEAGLE_ERR_UNSUPPORTED;

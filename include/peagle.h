@@ -56,7 +56,7 @@ typedef enum { PEAGLE_F32 = 0, PEAGLE_BF16 = 1 } peagle_dtype;
 typedef struct peagle_ctx peagle_ctx;
 
 /* Drafter dimensions.  Constraints (else PEAGLE_ERR_UNSUPPORTED):
- *   head_dim in {64, 128}; n_q_heads % n_kv_heads == 0; hidden % 64 == 0;
+ *   head_dim in {64, 128}; n_q_heads % n_kv_heads == 0; hidden % 64 == 0, <= 16384;
  *   intermediate % 64 == 0; (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0;
  *   max_batch * max_K <= 256; max_K <= 16. */
 typedef struct peagle_dims {
