@@ -848,12 +848,308 @@ __global__ void __launch_bounds__(256) masked_attn_kernel(MaskedAttnArgs a) {
     store_act<T>((T*)a.o, (size_t)a.nq * HD, i, a.M, a.split, h * HD + lane + 32 * e, o[e] * inv);
 }
 
+// =====================================================================================
+// Training-style masked attention on tensor cores (mma.sync m16n8k16, bf16 hi/lo parts
+// of Q and P, fp32 accumulation, online softmax in the log2 domain).  A CTA serves a
+// block of MASK_QROWS(G) consecutive rows for kv head g; its 64 MMA rows are the
+// (row, q head of group g) pairs.  Keys arrive as two runs of 64-key tiles:
+//   A  depth-1 rows by position, 0 .. the largest anchor p-d+1 of the block; row i sees
+//      position p' when p' <= p_i - d_i + 1
+//   B  all rows from the first row at position (smallest anchor + 1) to the block's
+//      last row; row i sees row (p', d') when d' >= 2, p' - d' = p_i - d_i, d' <= d_i
+//      (its chain rows (p_i - j, d_i - j), itself included)
+// Together the two runs hold every key the mask allows, each once (a depth-1 key is
+// only ever seen through run A).  Blocks run last-first: later rows have the longest
+// prefixes, so the long CTAs start in the first wave.
+// =====================================================================================
+constexpr int MASK_MMA_ROWS = 64;  // 4 warps x 16
+
+template <int HD>
+__global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) {
+  constexpr int ROWB = HD * 2;
+  constexpr int CH = ROWB / 16;
+  constexpr int TILEB = MMA_KT * ROWB;
+  constexpr int ND = HD / 8;
+  constexpr int KS = HD / 16;
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  __shared__ int s_kp[2][MMA_KT], s_kd[2][MMA_KT];
+  __shared__ int s_aend, s_amin, s_jb0;
+  pdl_enter();
+  const int G = a.nq / a.nkv;
+  const int QR = MASK_MMA_ROWS / G;
+  const int i0 = (int)(gridDim.x - 1 - blockIdx.x) * QR;
+  const int g = blockIdx.y;
+  const int iend = min(a.M, i0 + QR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  auto row_ok = [&](int p, int d) {
+    return p >= 0 && p < a.n && d >= 1 && d <= a.Kmax && p - d + 1 >= 0;
+  };
+  if (threadIdx.x == 0) {
+    s_aend = -1;
+    s_amin = 0x7fffffff;
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < iend - i0) {
+    const int p = a.row_p[i0 + threadIdx.x], d = a.row_d[i0 + threadIdx.x];
+    if (row_ok(p, d)) {
+      atomicMax(&s_aend, p - d + 1);
+      atomicMin(&s_amin, p - d + 1);
+    }
+  }
+  __syncthreads();
+  const int a_end = s_aend;
+  if (threadIdx.x == 0) {
+    // run B starts at the first row whose position exceeds the smallest anchor
+    // (rows are p-major; a violated order is reported by the row check and only
+    // changes which in-range rows are read)
+    int lo = 0, hi = iend;
+    const int P0 = s_amin + 1;
+    if (a_end >= 0) {
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a.row_p[mid] < P0) lo = mid + 1; else hi = mid;
+      }
+    } else {
+      lo = iend;
+    }
+    s_jb0 = lo;
+  }
+  __syncthreads();
+  const int jb0 = s_jb0;
+  const int ntA = a_end >= 0 ? a_end / MMA_KT + 1 : 0;
+  const int ntB = (iend - jb0 + MMA_KT - 1) / MMA_KT;
+  const int ntile = ntA + ntB;
+
+  const bf16* K1 = (const bf16*)a.k1 + (size_t)g * HD;
+  const bf16* V1 = (const bf16*)a.v1 + (size_t)g * HD;
+  const bf16* KR = (const bf16*)a.k + (size_t)g * HD;
+  const bf16* VR = (const bf16*)a.v + (size_t)g * HD;
+  const size_t kstride = (size_t)a.nkv * HD;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm_raw);
+  auto tile_k = [&](int buf) { return sbase + (uint32_t)(buf * 2 * TILEB); };
+  auto tile_v = [&](int buf) { return sbase + (uint32_t)(buf * 2 * TILEB + TILEB); };
+  auto load_tile = [&](int buf, int it) {
+    const bool runA = it < ntA;
+    const int t0 = runA ? it * MMA_KT : jb0 + (it - ntA) * MMA_KT;
+    const int lim = runA ? a_end + 1 : iend;  // exclusive end of the run
+    const bf16* ks = runA ? K1 : KR;
+    const bf16* vs = runA ? V1 : VR;
+    for (int idx = threadIdx.x; idx < MMA_KT * CH; idx += blockDim.x) {
+      const int r = idx / CH, ch = idx - r * CH;
+      const int key = t0 + r;
+      const bool ok = key < lim;
+      const size_t off = (size_t)(ok ? key : t0) * kstride + ch * 8;
+      const uint32_t so = (uint32_t)(r * ROWB + ((ch ^ (r & 7)) * 16));
+      cp_async16(tile_k(buf) + so, ks + off, ok ? 16 : 0);
+      cp_async16(tile_v(buf) + so, vs + off, ok ? 16 : 0);
+    }
+    if (!runA && threadIdx.x < MMA_KT) {
+      const int key = t0 + threadIdx.x;
+      const bool ok = key < lim;
+      s_kp[buf][threadIdx.x] = ok ? a.row_p[key] : 0;
+      s_kd[buf][threadIdx.x] = ok ? a.row_d[key] : 0;
+    }
+    cp_async_commit();
+  };
+  if (ntile > 0) load_tile(0, 0);
+
+  // this thread's two MMA rows: (query row, q head) and its mask parameters
+  const float qscale = a.scale * 1.4426950408889634f;
+  const int r0 = warp * 16 + gq, r1 = r0 + 8;
+  const int qi0 = i0 + r0 / G, qi1 = i0 + r1 / G;
+  const bool in0 = r0 < QR * G && qi0 < iend, in1 = r1 < QR * G && qi1 < iend;
+  const int h0 = g * G + r0 % G, h1 = g * G + r1 % G;
+  int lim0 = -1, lim1 = -1, dg0 = 0, dg1 = 0, dd0 = 0, dd1 = 0;  // anchor, p - d, d
+  if (in0) {
+    const int p = a.row_p[qi0], d = a.row_d[qi0];
+    if (row_ok(p, d)) { lim0 = p - d + 1; dg0 = p - d; dd0 = d; }
+  }
+  if (in1) {
+    const int p = a.row_p[qi1], d = a.row_d[qi1];
+    if (row_ok(p, d)) { lim1 = p - d + 1; dg1 = p - d; dd1 = d; }
+  }
+  const float* qg = (const float*)a.q;
+  const float* q0 = qg + ((size_t)(in0 ? qi0 : 0) * a.nq + h0) * HD;
+  const float* q1 = qg + ((size_t)(in1 ? qi1 : 0) * a.nq + h1) * HD;
+  uint32_t qa_hi[KS][4], qa_lo[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const int d0 = ks * 16 + 2 * tq, d1 = d0 + 8;
+    float x[8];
+    x[0] = in0 ? q0[d0] * qscale : 0.f;
+    x[1] = in0 ? q0[d0 + 1] * qscale : 0.f;
+    x[2] = in1 ? q1[d0] * qscale : 0.f;
+    x[3] = in1 ? q1[d0 + 1] * qscale : 0.f;
+    x[4] = in0 ? q0[d1] * qscale : 0.f;
+    x[5] = in0 ? q0[d1 + 1] * qscale : 0.f;
+    x[6] = in1 ? q1[d1] * qscale : 0.f;
+    x[7] = in1 ? q1[d1 + 1] * qscale : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) split2(x[2 * u], x[2 * u + 1], qa_hi[ks][u], qa_lo[ks][u]);
+  }
+  float o[ND][4];
+#pragma unroll
+  for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const bool active = warp * 16 < QR * G && i0 + (warp * 16) / G < iend;
+
+  for (int it = 0; it < ntile; ++it) {
+    const int buf = it & 1;
+    if (it + 1 < ntile) {
+      load_tile(buf ^ 1, it + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (active) {
+      float sc[8][4];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          const int mat = lane >> 3, rr = lane & 7;
+          const int key = np * 16 + ((mat >> 1) << 3) + rr;
+          const int ch = ks * 2 + (mat & 1);
+          const uint32_t addr = tile_k(buf) + (uint32_t)(key * ROWB + ((ch ^ (key & 7)) * 16));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma16816(sc[2 * np], qa_hi[ks], b0, b1);
+          mma16816(sc[2 * np], qa_lo[ks], b0, b1);
+          mma16816(sc[2 * np + 1], qa_hi[ks], b2, b3);
+          mma16816(sc[2 * np + 1], qa_lo[ks], b2, b3);
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (it < ntA) {
+        const int t0 = it * MMA_KT;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const int kp = t0 + n * 8 + 2 * tq;
+          sc[n][0] = kp <= lim0 ? sc[n][0] : -INFINITY;
+          sc[n][1] = kp + 1 <= lim0 ? sc[n][1] : -INFINITY;
+          sc[n][2] = kp <= lim1 ? sc[n][2] : -INFINITY;
+          sc[n][3] = kp + 1 <= lim1 ? sc[n][3] : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kk = n * 8 + 2 * tq + e;
+            const int kp = s_kp[buf][kk], kd = s_kd[buf][kk];
+            const bool c0 = kd >= 2 && kp - kd == dg0 && kd <= dd0;
+            const bool c1 = kd >= 2 && kp - kd == dg1 && kd <= dd1;
+            sc[n][e] = c0 ? sc[n][e] : -INFINITY;
+            sc[n][2 + e] = c1 ? sc[n][2 + e] : -INFINITY;
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float cr0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - base0);
+      const float cr1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - base1);
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        sc[n][0] = exp2f(sc[n][0] - base0);
+        sc[n][1] = exp2f(sc[n][1] - base0);
+        sc[n][2] = exp2f(sc[n][2] - base1);
+        sc[n][3] = exp2f(sc[n][3] - base1);
+        ps0 += sc[n][0] + sc[n][1];
+        ps1 += sc[n][2] + sc[n][3];
+      }
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+      l0 = l0 * cr0 + ps0;
+      l1 = l1 * cr1 + ps1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int n = 0; n < ND; ++n) {
+        o[n][0] *= cr0;
+        o[n][1] *= cr0;
+        o[n][2] *= cr1;
+        o[n][3] *= cr1;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ph[4], pl[4];
+        split2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+        split2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+        split2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+        split2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int dp = 0; dp < ND / 2; ++dp) {
+          const int mat = lane >> 3, rr = lane & 7;
+          const int key = kk * 16 + ((mat & 1) << 3) + rr;
+          const int ch = dp * 2 + (mat >> 1);
+          const uint32_t addr = tile_v(buf) + (uint32_t)(key * ROWB + ((ch ^ (key & 7)) * 16));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma16816(o[2 * dp], ph, b0, b1);
+          mma16816(o[2 * dp], pl, b0, b1);
+          mma16816(o[2 * dp + 1], ph, b2, b3);
+          mma16816(o[2 * dp + 1], pl, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // normalised output (rows outside the contract see no key and store zeros)
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
+  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  bf16* out = (bf16*)a.o;
+  const size_t ld = (size_t)a.nq * HD;
+#pragma unroll
+  for (int n = 0; n < ND; ++n) {
+    const int d = n * 8 + 2 * tq;
+    if (in0) {
+      store_act<bf16>(out, ld, qi0, a.M, a.split, h0 * HD + d, o[n][0] * inv0);
+      store_act<bf16>(out, ld, qi0, a.M, a.split, h0 * HD + d + 1, o[n][1] * inv0);
+    }
+    if (in1) {
+      store_act<bf16>(out, ld, qi1, a.M, a.split, h1 * HD + d, o[n][2] * inv1);
+      store_act<bf16>(out, ld, qi1, a.M, a.split, h1 * HD + d + 1, o[n][3] * inv1);
+    }
+  }
+}
+
+template <int HD>
+static void masked_mma_launch(const MaskedAttnArgs& a, cudaStream_t s) {
+  const int G = a.nq / a.nkv;
+  const int QR = MASK_MMA_ROWS / G;
+  const size_t sm = (size_t)4 * MMA_KT * HD * 2;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(masked_attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm);
+    attr_set = true;
+  }
+  dim3 grid((unsigned)cdiv(a.M, QR), (unsigned)a.nkv);
+  launch_pdl(masked_attn_mma_kernel<HD>, grid, dim3(128), sm, s, a);
+}
+
 void launch_masked_attention(bool bf16m, const MaskedAttnArgs& a, cudaStream_t s) {
   const long warps = (long)a.M * a.nq;
   dim3 grid((unsigned)((warps + 7) / 8));
   if (bf16m) {
-    if (a.hd == 64) launch_pdl(masked_attn_kernel<bf16, 64>, grid, dim3(256), 0, s, a);
-    else launch_pdl(masked_attn_kernel<bf16, 128>, grid, dim3(256), 0, s, a);
+    if (a.hd == 64) masked_mma_launch<64>(a, s); else masked_mma_launch<128>(a, s);
   } else {
     if (a.hd == 64) masked_attn_kernel<float, 64><<<grid, 256, 0, s>>>(a);
     else masked_attn_kernel<float, 128><<<grid, 256, 0, s>>>(a);
@@ -879,12 +1175,15 @@ __global__ void rows_scatter_kernel(int M, int n, int K, int Kmax, const int* ro
     if (ok) row_index[(size_t)p * (Kmax + 1) + d] = i; else raise_error(err, PEAGLE_DEV_BAD_ROW);
   }
 }
-__global__ void rows_check_kernel(int M, int Kmax, const int* row_p, const int* row_d,
+__global__ void rows_check_kernel(int M, int n, int Kmax, const int* row_p, const int* row_d,
                                   const int* row_index, unsigned* err) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += gridDim.x * blockDim.x) {
     const int p = row_p[i], d = row_d[i];
-    if (d >= 2 && p >= 1 && d <= Kmax + 1) {
-      if (row_index[(size_t)(p - 1) * (Kmax + 1) + (d - 1)] < 0) raise_error(err, PEAGLE_DEV_BAD_ROW);
+    // dependency closure: (p-1, d-1) for d >= 2 (its chain down to the anchor row), and
+    // (p-1, 1) for d = 1 (so every depth-1 row up to each anchor is present)
+    if (p >= 1 && p <= n && d >= 1 && d <= Kmax) {
+      const int dp = d >= 2 ? d - 1 : 1;
+      if (row_index[(size_t)(p - 1) * (Kmax + 1) + dp] < 0) raise_error(err, PEAGLE_DEV_BAD_ROW);
     }
   }
 }
@@ -895,7 +1194,7 @@ void launch_rows_prepare(int M, int n, int K, int Kmax, const int* row_p, const 
   rows_fill_kernel<<<cdiv(total, 256) < 1024 ? cdiv(total, 256) : 1024, 256, 0, s>>>(total, row_index);
   const int gb = cdiv(M, 256) < 1024 ? cdiv(M, 256) : 1024;
   rows_scatter_kernel<<<gb > 0 ? gb : 1, 256, 0, s>>>(M, n, K, Kmax, row_p, row_d, row_index, err);
-  rows_check_kernel<<<gb > 0 ? gb : 1, 256, 0, s>>>(M, Kmax, row_p, row_d, row_index, err);
+  rows_check_kernel<<<gb > 0 ? gb : 1, 256, 0, s>>>(M, n, Kmax, row_p, row_d, row_index, err);
 }
 
 // =====================================================================================

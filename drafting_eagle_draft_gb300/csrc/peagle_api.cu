@@ -135,6 +135,8 @@ static int validate_dims(const peagle_dims* d) {
   if (d->max_K > 16 || d->max_batch * d->max_K > 256) return PEAGLE_ERR_CAPACITY;
   if (d->max_K * (d->n_q_heads / d->n_kv_heads) > 128) return PEAGLE_ERR_UNSUPPORTED;
   if (d->max_rows > 0 && d->max_seq <= 0) return PEAGLE_ERR_INVALID;
+  // the masked attention tile holds 64 (row, q head) pairs of one kv head
+  if (d->max_rows > 0 && d->n_q_heads / d->n_kv_heads > 64) return PEAGLE_ERR_UNSUPPORTED;
   return PEAGLE_OK;
 }
 

@@ -58,7 +58,8 @@ typedef struct peagle_ctx peagle_ctx;
 /* Drafter dimensions.  Constraints (else PEAGLE_ERR_UNSUPPORTED):
  *   head_dim in {64, 128}; n_q_heads % n_kv_heads == 0; hidden % 64 == 0, <= 16384;
  *   intermediate % 64 == 0; (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0;
- *   max_batch * max_K <= 256; max_K <= 16. */
+ *   max_batch * max_K <= 256; max_K <= 16; max_K * (n_q_heads / n_kv_heads) <= 128;
+ *   n_q_heads / n_kv_heads <= 64 when max_rows > 0. */
 typedef struct peagle_dims {
   int32_t hidden;        /* H                                                     */
   int32_t n_layers;      /* N decoder layers                                      */
@@ -168,8 +169,10 @@ int peagle_append_kv(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv, int32_
  * depths 1-based, sorted p-major (by p, then d).  Row (p, 1) takes
  * embed[tokens[p]] and fc(hidden[p]); row (p, d >= 2) takes emb(mask) and
  * fc(h_shared).  RoPE position p.  Row (p, d) attends depth-1 rows p' <= p - d + 1,
- * its chain (p - j, d - j), j = 1 .. d-1, and itself; every chain row must be in the
- * set (COD sampling guarantees it).
+ * its chain (p - j, d - j), j = 1 .. d-1, and itself.  The row set must be closed under
+ * these dependencies: (p-1, d-1) present for every row with d >= 2, and (p-1, 1) for
+ * every depth-1 row with p >= 1 (COD sampling, a prefix p < P0 and a dependency closure
+ * all are); a row outside the contract sets BAD_ROW and its outputs are unspecified.
  *   n, K      sequence length (<= max_seq) and depth (<= 16)
  *   tokens    device int32 [n]; hidden device [n, 3H] (dims dtype)
  *   row_p, row_d device int32 [M]; M <= max_rows

@@ -46,6 +46,10 @@ def _compare(dims, ref_logits, ref_am, ref_margin, am, lg, what):
     (SMALL_BF16, 40, 8, 0.8),
     (SMALL_HD128, 30, 3, 0.7),
     (SMALL_BF16, 1, 4, 0.8),
+    # every depth kept at K = 16: a block's chain-key window spans several 64-key tiles
+    (SMALL_BF16, 120, 16, 1.0),
+    # several 64-key tiles of depth-1 keys, head_dim 128
+    (SMALL_HD128, 150, 8, 0.9),
 ])
 def test_forward_parallel_small(dims, n, K, r):
     m = pk()
@@ -79,6 +83,47 @@ def test_forward_parallel_rejects_bad_rows():
     am = torch.empty(M, dtype=torch.int32, device="cuda")
     m.peagle_forward_parallel(ctx, n, K, torch.from_numpy(tokens).cuda(), hidden.cuda(),
                               torch.from_numpy(rp).cuda(), torch.from_numpy(rd).cuda(), M, am)
+    assert m.peagle_status(ctx) == m.PEAGLE_ERR_DEVICE
+    assert m.peagle_device_error_bits(ctx) & m.PEAGLE_DEV_BAD_ROW
+    ctx.close()
+
+
+def test_forward_parallel_dependency_closure():
+    """A closed row set that is not a COD set: the dependency closure of a few deep rows
+    (depth-1 rows up to their anchors, their chains), inside a longer sequence whose last
+    positions have no depth-1 row at all."""
+    dims = SMALL_BF16
+    n, K = 160, 8
+    w = synth.make_weights(dims, 31)
+    tokens = synth.uniform_ints(n, 0, dims.target_vocab, 7)
+    hidden = synth.normal((n, 3 * dims.hidden), 8, 1.0, dims.torch_dtype)
+    full = np.array([(p, d) for p in range(n) for d in range(1, K + 1) if p - d + 1 >= 0],
+                    np.int64)
+    targets = np.array([(150, 8), (151, 5), (99, 4), (152, 2)], np.int64)
+    clo = O.dependency_closure(full, targets)
+    rp = clo[:, 0].astype(np.int32)
+    rd = clo[:, 1].astype(np.int32)
+    ctx = make_ctx(dims, w, 1, K, n, max_rows=len(rp), max_seq=n)
+    am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
+    ctx.close()
+    W = O.Weights64.from_synth(w)
+    rl, ra, rm = O.forward_parallel(W, dims, tokens, hidden, clo, bf16=O.DRAFT_BF16_CASTS)
+    _compare(dims, rl, ra, rm, am, lg, "fwd dependency closure")
+
+
+def test_forward_parallel_rejects_missing_depth1_row():
+    m = pk()
+    dims = SMALL_BF16
+    w = synth.make_weights(dims, 3)
+    n, K = 8, 4
+    tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
+    hidden = synth.normal((n, 3 * dims.hidden), 4, 1.0, dims.torch_dtype)
+    rp = np.array([0, 2, 3], np.int32)  # (2,1) without (1,1)
+    rd = np.array([1, 1, 1], np.int32)
+    ctx = make_ctx(dims, w, 1, K, 16, max_rows=16, max_seq=n)
+    am = torch.empty(3, dtype=torch.int32, device="cuda")
+    m.peagle_forward_parallel(ctx, n, K, torch.from_numpy(tokens).cuda(), hidden.cuda(),
+                              torch.from_numpy(rp).cuda(), torch.from_numpy(rd).cuda(), 3, am)
     assert m.peagle_status(ctx) == m.PEAGLE_ERR_DEVICE
     assert m.peagle_device_error_bits(ctx) & m.PEAGLE_DEV_BAD_ROW
     ctx.close()
