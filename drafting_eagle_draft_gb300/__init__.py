@@ -32,7 +32,8 @@ PEAGLE_BF16 = 1
 # every entry point declared in include/peagle.h
 EXPORTS = ("peagle_create", "peagle_draft", "peagle_verify_greedy", "peagle_append_kv",
            "peagle_forward_parallel", "peagle_cod_rows", "peagle_status",
-           "peagle_set_timing", "peagle_read_timing", "peagle_decode_attention_static",
+           "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
+           "peagle_decode_attention_static",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
 STAGES = ("fc", "qkv", "attn", "oproj", "gate_up", "down", "lm_head", "norm", "small")
 
@@ -93,6 +94,8 @@ def lib():
         L.peagle_decode_attention_static.argtypes = [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                                      _i32, _vp, _vp, _vp]
         L.peagle_read_timing.argtypes = [_vp, _vp, _vp]
+        L.peagle_read_pass_trace.argtypes = [_vp, _vp, _i32, _vp, _vp]
+        L.peagle_read_pass_trace.restype = _i32
         L.peagle_device_error_bits.argtypes = [_vp]
         L.peagle_device_error_bits.restype = _i32
         L.peagle_strerror.argtypes = [ctypes.c_int]
@@ -262,6 +265,23 @@ def peagle_read_timing(ctx: Context) -> dict:
     _check(lib().peagle_read_timing(ctx.handle, ms.ctypes.data, n.ctypes.data),
            "peagle_read_timing")
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(STAGES)}
+
+
+def peagle_read_pass_trace(ctx: Context):
+    """Per-CTA event times (ns) of every step of the latest pass-kernel call run with
+    timing enabled, as an int64 array [phases, ctas, 4] (activations ready, first MMA, last
+    accumulator, done; 0 where not applicable); None when none was traced."""
+    cap = 512 * 1024
+    buf = np.zeros(cap, np.uint64)
+    ph = ctypes.c_int32(0)
+    ct = ctypes.c_int32(0)
+    n = lib().peagle_read_pass_trace(ctx.handle, buf.ctypes.data, cap, ctypes.byref(ph),
+                                     ctypes.byref(ct))
+    if n < 0:
+        _check(n, "peagle_read_pass_trace")
+    if n == 0:
+        return None
+    return buf[:n].astype(np.int64).reshape(ph.value, ct.value, 4)
 
 
 def peagle_decode_attention_static(batch, K, n_q_heads, n_kv_heads, head_dim, q, k_cache,

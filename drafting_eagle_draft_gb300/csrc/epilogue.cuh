@@ -11,6 +11,8 @@
 //   RESID      residual stream += Y (o-proj, down-proj), fixed point
 //   SWIGLU     act = silu(gate) * up, with gate/up rows interleaved in 64-row blocks
 //   LMHEAD     optional fp32 logits + per-row argmax folded into a 64-bit atomicMax key
+//   QKV_FX     RoPE'd q and k, and v, added into fixed-point accumulators (additive form of
+//              QKV_ROPE; a later step converts them and writes the KV cache)
 // A tile never splits a head (hd in {64, 128}, tiles start at multiples of 128) nor a
 // gate/up block, so each epilogue only needs its own tile.  STORE and RESID are additive:
 // every split-K contributor adds its own partial with integer atomics (see fx_t), so they
@@ -21,7 +23,14 @@
 
 namespace peagle {
 
-enum EpiKind : int { EPI_STORE = 0, EPI_QKV_ROPE = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_LMHEAD = 4 };
+enum EpiKind : int {
+  EPI_STORE = 0,
+  EPI_QKV_ROPE = 1,
+  EPI_RESID = 2,
+  EPI_SWIGLU = 3,
+  EPI_LMHEAD = 4,
+  EPI_QKV_FX = 5  // additive QKV: RoPE'd partials added into fixed-point q / k,v buffers
+};
 
 struct EpiArgs {
   int kind;
@@ -59,7 +68,19 @@ struct EpiArgs {
   float* logits;          // [R, Nout] or null
   unsigned long long* keys;  // [R]
   unsigned* err;
+  // QKV_FX: fixed-point accumulators q [R, nq*hd] and k,v [R][2][nkv*hd] (zero beforehand)
+  fx_t* q_fx;
+  fx_t* kv_fx;
+  // deferred RMSNorm: when row_ss is set, the operand rows hold x * gamma and row r's
+  // result is scaled by rsqrt(row_ss[r] * ss_inv_n + ss_eps) (row_ss: sum of x^2, fixed
+  // point).  Applies to QKV_FX, SWIGLU and LMHEAD.
+  const fx_t* row_ss;
+  float ss_inv_n, ss_eps;
 };
+
+__device__ __forceinline__ float epi_row_scale(const EpiArgs& a, int r) {
+  return a.row_ss ? rsqrtf(from_fx(a.row_ss[r]) * a.ss_inv_n + a.ss_eps) : 1.f;
+}
 
 // Store an activation that feeds the next projection: a single value, or its bf16
 // hi part at row r and the bf16 rounding of the remainder at row r + R.
@@ -74,16 +95,20 @@ __device__ __forceinline__ void store_act(T* base, size_t row_stride, int r, int
 // Apply the epilogue to rows r0 .. r0+rcount-1 of a 128-feature tile starting at m0.
 // The tile value of row r0+i, feature m0+ml is src[i*ld + ml], plus src[(i+lo_off)*ld + ml]
 // when lo_off >= 0 (the lo-part product of a split activation operand).
+// rscale / rpos (optional, e.g. in shared memory): row r0+i's norm scale and RoPE position
+// for i < rcount, gathered by the caller so the loops below issue no dependent loads.
 template <typename T>
 __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src, int ld,
                                               int lo_off, int m0, int r0, int rcount, int tid,
-                                              int nthr) {
+                                              int nthr, const float* rscale = nullptr,
+                                              const int* rpos = nullptr) {
   const int mcount = min(128, a.Nout - m0);
   auto val = [&](int i, int ml) -> float {
     float v = src[(size_t)i * ld + ml];
     if (lo_off >= 0) v += src[(size_t)(i + lo_off) * ld + ml];
     return v;
   };
+  auto rsc = [&](int i) -> float { return rscale ? rscale[i] : epi_row_scale(a, r0 + i); };
   switch (a.kind) {
     case EPI_STORE:
     case EPI_RESID: {
@@ -99,8 +124,9 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
       T* act = (T*)a.act_out;
       for (int idx = tid; idx < rcount * 64; idx += nthr) {
         int i = idx >> 6, f = idx & 63;
-        float g = val(i, f);
-        float u = val(i, 64 + f);
+        const float sc = rsc(i);
+        float g = val(i, f) * sc;
+        float u = val(i, 64 + f) * sc;
         float s = g / (1.f + expf(-g));
         store_act<T>(act, a.I, r0 + i, a.R, a.out_split, (m0 >> 1) + f, s * u);
       }
@@ -187,11 +213,56 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
       }
       }
     } break;
+    case EPI_QKV_FX: {
+      // RoPE is a rotation and the row scale a constant, so each split-K partial can be
+      // rotated, scaled and added on its own: the fixed-point sums are exact and the same
+      // for any order of arrival.  One output feature per thread; the RoPE factors of
+      // eight rows are fetched before any of them is used.
+      const int hd = a.hd, half = hd >> 1;
+      const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd, kvw = a.nkv * hd;
+      for (int ml = tid; ml < mcount; ml += nthr) {
+        const int m = m0 + ml;
+        const int i = m % hd;
+        const int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
+        if (sec != 2 && i >= half) continue;  // handled together with its pair partner
+        for (int t0 = 0; t0 < rcount; t0 += 8) {
+          float2 cs[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int ti = t0 + u;
+            int pos = -1;
+            if (sec != 2 && ti < rcount) pos = rpos ? rpos[ti] : __ldg(a.row_pos + r0 + ti);
+            cs[u] = (pos >= 0 && pos < a.max_pos) ? __ldg(a.rope + (size_t)pos * half + i)
+                                                  : make_float2(1.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int ti = t0 + u;
+            if (ti >= rcount) break;
+            const int r = r0 + ti;
+            const float sc = rsc(ti);
+            const float v0 = val(ti, ml) * sc;
+            if (sec == 2) {
+              red_add_fx(a.kv_fx + ((size_t)r * 2 + 1) * kvw + (m - kend), to_fx(v0));
+              continue;
+            }
+            const float v1 = val(ti, ml + half) * sc;
+            const float out0 = v0 * cs[u].x - v1 * cs[u].y;
+            const float out1 = v1 * cs[u].x + v0 * cs[u].y;
+            fx_t* dst = sec == 0 ? a.q_fx + (size_t)r * qend + m
+                                 : a.kv_fx + (size_t)r * 2 * kvw + (m - qend);
+            red_add_fx(dst, to_fx(out0));
+            red_add_fx(dst + half, to_fx(out1));
+          }
+        }
+      }
+    } break;
     case EPI_LMHEAD: {
       if (a.logits) {
         for (int idx = tid; idx < rcount * 128; idx += nthr) {
           int i = idx >> 7, ml = idx & 127;
-          if (ml < mcount) a.logits[(size_t)(r0 + i) * a.Nout + m0 + ml] = val(i, ml);
+          if (ml < mcount)
+            a.logits[(size_t)(r0 + i) * a.Nout + m0 + ml] = val(i, ml) * rsc(i);
         }
       }
       // per row: best (value, index) over the tile -> one atomicMax per warp and row
@@ -199,8 +270,9 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
       const int nw = nthr >> 5;
       for (int i = tid >> 5; i < rcount; i += nw) {
         unsigned long long best = 0ull;
+        const float sc = rsc(i);
         for (int ml = lane; ml < mcount; ml += 32) {
-          unsigned long long k = argmax_key(val(i, ml), m0 + ml);
+          unsigned long long k = argmax_key(val(i, ml) * sc, m0 + ml);
           best = k > best ? k : best;
         }
 #pragma unroll

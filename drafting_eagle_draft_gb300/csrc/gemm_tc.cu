@@ -397,6 +397,14 @@ static size_t smem_bytes(int stages, int bn) {
          (size_t)(2 * stages + 4) * 8 + 16;
 }
 
+bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
+                   int ld, int box_rows) {
+  return encode_map(p, out, base, rows, cols, ld, box_rows);
+}
+float* tc_partials(TcGemmPlan* p) { return p->ws; }
+unsigned* tc_tile_counters(TcGemmPlan* p) { return p->counters; }
+int tc_max_tiles(TcGemmPlan* p) { return p->max_tiles; }
+
 void tc_destroy(TcGemmPlan* p) {
   if (!p) return;
   if (p->ws) cudaFree(p->ws);
@@ -449,7 +457,7 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   p.Kd = Kd;
   p.R = R;
   p.split = epi.in_split ? 1 : 0;
-  p.additive = (epi.kind == EPI_STORE || epi.kind == EPI_RESID) ? 1 : 0;
+  p.additive = (epi.kind == EPI_STORE || epi.kind == EPI_RESID || epi.kind == EPI_QKV_FX) ? 1 : 0;
   const int xrows = p.split ? 2 * R : R;
   p.two_box = 0;
   if (p.split && 2 * R <= 240) {

@@ -1,6 +1,7 @@
 // Tensor-core (tcgen05 + TMEM + TMA) GEMM of the bf16 draft pass: host interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "epilogue.cuh"
@@ -20,5 +21,14 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
 int tc_gemm(TcGemmPlan* p, const void* W, const void* X, int ldx, int Nout, int Kd, int R,
             const EpiArgs& epi, cudaStream_t s);
 void tc_destroy(TcGemmPlan* p);
+
+// Pieces of the plan shared with the persistent pass kernel: a cached 2D bf16 tensor map
+// (box 64 columns x box_rows rows, 128-byte swizzle), the partial slots
+// [2 * num_sms][256][128] fp32 and the per-tile counters (zero between projections).
+bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
+                   int ld, int box_rows);
+float* tc_partials(TcGemmPlan* p);
+unsigned* tc_tile_counters(TcGemmPlan* p);
+int tc_max_tiles(TcGemmPlan* p);
 
 }  // namespace peagle

@@ -1,0 +1,99 @@
+// Persistent kernel of the bf16 draft pass: the whole pass (fc, input rows, N decoder
+// layers, LM head, argmax) as one launch of one CTA per SM.  Host-side description.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace peagle {
+
+constexpr int PASS_MAX_LAYERS = 8;
+constexpr int PASS_MAX_GEMM = 3 + 4 * PASS_MAX_LAYERS;
+constexpr int PASS_MAX_PHASE = 5 + 9 * PASS_MAX_LAYERS;
+constexpr int PASS_MAX_ROWS = 120;                    // R = B*K (hi + lo rows <= 240)
+constexpr int PASS_SS_SLOTS = 2 + 2 * PASS_MAX_LAYERS;  // per-row sums of squares
+
+// RMSNorm is split in two: a step spread over all CTAs writes x * gamma (the projection's
+// operand) and adds each row's sum of squares into a fixed-point slot; the consuming
+// projection's epilogue scales its rows by rsqrt(mean + eps).
+enum PassPhaseKind : int {
+  PP_GEMM = 0,    // a projection on the tensor cores (its epilogue writes the next input)
+  PP_INPUT = 1,   // NTP / MTP inputs: e * g_in, f * g_hid (+ sums of squares), residual = f
+  PP_ATTN = 2,    // split-KV attention items (request, kv head, key chunk) -> partials
+  PP_MERGE = 3,   // chunk partials -> O (one warp per query row)
+  PP_NORM = 4,    // residual -> x * gamma (+ sums of squares)
+  PP_ARGMAX = 5,  // LM-head argmax keys -> draft tokens (d2t applied)
+  PP_QKVFIN = 6   // fixed-point q -> fp32 queries, k / v -> bf16 KV cache slots
+};
+
+// One projection: stream-K over (128-feature tile, 64-wide k-block) iterations, single
+// activation box of BN rows (hi rows [0,R), lo rows [R,2R) when split).
+struct PassGemm {
+  int Nout, Kd, R, split, additive, BN, lo_col, n_tiles, KB, Gm, phase;
+  int dep;  // phase whose completion the activation operand waits for (-1: none)
+  uint32_t idesc;
+  long long total;
+  EpiArgs epi;
+};
+
+struct PassPhase {
+  int kind;
+  int stage;           // PEAGLE_STAGE_* the step is reported under (timing)
+  int gemm;            // PP_GEMM: index into PassParams::gemm
+  int layer;           // PP_ATTN / PP_MERGE / PP_QKVFIN: decoder layer
+  int slot;            // PP_NORM: sum-of-squares slot
+  const void* gamma;   // PP_NORM: norm gain
+};
+
+// Scalars and pointers first: the kernel reads them often, the per-projection arrays at
+// the end rarely (the block is ~22 KB of kernel parameters).
+struct PassParams {
+  int n_gemm, n_phase;
+  int stages, b_stage_bytes, acc_stride, tmem_cols, uni_bytes;
+  // shapes
+  int B, K, R, H, split, Vt, chunk, nchunk;
+  int nq, nkv, hd, cap;
+  float eps;
+  size_t layer_stride;
+  // library-owned buffers
+  const void* embed;
+  const void* emb_mask;
+  const void* input_norm;
+  const void* hidden_norm;
+  fx_t* F;
+  const fx_t* f_shared;
+  void* X0;
+  void* Xn;
+  fx_t* res;
+  fx_t* ss;              // [PASS_SS_SLOTS][R] row sums of squares (0: e, 1: f, 2..: norms)
+  fx_t* q_fx;            // [R, nq*hd] fixed-point queries of the current layer
+  fx_t* kv_fx;           // [R][2][nkv*hd] fixed-point keys / values of the current layer
+  float* Qf;             // [R, nq*hd] fp32 queries read by attention
+  unsigned long long* keys;
+  int* row_pos;
+  const int* d2t;
+  float* ws;             // stream-K partial slots
+  unsigned* tile_cnt;    // per-tile contributor counters (zero between projections)
+  unsigned* phase_cnt;   // [n_phase + 1]: phase completion counts, then the abort flag
+  unsigned* err;
+  unsigned long long* trace;  // timing: [0] start, [j+1] completion of phase j (ns), or null
+  unsigned long long* trace_cta;  // timing: [phase][CTA][4] event times, or null
+  // per call
+  const int* seq_lens;
+  const int* new_token;
+  int* out_tokens;
+  AttnArgs att;        // per layer: kc / vc advanced by layer_stride bytes
+  PassPhase ph[PASS_MAX_PHASE];
+  PassGemm gemm[PASS_MAX_GEMM];
+  CUtensorMap tm[2 * PASS_MAX_GEMM];  // per projection: weights, activations
+};
+
+// Bytes of dynamic shared memory the kernel needs for `stages` ring stages.
+size_t pass_smem_bytes(int stages, int b_stage_bytes, int uni_bytes);
+// Launches the pass on `grid` CTAs (one per SM, co-resident); PEAGLE_OK or an error code.
+int pass_launch(const PassParams& P, int head_dim, int grid, cudaStream_t s);
+
+}  // namespace peagle

@@ -11,8 +11,13 @@
 
 #include "gemm_tc.h"
 #include "kernels.h"
+#include "pass_kernel.h"
+#include "tc_ptx.cuh"
 
 using namespace peagle;
+
+// pass-kernel calls whose phase times one timing read can report
+constexpr int PASS_TRACE_SLOTS = 64;
 
 struct peagle_ctx {
   peagle_dims d;
@@ -48,6 +53,19 @@ struct peagle_ctx {
   unsigned* err;
   unsigned last_err_bits;
   TcGemmPlan* tc;   // tensor-core GEMM state (bf16 only)
+  // persistent pass kernel (bf16): phase counters + abort flag, host-side parameter block
+  bool pass_on;
+  unsigned* pass_cnt;
+  PassParams* pp;
+  // timing of the pass kernel: per-call phase completion times (device slots) and the
+  // stage of each phase (host)
+  fx_t* pass_ss;    // [PASS_SS_SLOTS][PASS_MAX_ROWS] row sums of squares
+  fx_t* pass_qfx;   // [PASS_MAX_ROWS, nq*hd] fixed-point queries
+  fx_t* pass_kvfx;  // [PASS_MAX_ROWS][2][nkv*hd] fixed-point keys / values
+  unsigned long long* pass_trace;
+  std::vector<std::vector<int>> trace_stages;
+  unsigned long long* pass_trace_cta;  // per-CTA signal times of the latest traced pass
+  int trace_cta_phases;
   std::vector<void*> allocs;
   // optional per-stage timing: CUDA events recorded around each launch on its stream
   bool timing;
@@ -116,6 +134,7 @@ static void free_ctx(peagle_ctx* c) {
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->tc) tc_destroy(c->tc);
+  delete c->pp;
   delete c;
 }
 
@@ -310,13 +329,35 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
       return PEAGLE_ERR_CUDA;
     }
   }
+  // the whole bf16 pass as one persistent kernel, unless disabled (PEAGLE_PASS_KERNEL=0)
+  c->pass_on = false;
+  c->pp = nullptr;
+  c->pass_cnt = nullptr;
+  if (c->bf && d.n_layers <= PASS_MAX_LAYERS) {
+    const char* env = getenv("PEAGLE_PASS_KERNEL");
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+    if (coop && !(env && env[0] == '0')) {
+      TRY(dalloc(c, (void**)&c->pass_cnt, (size_t)(PASS_MAX_PHASE + 1) * 4));
+      TRY(dalloc(c, (void**)&c->pass_trace,
+                 (size_t)PASS_TRACE_SLOTS * (PASS_MAX_PHASE + 1) * 8));
+      TRY(dalloc(c, (void**)&c->pass_trace_cta, (size_t)PASS_MAX_PHASE * c->num_sms * 4 * 8));
+      const size_t pr = (size_t)PASS_MAX_ROWS;
+      TRY(dalloc(c, (void**)&c->pass_ss, (size_t)PASS_SS_SLOTS * pr * 8));
+      TRY(dalloc(c, (void**)&c->pass_qfx, pr * nq * hd * 8));
+      TRY(dalloc(c, (void**)&c->pass_kvfx, pr * 2 * nkv * hd * 8));
+      c->pp = new PassParams();
+      c->pass_on = true;
+    }
+  }
 #undef TRY
   *out = c;
   return PEAGLE_OK;
 }
 
-static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchunk) {
-  const int target = 2 * c->num_sms;
+static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchunk,
+                           int waves = 2) {
+  const int target = waves * c->num_sms;
   const int pairs = B * c->d.n_kv_heads;
   int want = (target + pairs - 1) / pairs;
   if (want < 1) want = 1;
@@ -326,6 +367,254 @@ static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchun
   if (ch < 64) ch = 64;
   *chunk = ch;
   *nchunk = (cap + ch - 1) / ch;
+}
+
+// ---- the draft pass as one persistent kernel (bf16) --------------------------------------
+// Fills the kernel's parameter block with the same steps, epilogues and buffers as the
+// multi-kernel path below.  Returns PEAGLE_ERR_UNSUPPORTED for shapes it does not cover
+// (the caller then runs the multi-kernel path).
+static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* seq_lens,
+                      const void* target_hidden, const int32_t* new_token, int K,
+                      int32_t* out_tokens, float* out_logits, cudaStream_t s) {
+  const peagle_dims& d = c->d;
+  const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
+  const int R = B * K, G = nq / nkv;
+  if (R > PASS_MAX_ROWS || K * G > 64 || d.n_layers > PASS_MAX_LAYERS)
+    return PEAGLE_ERR_UNSUPPORTED;
+  PassParams& P = *c->pp;
+  P.n_gemm = 0;
+  P.n_phase = 0;
+  const int grid = c->num_sms;
+  int bn_max = 16;
+  bool fail = false;
+  int cur_stage = PEAGLE_STAGE_FC;
+  auto add_phase = [&](int kind, int layer, const void* gamma) {
+    if (P.n_phase >= PASS_MAX_PHASE) {
+      fail = true;
+      return;
+    }
+    PassPhase& ph = P.ph[P.n_phase++];
+    ph.kind = kind;
+    ph.stage = kind == PP_GEMM ? cur_stage
+               : (kind == PP_ATTN || kind == PP_MERGE) ? PEAGLE_STAGE_ATTN
+               : kind == PP_ARGMAX ? PEAGLE_STAGE_SMALL : PEAGLE_STAGE_NORM;
+    ph.gemm = -1;
+    ph.layer = layer;
+    ph.slot = 0;
+    ph.gamma = gamma;
+  };
+  // a projection Y = W X^T over the R draft rows (W [Nout, Kd] with row stride ldw);
+  // `dep`: the phase its activation operand waits for (default: the phase before it)
+  auto add_gemm = [&](const void* W, int ldw, const void* X, int ldx, int Nout, int Kd, int rows,
+                      int split, const EpiArgs& e, int dep) {
+    if (P.n_gemm >= PASS_MAX_GEMM || P.n_phase >= PASS_MAX_PHASE) {
+      fail = true;
+      return;
+    }
+    PassGemm& m = P.gemm[P.n_gemm];
+    m.Nout = Nout;
+    m.Kd = Kd;
+    m.R = rows;
+    m.split = split;
+    m.additive =
+        (e.kind == EPI_STORE || e.kind == EPI_RESID || e.kind == EPI_QKV_FX) ? 1 : 0;
+    m.BN = ((split ? 2 * rows : rows) + 15) / 16 * 16;
+    m.lo_col = split ? rows : 0;
+    m.n_tiles = 1;
+    m.KB = Kd / 64;
+    const long long tiles = (long long)((Nout + 127) / 128) * m.n_tiles;
+    m.total = tiles * m.KB;
+    m.Gm = (int)(m.total < grid ? m.total : grid);
+    m.idesc = tc::idesc_bf16(128, m.BN);
+    m.epi = e;
+    if (tiles > tc_max_tiles(c->tc) || Kd % 64 || m.BN > 240) fail = true;
+    if (!tc_tensor_map(c->tc, &P.tm[2 * P.n_gemm], W, Nout, Kd, ldw, 128) ||
+        !tc_tensor_map(c->tc, &P.tm[2 * P.n_gemm + 1], X, split ? 2 * rows : rows, Kd, ldx,
+                       m.BN))
+      fail = true;
+    if (m.BN > bn_max) bn_max = m.BN;
+    m.phase = P.n_phase;
+    m.dep = dep == -2 ? P.n_phase - 1 : dep;
+    add_phase(PP_GEMM, -1, nullptr);
+    P.ph[P.n_phase - 1].gemm = P.n_gemm++;
+  };
+  const int split = 1;
+  const int qkv_out = (nq + 2 * nkv) * hd;
+  const size_t es = c->es;
+  const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
+  int slot = 2;  // sum-of-squares slots: 0 = e, 1 = f, then one per RMSNorm
+  auto scaled = [&](EpiArgs& e, int sl) {
+    e.row_ss = c->pass_ss + (size_t)sl * R;
+    e.ss_inv_n = 1.f / (float)H;
+    e.ss_eps = d.rms_eps;
+  };
+  {
+    EpiArgs e = epi_base(c, EPI_STORE, B, H);
+    e.out_fx = c->F;
+    e.out_ld = H;
+    cur_stage = PEAGLE_STAGE_FC;
+    add_gemm(c->fc, 3 * H, target_hidden, 3 * H, H, 3 * H, B, 0, e, -1);
+  }
+  add_phase(PP_INPUT, -1, nullptr);
+  const int input_phase = P.n_phase - 1;
+  for (int l = 0; l < d.n_layers; ++l) {
+    EpiArgs e = epi_base(c, EPI_QKV_FX, R, qkv_out);
+    e.in_split = split;
+    e.q_fx = c->pass_qfx;
+    e.kv_fx = c->pass_kvfx;
+    e.row_pos = c->row_pos;
+    cur_stage = PEAGLE_STAGE_QKV;
+    if (l == 0) {
+      // the first layer's 2H input [e * g_in || f * g_hid] has a norm scale per half:
+      // two projections over the halves of W_qkv, each scaled by its own row sums
+      scaled(e, 0);
+      add_gemm(c->qkv[0], 2 * H, c->X0, 2 * H, qkv_out, H, R, split, e, input_phase);
+      scaled(e, 1);
+      add_gemm((const char*)c->qkv[0] + (size_t)H * es, 2 * H, (const char*)c->X0 + (size_t)H * es,
+               2 * H, qkv_out, H, R, split, e, input_phase);
+    } else {
+      add_phase(PP_NORM, l, c->attn_norm[l]);
+      P.ph[P.n_phase - 1].slot = slot;
+      scaled(e, slot++);
+      add_gemm(c->qkv[l], H, c->Xn, H, qkv_out, H, R, split, e, -2);
+    }
+    add_phase(PP_QKVFIN, l, nullptr);
+    add_phase(PP_ATTN, l, nullptr);
+    add_phase(PP_MERGE, l, nullptr);
+    {
+      EpiArgs eo = epi_base(c, EPI_RESID, R, H);
+      eo.in_split = split;
+      eo.resid = c->res;
+      cur_stage = PEAGLE_STAGE_OPROJ;
+      add_gemm(c->o[l], nq * hd, c->O, nq * hd, H, nq * hd, R, split, eo, -2);
+    }
+    add_phase(PP_NORM, l, c->post_norm[l]);
+    P.ph[P.n_phase - 1].slot = slot;
+    {
+      EpiArgs eg = epi_base(c, EPI_SWIGLU, R, 2 * d.intermediate);
+      eg.in_split = split;
+      eg.out_split = split;
+      eg.act_out = c->act;
+      scaled(eg, slot++);
+      cur_stage = PEAGLE_STAGE_GATEUP;
+      add_gemm(c->gate_up[l], H, c->Xn, H, 2 * d.intermediate, H, R, split, eg, -2);
+    }
+    {
+      EpiArgs ed = epi_base(c, EPI_RESID, R, H);
+      ed.in_split = split;
+      ed.resid = c->res;
+      cur_stage = PEAGLE_STAGE_DOWN;
+      add_gemm(c->down[l], d.intermediate, c->act, d.intermediate, H, d.intermediate, R, split,
+               ed, -2);
+    }
+  }
+  add_phase(PP_NORM, -1, c->final_norm);
+  P.ph[P.n_phase - 1].slot = slot;
+  {
+    EpiArgs e = epi_base(c, EPI_LMHEAD, R, d.draft_vocab);
+    e.in_split = split;
+    e.logits = out_logits;
+    e.keys = c->keys;
+    scaled(e, slot++);
+    cur_stage = PEAGLE_STAGE_LMHEAD;
+    add_gemm(c->lm_head, H, c->Xn, H, d.draft_vocab, H, R, split, e, -2);
+  }
+  add_phase(PP_ARGMAX, -1, nullptr);
+  if (slot > PASS_SS_SLOTS) fail = true;
+  if (fail) return PEAGLE_ERR_UNSUPPORTED;
+
+  P.b_stage_bytes = bn_max * 128;
+  P.acc_stride = bn_max + 16;
+  uint32_t tc_cols = 32;
+  while (tc_cols < (uint32_t)(2 * P.acc_stride)) tc_cols <<= 1;
+  if (tc_cols > 512) return PEAGLE_ERR_UNSUPPORTED;
+  P.tmem_cols = (int)tc_cols;
+  const int att_bytes = 4 * 64 * hd * 2;
+  P.uni_bytes = att_bytes > 32 * 128 * 4 ? att_bytes : 32 * 128 * 4;
+  // dynamic shared memory: the 227 KB per-block limit minus the kernel's static part
+  const size_t smem_cap = 223 * 1024;
+  int stages = 2;
+  while (stages < 16 && pass_smem_bytes(stages + 1, P.b_stage_bytes, P.uni_bytes) <= smem_cap)
+    ++stages;
+  if (pass_smem_bytes(stages, P.b_stage_bytes, P.uni_bytes) > smem_cap)
+    return PEAGLE_ERR_UNSUPPORTED;
+  P.stages = stages;
+  P.B = B;
+  P.K = K;
+  P.R = R;
+  P.H = H;
+  P.split = split;
+  P.Vt = d.target_vocab;
+  P.eps = d.rms_eps;
+  // one attention item per CTA: each CTA streams its chunk's tiles back to back
+  int chunk, nchunk;
+  attention_plan(c, B, kv->capacity, &chunk, &nchunk, 1);
+  P.chunk = chunk;
+  P.nchunk = nchunk;
+  AttnArgs& a = P.att;
+  a.q = c->Qf;
+  a.split = split;
+  a.kc = kv->k;
+  a.vc = kv->v;
+  a.seq_lens = seq_lens;
+  a.o = c->O;
+  a.part = c->att_part;
+  a.counters = c->att_cnt;
+  a.B = B;
+  a.K = K;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.hd = hd;
+  a.cap = kv->capacity;
+  a.chunk = chunk;
+  a.nchunk = nchunk;
+  a.scale = 1.f / sqrtf((float)hd);
+  a.err = c->err;
+  P.layer_stride = layer_stride;
+  P.embed = c->embed;
+  P.emb_mask = c->emb_mask;
+  P.input_norm = c->input_norm;
+  P.hidden_norm = c->hidden_norm;
+  P.F = c->F;
+  P.f_shared = c->f_shared;
+  P.X0 = c->X0;
+  P.Xn = c->Xn;
+  P.res = c->res;
+  P.ss = c->pass_ss;
+  P.q_fx = c->pass_qfx;
+  P.kv_fx = c->pass_kvfx;
+  P.Qf = c->Qf;
+  P.nq = nq;
+  P.nkv = nkv;
+  P.hd = hd;
+  P.cap = kv->capacity;
+  P.keys = c->keys;
+  P.row_pos = c->row_pos;
+  P.d2t = c->d2t;
+  P.ws = tc_partials(c->tc);
+  P.tile_cnt = tc_tile_counters(c->tc);
+  P.phase_cnt = c->pass_cnt;
+  P.err = c->err;
+  P.seq_lens = seq_lens;
+  P.new_token = new_token;
+  P.out_tokens = out_tokens;
+  P.trace = nullptr;
+  P.trace_cta = nullptr;
+  if (c->timing && c->trace_stages.size() < (size_t)PASS_TRACE_SLOTS) {
+    P.trace_cta = c->pass_trace_cta;
+    c->trace_cta_phases = P.n_phase;
+    cudaError_t ze = cudaMemsetAsync(c->pass_trace_cta, 0, (size_t)P.n_phase * grid * 4 * 8, s);
+    if (ze != cudaSuccess) return cuda_fail(ze, "pass trace");
+    P.trace = c->pass_trace + c->trace_stages.size() * (PASS_MAX_PHASE + 1);
+    std::vector<int> st(P.n_phase);
+    for (int j = 0; j < P.n_phase; ++j) st[j] = P.ph[j].stage;
+    c->trace_stages.push_back(st);
+    cudaError_t te = cudaMemsetAsync(P.trace, 0, (size_t)(PASS_MAX_PHASE + 1) * 8, s);
+    if (te != cudaSuccess) return cuda_fail(te, "pass trace");
+  }
+  cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, (size_t)(P.n_phase + 1) * 4, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "pass counters");
+  return pass_launch(P, hd, grid, s);
 }
 
 extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
@@ -346,6 +635,11 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   const int split = use_split(c);
   const size_t es = c->es;
   const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
+  if (c->pass_on) {
+    const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K,
+                             out_draft_tokens, out_logits, s);
+    if (r != PEAGLE_ERR_UNSUPPORTED) return r;
+  }
 
   // S1: fc over the NTP rows' target hidden states, then the fused input rows
   {
@@ -643,6 +937,7 @@ extern "C" int peagle_set_timing(peagle_ctx* c, int32_t enable) {
   }
   c->timing = enable != 0;
   c->ev_used = 0;
+  c->trace_stages.clear();
   return PEAGLE_OK;
 }
 
@@ -662,7 +957,40 @@ extern "C" int peagle_read_timing(peagle_ctx* c, float* stage_ms, int32_t* stage
     stage_launches[st] += 1;
   }
   c->ev_used = 0;
+  // pass-kernel calls: the time from one phase's completion to the next is attributed to
+  // the later phase's stage (one "launch" per phase)
+  if (!c->trace_stages.empty()) {
+    const size_t n = c->trace_stages.size();
+    std::vector<unsigned long long> t(n * (PASS_MAX_PHASE + 1));
+    if (cudaMemcpy(t.data(), c->pass_trace, t.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    for (size_t k = 0; k < n; ++k) {
+      const unsigned long long* tk = t.data() + k * (PASS_MAX_PHASE + 1);
+      const std::vector<int>& st = c->trace_stages[k];
+      for (size_t j = 0; j < st.size(); ++j) {
+        const double ms = tk[j + 1] > tk[j] ? (double)(tk[j + 1] - tk[j]) * 1e-6 : 0.0;
+        stage_ms[st[j]] += (float)ms;
+        stage_launches[st[j]] += 1;
+      }
+    }
+    c->trace_stages.clear();
+  }
   return PEAGLE_OK;
+}
+
+extern "C" int32_t peagle_read_pass_trace(peagle_ctx* c, uint64_t* out, int32_t max_entries,
+                                          int32_t* out_phases, int32_t* out_ctas) {
+  if (!c || !out || max_entries < 0 || !out_phases || !out_ctas) return PEAGLE_ERR_INVALID;
+  *out_phases = 0;
+  *out_ctas = 0;
+  if (!c->pass_on || c->trace_cta_phases <= 0) return 0;
+  const int n = c->trace_cta_phases * c->num_sms * 4;
+  if (n > max_entries) return PEAGLE_ERR_CAPACITY;
+  if (cudaMemcpy(out, c->pass_trace_cta, (size_t)n * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PEAGLE_ERR_CUDA;
+  *out_phases = c->trace_cta_phases;
+  *out_ctas = c->num_sms;
+  return n;
 }
 
 extern "C" int32_t peagle_device_error_bits(const peagle_ctx* c) {

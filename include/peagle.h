@@ -218,6 +218,18 @@ int peagle_set_timing(peagle_ctx* ctx, int32_t enable);
  * stage (arrays of PEAGLE_NUM_STAGES) since the previous read, and reset them. */
 int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches);
 
+/* Diagnostics of the persistent pass kernel (the bf16 draft pass as one launch of one CTA
+ * per SM, used unless the environment variable PEAGLE_PASS_KERNEL=0 was set when the
+ * context was created).  For the latest pass run while timing was enabled, writes four
+ * globaltimer values (ns) per step of the pass and CTA, as out[(phase * ctas + cta) * 4 + k]:
+ * k = 0 the step's activations were seen ready, 1 its first MMA was issued, 2 its last
+ * accumulator was committed (projections only, else 0), 3 the CTA finished the step; and
+ * the two sizes.  Returns the number of entries (0 if no pass was traced),
+ * PEAGLE_ERR_CAPACITY if max_entries is too small.  The paper has no counterpart: this
+ * reports how this library schedules the pass. */
+int32_t peagle_read_pass_trace(peagle_ctx* ctx, uint64_t* out, int32_t max_entries,
+                               int32_t* out_phases, int32_t* out_ctas);
+
 /* Size of the library's static scratch array used by peagle_decode_attention_static. */
 #define PEAGLE_STATIC_ATTN_SCRATCH_BYTES (8u << 20)
 

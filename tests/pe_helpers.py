@@ -1,5 +1,7 @@
 """Shared helpers of the GPU parity tests: build contexts, run the draft pass through the
 C ABI, and compare with the fp64 oracle."""
+import os
+
 import numpy as np
 import torch
 
@@ -20,10 +22,22 @@ def pk():
     return m
 
 
-def make_ctx(dims, w, max_batch, max_K, max_positions, max_rows=0, max_seq=0):
+def make_ctx(dims, w, max_batch, max_K, max_positions, max_rows=0, max_seq=0,
+             pass_kernel=None):
+    """A context; pass_kernel True / False forces the persistent pass kernel on / off for
+    the bf16 draft pass (None: the library default)."""
     m = pk()
-    return m.peagle_create(w, m.make_dims(dims, max_batch, max_K, max_positions, max_rows,
-                                          max_seq))
+    old = os.environ.get("PEAGLE_PASS_KERNEL")
+    if pass_kernel is not None:
+        os.environ["PEAGLE_PASS_KERNEL"] = "1" if pass_kernel else "0"
+    try:
+        return m.peagle_create(w, m.make_dims(dims, max_batch, max_K, max_positions, max_rows,
+                                              max_seq))
+    finally:
+        if old is None:
+            os.environ.pop("PEAGLE_PASS_KERNEL", None)
+        else:
+            os.environ["PEAGLE_PASS_KERNEL"] = old
 
 
 def to_dev(inp, dev="cuda"):
