@@ -672,21 +672,21 @@ __global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) 
   const float* qg = (const float*)a.q;
   const float* q0 = qg + ((size_t)(in0 ? qi0 : 0) * a.nq + h0) * HD;
   const float* q1 = qg + ((size_t)(in1 ? qi1 : 0) * a.nq + h1) * HD;
-  uint32_t qa_hi[KS][4], qa_lo[KS][4];
+  uint32_t qa[KS][4];  // bf16 queries (the scale is applied to the scores)
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     const int d0 = ks * 16 + 2 * tq, d1 = d0 + 8;
     float x[8];
-    x[0] = in0 ? q0[d0] * qscale : 0.f;
-    x[1] = in0 ? q0[d0 + 1] * qscale : 0.f;
-    x[2] = in1 ? q1[d0] * qscale : 0.f;
-    x[3] = in1 ? q1[d0 + 1] * qscale : 0.f;
-    x[4] = in0 ? q0[d1] * qscale : 0.f;
-    x[5] = in0 ? q0[d1 + 1] * qscale : 0.f;
-    x[6] = in1 ? q1[d1] * qscale : 0.f;
-    x[7] = in1 ? q1[d1 + 1] * qscale : 0.f;
+    x[0] = in0 ? q0[d0] : 0.f;
+    x[1] = in0 ? q0[d0 + 1] : 0.f;
+    x[2] = in1 ? q1[d0] : 0.f;
+    x[3] = in1 ? q1[d0 + 1] : 0.f;
+    x[4] = in0 ? q0[d1] : 0.f;
+    x[5] = in0 ? q0[d1 + 1] : 0.f;
+    x[6] = in1 ? q1[d1] : 0.f;
+    x[7] = in1 ? q1[d1 + 1] : 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) split2(x[2 * u], x[2 * u + 1], qa_hi[ks][u], qa_lo[ks][u]);
+    for (int u = 0; u < 4; ++u) qa[ks][u] = pack_bf16(x[2 * u], x[2 * u + 1]);
   }
   float o[ND][4];
 #pragma unroll
@@ -717,11 +717,16 @@ __global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) 
           const uint32_t addr = tile_k(buf) + (uint32_t)(key * ROWB + ((ch ^ (key & 7)) * 16));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
-          mma16816(sc[2 * np], qa_hi[ks], b0, b1);
-          mma16816(sc[2 * np], qa_lo[ks], b0, b1);
-          mma16816(sc[2 * np + 1], qa_hi[ks], b2, b3);
-          mma16816(sc[2 * np + 1], qa_lo[ks], b2, b3);
+          mma16816(sc[2 * np], qa[ks], b0, b1);
+          mma16816(sc[2 * np + 1], qa[ks], b2, b3);
         }
+      }
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        sc[n][0] *= qscale;
+        sc[n][1] *= qscale;
+        sc[n][2] *= qscale;
+        sc[n][3] *= qscale;
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
       if (it < ntA) {
@@ -765,10 +770,11 @@ __global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) 
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
-        sc[n][0] = exp2f(sc[n][0] - base0);
-        sc[n][1] = exp2f(sc[n][1] - base0);
-        sc[n][2] = exp2f(sc[n][2] - base1);
-        sc[n][3] = exp2f(sc[n][3] - base1);
+        // probabilities rounded to bf16 once: the PV product and the row sum use the same
+        sc[n][0] = bf16r(exp2f(sc[n][0] - base0));
+        sc[n][1] = bf16r(exp2f(sc[n][1] - base0));
+        sc[n][2] = bf16r(exp2f(sc[n][2] - base1));
+        sc[n][3] = bf16r(exp2f(sc[n][3] - base1));
         ps0 += sc[n][0] + sc[n][1];
         ps1 += sc[n][2] + sc[n][3];
       }
@@ -789,11 +795,11 @@ __global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) 
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t ph[4], pl[4];
-        split2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
-        split2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
-        split2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
-        split2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+        uint32_t ph[4];
+        ph[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+        ph[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+        ph[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+        ph[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < ND / 2; ++dp) {
           const int mat = lane >> 3, rr = lane & 7;
@@ -803,9 +809,7 @@ __global__ void __launch_bounds__(128) masked_attn_mma_kernel(MaskedAttnArgs a) 
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(addr, b0, b1, b2, b3);
           mma16816(o[2 * dp], ph, b0, b1);
-          mma16816(o[2 * dp], pl, b0, b1);
           mma16816(o[2 * dp + 1], ph, b2, b3);
-          mma16816(o[2 * dp + 1], pl, b2, b3);
         }
       }
     }

@@ -31,7 +31,7 @@ Modes of arithmetic (argument ``bf16``):
     values are rounded to the nearest bf16 (ties to even) at the named storage points
     (x0: the 2H first-layer input, xn: normalised projection inputs, q, kv: keys and
     values, o: attention output, act: SwiGLU product, y: LM-head input).  The bf16 GPU
-    path stores bf16 only in the KV cache (DRAFT_BF16_CASTS); the default for bf16 dims.
+    path rounds keys, values and queries (DRAFT_BF16_CASTS); the default for bf16 dims.
     Accumulations, the residual stream, norms, RoPE and softmax stay float64 here.
 
 Parity status of each function (what pins it, besides this file) is tested in
@@ -210,10 +210,11 @@ def input_rows(W: Weights64, dims, target_hidden, new_token, K):
 
 CAST_POINTS = ("x0", "xn", "q", "kv", "o", "act", "y")
 # Rounding profile of the bf16 GPU path (draft pass and training-style forward):
-# activations travel as bf16 hi + lo pairs (about 16 significant bits) and queries in
-# fp32, so the only bf16 rounding left is the one the KV storage format imposes on keys
-# and values.
-DRAFT_BF16_CASTS = frozenset({"kv"})
+# projection inputs travel as bf16 hi + lo pairs (about 16 significant bits), so the bf16
+# roundings left are the KV storage format's (keys and values) and the attention
+# product's operands (post-RoPE queries; the softmax weights are rounded too, which this
+# profile does not model and the logit tolerance absorbs).
+DRAFT_BF16_CASTS = frozenset({"kv", "q"})
 # Every storage point rounded to bf16 (a plain all-bf16 pipeline); kept for comparisons.
 ALL_BF16_CASTS = frozenset(CAST_POINTS)
 
