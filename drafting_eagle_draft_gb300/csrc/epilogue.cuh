@@ -132,85 +132,83 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
       }
     } break;
     case EPI_QKV_ROPE: {
+      // One output feature per thread (consecutive threads write consecutive features);
+      // the rows' positions, depths and RoPE factors of a batch of 16 rows are fetched
+      // before any of them is used.
       const int hd = a.hd, half = hd >> 1;
       const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
-      constexpr int U = 8;
-      for (int base = tid; base < rcount * 128; base += nthr * U) {
-      // positions and RoPE factors of U elements are fetched before any is used
-      int pos_u[U];
-      float2 cs_u[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int idx = base + u * nthr;
-        pos_u[u] = idx < rcount * 128 ? __ldg(a.row_pos + r0 + (idx >> 7)) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int idx = base + u * nthr;
-        const int m = m0 + (idx & 127);
+      constexpr int U = 16;
+      for (int ml = tid; ml < mcount; ml += nthr) {
+        const int m = m0 + ml;
         const int i = m % hd;
-        const bool need = idx < rcount * 128 && m < kend && i < half && pos_u[u] >= 0 &&
-                          pos_u[u] < a.max_pos;
-        cs_u[u] = need ? __ldg(a.rope + (size_t)pos_u[u] * half + i) : make_float2(1.f, 0.f);
-      }
+        const int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
+        if (sec != 2 && i >= half) continue;  // handled together with its pair partner
+        const int g = sec == 0 ? 0 : (m - (sec == 1 ? qend : kend)) / hd;
+        for (int t0 = 0; t0 < rcount; t0 += U) {
+          int pos_u[U], dep_u[U];
+          float2 cs_u[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int idx = base + u * nthr;
-        if (idx >= rcount * 128) continue;
-        int ti = idx >> 7, ml = idx & 127;
-        int r = r0 + ti;
-        int m = m0 + ml;
-        if (ml >= mcount) continue;
-        int i = m % hd;
-        int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
-        const int pos = pos_u[u];
-        int b = 0;
-        if (a.decode) b = r / a.K;
-        if (a.decode && (pos < 0 || pos >= a.cap)) {
-          if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
-          if (sec != 0) continue;  // no cache slot for this row
-        }
-        float v0 = val(ti, ml);
-        float out0, out1 = 0.f;
-        if (sec == 2) {
-          out0 = v0;
-        } else {
-          if (i >= half) continue;  // handled together with its pair partner
-          float v1 = val(ti, ml + half);
-          const float2 cs = cs_u[u];
-          out0 = v0 * cs.x - v1 * cs.y;
-          out1 = v1 * cs.x + v0 * cs.y;
-        }
-        if (sec == 0) {
-          if (a.q_f32) {
-            float* q = (float*)a.q_out + (size_t)r * a.nq * hd + m;
-            q[0] = out0;
-            q[half] = out1;
-          } else {
-            T* q = (T*)a.q_out + (size_t)r * a.nq * hd + m;
-            q[0] = from_f32<T>(out0);
-            q[half] = from_f32<T>(out1);
+          for (int u = 0; u < U; ++u) {
+            const int ti = t0 + u;
+            pos_u[u] = ti < rcount ? (rpos ? rpos[ti] : __ldg(a.row_pos + r0 + ti)) : -1;
+            dep_u[u] = (ti < rcount && !a.decode && a.row_depth) ? __ldg(a.row_depth + r0 + ti) : 0;
           }
-        } else {
-          int g = (m - (sec == 1 ? qend : kend)) / hd;
-          T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
-          size_t off;
-          if (a.decode)
-            off = (((size_t)b * a.nkv + g) * a.cap + pos) * hd + i;
-          else
-            off = ((size_t)r * a.nkv + g) * hd + i;
-          dst[off] = from_f32<T>(out0);
-          if (sec == 1) dst[off + half] = from_f32<T>(out1);
-          if (!a.decode && a.row_depth && a.row_depth[r] == 1 && pos >= 0 && pos < a.n_seq) {
-            T* d1 = (T*)(sec == 1 ? a.k1_dst : a.v1_dst);
-            if (d1) {
-              size_t o1 = ((size_t)pos * a.nkv + g) * hd + i;
-              d1[o1] = from_f32<T>(out0);
-              if (sec == 1) d1[o1 + half] = from_f32<T>(out1);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const bool need = sec != 2 && pos_u[u] >= 0 && pos_u[u] < a.max_pos;
+            cs_u[u] = need ? __ldg(a.rope + (size_t)pos_u[u] * half + i) : make_float2(1.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int ti = t0 + u;
+            if (ti >= rcount) break;
+            const int r = r0 + ti;
+            const int pos = pos_u[u];
+            int b = 0;
+            if (a.decode) b = r / a.K;
+            if (a.decode && (pos < 0 || pos >= a.cap)) {
+              if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
+              if (sec != 0) continue;  // no cache slot for this row
+            }
+            const float v0 = val(ti, ml);
+            float out0, out1 = 0.f;
+            if (sec == 2) {
+              out0 = v0;
+            } else {
+              const float v1 = val(ti, ml + half);
+              out0 = v0 * cs_u[u].x - v1 * cs_u[u].y;
+              out1 = v1 * cs_u[u].x + v0 * cs_u[u].y;
+            }
+            if (sec == 0) {
+              if (a.q_f32) {
+                float* q = (float*)a.q_out + (size_t)r * a.nq * hd + m;
+                q[0] = out0;
+                q[half] = out1;
+              } else {
+                T* q = (T*)a.q_out + (size_t)r * a.nq * hd + m;
+                q[0] = from_f32<T>(out0);
+                q[half] = from_f32<T>(out1);
+              }
+            } else {
+              T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
+              size_t off;
+              if (a.decode)
+                off = (((size_t)b * a.nkv + g) * a.cap + pos) * hd + i;
+              else
+                off = ((size_t)r * a.nkv + g) * hd + i;
+              dst[off] = from_f32<T>(out0);
+              if (sec == 1) dst[off + half] = from_f32<T>(out1);
+              if (!a.decode && dep_u[u] == 1 && pos >= 0 && pos < a.n_seq) {
+                T* d1 = (T*)(sec == 1 ? a.k1_dst : a.v1_dst);
+                if (d1) {
+                  const size_t o1 = ((size_t)pos * a.nkv + g) * hd + i;
+                  d1[o1] = from_f32<T>(out0);
+                  if (sec == 1) d1[o1 + half] = from_f32<T>(out1);
+                }
+              }
             }
           }
         }
-      }
       }
     } break;
     case EPI_QKV_FX: {

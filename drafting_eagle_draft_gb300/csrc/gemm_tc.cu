@@ -48,9 +48,14 @@ struct TcParams {
   int lo_col;   // split: TMEM column of the lo part of tile row 0
   int two_box;  // split with several tiles: hi and lo rows come from two 128-row boxes
   int n_tiles;  // row tiles
+  int m_tiles;  // 128-feature weight tiles
+  int m_inner;  // tile order: weight tiles vary fastest (the weights are re-read per row
+                // tile and must stay in L2), else row tiles vary fastest
   int KB;       // k-blocks of 64
-  long long total;  // tiles * KB
+  long long total;  // stream-K iterations: (tiles - dp_waves * G) * KB
   int G;        // CTAs
+  int dp_waves; // whole tiles per CTA taken first in waves (tile = w * G + c), before the
+                // stream-K split of the remaining tiles
   int stages;
   uint32_t tmem_cols;
   float* ws;          // partial slots [2G][BN][128]
@@ -58,8 +63,46 @@ struct TcParams {
   unsigned* err;
 };
 
+// Stream-K space: iterations (tile - dp_waves * G) * KB + kb of the tiles left after the
+// whole-tile waves; CTA c owns [range_begin(c), range_begin(c + 1)).
 __device__ __forceinline__ long long range_begin(long long c, const TcParams& p) {
   return c * p.total / p.G;
+}
+
+// This CTA's iterations v = 0 .. n-1: first dp_waves whole tiles (w * G + c), then its
+// stream-K range.  Large-M GEMMs get whole-tile waves so that concurrently running CTAs
+// work on neighbouring tiles (L2 reuse); decode-sized GEMMs are pure stream-K.
+struct Work {
+  long long dpv;            // iterations in whole-tile waves
+  long long sk_beg, sk_end; // stream-K range
+  long long n;
+};
+__device__ __forceinline__ Work make_work(const TcParams& p, int c) {
+  Work w;
+  w.dpv = (long long)p.dp_waves * p.KB;
+  w.sk_beg = range_begin(c, p);
+  w.sk_end = range_begin(c + 1, p);
+  w.n = w.dpv + (w.sk_end - w.sk_beg);
+  return w;
+}
+// tile and k-block of iteration v; *seg_end = end of the tile segment containing v
+__device__ __forceinline__ int work_tile(const TcParams& p, const Work& w, int c, long long v,
+                                         int* kb, long long* seg_end) {
+  if (v < w.dpv) {
+    const int wv = (int)(v / p.KB);
+    *kb = (int)(v - (long long)wv * p.KB);
+    if (seg_end) *seg_end = (long long)(wv + 1) * p.KB;
+    return wv * p.G + c;
+  }
+  const long long it = w.sk_beg + (v - w.dpv);
+  const int t = (int)(it / p.KB);
+  *kb = (int)(it - (long long)t * p.KB);
+  if (seg_end) {
+    long long e = (long long)(t + 1) * p.KB;
+    if (e > w.sk_end) e = w.sk_end;
+    *seg_end = w.dpv + (e - w.sk_beg);
+  }
+  return p.dp_waves * p.G + t;
 }
 // CTA whose stream-K range contains iteration `it`
 __device__ __forceinline__ int owner_of(long long it, const TcParams& p) {
@@ -70,6 +113,13 @@ __device__ __forceinline__ int owner_of(long long it, const TcParams& p) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int tile_m(int tile, const TcParams& p) {
+  return p.m_inner ? tile % p.m_tiles : tile / p.n_tiles;
+}
+__device__ __forceinline__ int tile_n(int tile, const TcParams& p) {
+  return p.m_inner ? tile / p.m_tiles : tile % p.n_tiles;
+}
 
 // Activation operand of k-block kb for row tile nt: one box of BN rows, or (split over
 // several tiles) the tile's 128 hi rows followed by its 128 lo rows.
@@ -129,43 +179,47 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   const uint32_t tmem = *s_tmem;
   tc::pdl_launch_dependents();
 
-  const long long beg = range_begin(c, p), end = range_begin(c + 1, p);
+  const Work wk = make_work(p, c);
   const int KB = p.KB;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = tc::policy_evict_first();
-      const uint64_t pol_x = tc::policy_evict_last();
+      // the operand read once streams through L2 (evict first); the one cycled across
+      // tiles stays (evict last): activations for decode-sized GEMMs, weights when the
+      // weight tiles vary fastest
+      const uint64_t pol_w = p.m_inner ? tc::policy_evict_last() : tc::policy_evict_first();
+      const uint64_t pol_x = p.m_inner ? tc::policy_evict_first() : tc::policy_evict_last();
       const uint32_t bytes = A_BYTES + B_BYTES;
-      const long long n_it = end - beg;
+      const long long n_it = wk.n;
       const int npre = (int)(n_it < S ? n_it : S);
       for (int i = 0; i < npre; ++i) {
-        const long long it = beg + i;
-        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
+        int kb;
+        const int tile = work_tile(p, wk, c, i, &kb, nullptr);
         tc::mbar_expect_tx(&full[i], bytes);
-        tc::tma_load_2d(sA + (size_t)i * A_BYTES, &tmW, kb * 64, (tile / p.n_tiles) * 128, &full[i],
+        tc::tma_load_2d(sA + (size_t)i * A_BYTES, &tmW, kb * 64, tile_m(tile, p) * 128, &full[i],
                         pol_w);
       }
       tc::pdl_wait();
       for (int i = 0; i < npre; ++i) {
-        const long long it = beg + i;
-        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
-        load_b(sB + (size_t)i * B_BYTES, &tmX, kb, tile % p.n_tiles, &full[i], pol_x, p);
+        int kb;
+        const int tile = work_tile(p, wk, c, i, &kb, nullptr);
+        load_b(sB + (size_t)i * B_BYTES, &tmX, kb, tile_n(tile, p), &full[i], pol_x, p);
       }
       int stage = npre % S;
       uint32_t ph = (npre == S) ? 1u : 0u;
-      for (long long it = beg + npre; it < end; ++it) {
+      for (long long it = npre; it < n_it; ++it) {
         if (!tc::mbar_wait(&empty[stage], ph ^ 1u, s_abort)) {
           raise_error(p.err, PEAGLE_DEV_TIMEOUT);
           *s_abort = 1;
           break;
         }
-        const int tile = (int)(it / KB), kb = (int)(it - (long long)tile * KB);
+        int kb;
+        const int tile = work_tile(p, wk, c, it, &kb, nullptr);
         tc::mbar_expect_tx(&full[stage], bytes);
-        tc::tma_load_2d(sA + (size_t)stage * A_BYTES, &tmW, kb * 64, (tile / p.n_tiles) * 128,
+        tc::tma_load_2d(sA + (size_t)stage * A_BYTES, &tmW, kb * 64, tile_m(tile, p) * 128,
                         &full[stage], pol_w);
-        load_b(sB + (size_t)stage * B_BYTES, &tmX, kb, tile % p.n_tiles, &full[stage], pol_x, p);
+        load_b(sB + (size_t)stage * B_BYTES, &tmX, kb, tile_n(tile, p), &full[stage], pol_x, p);
         if (++stage == S) {
           stage = 0;
           ph ^= 1u;
@@ -180,10 +234,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       uint32_t ph = 0;
       int seg = 0;
       bool ok = true;
-      for (long long it = beg; it < end && ok;) {
-        const int tile = (int)(it / KB);
-        long long seg_end = (long long)(tile + 1) * KB;
-        if (seg_end > end) seg_end = end;
+      for (long long it = 0; it < wk.n && ok;) {
+        int kb0;
+        long long seg_end;
+        work_tile(p, wk, c, it, &kb0, &seg_end);
         const int buf = seg & 1;
         const uint32_t use = (uint32_t)(seg >> 1);
         if (!tc::mbar_wait(&acce[buf], (use & 1u) ^ 1u, s_abort)) {
@@ -224,10 +278,11 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     const int ml = quarter * 32 + lane;   // tile feature = TMEM lane
     const int R = p.R;
     int seg = 0;
-    for (long long it = beg; it < end;) {
-      const int tile = (int)(it / KB);
-      long long seg_end = (long long)(tile + 1) * KB;
-      if (seg_end > end) seg_end = end;
+    for (long long it = 0; it < wk.n;) {
+      int kb0;
+      long long seg_end;
+      const int tile = work_tile(p, wk, c, it, &kb0, &seg_end);
+      const bool whole = it < wk.dpv;  // a wave tile: this CTA is its only contributor
       it = seg_end;
       const int buf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
@@ -241,12 +296,13 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       epi_bar();
       if (*s_abort) break;
       tc::fence_after_sync();
-      const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+      const int mt = tile_m(tile, p), nt = tile_n(tile, p);
       const int m0 = mt * 128;
       const int row0 = nt * p.rpt;               // first logical row of this tile
       const int lrows = min(p.rpt, R - row0);    // logical rows in this tile
-      const long long t_beg = (long long)tile * KB;
-      const int cf = owner_of(t_beg, p), cl = owner_of(t_beg + KB - 1, p);
+      const long long t_beg = (long long)(tile - p.dp_waves * p.G) * KB;  // stream-K space
+      const int cf = whole ? c : owner_of(t_beg, p);
+      const int cl = whole ? c : owner_of(t_beg + KB - 1, p);
       const uint32_t tb = tmem + (uint32_t)(buf * p.BN) + ((uint32_t)(quarter * 32) << 16);
       // chunking: split tiles take 16 logical rows per chunk (hi + lo columns), others 32
       const int step = p.split ? 16 : 32;
@@ -482,9 +538,19 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   p.KB = Kd / 64;
   const int m_tiles = (Nout + 127) / 128;
   const long long tiles = (long long)m_tiles * p.n_tiles;
+  p.m_tiles = m_tiles;
+  // Concurrent CTAs work on neighbouring tiles: with weight tiles innermost all of W is
+  // touched while a few row tiles are live, so W is read from DRAM once if it fits in L2;
+  // with row tiles innermost the same holds for the activations.  Cycle the smaller one.
+  {
+    const long long wbytes = (long long)Nout * Kd * 2;
+    const long long xbytes = (long long)xrows * Kd * 2;
+    p.m_inner = (p.n_tiles > 1 && wbytes < xbytes) ? 1 : 0;
+  }
   if (tiles > pl->max_tiles || Kd % 64) return PEAGLE_ERR_CAPACITY;
-  p.total = tiles * p.KB;
-  p.G = (int)(p.total < pl->num_sms ? p.total : pl->num_sms);
+  p.G = (int)(tiles * p.KB < pl->num_sms ? tiles * p.KB : pl->num_sms);
+  p.dp_waves = p.n_tiles > 1 ? (int)(tiles / p.G) : 0;
+  p.total = (tiles - (long long)p.dp_waves * p.G) * p.KB;
   // shared memory ring: decode-sized tiles keep ~110 KB so a second CTA (the next
   // kernel's, under programmatic dependent launch) fits on the SM; large tiles take more
   const size_t budget = p.BN <= 64 ? 112 * 1024 : 220 * 1024;
