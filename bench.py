@@ -126,6 +126,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM bytes (read + write) of one pass-kernel launch on decode_b1, from the ncu capture
+# summarised in profiles/pass_kernel_decode_b1.md (dram__bytes_read.sum + _write.sum)
+PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_053_911_296
+
+
 def gemm_weight_bytes(dims) -> int:
     """Weight bytes one draft pass streams through the projections."""
     H, I, Vd = dims.hidden, dims.intermediate, dims.draft_vocab
@@ -303,9 +308,12 @@ def run_ours(args, rank, world, dist):
     lens = inp["seq_lens"]
     total_bytes = wbytes + kv_bytes(dims, lens, K)
     roofline_us = total_bytes / (pk_["hbm_gbs"] * 1e9) * 1e6
+    traffic = None
     if pass_kernel:
         kern = "pass_kernel (the whole draft pass, one launch)"
         kern_bytes, kern_ms, kern_launches = total_bytes, draft_ms, 1
+        if wl.name == "decode_b1":
+            traffic = PASS_KERNEL_DECODE_B1_DRAM_BYTES
     else:
         gemm_stages = ("fc", "qkv", "oproj", "gate_up", "down", "lm_head")
         kern = "tc_gemm_kernel (all projection launches)"
@@ -344,7 +352,7 @@ def run_ours(args, rank, world, dist):
                        "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
             "roofline": {"bound": "hbm", "kernel": kern,
                          "achieved": round(achieved, 1), "peak": pk_["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk_["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / pk_["hbm_gbs"], 4), "traffic": traffic,
                          "bytes_per_launch": kern_bytes, "launches_per_step": kern_launches,
                          "kernel_ms_per_step": round(kern_ms, 4),
                          "peak_source": pk_["source"] + " (burst copy)",
