@@ -31,7 +31,8 @@ PEAGLE_BF16 = 1
 
 # every entry point declared in include/peagle.h
 EXPORTS = ("peagle_create", "peagle_draft", "peagle_verify_greedy", "peagle_append_kv",
-           "peagle_forward_parallel", "peagle_cod_rows", "peagle_status",
+           "peagle_forward_parallel", "peagle_cod_rows", "peagle_sequence_partition",
+           "peagle_status",
            "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
            "peagle_decode_attention_static",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
@@ -89,6 +90,7 @@ def lib():
         L.peagle_forward_parallel.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp,
                                               _vp, _vp]
         L.peagle_cod_rows.argtypes = [_i32, _i32, ctypes.c_double, _vp, _vp, _vp, _i32]
+        L.peagle_sequence_partition.argtypes = [_i32, _vp, _vp, _i32, _vp, _vp]
         L.peagle_status.argtypes = [_vp]
         L.peagle_set_timing.argtypes = [_vp, _i32]
         L.peagle_decode_attention_static.argtypes = [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
@@ -247,6 +249,18 @@ def peagle_cod_rows(n, K, ratio, uniforms):
     if m < 0:
         raise PeagleError(m, "peagle_cod_rows")
     return rp[:m].copy(), rd[:m].copy()
+
+
+def peagle_sequence_partition(row_p, row_d, boundaries):
+    """Chunk index of every retained row (host arrays; see include/peagle.h)."""
+    rp = np.ascontiguousarray(row_p, np.int32)
+    rd = np.ascontiguousarray(row_d, np.int32)
+    bd = np.ascontiguousarray(boundaries, np.int32)
+    out = np.empty(len(rp), np.int32)
+    _check(lib().peagle_sequence_partition(len(rp), rp.ctypes.data, rd.ctypes.data, len(bd),
+                                           bd.ctypes.data, out.ctypes.data),
+           "peagle_sequence_partition")
+    return out
 
 
 def peagle_status(ctx: Context) -> int:

@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "gemm_tc.h"
@@ -425,6 +426,10 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     const long long tiles = (long long)((Nout + 127) / 128) * m.n_tiles;
     m.total = tiles * m.KB;
     m.Gm = (int)(m.total < grid ? m.total : grid);
+    // A projection whose epilogue needs whole tiles (SwiGLU, LM head) pays a cross-CTA
+    // fix-up at the end of every shared tile.  With between G/2 and G tiles, one whole tile
+    // per CTA streams the same bytes from HBM (the idle CTAs' share is small) without it.
+    if (!m.additive && tiles <= grid && 2 * tiles >= grid) m.Gm = (int)tiles;
     m.idesc = tc::idesc_bf16(128, m.BN);
     m.epi = e;
     if (tiles > tc_max_tiles(c->tc) || Kd % 64 || m.BN > 240) fail = true;
@@ -911,6 +916,46 @@ extern "C" int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double*
     prev.swap(cur);
   }
   return count;
+}
+
+extern "C" int peagle_sequence_partition(int32_t M, const int32_t* row_p, const int32_t* row_d,
+                                         int32_t n_chunks, const int32_t* boundaries,
+                                         int32_t* out_chunk) {
+  if (M < 0 || n_chunks < 1 || !boundaries || (M > 0 && (!row_p || !row_d || !out_chunk)))
+    return PEAGLE_ERR_INVALID;
+  if (boundaries[0] != 0) return PEAGLE_ERR_INVALID;
+  for (int s = 1; s < n_chunks; ++s)
+    if (boundaries[s] <= boundaries[s - 1]) return PEAGLE_ERR_INVALID;
+  constexpr int DMAX = 64;
+  // chunk of (p, d) for the current and the previous position (rows are p-major)
+  std::vector<int> prev(DMAX + 1, -1), cur(DMAX + 1, -1);
+  int cur_p = -1, s = 0;
+  for (int i = 0; i < M; ++i) {
+    const int p = row_p[i], d = row_d[i];
+    if (p < 0 || d < 1 || d > DMAX) return PEAGLE_ERR_INVALID;
+    if (i > 0 && (p < row_p[i - 1] || (p == row_p[i - 1] && d <= row_d[i - 1])))
+      return PEAGLE_ERR_INVALID;  // not p-major
+    if (p != cur_p) {
+      if (p == cur_p + 1) {
+        prev.swap(cur);
+      } else {
+        std::fill(prev.begin(), prev.end(), -1);
+      }
+      std::fill(cur.begin(), cur.end(), -1);
+      cur_p = p;
+    }
+    int ch;
+    if (d <= 2) {
+      while (s + 1 < n_chunks && boundaries[s + 1] <= p) ++s;  // p only grows
+      ch = s;
+    } else {
+      ch = prev[d - 1];  // Chunk(p, d) = Chunk(p-1, d-1)
+      if (ch < 0) return PEAGLE_ERR_INVALID;  // dependency not in the set
+    }
+    cur[d] = ch;
+    out_chunk[i] = ch;
+  }
+  return PEAGLE_OK;
 }
 
 extern "C" int peagle_status(peagle_ctx* c) {

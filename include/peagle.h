@@ -190,6 +190,18 @@ int peagle_forward_parallel(peagle_ctx* ctx, int32_t n, int32_t K, const int32_t
 int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double* uniforms,
                     int32_t* out_p, int32_t* out_d, int32_t max_out);
 
+/* Host-side sequence partitioning ("P-EAGLE: Parallel-Drafting EAGLE with Scalable
+ * Training", section 3.2): assigns each retained row (p, d), given p-major in
+ * row_p / row_d (host int32 [M]), to one of n_chunks chunks whose start positions are
+ * boundaries[0] = 0 < boundaries[1] < ... (host int32).  Rows of depth 1 and 2 go to the
+ * chunk containing their position; a row of depth d >= 3 to the chunk of (p-1, d-1).
+ * Writes out_chunk (host int32 [M]).  Chunk c's forward runs on its own rows plus every
+ * depth-1 row below its end boundary (a dependency-closed set: one
+ * peagle_forward_parallel call).  Returns PEAGLE_OK, or PEAGLE_ERR_INVALID for
+ * non-increasing boundaries, rows not p-major, depth > 64 or a missing dependency. */
+int peagle_sequence_partition(int32_t M, const int32_t* row_p, const int32_t* row_d,
+                              int32_t n_chunks, const int32_t* boundaries, int32_t* out_chunk);
+
 /* Synchronise the context's device work and return PEAGLE_OK, PEAGLE_ERR_DEVICE if
  * the device error word is non-zero (the word is then cleared), or PEAGLE_ERR_CUDA
  * if a sticky CUDA error is pending. */

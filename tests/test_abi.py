@@ -109,3 +109,31 @@ def test_cod_rows_capacity_error(pk):
     rc = L.peagle_cod_rows(10, 4, ctypes.c_double(0.8), u.ctypes.data, out.ctypes.data,
                            out.ctypes.data, 5)
     assert rc == pk.PEAGLE_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("n,K,r,bnd", [
+    (64, 8, 0.8, [0, 16, 32, 48]),
+    (500, 8, 0.7, [0, 100, 101, 333]),
+    (200, 16, 1.0, [0, 7]),
+    (33, 4, 0.8, [0]),
+])
+def test_sequence_partition_matches_oracle(pk, n, K, r, bnd):
+    u = synth.cod_uniforms(n, K, seed=3 * n + K)
+    rp, rd = pk.peagle_cod_rows(n, K, r, u)
+    got = pk.peagle_sequence_partition(rp, rd, bnd)
+    ref, _ = O.sequence_partition(np.stack([rp, rd], 1), bnd)
+    assert np.array_equal(got, ref)
+
+
+def test_sequence_partition_rejects_bad_input(pk):
+    rp = np.array([0, 1, 1, 2, 2, 2], np.int32)
+    rd = np.array([1, 1, 2, 1, 2, 3], np.int32)
+    assert np.array_equal(pk.peagle_sequence_partition(rp, rd, [0, 2]), [0, 0, 0, 1, 1, 0])
+    for bnd in ([1, 2], [0, 2, 2], [0, 3, 1]):  # must start at 0 and increase
+        with pytest.raises(pk.PeagleError):
+            pk.peagle_sequence_partition(rp, rd, bnd)
+    with pytest.raises(pk.PeagleError):  # not p-major
+        pk.peagle_sequence_partition(rp[::-1], rd[::-1], [0])
+    with pytest.raises(pk.PeagleError):  # (2, 3) without (1, 2)
+        pk.peagle_sequence_partition(np.array([0, 1, 2, 2], np.int32),
+                                     np.array([1, 1, 1, 3], np.int32), [0])

@@ -111,6 +111,34 @@ def test_forward_parallel_dependency_closure():
     _compare(dims, rl, ra, rm, am, lg, "fwd dependency closure")
 
 
+def test_sequence_partitioned_forward_matches_full():
+    """Sequence partitioning (3.2): each chunk's rows, run with every depth-1 row below the
+    chunk's end as context (one dependency-closed call), give the same outputs as the
+    unpartitioned forward over all rows."""
+    m = pk()
+    dims = SMALL_BF16
+    n, K, r = 180, 8, 0.8
+    w = synth.make_weights(dims, 41)
+    tokens = synth.uniform_ints(n, 0, dims.target_vocab, 9)
+    hidden = synth.normal((n, 3 * dims.hidden), 10, 1.0, dims.torch_dtype)
+    rp, rd = m.peagle_cod_rows(n, K, r, synth.cod_uniforms(n, K, seed=12))
+    bnd = [0, 50, 110, 150]
+    chunk = m.peagle_sequence_partition(rp, rd, bnd)
+    ctx = make_ctx(dims, w, 1, K, n, max_rows=len(rp), max_seq=n)
+    am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
+    for c in range(len(bnd)):
+        end = bnd[c + 1] if c + 1 < len(bnd) else n
+        sel = (chunk == c) | ((rd == 1) & (rp < end))
+        own = chunk[sel] == c
+        am_c, lg_c = _run_fwd(ctx, dims, tokens, hidden, rp[sel], rd[sel], n, K)
+        err = float(np.max(np.abs(lg_c[own] - lg[sel][own])))
+        assert err < 2e-3, f"chunk {c}: {err:.3e}"
+        ok = np.sort(lg[sel][own], axis=1)
+        margin = ok[:, -1] - ok[:, -2]
+        assert np.array_equal(am_c[own][margin > 1e-2], am[sel][own][margin > 1e-2])
+    ctx.close()
+
+
 def test_forward_parallel_rejects_missing_depth1_row():
     m = pk()
     dims = SMALL_BF16
