@@ -68,9 +68,18 @@ constexpr int MMA_KT = 64;  // keys per tile
 
 // One work item: chunk c of (request b, kv head g), run by the nthr threads tid = 0 ..
 // nthr-1 of a thread group (>= 32 * ceil(rows / 16)) that synchronises with bar().
-template <int HD, typename Bar>
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  if (n <= 0) cp_async_wait<0>();
+  else if (n == 1) cp_async_wait<1>();
+  else if (n == 2) cp_async_wait<2>();
+  else cp_async_wait<3>();
+}
+
+// NBUF K/V tile buffers (<= 4): the loads of up to NBUF tiles are in flight at once.
+template <int HD, int NBUF, typename Bar>
 __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, int c, int tid,
                                               int nthr, uint8_t* sm_raw, Bar bar) {
+  static_assert(NBUF >= 2 && NBUF <= 4, "1 < NBUF <= 4");
   constexpr int ROWB = HD * 2;           // bytes per key row
   constexpr int CH = ROWB / 16;          // 16-byte chunks per row
   constexpr int TILEB = MMA_KT * ROWB;   // bytes per K (or V) tile
@@ -90,7 +99,7 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
   const bf16* kc = (const bf16*)a.kc + head_off;
   const bf16* vc = (const bf16*)a.vc + head_off;
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm_raw);
-  // smem: [buf 0: K tile, V tile][buf 1: K tile, V tile]
+  // smem: NBUF x [K tile, V tile]
   auto tile_k = [&](int buf) { return sbase + (uint32_t)(buf * 2 * TILEB); };
   auto tile_v = [&](int buf) { return sbase + (uint32_t)(buf * 2 * TILEB + TILEB); };
   auto load_tile = [&](int buf, int t0) {
@@ -137,15 +146,12 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const bool active = warp * 16 < rows;
   const int ntile = (kend - kbeg + MMA_KT - 1) / MMA_KT;
+  int loaded = 1;  // tile 0 was issued before the queries
+  for (; loaded < ntile && loaded < NBUF; ++loaded) load_tile(loaded, kbeg + loaded * MMA_KT);
   for (int it = 0; it < ntile; ++it) {
-    const int buf = it & 1;
+    const int buf = it % NBUF;
     const int t0 = kbeg + it * MMA_KT;
-    if (it + 1 < ntile) {
-      load_tile(buf ^ 1, t0 + MMA_KT);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    cp_async_wait_n(loaded - 1 - it);  // groups committed after tile it may stay in flight
     bar();
     if (active) {
       // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
@@ -246,6 +252,10 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
       }
     }
     bar();
+    if (loaded < ntile) {  // the buffer just consumed takes the next tile
+      load_tile(loaded % NBUF, kbeg + loaded * MMA_KT);
+      ++loaded;
+    }
   }
   // ---- partials: m and l in natural-log units, o unnormalised
   const int rows_alloc = rows;

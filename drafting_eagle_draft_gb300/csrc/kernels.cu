@@ -404,8 +404,8 @@ template <int HD>
 __global__ void __launch_bounds__(256) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t sm_raw[];
   pdl_enter();
-  attn_mma_item<HD>(a, blockIdx.z, blockIdx.y, blockIdx.x, threadIdx.x, blockDim.x, sm_raw,
-                    []() { __syncthreads(); });
+  attn_mma_item<HD, 2>(a, blockIdx.z, blockIdx.y, blockIdx.x, threadIdx.x, blockDim.x, sm_raw,
+                       []() { __syncthreads(); });
 }
 
 // Merge of the split-KV partials as its own grid: warp w of CTA (x, g, b) merges query

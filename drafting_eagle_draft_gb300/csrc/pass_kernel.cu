@@ -163,11 +163,13 @@ __device__ __forceinline__ void trace_ev(const PassParams& P, int ph, int k) {
     P.trace_cta[((size_t)ph * gridDim.x + blockIdx.x) * 4 + k] = tc::globaltimer();
 }
 
-// Every worker has finished its part of phase `ph`: publish it.
+// Every worker has finished its part of phase `ph`: publish it.  The CTA barrier orders
+// the workers' writes before thread 0's fence, which makes them visible at GPU scope before
+// the release add (the pattern of a cooperative grid barrier).
 __device__ __forceinline__ void wk_signal(const PassParams& P, int ph, int et) {
-  __threadfence();
   wk_bar();
   if (et == 0) {
+    __threadfence();
     fence_proxy_async_global();
     red_release_add(P.phase_cnt + ph, 1u);
     // timing: the phase completes when its last CTA signals
@@ -733,7 +735,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               const int cc = i % a.nchunk;
               const int g = (i / a.nchunk) % a.nkv;
               const int b = i / (a.nchunk * a.nkv);
-              attn_mma_item<HD>(a, b, g, cc, et, 128, uni, []() { wk_bar(); });
+              attn_mma_item<HD, pass_att_nbuf(HD)>(a, b, g, cc, et, 128, uni,
+                                                   []() { wk_bar(); });
             }
           } else {
             const int n_items = rows * a.nkv * a.B;

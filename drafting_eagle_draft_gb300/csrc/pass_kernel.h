@@ -15,6 +15,10 @@ constexpr int PASS_MAX_GEMM = 3 + 4 * PASS_MAX_LAYERS;
 constexpr int PASS_MAX_PHASE = 5 + 9 * PASS_MAX_LAYERS;
 constexpr int PASS_MAX_ROWS = 120;                    // R = B*K (hi + lo rows <= 240)
 constexpr int PASS_SS_SLOTS = 2 + 2 * PASS_MAX_LAYERS;  // per-row sums of squares
+// K/V tile buffers of an attention item (64 keys each).  Deeper pipelines (all four tiles
+// of a 256-key chunk in flight) measured no faster: an item is bound by its compute and
+// the step's latency chain, and the shared memory is worth more as weight-ring stages.
+constexpr int pass_att_nbuf(int) { return 2; }
 
 // RMSNorm is split in two: a step spread over all CTAs writes x * gamma (the projection's
 // operand) and adds each row's sum of squares into a fixed-point slot; the consuming

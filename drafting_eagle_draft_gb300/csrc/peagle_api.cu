@@ -534,7 +534,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   while (tc_cols < (uint32_t)(2 * P.acc_stride)) tc_cols <<= 1;
   if (tc_cols > 512) return PEAGLE_ERR_UNSUPPORTED;
   P.tmem_cols = (int)tc_cols;
-  const int att_bytes = 4 * 64 * hd * 2;
+  const int att_bytes = pass_att_nbuf(hd) * 2 * 64 * hd * 2;
   P.uni_bytes = att_bytes > 32 * 128 * 4 ? att_bytes : 32 * 128 * 4;
   // dynamic shared memory: the 227 KB per-block limit minus the kernel's static part
   const size_t smem_cap = 223 * 1024;
