@@ -34,7 +34,8 @@
 
 namespace peagle {
 
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 192;  // one epilogue group (decode-sized GEMMs)
+constexpr int TC_THREADS2 = 320; // two epilogue groups (large-M GEMMs)
 constexpr int A_BYTES = 128 * 128;  // one 128 x 64 bf16 weight tile
 constexpr int STAGE_F_BYTES = 32 * 128 * 4;
 
@@ -112,7 +113,15 @@ __device__ __forceinline__ int owner_of(long long it, const TcParams& p) {
   return (int)c;
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barriers: 1 + g for epilogue group g (128 threads), 3 for all epilogue warps
+__device__ __forceinline__ void epi_bar(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+}
+template <int NEG>
+__device__ __forceinline__ void epi_bar_all() {
+  if (NEG == 1) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 3, %0;" ::"n"(128 * NEG) : "memory");
+}
 
 __device__ __forceinline__ int tile_m(int tile, const TcParams& p) {
   return p.m_inner ? tile % p.m_tiles : tile / p.n_tiles;
@@ -133,9 +142,12 @@ __device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* m, int k
   }
 }
 
-// two CTAs per SM: under programmatic dependent launch the next projection's CTA starts
-// (and prefetches its weights) beside this one
-__global__ void __launch_bounds__(TC_THREADS, 2)
+// NEG epilogue groups of four warps.  NEG = 1 (decode-sized): two CTAs per SM, so under
+// programmatic dependent launch the next projection's CTA starts (and prefetches its
+// weights) beside this one.  NEG = 2 (large M, tensor-bound): the two groups drain
+// alternate row chunks of a tile, each with its own half of the staging buffer.
+template <int NEG>
+__global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 ? 2 : 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const TcParams p, const EpiArgs epi) {
   extern __shared__ uint8_t smem_raw[];
@@ -162,7 +174,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&accf[i], 1);
-      tc::mbar_init(&acce[i], 128);
+      tc::mbar_init(&acce[i], 128 * NEG);
     }
     *s_abort = 0;
     tc::fence_barrier_init();
@@ -273,10 +285,13 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
-    const int et = threadIdx.x - 64;      // 0 .. 127
-    const int quarter = warp & 3;         // TMEM lane quarter this warp may access
-    const int ml = quarter * 32 + lane;   // tile feature = TMEM lane
+    const int eg = (threadIdx.x - 64) >> 7;  // epilogue group
+    const int et = (threadIdx.x - 64) & 127; // 0 .. 127 within the group
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
+    const int ml = quarter * 32 + lane;      // tile feature = TMEM lane
     const int R = p.R;
+    // staging: [32 / NEG rows][128] fp32 per group
+    float* gstg = stg + (size_t)eg * (32 / NEG) * 128;
     int seg = 0;
     for (long long it = 0; it < wk.n;) {
       int kb0;
@@ -287,13 +302,13 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       const int buf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
       ++seg;
-      // one thread observes the accumulator barrier; the named barrier publishes the
-      // outcome so the four warps stay in lock-step even if the wait gives up
+      // one thread per group observes the accumulator barrier; the group's named barrier
+      // publishes the outcome so its warps stay in lock-step even if the wait gives up
       if (et == 0 && !tc::mbar_wait(&accf[buf], use & 1u, s_abort)) {
         raise_error(p.err, PEAGLE_DEV_TIMEOUT);
         *s_abort = 1;
       }
-      epi_bar();
+      epi_bar(eg);
       if (*s_abort) break;
       tc::fence_after_sync();
       const int mt = tile_m(tile, p), nt = tile_n(tile, p);
@@ -304,43 +319,66 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       const int cf = whole ? c : owner_of(t_beg, p);
       const int cl = whole ? c : owner_of(t_beg + KB - 1, p);
       const uint32_t tb = tmem + (uint32_t)(buf * p.BN) + ((uint32_t)(quarter * 32) << 16);
-      // chunking: split tiles take 16 logical rows per chunk (hi + lo columns), others 32
-      const int step = p.split ? 16 : 32;
+      // chunking: split tiles take 16 / NEG logical rows per chunk (hi + lo columns), others
+      // 32 / NEG; chunk ch belongs to group ch % NEG
+      const int step = (p.split ? 16 : 32) / NEG;
       const int nch = (lrows + step - 1) / step;
       if (cf == cl || p.additive) {
         // ---- sole owner, or an additive epilogue (each contributor adds its own partial):
         //      TMEM -> staging -> epilogue
-        for (int ch = 0; ch < nch; ++ch) {
+        for (int ch = eg; ch < nch; ch += NEG) {
           const int i0 = ch * step;
-          float v[16], w[16];
+          if (NEG == 1) {
+            float v[16], w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) w[j] = 0.f;
-          tc::tmem_ld16(tb + i0, v);
-          if (p.split) {
-            tc::tmem_ld16(tb + p.lo_col + i0, w);
-          } else if (i0 + 16 < p.BN) {
-            tc::tmem_ld16(tb + i0 + 16, w);
-          }
-          tc::tmem_ld_wait();
+            for (int j = 0; j < 16; ++j) w[j] = 0.f;
+            tc::tmem_ld16(tb + i0, v);
+            if (p.split) {
+              tc::tmem_ld16(tb + p.lo_col + i0, w);
+            } else if (i0 + 16 < p.BN) {
+              tc::tmem_ld16(tb + i0 + 16, w);
+            }
+            tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            stg[j * 128 + ml] = v[j];
-            stg[(16 + j) * 128 + ml] = w[j];
+            for (int j = 0; j < 16; ++j) {
+              gstg[j * 128 + ml] = v[j];
+              gstg[(16 + j) * 128 + ml] = w[j];
+            }
+          } else {
+            float v[8], w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = 0.f;
+            tc::tmem_ld8(tb + i0, v);
+            if (p.split) {
+              tc::tmem_ld8(tb + p.lo_col + i0, w);
+            } else if (i0 + 8 < p.BN) {
+              tc::tmem_ld8(tb + i0 + 8, w);
+            }
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              gstg[j * 128 + ml] = v[j];
+              gstg[(8 + j) * 128 + ml] = w[j];
+            }
           }
-          if (ch == nch - 1) {
+          if (ch + NEG >= nch) {  // this group's last TMEM read of the segment
             tc::fence_before_sync();
             tc::mbar_arrive(&acce[buf]);
           }
-          epi_bar();
-          epilogue_tile<bf16>(epi, stg, 128, p.split ? 16 : -1, m0, row0 + i0,
+          epi_bar(eg);
+          epilogue_tile<bf16>(epi, gstg, 128, p.split ? 16 / NEG : -1, m0, row0 + i0,
                               min(step, lrows - i0), et, 128);
-          epi_bar();
+          epi_bar(eg);
+        }
+        if (eg >= nch) {  // a group without a chunk still releases the accumulator
+          tc::fence_before_sync();
+          tc::mbar_arrive(&acce[buf]);
         }
       } else {
         // ---- shared tile: write this CTA's partial, the last contributor reduces
         const int slot = (range_begin(c, p) >= t_beg) ? 2 * c : 2 * c + 1;
         float* wsl = p.ws + (size_t)slot * p.BN * 128;
-        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+        for (int c0 = eg * 16; c0 < p.BN; c0 += 16 * NEG) {
           float v[16];
           tc::tmem_ld16(tb + c0, v);
           tc::tmem_ld_wait();
@@ -349,26 +387,28 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&acce[buf]);
-        epi_bar();
-        if (et == 0) {
+        epi_bar_all<NEG>();
+        if (eg == 0 && et == 0) {
           const unsigned prev = atom_add_acq_rel(p.counters + tile, 1u);
           *s_flag = (prev == (unsigned)(cl - cf)) ? 1 : 0;
         }
-        epi_bar();
+        epi_bar_all<NEG>();
         if (*s_flag) {
           // contributor cf's share of this tile is its last segment unless its range starts
           // exactly at the tile; every later contributor's share is its first segment
           const int slot_f = (range_begin(cf, p) == t_beg) ? 2 * cf : 2 * cf + 1;
-          for (int ch = 0; ch < nch; ++ch) {
+          constexpr int SR = 32 / NEG;  // staging rows per chunk
+          const int half = p.split ? SR / 2 : SR;
+          for (int ch = eg; ch < nch; ch += NEG) {
             const int i0 = ch * step;
-            // staging rows [0,16) / [16,32): hi / lo parts (split) or rows i0.. (plain)
-            int col[32];
-            float acc[32];
+            // staging rows [0,half) / [half,2 half): hi / lo parts (split) or rows i0..
+            int col[SR];
+            float acc[SR];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < SR; ++j) {
               if (p.split) {
-                const int ii = i0 + (j & 15);
-                col[j] = min((j < 16) ? ii : p.lo_col + ii, p.BN - 1);
+                const int ii = i0 + (j % half);
+                col[j] = min((j < half) ? ii : p.lo_col + ii, p.BN - 1);
               } else {
                 col[j] = min(i0 + j, p.BN - 1);
               }
@@ -377,16 +417,17 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
             for (int cc = cf; cc <= cl; ++cc) {
               const float* src = p.ws + (size_t)(cc == cf ? slot_f : 2 * cc) * p.BN * 128 + ml;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) acc[j] += __ldcg(src + (size_t)col[j] * 128);
+              for (int j = 0; j < SR; ++j) acc[j] += __ldcg(src + (size_t)col[j] * 128);
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stg[j * 128 + ml] = acc[j];
-            epi_bar();
-            epilogue_tile<bf16>(epi, stg, 128, p.split ? 16 : -1, m0, row0 + i0,
+            for (int j = 0; j < SR; ++j) gstg[j * 128 + ml] = acc[j];
+            epi_bar(eg);
+            epilogue_tile<bf16>(epi, gstg, 128, p.split ? half : -1, m0, row0 + i0,
                                 min(step, lrows - i0), et, 128);
-            epi_bar();
+            epi_bar(eg);
           }
-          if (et == 0) p.counters[tile] = 0u;
+          epi_bar_all<NEG>();
+          if (eg == 0 && et == 0) p.counters[tile] = 0u;
         }
       }
     }
@@ -491,7 +532,9 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
     tc_destroy(p);
     return PEAGLE_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           227 * 1024) != cudaSuccess ||
+      cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess) {
     tc_destroy(p);
     return PEAGLE_ERR_CUDA;
@@ -536,6 +579,8 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     p.n_tiles = (R + p.BN - 1) / p.BN;
   }
   p.KB = Kd / 64;
+  // large-M projections are tensor-bound: two epilogue groups keep up with the MMA
+  const int neg = p.n_tiles > 1 ? 2 : 1;
   const int m_tiles = (Nout + 127) / 128;
   const long long tiles = (long long)m_tiles * p.n_tiles;
   p.m_tiles = m_tiles;
@@ -570,7 +615,7 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   if (!encode_map(pl, &mx, X, xrows, Kd, ldx, p.two_box ? 128 : p.BN)) return PEAGLE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(TC_THREADS);
+  cfg.blockDim = dim3(neg == 1 ? TC_THREADS : TC_THREADS2);
   cfg.dynamicSmemBytes = smem_bytes(stages, p.BN);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -578,7 +623,8 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, mw, mx, p, epi);
+  cudaError_t e = neg == 1 ? cudaLaunchKernelEx(&cfg, tc_gemm_kernel<1>, mw, mx, p, epi)
+                            : cudaLaunchKernelEx(&cfg, tc_gemm_kernel<2>, mw, mx, p, epi);
   return e == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
 }
 
