@@ -313,10 +313,39 @@ def draft_pass(W: Weights64, dims, cache_k, cache_v, seq_lens, target_hidden, ne
     """
     if bf16 is None:
         bf16 = DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    E, Hin = input_rows(W, dims, target_hidden, new_token, K)
+    return _drafter_block(W, dims, cache_k, cache_v, seq_lens, E, Hin, K, bf16)
+
+
+def catch_up(W: Weights64, dims, cache_k, cache_v, seq_lens, hidden, tokens, bf16=None):
+    """Drafter catch-up: T accepted tokens per request run as depth-1 (NTP) rows.
+
+    Row t of request b takes embed[tokens[b, t]] and fc(hidden[b, t]) (the target's
+    hidden states captured for that token), sits at position seq_lens[b] + t, and attends
+    to the cached context and to rows 0..t -- the causal depth-1 attention of the
+    training mask ("Flex-attention mask": depth-0 positions see each other causally), run
+    over the new tokens of a speculative round so that their keys and values enter the
+    drafter's cache ([TD] "Technical Architecture", stage 1).
+    hidden: [B, T, 3H]; tokens: [B, T].  Returns a DraftResult over the T rows (k_rows /
+    v_rows are the keys and values written for slots seq_lens[b] + t).
+    """
+    if bf16 is None:
+        bf16 = DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    hid = to64(hidden)
+    B, T = hid.shape[0], hid.shape[1]
+    tokens = np.asarray(tokens)
+    E = np.stack([to64(W.embed[int(tokens[b, t])]) for b in range(B) for t in range(T)])
+    Hin = hid.reshape(B * T, -1)
+    return _drafter_block(W, dims, cache_k, cache_v, seq_lens, E, Hin, T, bf16)
+
+
+def _drafter_block(W: Weights64, dims, cache_k, cache_v, seq_lens, E, Hin, K, bf16):
+    """N decoder layers and the LM head over a K-row block per request (row r = b*K + j at
+    position seq_lens[b] + j, causal within the block) given the rows' embeddings E and
+    3H hidden inputs Hin."""
     cast = _cast_fn(bf16, "xn")
     seq_lens = np.asarray(seq_lens, np.int64)
     B = len(seq_lens)
-    E, Hin = input_rows(W, dims, target_hidden, new_token, K)
     x0, res = first_layer_input(W, dims, E, Hin, bf16)
     pos = np.array([seq_lens[b] + j for b in range(B) for j in range(K)], np.int64)
     k_rows, v_rows = [], []

@@ -529,3 +529,51 @@ def test_training_forward_prefix_closure():
     idx = {(int(p), int(d)): i for i, (p, d) in enumerate(clo)}
     for t, (p, d) in enumerate(tgt):
         assert np.allclose(sub[idx[(int(p), int(d))]], full[len(rows) - 3 + t], atol=1e-10)
+
+
+# ------------------------------------------------------------------ drafter catch-up
+
+
+def _catch_inputs(dims, T, L, seed):
+    w = synth.make_weights(dims, seed)
+    wl = synth.Workload("s", dims, 1, 4, (L,))
+    inp = synth.make_decode_inputs(wl, seed + 1, capacity=L + T + 4)
+    hid = synth.normal((1, T, 3 * dims.hidden), seed + 2, 1.0)
+    tok = synth.uniform_ints(T, 0, dims.target_vocab, seed + 3).reshape(1, T)
+    return O.Weights64.from_synth(w), inp, hid, tok
+
+
+def test_catch_up_on_empty_cache_is_the_causal_depth1_forward():
+    """With no cached context, the catch-up rows are exactly the depth-1 rows of the
+    training-style forward (plain causal attention): two independently written paths."""
+    dims = synth.DIMS_TINY
+    T = 6
+    W, inp, hid, tok = _catch_inputs(dims, T, 0, 31)
+    r = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], [0], hid, tok, bf16=False)
+    rows = np.array([(p, 1) for p in range(T)])
+    lg, am, _ = O.forward_parallel(W, dims, tok[0], hid[0], rows, bf16=False)
+    assert np.max(np.abs(r.logits[0] - lg)) < 1e-12
+    assert np.array_equal(r.argmax[0], am)
+
+
+def test_catch_up_single_row_is_the_ntp_row():
+    dims = synth.DIMS_TINY
+    W, inp, hid, tok = _catch_inputs(dims, 1, 9, 41)
+    r = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], [9], hid, tok, bf16=False)
+    d = O.draft_pass(W, dims, inp["cache_k"], inp["cache_v"], [9], hid[:, 0], tok[:, 0], 1,
+                     bf16=False)
+    assert np.max(np.abs(r.logits - d.logits)) < 1e-12
+    for li in range(dims.n_layers):
+        assert np.max(np.abs(r.k_rows[li] - d.k_rows[li])) < 1e-12
+
+
+def test_catch_up_is_causal():
+    dims = synth.DIMS_TINY
+    T = 4
+    W, inp, hid, tok = _catch_inputs(dims, T, 5, 51)
+    a = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], [5], hid, tok, bf16=False)
+    tok2 = tok.copy()
+    tok2[0, T - 1] = (tok2[0, T - 1] + 1) % dims.target_vocab
+    b = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], [5], hid, tok2, bf16=False)
+    assert np.array_equal(a.logits[0, : T - 1], b.logits[0, : T - 1])
+    assert np.max(np.abs(a.logits[0, T - 1] - b.logits[0, T - 1])) > 1e-6
