@@ -30,7 +30,8 @@ PEAGLE_F32 = 0
 PEAGLE_BF16 = 1
 
 # every entry point declared in include/peagle.h
-EXPORTS = ("peagle_create", "peagle_draft", "peagle_verify_greedy", "peagle_append_kv",
+EXPORTS = ("peagle_create", "peagle_draft", "peagle_catch_up", "peagle_verify_greedy",
+           "peagle_append_kv",
            "peagle_forward_parallel", "peagle_cod_rows", "peagle_sequence_partition",
            "peagle_status",
            "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
@@ -84,6 +85,8 @@ def lib():
                                     ctypes.POINTER(_vp)]
         L.peagle_draft.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _vp, _i32,
                                    _vp, _vp, _vp]
+        L.peagle_catch_up.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _vp, _i32,
+                                      _vp, _vp, _vp]
         L.peagle_verify_greedy.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
         L.peagle_append_kv.argtypes = [_vp, _i32, ctypes.POINTER(PeagleKV), _vp, _vp, _i32,
                                        _vp, _vp, _i32, _vp]
@@ -210,6 +213,15 @@ def peagle_draft(ctx: Context, batch, kv: PeagleKV, seq_lens, target_hidden, new
                               _ptr(target_hidden), _ptr(new_token), int(K),
                               _ptr(out_draft_tokens), _ptr(out_logits), _stream_ptr(stream)),
            "peagle_draft")
+
+
+def peagle_catch_up(ctx: Context, batch, kv: PeagleKV, seq_lens, hidden, tokens, T,
+                    out_tokens=None, out_logits=None, stream=None):
+    """Run the accepted tokens through the drafter and write their K/V (include/peagle.h)."""
+    _check(lib().peagle_catch_up(ctx.handle, int(batch), ctypes.byref(kv), _ptr(seq_lens),
+                                 _ptr(hidden), _ptr(tokens), int(T), _ptr(out_tokens),
+                                 _ptr(out_logits), _stream_ptr(stream)),
+           "peagle_catch_up")
 
 
 def peagle_verify_greedy(batch, K, draft_tokens, target_argmax, out_accept_len, out_bonus,

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(ROW_THREADS) input_fusion_kernel(
   if (mode == 0) {
     src = r / K;
     ntp = (r - src * K) == 0;
+  } else if (mode == 2) {  // catch-up: row r has its own token and fc row
+    src = r;
+    ntp = true;
   } else {
     src = row_p[r];
     ntp = row_d[r] == 1;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(ROW_THREADS) input_fusion_kernel(
     if (ntp) f[i] = 0;
   }
   if (threadIdx.x == 0 && keys) keys[r] = 0ull;
-  if (threadIdx.x == 0 && mode == 0 && row_pos_out) row_pos_out[r] = seq_lens[src] + (r - src * K);
+  if (threadIdx.x == 0 && mode != 1 && row_pos_out) row_pos_out[r] = seq_lens[r / K] + r % K;
 }
 
 template <typename T>
@@ -909,7 +912,7 @@ __global__ void argmax_decode_kernel(int R, unsigned long long* keys, const int*
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
   const int idx = argmax_key_index(keys[r]);
-  out[r] = d2t ? idx + d2t[idx] : idx;
+  if (out) out[r] = d2t ? idx + d2t[idx] : idx;
   keys[r] = 0ull;
 }
 

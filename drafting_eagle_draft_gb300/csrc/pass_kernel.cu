@@ -212,7 +212,8 @@ __device__ void step_input(const PassParams& P, int c, int G, int et, unsigned l
   int c0, c1;
   col_range(P, c, G, c0, c1);
   const int nc = c1 - c0;
-  for (int b = et; b < P.B; b += 128) {
+  const int n_tok = P.all_ntp ? R : P.B;  // catch-up: a token per row
+  for (int b = et; b < n_tok; b += 128) {
     int tok = P.new_token[b];
     if (tok < 0 || tok >= P.Vt) {
       if (c == 0) raise_error(P.err, PEAGLE_DEV_BAD_TOKEN);
@@ -235,11 +236,13 @@ __device__ void step_input(const PassParams& P, int c, int G, int et, unsigned l
       const bool ok = idx < R * nc;
       const int r = ok ? idx / nc : 0, col = ok ? c0 + idx - (idx / nc) * nc : c0;
       const int b = r / K, j = r - b * K;
+      const bool ntp = P.all_ntp || j == 0;
+      const int src = P.all_ntp ? r : b;  // token / fc row of an NTP row
       rr[u] = ok ? r : -1;
       cc[u] = col;
-      const bf16* e = j == 0 ? (const bf16*)P.embed + (size_t)s_tok[b] * H : (const bf16*)P.emb_mask;
+      const bf16* e = ntp ? (const bf16*)P.embed + (size_t)s_tok[src] * H : (const bf16*)P.emb_mask;
       ev[u] = ok ? ld(e + col) : 0.f;
-      fq[u] = ok ? (j == 0 ? P.F[(size_t)b * H + col] : P.f_shared[col]) : 0;
+      fq[u] = ok ? (ntp ? P.F[(size_t)src * H + col] : P.f_shared[col]) : 0;
       g1[u] = ok ? ld(gi + col) : 0.f;
       g2[u] = ok ? ld(gh + col) : 0.f;
     }
@@ -252,7 +255,9 @@ __device__ void step_input(const PassParams& P, int c, int G, int et, unsigned l
       store_act<bf16>(X0, 2 * H, r, R, P.split, col, ev[u] * g1[u]);
       store_act<bf16>(X0, 2 * H, r, R, P.split, H + col, fv * g2[u]);
       P.res[(size_t)r * H + col] = fq[u];
-      if (r % K == 0) P.F[(size_t)(r / K) * H + col] = 0;  // read only here: clear for the next pass
+      // the fc rows are read only here: clear them for the next pass
+      if (P.all_ntp) P.F[(size_t)r * H + col] = 0;
+      else if (r % K == 0) P.F[(size_t)(r / K) * H + col] = 0;
       atomicAdd(&s_rs[r], (unsigned long long)to_fx(ev[u] * ev[u]));
       atomicAdd(&s_rs[PASS_MAX_ROWS + r], (unsigned long long)to_fx(fv * fv));
     }
@@ -581,6 +586,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     unsigned* const tile_cnt = P.tile_cnt;
     int seg = 0;
     bool alive = true;
+    // sums-of-squares slots start at zero: cleared before this CTA signals the first step,
+    // so before any CTA's input step accumulates into them
+    if (c == 0)
+      for (int i = et; i < PASS_SS_SLOTS * P.R; i += 128) P.ss[i] = 0;
     for (int j = 0; j < n_phase && alive; ++j) {
       const PassPhase& ph = P.ph[j];
       if (ph.kind == PP_GEMM) {
@@ -752,12 +761,11 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             }
           }
         } else if (ph.kind == PP_ARGMAX) {
-          for (int r = c * 128 + et; r < P.R; r += G * 128) {
-            const int idx = argmax_key_index(P.keys[r]);
-            P.out_tokens[r] = P.d2t ? idx + P.d2t[idx] : idx;
-          }
-          // every sum-of-squares slot has been consumed: clear them for the next pass
-          for (int i = c * 128 + et; i < PASS_SS_SLOTS * P.R; i += G * 128) P.ss[i] = 0;
+          if (P.out_tokens)
+            for (int r = c * 128 + et; r < P.R; r += G * 128) {
+              const int idx = argmax_key_index(P.keys[r]);
+              P.out_tokens[r] = P.d2t ? idx + P.d2t[idx] : idx;
+            }
         }
       }
       wk_signal(P, j, et);

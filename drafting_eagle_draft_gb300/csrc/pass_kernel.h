@@ -87,8 +87,9 @@ struct PassParams {
   unsigned long long* trace_cta;  // timing: [phase][CTA][4] event times, or null
   // per call
   const int* seq_lens;
-  const int* new_token;
-  int* out_tokens;
+  const int* new_token;  // draft: [B] new tokens; catch-up: [B * K] tokens of the rows
+  int all_ntp;           // catch-up: every row takes its own token and hidden state
+  int* out_tokens;       // [R] or null
   AttnArgs att;        // per layer: kc / vc advanced by layer_stride bytes
   PassPhase ph[PASS_MAX_PHASE];
   PassGemm gemm[PASS_MAX_GEMM];

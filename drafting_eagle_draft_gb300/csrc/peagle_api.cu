@@ -286,7 +286,8 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   const int logical_rows = d.max_batch * d.max_K > d.max_rows ? d.max_batch * d.max_K : d.max_rows;
   c->rows_max = 2 * logical_rows;
   const int R = c->rows_max;
-  const int fr = d.max_batch > d.max_seq ? d.max_batch : d.max_seq;
+  // fc outputs: one per request (draft pass), per row (catch-up) or per position (forward)
+  const int fr = d.max_batch * d.max_K > d.max_seq ? d.max_batch * d.max_K : d.max_seq;
   TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 8));
   TRY(dalloc(c, (void**)&c->f_shared, (size_t)H * 8));
   TRY(dalloc(c, &c->X0, (size_t)R * 2 * H * es));
@@ -375,7 +376,7 @@ static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchun
 // multi-kernel path below.  Returns PEAGLE_ERR_UNSUPPORTED for shapes it does not cover
 // (the caller then runs the multi-kernel path).
 static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* seq_lens,
-                      const void* target_hidden, const int32_t* new_token, int K,
+                      const void* target_hidden, const int32_t* new_token, int K, bool all_ntp,
                       int32_t* out_tokens, float* out_logits, cudaStream_t s) {
   const peagle_dims& d = c->d;
   const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
@@ -458,7 +459,9 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     e.out_fx = c->F;
     e.out_ld = H;
     cur_stage = PEAGLE_STAGE_FC;
-    add_gemm(c->fc, 3 * H, target_hidden, 3 * H, H, 3 * H, B, 0, e, -1);
+    const int fc_rows = all_ntp ? R : B;  // catch-up: every row has its own hidden state
+    e.R = fc_rows;
+    add_gemm(c->fc, 3 * H, target_hidden, 3 * H, H, 3 * H, fc_rows, 0, e, -1);
   }
   add_phase(PP_INPUT, -1, nullptr);
   const int input_phase = P.n_phase - 1;
@@ -513,9 +516,10 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
                ed, -2);
     }
   }
-  add_phase(PP_NORM, -1, c->final_norm);
-  P.ph[P.n_phase - 1].slot = slot;
-  {
+  const bool lm = out_tokens || out_logits;  // the catch-up may skip the LM head
+  if (lm) add_phase(PP_NORM, -1, c->final_norm);
+  if (lm) P.ph[P.n_phase - 1].slot = slot;
+  if (lm) {
     EpiArgs e = epi_base(c, EPI_LMHEAD, R, d.draft_vocab);
     e.in_split = split;
     e.logits = out_logits;
@@ -524,7 +528,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     cur_stage = PEAGLE_STAGE_LMHEAD;
     add_gemm(c->lm_head, H, c->Xn, H, d.draft_vocab, H, R, split, e, -2);
   }
-  add_phase(PP_ARGMAX, -1, nullptr);
+  if (lm) add_phase(PP_ARGMAX, -1, nullptr);
   if (slot > PASS_SS_SLOTS) fail = true;
   if (fail) return PEAGLE_ERR_UNSUPPORTED;
 
@@ -602,6 +606,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   P.err = c->err;
   P.seq_lens = seq_lens;
   P.new_token = new_token;
+  P.all_ntp = all_ntp ? 1 : 0;
   P.out_tokens = out_tokens;
   P.trace = nullptr;
   P.trace_cta = nullptr;
@@ -622,13 +627,12 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   return pass_launch(P, hd, grid, s);
 }
 
-extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
-                            const int32_t* seq_lens, const void* target_hidden,
-                            const int32_t* new_token, int32_t K, int32_t* out_draft_tokens,
-                            float* out_logits, void* stream) {
-  if (!c || !kv || !kv->k || !kv->v || !seq_lens || !target_hidden || !new_token ||
-      !out_draft_tokens)
-    return PEAGLE_ERR_INVALID;
+// The draft pass (all_ntp = false: row 0 of each request NTP, rows 1.. MTP) and the
+// catch-up pass (all_ntp: every row takes its own token and hidden state).
+static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
+                      const int32_t* seq_lens, const void* target_hidden,
+                      const int32_t* new_token, int32_t K, bool all_ntp,
+                      int32_t* out_draft_tokens, float* out_logits, cudaStream_t stream) {
   const peagle_dims& d = c->d;
   if (batch < 1 || K < 1) return PEAGLE_ERR_INVALID;
   if (batch > d.max_batch || K > d.max_K || batch > kv->batch) return PEAGLE_ERR_CAPACITY;
@@ -641,20 +645,22 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   const size_t es = c->es;
   const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
   if (c->pass_on) {
-    const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K,
+    const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K, all_ntp,
                              out_draft_tokens, out_logits, s);
     if (r != PEAGLE_ERR_UNSUPPORTED) return r;
   }
 
   // S1: fc over the NTP rows' target hidden states, then the fused input rows
+  const int fc_rows = all_ntp ? R : batch;
   {
-    EpiArgs e = epi_base(c, EPI_STORE, batch, H);
+    EpiArgs e = epi_base(c, EPI_STORE, fc_rows, H);
     e.out_fx = c->F;
     e.out_ld = H;
-    GEMM(PEAGLE_STAGE_FC, c, c->fc, target_hidden, 3 * H, H, 3 * H, batch, e, s);
+    GEMM(PEAGLE_STAGE_FC, c, c->fc, target_hidden, 3 * H, H, 3 * H, fc_rows, e, s);
   }
   TIMED(PEAGLE_STAGE_NORM,
-        launch_input_fusion(c->bf, 0, R, K, batch, H, c->embed, d.target_vocab, c->emb_mask,
+        launch_input_fusion(c->bf, all_ntp ? 2 : 0, R, K, fc_rows, H, c->embed, d.target_vocab,
+                            c->emb_mask,
                             c->F, c->f_shared, new_token, nullptr, nullptr, c->input_norm,
                             c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, seq_lens,
                             c->row_pos, c->err, s));
@@ -730,7 +736,12 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       GEMM(PEAGLE_STAGE_DOWN, c, c->down[l], c->act, d.intermediate, H, d.intermediate, R, e, s);
     }
   }
-  // S6: final norm, LM head with fused argmax, d2t remap
+  // S6: final norm, LM head with fused argmax, d2t remap (skipped by a catch-up pass that
+  // asks for neither tokens nor logits)
+  if (!out_draft_tokens && !out_logits) {
+    cudaError_t ce = cudaGetLastError();
+    return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_catch_up launch");
+  }
   TIMED(PEAGLE_STAGE_NORM,
         launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, split, c->Xn, s));
   {
@@ -740,9 +751,33 @@ extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
     e.keys = c->keys;
     GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_head, c->Xn, H, d.draft_vocab, H, R, e, s);
   }
-  TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, out_draft_tokens, s));
+  if (out_draft_tokens)
+    TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, out_draft_tokens, s));
+  else
+    TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, nullptr, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_draft launch");
+}
+
+extern "C" int peagle_draft(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
+                            const int32_t* seq_lens, const void* target_hidden,
+                            const int32_t* new_token, int32_t K, int32_t* out_draft_tokens,
+                            float* out_logits, void* stream) {
+  if (!c || !kv || !kv->k || !kv->v || !seq_lens || !target_hidden || !new_token ||
+      !out_draft_tokens)
+    return PEAGLE_ERR_INVALID;
+  return draft_impl(c, batch, kv, seq_lens, target_hidden, new_token, K, false,
+                    out_draft_tokens, out_logits, (cudaStream_t)stream);
+}
+
+extern "C" int peagle_catch_up(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
+                               const int32_t* seq_lens, const void* hidden,
+                               const int32_t* tokens, int32_t T, int32_t* out_tokens,
+                               float* out_logits, void* stream) {
+  if (!c || !kv || !kv->k || !kv->v || !seq_lens || !hidden || !tokens)
+    return PEAGLE_ERR_INVALID;
+  return draft_impl(c, batch, kv, seq_lens, hidden, tokens, T, true, out_tokens, out_logits,
+                    (cudaStream_t)stream);
 }
 
 extern "C" int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* draft_tokens,

@@ -137,6 +137,23 @@ int peagle_draft(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv, const int3
                  const void* target_hidden, const int32_t* new_token, int32_t K,
                  int32_t* out_draft_tokens, float* out_logits, void* stream);
 
+/* Drafter catch-up ("P-EAGLE: A Technical Deep Dive into Parallel Speculative Decoding",
+ * section "Technical Architecture", stage 1 of a round): the T tokens a request accepted
+ * (and their captured target hidden states) run through the drafter as depth-1 rows --
+ * row t takes embed[tokens[b, t]] and fc(hidden[b, t]) at position seq_lens[b] + t and
+ * attends to the cached context and rows 0..t ("Speeding LLM inference with P-EAGLE in
+ * vLLM/Speculators", "Flex-attention mask": depth-1 rows are causal among themselves) --
+ * and their keys and values are written to cache slots seq_lens[b] + t.  seq_lens is not
+ * advanced: commit with peagle_append_kv (k_rows = NULL, n_commit = T).
+ *   hidden    device [batch, T, 3H] (dims dtype); tokens device int32 [batch, T]
+ *   out_tokens device int32 [batch, T] (greedy next token of each row, target vocab) or
+ *   NULL; out_logits fp32 [batch, T, Vd] or NULL; with both NULL the final norm and the
+ *   LM head are skipped.
+ * Constraints and device checks as for peagle_draft (T plays K). */
+int peagle_catch_up(peagle_ctx* ctx, int32_t batch, const peagle_kv* kv,
+                    const int32_t* seq_lens, const void* hidden, const int32_t* tokens,
+                    int32_t T, int32_t* out_tokens, float* out_logits, void* stream);
+
 /* Greedy verification ("EAGLE-4 overview"): for each request, the longest prefix of
  * draft_tokens[b, :] equal to target_argmax[b, :], plus one bonus token.
  *   draft_tokens   device int32 [batch, K]
