@@ -186,11 +186,15 @@ def run_ours(args, rank, world, dist):
     tgt_np, _ = synth.geometric_target_argmax(toks.cpu().numpy(), dims.target_vocab, 0.7, 6)
     tgt = torch.from_numpy(tgt_np).to(dev)
 
+    # the step commits the draft block's NTP row (the new token's K/V; the accepted drafts'
+    # own K/V come from a catch-up pass with their target hidden states)
+    ntp_only = torch.zeros(B, dtype=torch.int32, device=dev)
+
     def step():
         sl.copy_(sl0)
         pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
         pk.peagle_verify_greedy(B, K, toks, tgt, acc, bonus, stream)
-        pk.peagle_append_kv(ctx, B, kv, sl, acc, stream=stream, n_extra=1)
+        pk.peagle_append_kv(ctx, B, kv, sl, ntp_only, stream=stream, n_extra=1)
 
     # warm-up (eager), then capture one step in a CUDA graph
     with torch.cuda.stream(stream):
@@ -285,7 +289,7 @@ def run_ours(args, rank, world, dist):
         sl.copy_(sl_h, non_blocking=True)
         pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
         pk.peagle_verify_greedy(B, K, toks, tgt, acc, bonus, stream)
-        pk.peagle_append_kv(ctx, B, kv, sl, acc, stream=stream, n_extra=1)
+        pk.peagle_append_kv(ctx, B, kv, sl, ntp_only, stream=stream, n_extra=1)
         toks_h.copy_(toks, non_blocking=True)
         acc_h.copy_(acc, non_blocking=True)
         bonus_h.copy_(bonus, non_blocking=True)
