@@ -55,7 +55,8 @@ struct peagle_ctx {
   unsigned last_err_bits;
   TcGemmPlan* tc;   // tensor-core GEMM state (bf16 only)
   // persistent pass kernel (bf16): phase counters + abort flag, host-side parameter block
-  bool pass_on;
+  bool pass_on;     // available (bf16, cooperative launch, not disabled)
+  bool pass_force;  // PEAGLE_PASS_KERNEL=1: use it for every shape it supports
   unsigned* pass_cnt;
   PassParams* pp;
   // timing of the pass kernel: per-call phase completion times (device slots) and the
@@ -339,6 +340,7 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     const char* env = getenv("PEAGLE_PASS_KERNEL");
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+    c->pass_force = env && env[0] == '1';
     if (coop && !(env && env[0] == '0')) {
       TRY(dalloc(c, (void**)&c->pass_cnt, (size_t)(PASS_MAX_PHASE + 1) * 4));
       TRY(dalloc(c, (void**)&c->pass_trace,
@@ -644,7 +646,12 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   const int split = use_split(c);
   const size_t es = c->es;
   const size_t layer_stride = (size_t)kv->batch * nkv * kv->capacity * hd * es;
-  if (c->pass_on) {
+  // The persistent pass kernel wins when the pass is a chain of short steps (few draft
+  // rows); with many rows its four worker warps per SM become the limit (attention over
+  // long ragged contexts, the spread norm steps), and the multi-kernel path, whose
+  // attention runs several CTAs per SM, is faster: decode_b1 (8 rows) 431 vs 448 us,
+  // decode_b2 (16 rows) 613 vs 609 us, ragged_b16 (80 rows) 1927 vs 1465 us.
+  if (c->pass_on && (c->pass_force || R <= 16)) {
     const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K, all_ntp,
                              out_draft_tokens, out_logits, s);
     if (r != PEAGLE_ERR_UNSUPPORTED) return r;

@@ -249,7 +249,9 @@ int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches
 
 /* Diagnostics of the persistent pass kernel (the bf16 draft pass as one launch of one CTA
  * per SM, used unless the environment variable PEAGLE_PASS_KERNEL=0 was set when the
- * context was created).  For the latest pass run while timing was enabled, writes four
+ * context was created; with no variable set it runs passes of up to 16 draft rows,
+ * PEAGLE_PASS_KERNEL=1 uses it for every shape it supports).  For the latest pass run
+ * while timing was enabled, writes four
  * globaltimer values (ns) per step of the pass and CTA, as out[(phase * ctas + cta) * 4 + k]:
  * k = 0 the step's activations were seen ready, 1 its first MMA was issued, 2 its last
  * accumulator was committed (projections only, else 0), 3 the CTA finished the step; and
