@@ -215,6 +215,8 @@ CAST_POINTS = ("x0", "xn", "q", "kv", "o", "act", "y")
 # product's operands (post-RoPE queries; the softmax weights are rounded too, which this
 # profile does not model and the logit tolerance absorbs).
 DRAFT_BF16_CASTS = frozenset({"kv", "q"})
+# The training-style forward rounds at the same points.
+FORWARD_BF16_CASTS = DRAFT_BF16_CASTS
 # Every storage point rounded to bf16 (a plain all-bf16 pipeline); kept for comparisons.
 ALL_BF16_CASTS = frozenset(CAST_POINTS)
 
@@ -507,7 +509,7 @@ def forward_parallel(W: Weights64, dims, tokens, hidden, rows, bf16=None):
     Returns (logits [M, Vd], argmax [M], margin [M]).
     """
     if bf16 is None:
-        bf16 = DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+        bf16 = FORWARD_BF16_CASTS if dims.dtype == "bf16" else False
     cx0, cxn, cq, ckv = (_cast_fn(bf16, k) for k in ("x0", "xn", "q", "kv"))
     co, cact = _cast_fn(bf16, "o"), _cast_fn(bf16, "act")
     rows = np.asarray(rows, np.int64)

@@ -64,7 +64,7 @@ def test_forward_parallel_small(dims, n, K, r):
     am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
     ctx.close()
     W = O.Weights64.from_synth(w)
-    casts = O.DRAFT_BF16_CASTS if dims.dtype == "bf16" else False
+    casts = O.FORWARD_BF16_CASTS if dims.dtype == "bf16" else False
     ref_logits, ref_am, ref_margin = O.forward_parallel(W, dims, tokens, hidden, rows, bf16=casts)
     _compare(dims, ref_logits, ref_am, ref_margin, am, lg, f"fwd n={n} K={K}")
 
@@ -107,7 +107,7 @@ def test_forward_parallel_dependency_closure():
     am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
     ctx.close()
     W = O.Weights64.from_synth(w)
-    rl, ra, rm = O.forward_parallel(W, dims, tokens, hidden, clo, bf16=O.DRAFT_BF16_CASTS)
+    rl, ra, rm = O.forward_parallel(W, dims, tokens, hidden, clo, bf16=O.FORWARD_BF16_CASTS)
     _compare(dims, rl, ra, rm, am, lg, "fwd dependency closure")
 
 
@@ -178,12 +178,12 @@ def test_train_fwd_full_prefix_and_tail():
     W = O.Weights64.from_synth(w, lazy=True)
     pre = rows[rows[:, 0] < 96]
     rl, ra, rm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], pre,
-                                    bf16=O.DRAFT_BF16_CASTS)
+                                    bf16=O.FORWARD_BF16_CASTS)
     _compare(dims, rl, ra, rm, am[: len(pre)], lg[: len(pre)], "train_fwd prefix")
     tail = rows[-3:]
     clo = O.dependency_closure(rows, tail)
     cl, ca, cm = O.forward_parallel(W, dims, ti["tokens"], ti["hidden"], clo,
-                                    bf16=O.DRAFT_BF16_CASTS)
+                                    bf16=O.FORWARD_BF16_CASTS)
     idx = {(int(p), int(d)): i for i, (p, d) in enumerate(clo)}
     sel = [idx[(int(p), int(d))] for p, d in tail]
     _compare(dims, cl[sel], ca[sel], cm[sel], am[-3:], lg[-3:], "train_fwd tail")
