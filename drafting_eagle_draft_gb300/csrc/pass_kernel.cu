@@ -164,12 +164,11 @@ __device__ __forceinline__ void trace_ev(const PassParams& P, int ph, int k) {
 }
 
 // Every worker has finished its part of phase `ph`: publish it.  The CTA barrier orders
-// the workers' writes before thread 0's fence, which makes them visible at GPU scope before
-// the release add (the pattern of a cooperative grid barrier).
+// the workers' writes before thread 0's release add, whose release semantics (cumulative
+// at GPU scope) make them visible to every CTA that acquires the count.
 __device__ __forceinline__ void wk_signal(const PassParams& P, int ph, int et) {
   wk_bar();
   if (et == 0) {
-    __threadfence();
     fence_proxy_async_global();
     red_release_add(P.phase_cnt + ph, 1u);
     // timing: the phase completes when its last CTA signals
@@ -606,6 +605,19 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         }
         wk_bar();
         const EpiArgs& epi = *s_epi;
+        // the first row chunk's norm scales and RoPE positions, read while the tensor
+        // cores work (the norm step this projection depends on must be complete)
+        const int step = split ? 16 : 32;
+        if (c < Gm) {
+          if (!wk_wait_phase(P, m.dep, et, s_abort, s_flag)) {
+            alive = false;
+            break;
+          }
+          if (et < min(step, mR)) {
+            s_rscale[et] = epi_row_scale(epi, et);
+            s_rpos[et] = epi.row_pos ? epi.row_pos[et] : 0;
+          }
+        }
         if (c < Gm) {
           const long long beg = rbeg(c, total, Gm), end = rbeg(c + 1, total, Gm);
           for (long long it = beg; it < end;) {
@@ -632,7 +644,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             const long long t_beg = (long long)tile * KB;
             const int cf = owner(t_beg, total, Gm), cl = owner(t_beg + KB - 1, total, Gm);
             const uint32_t tb = tmem + (uint32_t)(buf * acc_stride) + ((uint32_t)(quarter * 32) << 16);
-            const int step = split ? 16 : 32;
             const int nch = (lrows + step - 1) / step;
             if (cf == cl || additive) {
               for (int ch = 0; ch < nch; ++ch) {
@@ -656,7 +667,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                   tc::fence_before_sync();
                   tc::mbar_arrive(&acce[buf]);
                 }
-                if (et < min(step, lrows - i0)) {
+                if (nch > 1 && et < min(step, lrows - i0)) {
                   s_rscale[et] = epi_row_scale(epi, row0 + i0 + et);
                   s_rpos[et] = epi.row_pos ? epi.row_pos[row0 + i0 + et] : 0;
                 }
@@ -707,7 +718,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                   }
 #pragma unroll
                   for (int q = 0; q < 32; ++q) stg[q * 128 + ml] = acc[q];
-                  if (et < min(step, lrows - i0)) {
+                  if (nch > 1 && et < min(step, lrows - i0)) {
                     s_rscale[et] = epi_row_scale(epi, row0 + i0 + et);
                     s_rpos[et] = epi.row_pos ? epi.row_pos[row0 + i0 + et] : 0;
                   }
