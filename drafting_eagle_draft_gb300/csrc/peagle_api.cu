@@ -363,7 +363,8 @@ static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchun
                            int waves = 2) {
   const int target = waves * c->num_sms;
   const int pairs = B * c->d.n_kv_heads;
-  int want = (target + pairs - 1) / pairs;
+  // one wave (the pass kernel: one item per CTA) must not spill a few items into a second
+  int want = waves == 1 ? target / pairs : (target + pairs - 1) / pairs;
   if (want < 1) want = 1;
   if (want > c->att_chunks_max) want = c->att_chunks_max;
   int ch = (cap + want - 1) / want;
