@@ -24,6 +24,7 @@
 // activation loads after it.
 #include <cuda.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <map>
 #include <mutex>
@@ -439,6 +440,250 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
   }
 }
 
+// -------------------------------------------------------------------------------------
+// CTA-pair variant for large-M GEMMs (the training-style forward): a cluster of two CTAs
+// on neighbouring SMs runs one tcgen05.mma.cta_group::2 of M = 256 weight rows x N = 256
+// activation rows.  Each CTA loads its own 128 weight rows and half of the activation
+// rows (the hi rows in the even CTA, the lo rows in the odd one, or rows 0-127 / 128-255),
+// so a k-block moves 32 KB into each SM instead of 48 KB: the operand stream from L2 is
+// what bounds the single-CTA kernel at about half the tensor peak.  The accumulator is
+// 128 lanes x 256 columns in each CTA's tensor memory, drained by each CTA's own epilogue.
+// Tiles are whole (no stream-K): pair-tile t = wave * pairs + pair.
+//
+// Hand-offs: both CTAs' loads of a stage complete on the even CTA's stage barrier (the
+// pair form of the tensor load), where the single issuing thread waits.  The MMA's commits
+// arrive on the stage-free and accumulator-full barriers of both CTAs (multicast); each
+// CTA's epilogue releases an accumulator with one arrive per group on the even CTA's
+// barrier.
+__device__ __forceinline__ int pair_tile_m(int t, const TcParams& p) {
+  return p.m_inner ? t % p.m_tiles : t / p.n_tiles;
+}
+__device__ __forceinline__ int pair_tile_n(int t, const TcParams& p) {
+  return p.m_inner ? t / p.m_tiles : t % p.n_tiles;
+}
+
+__global__ void __launch_bounds__(TC_THREADS2, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmX, const TcParams p,
+                        const EpiArgs epi) {
+  constexpr int NEG = 2;
+  constexpr int HB = 128 * 128;  // half of the activation rows of a k-block (128 x 64 bf16)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int S = p.stages;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + (size_t)S * A_BYTES;
+  float* stg = (float*)(sB + (size_t)S * HB);
+  uint64_t* full = (uint64_t*)((uint8_t*)stg + STAGE_F_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint64_t* acce = accf + 2;
+  uint64_t* done_bar = acce + 2;
+  uint32_t* s_tmem = (uint32_t*)(done_bar + 1);
+  volatile int* s_abort = (volatile int*)(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_ctarank();
+  const bool lead = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int T = p.m_tiles * p.n_tiles;  // pair-tiles
+  const int KB = p.KB;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);  // even CTA: its producer's arrive, both CTAs' bytes
+      tc::mbar_init(&empty[i], 1);           // the MMA's multicast commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&accf[i], 1);
+      tc::mbar_init(&acce[i], 2 * NEG);  // one arrive per epilogue group of each CTA
+    }
+    tc::mbar_init(done_bar, 1);
+    *s_abort = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmX);
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tc::tmem_alloc_pair(s_tmem, p.tmem_cols);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  tc::pdl_launch_dependents();
+
+  // this pair's tiles: t = pair, pair + npairs, ...
+  const int my_tiles = pair < T ? (T - 1 - pair) / npairs + 1 : 0;
+  const long long n_it = (long long)my_tiles * KB;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = p.m_inner ? tc::policy_evict_last() : tc::policy_evict_first();
+      const uint64_t pol_x = p.m_inner ? tc::policy_evict_first() : tc::policy_evict_last();
+      const uint32_t bytes = 2 * (A_BYTES + HB);  // both CTAs' loads count on the even one
+      const uint32_t lead_full = tc::mapa_shared(full, 0);
+      // A and B halves into this CTA's stage, completing on the even CTA's barrier
+      auto load = [&](int st, int kb, int wr, int xr, bool a, bool b) {
+        if (a)
+          tc::tma_load_2d_pair(sA + (size_t)st * A_BYTES, &tmW, kb * 64, wr,
+                               lead_full + (uint32_t)(st * 8), pol_w);
+        if (b)
+          tc::tma_load_2d_pair(sB + (size_t)st * HB, &tmX, kb * 64, xr,
+                               lead_full + (uint32_t)(st * 8), pol_x);
+      };
+      auto coords = [&](long long it, int* kb, int* wrow, int* xrow) {
+        const int ti = (int)(it / KB);
+        *kb = (int)(it - (long long)ti * KB);
+        const int t = pair + ti * npairs;
+        const int mt = pair_tile_m(t, p), nt = pair_tile_n(t, p);
+        *wrow = (2 * mt + (int)rank) * 128;
+        *xrow = p.split ? (rank ? p.R : 0) + nt * 128 : nt * 256 + (int)rank * 128;
+      };
+      const int npre = (int)(n_it < S ? n_it : S);
+      for (int i = 0; i < npre; ++i) {
+        int kb, wr, xr;
+        coords(i, &kb, &wr, &xr);
+        if (lead) tc::mbar_expect_tx(&full[i], bytes);
+        load(i, kb, wr, xr, true, false);
+      }
+      tc::pdl_wait();
+      for (int i = 0; i < npre; ++i) {
+        int kb, wr, xr;
+        coords(i, &kb, &wr, &xr);
+        load(i, kb, wr, xr, false, true);
+      }
+      int stage = npre % S;
+      uint32_t ph = (npre == S) ? 1u : 0u;
+      for (long long it = npre; it < n_it; ++it) {
+        if (!tc::mbar_wait_cluster(&empty[stage], ph ^ 1u, s_abort)) {
+          raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        int kb, wr, xr;
+        coords(it, &kb, &wr, &xr);
+        if (lead) tc::mbar_expect_tx(&full[stage], bytes);
+        load(stage, kb, wr, xr, true, true);
+        if (++stage == S) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && lead) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      const uint32_t idesc = tc::idesc_bf16(256, 256);
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int ti = 0; ti < my_tiles && ok; ++ti) {
+        const int buf = ti & 1;
+        const uint32_t use = (uint32_t)(ti >> 1);
+        if (!tc::mbar_wait_cluster(&acce[buf], (use & 1u) ^ 1u, s_abort)) {
+          raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(buf * 256);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait_cluster(&full[stage], ph, s_abort)) {
+            raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)stage * A_BYTES));
+          const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)stage * HB));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          issued = true;
+          tc::mma_commit_pair(&empty[stage], (uint16_t)3);
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit_pair(&accf[buf], (uint16_t)3);
+      }
+      // every MMA (they write both CTAs' tensor memory) is complete before the pair parts
+      if (issued) {
+        tc::mma_commit_pair(done_bar, (uint16_t)1);
+        int never = 0;
+        tc::mbar_wait(done_bar, 0, &never, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int eg = (threadIdx.x - 64) >> 7;
+    const int et = (threadIdx.x - 64) & 127;
+    const int quarter = warp & 3;
+    const int ml = quarter * 32 + lane;
+    const int R = p.R;
+    float* gstg = stg + (size_t)eg * (32 / NEG) * 128;
+    const uint32_t lead_acce = tc::mapa_shared(acce, 0);
+    auto release = [&](int buf) {  // this group is done reading accumulator `buf`
+      if (lead) tc::mbar_arrive(&acce[buf]);
+      else tc::mbar_arrive_remote(lead_acce + (uint32_t)(buf * 8));
+    };
+    for (int ti = 0; ti < my_tiles; ++ti) {
+      const int t = pair + ti * npairs;
+      const int buf = ti & 1;
+      const uint32_t use = (uint32_t)(ti >> 1);
+      if (et == 0 && !tc::mbar_wait_cluster(&accf[buf], use & 1u, s_abort)) {
+        raise_error(p.err, PEAGLE_DEV_TIMEOUT);
+        *s_abort = 1;
+      }
+      epi_bar(eg);
+      if (*s_abort) break;
+      tc::fence_after_sync();
+      const int mt = pair_tile_m(t, p), nt = pair_tile_n(t, p);
+      const int m0 = (2 * mt + (int)rank) * 128;
+      const int row0 = nt * p.rpt;
+      const int lrows = min(p.rpt, R - row0);
+      const uint32_t tb = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quarter * 32) << 16);
+      const int step = (p.split ? 16 : 32) / NEG;
+      const int nch = (lrows + step - 1) / step;
+      for (int ch = eg; ch < nch; ch += NEG) {
+        const int i0 = ch * step;
+        float v[8], w[8];
+        tc::tmem_ld8(tb + i0, v);
+        tc::tmem_ld8(tb + (p.split ? p.lo_col : 8) + i0, w);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          gstg[j * 128 + ml] = v[j];
+          gstg[(8 + j) * 128 + ml] = w[j];
+        }
+        const bool last = ch + NEG >= nch;
+        if (last) tc::fence_before_sync();
+        epi_bar(eg);
+        if (last && et == 0) release(buf);
+        if (m0 < epi.Nout)
+          epilogue_tile<bf16>(epi, gstg, 128, p.split ? 16 / NEG : -1, m0, row0 + i0,
+                              min(step, lrows - i0), et, 128);
+        epi_bar(eg);
+      }
+      if (eg >= nch && et == 0) release(buf);
+    }
+  }
+  __syncwarp();
+  tc::fence_before_sync();
+  tc::cluster_sync();  // no CTA leaves while its partner's MMAs or arrivals may target it
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, p.tmem_cols);
+  }
+}
+
 // =====================================================================================
 // host side
 // =====================================================================================
@@ -449,6 +694,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 struct TcGemmPlan {
   int num_sms;
+  bool pair;  // large-M GEMMs on CTA pairs (PEAGLE_GEMM_PAIR=0 turns it off)
+  int pair_clusters;  // CTA pairs that fit on the GPU at once (a cluster stays in one GPC)
   int max_bn;
   float* ws;
   unsigned* counters;
@@ -489,6 +736,10 @@ static bool encode_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int ro
   return true;
 }
 
+static size_t smem_bytes_pair(int stages) {
+  return 1024 + (size_t)stages * (A_BYTES + 128 * 128) + STAGE_F_BYTES +
+         (size_t)(2 * stages + 5) * 8 + 16;
+}
 static size_t smem_bytes(int stages, int bn) {
   return 1024 /*align slack*/ + (size_t)stages * (A_BYTES + bn * 128) + STAGE_F_BYTES +
          (size_t)(2 * stages + 4) * 8 + 16;
@@ -532,12 +783,43 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
     tc_destroy(p);
     return PEAGLE_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           227 * 1024) != cudaSuccess ||
+      cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess ||
       cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess) {
     tc_destroy(p);
     return PEAGLE_ERR_CUDA;
+  }
+  {
+    // a persistent grid of pairs must be resident at once: as many pairs as clusters of
+    // two fit (each GPC holds an even number of the CTAs), not num_sms / 2
+    const char* env = getenv("PEAGLE_GEMM_PAIR");
+    p->pair = !(env && env[0] == '0');
+    p->pair_clusters = 0;
+    int stages = 2;
+    while (stages < 8 && smem_bytes_pair(stages + 1) <= 220 * 1024) ++stages;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.blockDim = dim3(TC_THREADS2);
+    cfg.dynamicSmemBytes = smem_bytes_pair(stages);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, tc_gemm_pair_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      nc = 0;
+    }
+    p->pair_clusters = nc < num_sms / 2 ? nc : num_sms / 2;
+    if (getenv("PEAGLE_GEMM_PAIR_INFO"))
+      fprintf(stderr, "peagle: %d CTA pairs resident at once (%d SMs)\n", p->pair_clusters,
+              num_sms);
   }
   *out = p;
   return PEAGLE_OK;
@@ -579,6 +861,49 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     p.n_tiles = (R + p.BN - 1) / p.BN;
   }
   p.KB = Kd / 64;
+  if (pl->pair && p.n_tiles > 1 && Kd % 64 == 0 && pl->pair_clusters > 0) {
+    // CTA pairs: pair-tiles of 256 weight rows x (128 logical rows, hi + lo, or 256 rows)
+    TcParams q = p;
+    q.BN = 256;
+    q.rpt = p.split ? 128 : 256;
+    q.lo_col = p.split ? 128 : 0;
+    q.n_tiles = (R + q.rpt - 1) / q.rpt;
+    q.m_tiles = (Nout + 255) / 256;
+    const long long wbytes = (long long)Nout * Kd * 2;
+    const long long xbytes = (long long)xrows * Kd * 2;
+    q.m_inner = wbytes < xbytes ? 1 : 0;
+    const long long T = (long long)q.m_tiles * q.n_tiles;
+    const int npairs = (int)(T < pl->pair_clusters ? T : pl->pair_clusters);
+    q.G = npairs;
+    q.dp_waves = 0;
+    q.total = 0;
+    int stages = 2;
+    while (stages < 8 && smem_bytes_pair(stages + 1) <= 220 * 1024) ++stages;
+    q.stages = stages;
+    q.tmem_cols = 512;
+    q.ws = pl->ws;
+    q.counters = pl->counters;
+    q.err = pl->err;
+    CUtensorMap mw, mx;
+    if (!encode_map(pl, &mw, W, Nout, Kd, Kd, 128)) return PEAGLE_ERR_CUDA;
+    if (!encode_map(pl, &mx, X, xrows, Kd, ldx, 128)) return PEAGLE_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * npairs);
+    cfg.blockDim = dim3(TC_THREADS2);
+    cfg.dynamicSmemBytes = smem_bytes_pair(stages);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, mw, mx, q, epi);
+    return e == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+  }
   // large-M projections are tensor-bound: two epilogue groups keep up with the MMA
   const int neg = p.n_tiles > 1 ? 2 : 1;
   const int m_tiles = (Nout + 127) / 128;
