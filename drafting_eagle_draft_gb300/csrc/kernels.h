@@ -36,6 +36,7 @@ struct MaskedAttnArgs {
   int split;
   int M, n, Kmax, nq, nkv, hd;
   float scale;
+  unsigned* err;          // device error word (timeouts of the tensor-core kernel)
 };
 
 // fp32-accumulating FFMA GEMM: Y[r, m] = sum_k X[r, k] W[m, k]; then the fused epilogue.
@@ -56,6 +57,10 @@ void launch_rmsnorm(bool bf16, int R, int H, const fx_t* res, const void* gamma,
 void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);
 
 void launch_masked_attention(bool bf16, const MaskedAttnArgs& a, cudaStream_t s);
+// The same attention on tcgen05 tensor cores (bf16, head_dim 64, 128 % (nq / nkv) == 0);
+// PEAGLE_ERR_UNSUPPORTED for other shapes (nothing launched).  `plan` encodes the TMA maps.
+struct TcGemmPlan;
+int masked_attn_tc_launch(TcGemmPlan* plan, const MaskedAttnArgs& a, cudaStream_t s);
 
 void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* out_tokens,
                           cudaStream_t s);

@@ -57,6 +57,7 @@ struct peagle_ctx {
   // persistent pass kernel (bf16): phase counters + abort flag, host-side parameter block
   bool pass_on;     // available (bf16, cooperative launch, not disabled)
   bool pass_force;  // PEAGLE_PASS_KERNEL=1: use it for every shape it supports
+  bool masked_tc;   // training forward: tcgen05 masked attention (PEAGLE_MASKED_TC=0: off)
   unsigned* pass_cnt;
   PassParams* pp;
   // timing of the pass kernel: per-call phase completion times (device slots) and the
@@ -331,6 +332,10 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
       free_ctx(c);
       return PEAGLE_ERR_CUDA;
     }
+  }
+  {
+    const char* env = getenv("PEAGLE_MASKED_TC");
+    c->masked_tc = !(env && env[0] == '0');
   }
   // the whole bf16 pass as one persistent kernel, unless disabled (PEAGLE_PASS_KERNEL=0)
   c->pass_on = false;
@@ -894,7 +899,13 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       a.nkv = nkv;
       a.hd = hd;
       a.scale = 1.f / sqrtf((float)hd);
-      TIMED(PEAGLE_STAGE_ATTN, launch_masked_attention(c->bf, a, s));
+      a.err = c->err;
+      // tcgen05 kernel for bf16 and head_dim 64, else the mma.sync / fp32 kernels
+      TIMED(PEAGLE_STAGE_ATTN, {
+        int ar = PEAGLE_ERR_UNSUPPORTED;
+        if (c->bf && c->masked_tc) ar = masked_attn_tc_launch(c->tc, a, s);
+        if (ar == PEAGLE_ERR_UNSUPPORTED) launch_masked_attention(c->bf, a, s);
+      });
     }
     {
       EpiArgs e = epi_base(c, EPI_RESID, M, H);
