@@ -473,14 +473,15 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
   const int S = p.stages;
   uint8_t* sA = smem;
   uint8_t* sB = sA + (size_t)S * A_BYTES;
-  float* stg = (float*)(sB + (size_t)S * HB);
-  uint64_t* full = (uint64_t*)((uint8_t*)stg + STAGE_F_BYTES);
+  float* stg = (float*)(sB + (size_t)S * HB);  // [NEG][32][128] fp32 epilogue staging
+  uint64_t* full = (uint64_t*)((uint8_t*)stg + NEG * STAGE_F_BYTES);
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 2;
   uint64_t* done_bar = acce + 2;
   uint32_t* s_tmem = (uint32_t*)(done_bar + 1);
   volatile int* s_abort = (volatile int*)(s_tmem + 1);
+  __shared__ int s_rpos[NEG][128];  // RoPE positions of the tile's rows, per epilogue group
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_ctarank();
@@ -628,8 +629,10 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
     const int quarter = warp & 3;
     const int ml = quarter * 32 + lane;
     const int R = p.R;
-    float* gstg = stg + (size_t)eg * (32 / NEG) * 128;
+    float* gstg = stg + (size_t)eg * 32 * 128;
     const uint32_t lead_acce = tc::mapa_shared(acce, 0);
+    // a RoPE epilogue reads its rows' positions from a table filled while the MMAs run
+    const bool pos_tab = epi.row_pos != nullptr && p.rpt <= 128;
     auto release = [&](int buf) {  // this group is done reading accumulator `buf`
       if (lead) tc::mbar_arrive(&acce[buf]);
       else tc::mbar_arrive_remote(lead_acce + (uint32_t)(buf * 8));
@@ -638,6 +641,11 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
       const int t = pair + ti * npairs;
       const int buf = ti & 1;
       const uint32_t use = (uint32_t)(ti >> 1);
+      const int mt = pair_tile_m(t, p), nt = pair_tile_n(t, p);
+      const int m0 = (2 * mt + (int)rank) * 128;
+      const int row0 = nt * p.rpt;
+      const int lrows = min(p.rpt, R - row0);
+      if (pos_tab && et < lrows) s_rpos[eg][et] = epi.row_pos[row0 + et];
       if (et == 0 && !tc::mbar_wait_cluster(&accf[buf], use & 1u, s_abort)) {
         raise_error(p.err, PEAGLE_DEV_TIMEOUT);
         *s_abort = 1;
@@ -645,31 +653,29 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
       epi_bar(eg);
       if (*s_abort) break;
       tc::fence_after_sync();
-      const int mt = pair_tile_m(t, p), nt = pair_tile_n(t, p);
-      const int m0 = (2 * mt + (int)rank) * 128;
-      const int row0 = nt * p.rpt;
-      const int lrows = min(p.rpt, R - row0);
       const uint32_t tb = tmem + (uint32_t)(buf * 256) + ((uint32_t)(quarter * 32) << 16);
-      const int step = (p.split ? 16 : 32) / NEG;
+      // chunks of 16 logical rows (hi + lo columns) or 32 rows; chunk ch to group ch % NEG
+      const int step = p.split ? 16 : 32;
       const int nch = (lrows + step - 1) / step;
       for (int ch = eg; ch < nch; ch += NEG) {
         const int i0 = ch * step;
-        float v[8], w[8];
-        tc::tmem_ld8(tb + i0, v);
-        tc::tmem_ld8(tb + (p.split ? p.lo_col : 8) + i0, w);
+        float v[16], w[16];
+        tc::tmem_ld16(tb + i0, v);
+        tc::tmem_ld16(tb + (p.split ? p.lo_col : 16) + i0, w);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           gstg[j * 128 + ml] = v[j];
-          gstg[(8 + j) * 128 + ml] = w[j];
+          gstg[(16 + j) * 128 + ml] = w[j];
         }
         const bool last = ch + NEG >= nch;
         if (last) tc::fence_before_sync();
         epi_bar(eg);
         if (last && et == 0) release(buf);
         if (m0 < epi.Nout)
-          epilogue_tile<bf16>(epi, gstg, 128, p.split ? 16 / NEG : -1, m0, row0 + i0,
-                              min(step, lrows - i0), et, 128);
+          epilogue_tile<bf16>(epi, gstg, 128, p.split ? 16 : -1, m0, row0 + i0,
+                              min(step, lrows - i0), et, 128, nullptr,
+                              pos_tab ? &s_rpos[eg][i0] : nullptr);
         epi_bar(eg);
       }
       if (eg >= nch && et == 0) release(buf);
@@ -737,9 +743,12 @@ static bool encode_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int ro
 }
 
 static size_t smem_bytes_pair(int stages) {
-  return 1024 + (size_t)stages * (A_BYTES + 128 * 128) + STAGE_F_BYTES +
+  return 1024 + (size_t)stages * (A_BYTES + 128 * 128) + 2 * STAGE_F_BYTES +
          (size_t)(2 * stages + 5) * 8 + 16;
 }
+// dynamic shared memory of the pair kernel: the 227 KB per-block limit less its 1 KB of
+// static RoPE position tables
+constexpr size_t PAIR_SMEM_BUDGET = 226 * 1024;
 static size_t smem_bytes(int stages, int bn) {
   return 1024 /*align slack*/ + (size_t)stages * (A_BYTES + bn * 128) + STAGE_F_BYTES +
          (size_t)(2 * stages + 4) * 8 + 16;
@@ -784,7 +793,7 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
     return PEAGLE_ERR_CUDA;
   }
   if (cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           227 * 1024) != cudaSuccess ||
+                           (int)PAIR_SMEM_BUDGET) != cudaSuccess ||
       cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess ||
       cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -799,7 +808,7 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
     p->pair = !(env && env[0] == '0');
     p->pair_clusters = 0;
     int stages = 2;
-    while (stages < 8 && smem_bytes_pair(stages + 1) <= 220 * 1024) ++stages;
+    while (stages < 8 && smem_bytes_pair(stages + 1) <= PAIR_SMEM_BUDGET) ++stages;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms / 2));
     cfg.blockDim = dim3(TC_THREADS2);
@@ -878,7 +887,7 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     q.dp_waves = 0;
     q.total = 0;
     int stages = 2;
-    while (stages < 8 && smem_bytes_pair(stages + 1) <= 220 * 1024) ++stages;
+    while (stages < 8 && smem_bytes_pair(stages + 1) <= PAIR_SMEM_BUDGET) ++stages;
     q.stages = stages;
     q.tmem_cols = 512;
     q.ws = pl->ws;
