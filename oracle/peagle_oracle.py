@@ -252,6 +252,10 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
     (row j of request b sits at seq_lens[b] + j).  Attention of row j: the cached
     keys 0..seq_lens[b]-1 plus the draft block's rows 0..j (causal), GQA with
     q head h reading kv head h // (nq/nkv), scale 1/sqrt(hd).
+    With dims.attn_window = W > 0 (sliding-window drafter attention, [E4] "EAGLE-4
+    overview": the drafter attends to the most recent 4,096 positions; "Long contexts"),
+    row j sees only the keys at positions pos - W + 1 .. pos.  Reading: the window counts
+    the query's own position.
     Returns (res_out, k_draft [B,K,nkv,hd], v_draft).
     """
     cq, ckv, co = _cast_fn(bf16, "q"), _cast_fn(bf16, "kv"), _cast_fn(bf16, "o")
@@ -268,6 +272,7 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
     k = ckv(rope(k, pos[:, None], dims.rope_theta))
     v = ckv(v)
     scale = 1.0 / math.sqrt(hd)
+    window = int(getattr(dims, "attn_window", 0) or 0)
     o = np.empty((R, nq, hd))
     kd = k.reshape(B, K, nkv, hd)
     vd = v.reshape(B, K, nkv, hd)
@@ -277,9 +282,11 @@ def decoder_layer_decode(L, layer_idx, dims, a, res, pos, cache_k, cache_v, seq_
             keys = np.concatenate([to64(cache_k[b, g, :Lb]), kd[b, :, g]], axis=0)
             vals = np.concatenate([to64(cache_v[b, g, :Lb]), vd[b, :, g]], axis=0)
             for j in range(K):
-                n_vis = Lb + j + 1
+                n_vis = Lb + j + 1  # key index = position
+                lo = max(0, n_vis - window) if window > 0 else 0
                 for h in range(g * G, (g + 1) * G):
-                    o[b * K + j, h] = attend(q[b * K + j, h], keys[:n_vis], vals[:n_vis], scale)
+                    o[b * K + j, h] = attend(q[b * K + j, h], keys[lo:n_vis], vals[lo:n_vis],
+                                             scale)
     o = co(o.reshape(R, nq * hd))
     res = res + linear(o, L["o"])
     u = cx(rmsnorm(res, L["post_norm"], dims.rms_eps))

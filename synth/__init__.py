@@ -45,6 +45,7 @@ class Dims:
     rms_eps: float
     dtype: str  # "f32" or "bf16"
     d2t: str  # "identity" or "monotone"
+    attn_window: int = 0  # drafter attention window in positions (0: the whole context)
 
     @property
     def qkv_out(self) -> int:

@@ -577,3 +577,73 @@ def test_catch_up_is_causal():
     b = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], [5], hid, tok2, bf16=False)
     assert np.array_equal(a.logits[0, : T - 1], b.logits[0, : T - 1])
     assert np.max(np.abs(a.logits[0, T - 1] - b.logits[0, T - 1])) > 1e-6
+
+
+# ---------------------------------------------------------------- sliding-window attention
+# ([E4] "EAGLE-4 overview": the drafter attends to the most recent 4,096 positions)
+
+
+def test_window_covering_the_context_is_full_attention():
+    """A window at least as long as the context plus the draft block changes nothing."""
+    dims = _tiny_dims(n_layers=2)
+    w = _tiny_weights(dims)
+    inp = _tiny_inputs(dims, 2, 4, 9)
+    full = _run(dims, w, inp, 4)
+    for W in (13, 14, 100):
+        r = _run(synth.shrink(dims, attn_window=W), w, inp, 4)
+        assert np.allclose(r.logits, full.logits, atol=1e-12)
+    r = _run(synth.shrink(dims, attn_window=12), w, inp, 4)  # row 3 (position 12) loses key 0
+    assert np.allclose(r.logits[:, :3], full.logits[:, :3], atol=1e-12)
+    assert not np.allclose(r.logits[:, 3], full.logits[:, 3])
+
+
+def test_window_of_one_position_is_self_attention():
+    """W = 1: every row sees only its own key, whatever the cache holds, so each row is
+    the single-key closed form: residual f + W_o(v of its kv heads) (down-proj zeroed),
+    v = W_v x0, x0 = [RMSNorm(e) || RMSNorm(f)] with e, f the row's NTP or MTP inputs."""
+    dims = _tiny_dims(rms_eps=0.0, attn_window=1)
+    w = _tiny_weights(dims)
+    w["layers"][0]["down"] = _zero(w["layers"][0]["down"])
+    K = 3
+    inp = _tiny_inputs(dims, 2, K, 6)
+    r = _run(dims, w, inp, K)
+    H, nq, nkv, hd = dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    wv = w["layers"][0]["qkv"].double().numpy()[(nq + nkv) * hd:]
+    wo = w["layers"][0]["o"].double().numpy()
+    fc = w["fc"].double().numpy()
+    for b in range(2):
+        for j in range(K):
+            if j == 0:
+                e = w["embed"][int(inp["new_token"][b])].double().numpy()
+                f = fc @ inp["target_hidden"][b].double().numpy()
+            else:
+                e = w["emb_mask"].double().numpy()
+                f = fc @ w["h_shared"].double().numpy()
+            x0 = np.concatenate([_rms(e), _rms(f)])
+            v = (wv @ x0).reshape(nkv, hd)
+            o = np.concatenate([v[h // (nq // nkv)] for h in range(nq)])
+            exp = w["lm_head"].double().numpy() @ _rms(f + wo @ o)
+            assert np.allclose(r.logits[b, j], exp, atol=1e-10)
+
+
+def test_window_ignores_keys_outside_it():
+    """With W = 5, L = 8 and K = 3, row j sees positions 4 + j .. 8 + j: changing cached
+    positions 0..3 changes no row; changing position 4 changes row 0 only (one layer, so
+    rows meet only through the draft block's own keys)."""
+    dims = _tiny_dims(attn_window=5)
+    w = _tiny_weights(dims)
+    inp = _tiny_inputs(dims, 1, 3, 8)
+    base = _run(dims, w, inp, 3)
+    far = {k: v for k, v in inp.items()}
+    far["cache_k"] = inp["cache_k"].clone()
+    far["cache_v"] = inp["cache_v"].clone()
+    far["cache_k"][:, :, :, :4] += 1.5
+    far["cache_v"][:, :, :, :4] -= 2.0
+    assert np.allclose(_run(dims, w, far, 3).logits, base.logits, atol=1e-12)
+    edge = {k: v for k, v in inp.items()}
+    edge["cache_k"] = inp["cache_k"].clone()
+    edge["cache_v"] = inp["cache_v"].clone()
+    edge["cache_v"][:, :, :, 4] += 3.0
+    r = _run(dims, w, edge, 3)
+    assert not np.allclose(r.logits[0, 0], base.logits[0, 0])
+    assert np.allclose(r.logits[0, 1:], base.logits[0, 1:], atol=1e-12)
