@@ -47,7 +47,8 @@ class PeagleDims(ctypes.Structure):
     _fields_ = [(n, _i32) for n in (
         "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "intermediate",
         "draft_vocab", "target_vocab", "max_batch", "max_K", "max_rows", "max_seq",
-        "max_positions", "dtype")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+        "max_positions", "dtype")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                                      ("attn_window", _i32)]
 
 
 class PeagleWeights(ctypes.Structure):
@@ -143,7 +144,8 @@ def make_dims(dims, max_batch, max_K, max_positions, max_rows=0, max_seq=0) -> P
                       target_vocab=dims.target_vocab, max_batch=max_batch, max_K=max_K,
                       max_rows=max_rows, max_seq=max_seq, max_positions=max_positions,
                       dtype=PEAGLE_F32 if dims.dtype == "f32" else PEAGLE_BF16,
-                      rope_theta=dims.rope_theta, rms_eps=dims.rms_eps)
+                      rope_theta=dims.rope_theta, rms_eps=dims.rms_eps,
+                      attn_window=int(getattr(dims, "attn_window", 0) or 0))
 
 
 class Context:

@@ -66,6 +66,25 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr int MMA_KT = 64;  // keys per tile
 
+// Keys of request b's split-KV items: positions [*first, *total).  total = L + K (capped
+// at the cache capacity; overflow is reported by the QKV epilogue).  With a sliding window
+// of W positions ("EAGLE-4", "EAGLE-4 overview"), row j sees L + j - W + 1 .. L + j, so
+// the items start at row 0's first visible key; item c covers [first + c * chunk, ...).
+__device__ __forceinline__ void attn_span(const AttnArgs& a, int L, int* first, int* total) {
+  int t = L + a.K;
+  if (t > a.cap) t = a.cap;
+  int f = 0;
+  if (a.window > 0) {
+    f = L - a.window + 1;
+    if (f < 0) f = 0;
+  }
+  *first = f;
+  *total = t;
+}
+__device__ __forceinline__ int attn_nvalid(const AttnArgs& a, int first, int total) {
+  return total > first ? (total - first + a.chunk - 1) / a.chunk : 0;
+}
+
 // One work item: chunk c of (request b, kv head g), run by the nthr threads tid = 0 ..
 // nthr-1 of a thread group (>= 32 * ceil(rows / 16)) that synchronises with bar().
 __device__ __forceinline__ void cp_async_wait_n(int n) {
@@ -88,9 +107,9 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
   const int G = a.nq / a.nkv;
   const int rows = a.K * G;
   const int L = a.seq_lens[b];
-  int total = L + a.K;
-  if (total > a.cap) total = a.cap;  // overflow is reported by the QKV epilogue
-  const int kbeg = c * a.chunk;
+  int first, total;
+  attn_span(a, L, &first, &total);
+  const int kbeg = first + c * a.chunk;
   if (kbeg >= total || L < 0) return;
   const int kend = min(total, kbeg + a.chunk);
   const int warp = tid >> 5, lane = tid & 31;
@@ -140,6 +159,9 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
     for (int u = 0; u < 4; ++u) qa[ks][u] = pack_bf16(x[2 * u], x[2 * u + 1]);
   }
   const int lim0 = L + j0, lim1 = L + j1;  // last visible key of each row
+  // first visible key of each row (sliding window), else the start of the context
+  const int lo0 = a.window > 0 ? lim0 - a.window + 1 : 0;
+  const int lo1 = a.window > 0 ? lim1 - a.window + 1 : 0;
   float o[ND][4];
 #pragma unroll
   for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -186,10 +208,10 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
         const int kp = t0 + n * 8 + 2 * tq;
-        sc[n][0] = (kp < kend && kp <= lim0 && v0) ? sc[n][0] : -INFINITY;
-        sc[n][1] = (kp + 1 < kend && kp + 1 <= lim0 && v0) ? sc[n][1] : -INFINITY;
-        sc[n][2] = (kp < kend && kp <= lim1 && v1) ? sc[n][2] : -INFINITY;
-        sc[n][3] = (kp + 1 < kend && kp + 1 <= lim1 && v1) ? sc[n][3] : -INFINITY;
+        sc[n][0] = (kp < kend && kp <= lim0 && kp >= lo0 && v0) ? sc[n][0] : -INFINITY;
+        sc[n][1] = (kp + 1 < kend && kp + 1 <= lim0 && kp + 1 >= lo0 && v0) ? sc[n][1] : -INFINITY;
+        sc[n][2] = (kp < kend && kp <= lim1 && kp >= lo1 && v1) ? sc[n][2] : -INFINITY;
+        sc[n][3] = (kp + 1 < kend && kp + 1 <= lim1 && kp + 1 >= lo1 && v1) ? sc[n][3] : -INFINITY;
         mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
         mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
       }

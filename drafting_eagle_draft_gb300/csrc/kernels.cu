@@ -304,9 +304,9 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
   const int G = a.nq / a.nkv;
   const int rows = a.K * G;
   const int L = a.seq_lens[b];
-  int total = L + a.K;
-  if (total > a.cap) total = a.cap;  // overflow is reported by the QKV epilogue
-  const int kbeg = c * a.chunk;
+  int first, total;
+  attn_span(a, L, &first, &total);
+  const int kbeg = first + c * a.chunk;
   if (kbeg >= total || L < 0) return;
   const int kend = min(total, kbeg + a.chunk);
   float* qs = smem;                       // [rows][HD]
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
       if (rr >= rows) break;
       const int j = rr / G;
       const int kp = t0 + lane;
-      const bool valid = kp < kend && kp <= L + j;
+      const bool valid = kp < kend && kp <= L + j && (a.window <= 0 || kp > L + j - a.window);
       float s = 0.f;
       const float* q = qs + rr * HD;
       const float* kr = ks + lane * (HD + 1);
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
     }
   }
   __syncthreads();
-  const int nvalid = cdiv(total, a.chunk);
+  const int nvalid = attn_nvalid(a, first, total);
   if (threadIdx.x == 0) {
     unsigned prev = atom_add_acq_rel(a.counters + b * a.nkv + g, 1u);
     s_last = (prev == (unsigned)(nvalid - 1));
@@ -422,10 +422,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rr = blockIdx.x * 4 + warp;
   const int L = a.seq_lens[b];
-  int total = L + a.K;
-  if (total > a.cap) total = a.cap;
-  if (rr >= rows || L < 0 || total <= 0) return;
-  attn_merge_rows<T, HD>(a, b, g, rows, cdiv(total, a.chunk), rr, rr + 1, lane);
+  int first, total;
+  attn_span(a, L, &first, &total);
+  if (rr >= rows || L < 0 || total <= first) return;
+  attn_merge_rows<T, HD>(a, b, g, rows, attn_nvalid(a, first, total), rr, rr + 1, lane);
 }
 
 template <int HD>

@@ -19,6 +19,7 @@ struct AttnArgs {
   float* part;            // split-KV partials
   unsigned* counters;     // [B * nkv], zero between launches
   int B, K, nq, nkv, hd, cap, chunk, nchunk;
+  int window;             // sliding window in positions (0: whole context); see attn_span
   float scale;
   unsigned* err;
 };

@@ -765,10 +765,11 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               const int g = (i / rows) % a.nkv;
               const int b = i / (rows * a.nkv);
               const int L = a.seq_lens[b];
-              int total = L + a.K;
-              if (total > a.cap) total = a.cap;
-              if (L < 0 || total <= 0) continue;
-              attn_merge_rows<bf16, HD>(a, b, g, rows, cdiv(total, a.chunk), rr, rr + 1, lane);
+              int first, total;
+              attn_span(a, L, &first, &total);
+              if (L < 0 || total <= first) continue;
+              attn_merge_rows<bf16, HD>(a, b, g, rows, attn_nvalid(a, first, total), rr, rr + 1,
+                                        lane);
             }
           }
         } else if (ph.kind == PP_ARGMAX) {

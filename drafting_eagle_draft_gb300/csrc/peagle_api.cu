@@ -157,6 +157,7 @@ static int validate_dims(const peagle_dims* d) {
   if (d->max_K > 16 || d->max_batch * d->max_K > 256) return PEAGLE_ERR_CAPACITY;
   if (d->max_K * (d->n_q_heads / d->n_kv_heads) > 128) return PEAGLE_ERR_UNSUPPORTED;
   if (d->max_rows > 0 && d->max_seq <= 0) return PEAGLE_ERR_INVALID;
+  if (d->attn_window < 0) return PEAGLE_ERR_INVALID;
   // the masked attention tile holds 64 (row, q head) pairs of one kv head
   if (d->max_rows > 0 && d->n_q_heads / d->n_kv_heads > 64) return PEAGLE_ERR_UNSUPPORTED;
   return PEAGLE_OK;
@@ -364,6 +365,13 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   return PEAGLE_OK;
 }
 
+// Keys a request's split-KV items cover: the whole cache, or with a sliding window of W
+// positions at most W + K - 1 of them (row 0's window through the last draft row).
+static int attention_span(peagle_ctx* c, int cap, int K) {
+  const int w = c->d.attn_window;
+  return (w > 0 && w + K < cap) ? w + K : cap;
+}
+
 static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchunk,
                            int waves = 2) {
   const int target = waves * c->num_sms;
@@ -565,7 +573,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   P.eps = d.rms_eps;
   // one attention item per CTA: each CTA streams its chunk's tiles back to back
   int chunk, nchunk;
-  attention_plan(c, B, kv->capacity, &chunk, &nchunk, 1);
+  attention_plan(c, B, attention_span(c, kv->capacity, K), &chunk, &nchunk, 1);
   P.chunk = chunk;
   P.nchunk = nchunk;
   AttnArgs& a = P.att;
@@ -585,6 +593,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   a.cap = kv->capacity;
   a.chunk = chunk;
   a.nchunk = nchunk;
+  a.window = d.attn_window;
   a.scale = 1.f / sqrtf((float)hd);
   a.err = c->err;
   P.layer_stride = layer_stride;
@@ -678,7 +687,7 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
                             c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, seq_lens,
                             c->row_pos, c->err, s));
   int chunk, nchunk;
-  attention_plan(c, batch, kv->capacity, &chunk, &nchunk);
+  attention_plan(c, batch, attention_span(c, kv->capacity, K), &chunk, &nchunk);
   for (int l = 0; l < d.n_layers; ++l) {
     const void* a_in = c->X0;
     int din = 2 * H;
@@ -721,6 +730,7 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       a.cap = kv->capacity;
       a.chunk = chunk;
       a.nchunk = nchunk;
+      a.window = d.attn_window;
       a.scale = 1.f / sqrtf((float)hd);
       a.err = c->err;
       TIMED(PEAGLE_STAGE_ATTN, launch_attention_decode(c->bf, a, s));
@@ -834,6 +844,7 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   if (n < 1 || K < 1 || M < 1) return PEAGLE_ERR_INVALID;
   if (d.max_rows <= 0 || M > d.max_rows || n > d.max_seq || K > 16) return PEAGLE_ERR_CAPACITY;
   if (n > d.max_positions) return PEAGLE_ERR_CAPACITY;
+  if (d.attn_window > 0) return PEAGLE_ERR_UNSUPPORTED;  // the training mask has no window
   cudaStream_t s = (cudaStream_t)stream;
   const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
   const int qkv_out = (nq + 2 * nkv) * hd;

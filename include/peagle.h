@@ -77,6 +77,12 @@ typedef struct peagle_dims {
   int32_t dtype;         /* peagle_dtype                                          */
   float rope_theta;      /* RoPE base                                             */
   float rms_eps;         /* RMSNorm epsilon                                       */
+  int32_t attn_window;   /* sliding-window drafter attention ("EAGLE-4", section
+                            "EAGLE-4 overview"): a draft-block row at position pos
+                            sees only the keys at positions pos - attn_window + 1
+                            .. pos.  0 = the whole context.  Draft and catch-up
+                            passes only; peagle_forward_parallel rejects a window
+                            with PEAGLE_ERR_UNSUPPORTED.                         */
 } peagle_dims;
 
 /* Drafter weights (host or device pointers; dtype = dims.dtype for every float
