@@ -12,6 +12,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode_b1|decode_b2|ragged_b16]
 
+Two extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
+COD 0.8) and sliding_window (the concurrency-2 workload with and without a 4096-position
+drafter attention window); --no-train-fwd / --no-window skip them.
+
 --impl reference times the fp64 oracle on the host cores instead (a deliberately slow
 plain program; see the cpu_baseline object).  Under torchrun each rank runs an
 independent replica on its own GPU (the pass shards by request: no collective).
@@ -48,6 +52,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-train-fwd", action="store_true",
                     help="skip the training-style masked forward measurement")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the sliding-window attention measurement")
     return ap.parse_args()
 
 
@@ -374,7 +380,62 @@ def run_ours(args, rank, world, dist):
     ctx.close()
     if rank == 0 and world == 1 and not args.no_train_fwd:
         out["train_fwd"] = train_fwd_measure(dev)
+    if rank == 0 and world == 1 and not args.no_window:
+        out["sliding_window"] = window_measure(dev)
     return out
+
+
+def window_measure(dev, window=4096, reps=20):
+    """Sliding-window drafter attention on the concurrency-2 workload (contexts 8192 and
+    10240, K=8): draft-pass time as a CUDA graph with a 4096-position window and with full
+    attention on the same inputs, and the cached keys / values each pass reads."""
+    import torch
+
+    import drafting_eagle_draft_gb300 as pk
+
+    wl = synth.WORKLOADS["decode_b2"]
+    w = synth.make_weights(wl.dims, 1234)
+    inp = synth.make_decode_inputs(wl, 99)
+    B, K, cap = wl.batch, wl.K, inp["capacity"]
+    ck, cv = inp["cache_k"].to(dev), inp["cache_v"].to(dev)
+    kv = pk.kv_struct(ck, cv, cap, B)
+    sl = torch.from_numpy(inp["seq_lens"]).to(dev)
+    th = inp["target_hidden"].to(dev)
+    nt = torch.from_numpy(inp["new_token"]).to(dev)
+    res = {}
+    for name, W in (("window", window), ("full", 0)):
+        dims = synth.shrink(wl.dims, attn_window=W)
+        ctx = pk.peagle_create(w, pk.make_dims(dims, B, K, cap))
+        toks = torch.zeros(B, K, dtype=torch.int32, device=dev)
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, s)
+        s.synchronize()
+        assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, s)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        e1.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps * 1e3
+        ctx.close()
+    lens = [int(x) for x in inp["seq_lens"]]
+    kvb = lambda span: sum(span(L) for L in lens) * wl.dims.n_kv_heads * wl.dims.head_dim * 2 * 2 \
+        * wl.dims.n_layers
+    return {"workload": "decode_b2 (contexts %s, K=%d)" % ("/".join(map(str, lens)), K),
+            "window": window, "us_per_pass": round(res["window"], 2),
+            "us_per_pass_full": round(res["full"], 2),
+            "kv_bytes_per_pass": kvb(lambda L: min(L + K, window + K - 1)),
+            "kv_bytes_per_pass_full": kvb(lambda L: L + K)}
 
 
 def train_fwd_measure(dev, reps=3):
