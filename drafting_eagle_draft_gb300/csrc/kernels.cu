@@ -260,8 +260,74 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(int H, const fx_t*
   }
 }
 
+// bf16 variant with 16-byte accesses: 128 threads per row, each owning G groups of 8
+// consecutive features (eight fixed-point values in, eight bf16 hi and lo parts out).
+template <int G>
+__global__ void __launch_bounds__(128) rmsnorm_v8_kernel(int H, const fx_t* __restrict__ res,
+                                                         const bf16* __restrict__ gamma,
+                                                         float eps, int split,
+                                                         bf16* __restrict__ out) {
+  __shared__ float red[32];
+  pdl_enter();
+  const int r = blockIdx.x, R = gridDim.x;
+  const int ng = H >> 3;
+  const longlong2* x = (const longlong2*)(res + (size_t)r * H);
+  float v[G][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int gi = threadIdx.x + k * 128;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const longlong2 q = gi < ng ? x[gi * 4 + u] : make_longlong2(0, 0);
+      v[k][2 * u] = from_fx(q.x);
+      v[k][2 * u + 1] = from_fx(q.y);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += v[k][e] * v[k][e];
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / H + eps);
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int gi = threadIdx.x + k * 128;
+    if (gi >= ng) break;
+    const uint4 gw = *(const uint4*)(gamma + gi * 8);
+    const bf16* gb = (const bf16*)&gw;
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float y0 = v[k][2 * u] * inv * __bfloat162float(gb[2 * u]);
+      const float y1 = v[k][2 * u + 1] * inv * __bfloat162float(gb[2 * u + 1]);
+      const bf16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+      const bf16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
+      const bf16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+      wh[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      wl[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    *(uint4*)(out + (size_t)r * H + gi * 8) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    if (split)
+      *(uint4*)(out + (size_t)(r + R) * H + gi * 8) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
+}
+
 void launch_rmsnorm(bool bf16m, int R, int H, const fx_t* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s) {
+  if (bf16m && H % 8 == 0 && H <= 16 * 128 * 8) {
+    const int G = (H / 8 + 127) / 128;
+#define PEAGLE_RMS8_CASE(N)                                                              \
+  case N:                                                                                \
+    launch_pdl(rmsnorm_v8_kernel<N>, dim3(R), dim3(128), 0, s, H, res, (const bf16*)gamma, \
+               eps, split, (bf16*)out);                                                  \
+    return;
+    switch (G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16) {
+      PEAGLE_RMS8_CASE(2)
+      PEAGLE_RMS8_CASE(4)
+      PEAGLE_RMS8_CASE(8)
+      PEAGLE_RMS8_CASE(16)
+    }
+#undef PEAGLE_RMS8_CASE
+  }
   const int npt = row_npt(H);
 #define PEAGLE_RMS_CASE(N)                                                                 \
   case N:                                                                                  \
