@@ -135,6 +135,8 @@ class Weights64:
     lm_head: np.ndarray
     d2t: np.ndarray
     layers: list
+    lm_proj: object = None   # efficient LM head: [rank, H] projection of the head input
+    lm_score: object = None  # efficient LM head: [Vd, rank] scores of the projection
 
     @staticmethod
     def from_synth(w, lazy=False):
@@ -153,6 +155,8 @@ class Weights64:
             d2t=np.asarray(w["d2t"], np.int64),
             layers=[{k: (to64(v) if k.endswith("norm") else conv(v)) for k, v in L.items()}
                     for L in w["layers"]],
+            lm_proj=to64(w["lm_proj"]) if "lm_proj" in w else None,
+            lm_score=to64(w["lm_score"]) if "lm_score" in w else None,
         )
 
 
@@ -178,6 +182,7 @@ class DraftResult:
     margin: np.ndarray  # [B, K] top-1 minus top-2 logit
     k_rows: list  # per layer [B, K, nkv, hd] keys written for the draft block (post-RoPE)
     v_rows: list  # per layer [B, K, nkv, hd]
+    approx: object = None  # efficient LM head: [B, K, Vd] rank-r scores (else None)
 
 
 def input_rows(W: Weights64, dims, target_hidden, new_token, K):
@@ -303,12 +308,44 @@ def lm_head_argmax(W: Weights64, dims, res, bf16):
     """
     cast = _cast_fn(bf16, "y")
     y = cast(rmsnorm(res, W.final_norm, dims.rms_eps))
+    if getattr(dims, "lm_rank", 0) and W.lm_proj is not None:
+        return _efficient_head(W, dims, y)
     logits = linear(y, W.lm_head)
     am = np.argmax(logits, axis=-1)  # first occurrence = lowest index on ties
     top2 = np.partition(logits, -2, axis=-1)[:, -2:]
     margin = top2[:, 1] - top2[:, 0]
     tokens = am + W.d2t[am]
     return logits, am, tokens, margin
+
+
+def _efficient_head(W: Weights64, dims, y):
+    """Efficient LM head ([E4] "EAGLE-4 overview": a rank-128 projection scores the whole
+    vocabulary, the full head then scores only the best 128 candidates; "Training with
+    TorchSpec": a low-rank approximation selects the top 128 tokens).
+
+    approx = lm_score (lm_proj y); the candidates are the lm_topk largest approx scores
+    (ties: lower index first); their exact logits lm_head[c] . y decide (ties: lower
+    index).  Returns (logits, argmax, tokens, margin, approx) with logits = the exact
+    logits at the candidates and -inf elsewhere, margin = top-1 minus top-2 exact logit
+    among the candidates.
+    """
+    approx = linear(linear(y, W.lm_proj), W.lm_score)
+    R, Vd = approx.shape
+    k = min(int(dims.lm_topk), Vd)
+    logits = np.full((R, Vd), -np.inf)
+    am = np.empty(R, np.int64)
+    margin = np.empty(R)
+    for r in range(R):
+        order = np.lexsort((np.arange(Vd), -approx[r]))  # value descending, index ascending
+        cand = np.sort(order[:k])
+        ex = _mat(W.lm_head)[cand] @ y[r]
+        logits[r, cand] = ex
+        best = ex.max()
+        am[r] = cand[ex == best].min()
+        top2 = np.sort(ex)[-2:] if k > 1 else np.array([-np.inf, best])
+        margin[r] = top2[1] - top2[0]
+    tokens = am + W.d2t[am]
+    return logits, am, tokens, margin, approx
 
 
 def draft_pass(W: Weights64, dims, cache_k, cache_v, seq_lens, target_hidden, new_token, K,
@@ -364,10 +401,12 @@ def _drafter_block(W: Weights64, dims, cache_k, cache_v, seq_lens, E, Hin, K, bf
                                            seq_lens, K, bf16)
         k_rows.append(kd)
         v_rows.append(vd)
-    logits, am, tokens, margin = lm_head_argmax(W, dims, res, bf16)
+    head = lm_head_argmax(W, dims, res, bf16)
+    logits, am, tokens, margin = head[:4]
     Vd = logits.shape[-1]
+    approx = head[4].reshape(B, K, Vd) if len(head) > 4 else None
     return DraftResult(logits.reshape(B, K, Vd), am.reshape(B, K), tokens.reshape(B, K),
-                       margin.reshape(B, K), k_rows, v_rows)
+                       margin.reshape(B, K), k_rows, v_rows, approx)
 
 
 # ----------------------------------------------------------------------------------
@@ -562,7 +601,7 @@ def forward_parallel(W: Weights64, dims, tokens, hidden, rows, bf16=None):
         u = cxn(rmsnorm(res, L["post_norm"], dims.rms_eps))
         act = cact(silu(linear(u, L["gate"])) * linear(u, L["up"]))
         res = res + linear(act, L["down"])
-    logits, am, _, margin = lm_head_argmax(W, dims, res, bf16)
+    logits, am, _, margin = lm_head_argmax(W, dims, res, bf16)[:4]
     return logits, am, margin
 
 

@@ -46,6 +46,8 @@ class Dims:
     dtype: str  # "f32" or "bf16"
     d2t: str  # "identity" or "monotone"
     attn_window: int = 0  # drafter attention window in positions (0: the whole context)
+    lm_rank: int = 0  # efficient LM head: rank of the scoring projection (0: full head)
+    lm_topk: int = 0  # efficient LM head: candidates the full head scores
 
     @property
     def qkv_out(self) -> int:
@@ -171,6 +173,19 @@ def make_weights(dims: Dims, seed: int = 1234) -> dict:
         "d2t": make_d2t(dims, next(s)),
         "layers": [],
     }
+    if dims.lm_rank > 0:
+        # rank-r scoring factors (lm_score lm_proj approximates the LM head) and a head
+        # that is that product plus N(0, 0.005^2), all in the head's N(0, 0.02^2) scale
+        # (own seeds: the other weights are drawn exactly as without the factors)
+        r = dims.lm_rank
+        s2 = iter(np.random.SeedSequence(seed + 7919).spawn(3))
+        std = float(np.sqrt(0.02 / np.sqrt(r)))
+        proj = normal((r, H), next(s2), std, torch.float32)
+        score = normal((dims.draft_vocab, r), next(s2), std, torch.float32)
+        head = score @ proj + normal((dims.draft_vocab, H), next(s2), 0.005, torch.float32)
+        w["lm_proj"] = proj.to(dt)
+        w["lm_score"] = score.to(dt)
+        w["lm_head"] = head.to(dt)
     for layer in range(dims.n_layers):
         din = 2 * H if layer == 0 else H
         w["layers"].append({

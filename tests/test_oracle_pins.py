@@ -647,3 +647,57 @@ def test_window_ignores_keys_outside_it():
     r = _run(dims, w, edge, 3)
     assert not np.allclose(r.logits[0, 0], base.logits[0, 0])
     assert np.allclose(r.logits[0, 1:], base.logits[0, 1:], atol=1e-12)
+
+
+# ---------------------------------------------------------------- efficient LM head
+# ([E4] "EAGLE-4 overview": a rank-128 projection scores the vocabulary, the full head
+# scores the best 128 candidates)
+
+
+def _eff_dims(**kw):
+    return _tiny_dims(lm_rank=4, lm_topk=6, draft_vocab=50, **kw)
+
+
+def test_efficient_head_with_every_candidate_is_the_full_head():
+    dims = _eff_dims()
+    w = _tiny_weights(dims)
+    inp = _tiny_inputs(dims, 2, 3, 5)
+    full = _run(synth.shrink(dims, lm_rank=0, lm_topk=0), w, inp, 3)
+    allc = _run(synth.shrink(dims, lm_topk=dims.draft_vocab), w, inp, 3)
+    assert np.array_equal(allc.argmax, full.argmax)
+    assert np.array_equal(allc.tokens, full.tokens)
+    assert np.allclose(allc.logits, full.logits, atol=1e-12)
+
+
+def test_efficient_head_on_an_exactly_low_rank_head_is_the_full_argmax():
+    """lm_head = lm_score lm_proj: the rank-r scores are the exact logits, so the best
+    candidate is the full head's argmax for any candidate count."""
+    dims = _eff_dims()
+    w = _tiny_weights(dims)
+    w["lm_head"] = w["lm_score"].double() @ w["lm_proj"].double()
+    inp = _tiny_inputs(dims, 2, 3, 5)
+    full = _run(synth.shrink(dims, lm_rank=0, lm_topk=0), w, inp, 3)
+    for k in (1, 2, 6):
+        r = _run(synth.shrink(dims, lm_topk=k), w, inp, 3)
+        assert np.array_equal(r.argmax, full.argmax)
+        assert np.allclose(r.approx, full.logits, atol=1e-10)
+
+
+def test_efficient_head_candidates_and_winner_by_brute_force():
+    """The finite logits sit exactly at the lm_topk largest rank-r scores, equal the full
+    head's logits there, and the token is the best of them (brute force per row)."""
+    dims = _eff_dims()
+    w = _tiny_weights(dims)
+    inp = _tiny_inputs(dims, 2, 3, 5)
+    r = _run(dims, w, inp, 3)
+    full = _run(synth.shrink(dims, lm_rank=0, lm_topk=0), w, inp, 3)
+    for b in range(2):
+        for j in range(3):
+            ranked = sorted(range(dims.draft_vocab), key=lambda i: (-r.approx[b, j, i], i))
+            cand = set(ranked[:dims.lm_topk])
+            assert set(np.nonzero(np.isfinite(r.logits[b, j]))[0].tolist()) == cand
+            for c in cand:
+                assert abs(r.logits[b, j, c] - full.logits[b, j, c]) < 1e-12
+            best = max(cand, key=lambda i: (full.logits[b, j, i], -i))
+            assert r.argmax[b, j] == best
+            assert r.tokens[b, j] == best + int(w["d2t"][best])
