@@ -48,7 +48,8 @@ class PeagleDims(ctypes.Structure):
         "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "intermediate",
         "draft_vocab", "target_vocab", "max_batch", "max_K", "max_rows", "max_seq",
         "max_positions", "dtype")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                                      ("attn_window", _i32)]
+                                      ("attn_window", _i32), ("lm_rank", _i32),
+                                      ("lm_topk", _i32)]
 
 
 class PeagleWeights(ctypes.Structure):
@@ -57,7 +58,8 @@ class PeagleWeights(ctypes.Structure):
                 ("o", ctypes.POINTER(_vp)), ("attn_norm", ctypes.POINTER(_vp)),
                 ("post_norm", ctypes.POINTER(_vp)), ("gate", ctypes.POINTER(_vp)),
                 ("up", ctypes.POINTER(_vp)), ("down", ctypes.POINTER(_vp)),
-                ("final_norm", _vp), ("lm_head", _vp), ("d2t", _vp)]
+                ("final_norm", _vp), ("lm_head", _vp), ("d2t", _vp), ("lm_proj", _vp),
+                ("lm_score", _vp)]
 
 
 class PeagleKV(ctypes.Structure):
@@ -145,7 +147,9 @@ def make_dims(dims, max_batch, max_K, max_positions, max_rows=0, max_seq=0) -> P
                       max_rows=max_rows, max_seq=max_seq, max_positions=max_positions,
                       dtype=PEAGLE_F32 if dims.dtype == "f32" else PEAGLE_BF16,
                       rope_theta=dims.rope_theta, rms_eps=dims.rms_eps,
-                      attn_window=int(getattr(dims, "attn_window", 0) or 0))
+                      attn_window=int(getattr(dims, "attn_window", 0) or 0),
+                      lm_rank=int(getattr(dims, "lm_rank", 0) or 0),
+                      lm_topk=int(getattr(dims, "lm_topk", 0) or 0))
 
 
 class Context:
@@ -198,7 +202,9 @@ def peagle_create(weights: dict, cdims: PeagleDims) -> Context:
         qkv=arr("qkv"), o=arr("o"), attn_norm=arr("attn_norm", True),
         post_norm=arr("post_norm"), gate=arr("gate"), up=arr("up"), down=arr("down"),
         final_norm=p(weights["final_norm"]), lm_head=p(weights["lm_head"]),
-        d2t=p(np.asarray(weights["d2t"], np.int32)))
+        d2t=p(np.asarray(weights["d2t"], np.int32)),
+        lm_proj=p(weights["lm_proj"]) if weights.get("lm_proj") is not None else None,
+        lm_score=p(weights["lm_score"]) if weights.get("lm_score") is not None else None)
     h = _vp()
     _check(lib().peagle_create(ctypes.byref(w), ctypes.byref(cdims), ctypes.byref(h)),
            "peagle_create")

@@ -988,6 +988,164 @@ void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* 
 }
 
 // =====================================================================================
+// Efficient LM head ("EAGLE-4", "EAGLE-4 overview": a rank-128 projection scores the
+// vocabulary, the full head scores the best candidates).
+// =====================================================================================
+// Fixed-point rows [R][n] -> the next projection's operand ([2R][n] bf16 hi / lo, or
+// [R][n] fp32); the fixed-point rows are cleared for the next pass.
+template <typename T>
+__global__ void fx_to_act_kernel(int R, int n, fx_t* __restrict__ src, int split,
+                                 T* __restrict__ dst) {
+  pdl_enter();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R * n; i += gridDim.x * blockDim.x) {
+    const int r = i / n, col = i - r * n;
+    store_act<T>(dst, n, r, R, split, col, from_fx(src[i]));
+    src[i] = 0;
+  }
+}
+
+void launch_fx_to_act(bool bf16m, int R, int n, fx_t* src, int split, void* dst,
+                      cudaStream_t s) {
+  const int blocks = cdiv(R * n, 256) < 1024 ? cdiv(R * n, 256) : 1024;
+  if (bf16m)
+    launch_pdl(fx_to_act_kernel<bf16>, dim3(blocks), dim3(256), 0, s, R, n, src, split,
+               (bf16*)dst);
+  else
+    launch_pdl(fx_to_act_kernel<float>, dim3(blocks), dim3(256), 0, s, R, n, src, 0,
+               (float*)dst);
+}
+
+// Top-k of one row of scores per CTA (256 threads): radix selection of the k-th largest
+// orderable key (four passes of 8 bits), then the keys above it and, in index order,
+// enough of the keys equal to it.  cand[r][0 .. k) = the chosen indices (any order).
+__device__ __forceinline__ unsigned score_key(float v) {
+  if (v == 0.f) v = 0.f;
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(int n, int k, const float* __restrict__ score,
+                                                   int* __restrict__ cand) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_prefix, s_need, s_count;
+  __shared__ unsigned wsum[8];
+  pdl_enter();
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float* x = score + (size_t)r * n;
+  int* out = cand + (size_t)r * k;
+  unsigned prefix = 0, mask = 0, need = (unsigned)k;  // the k-th largest key has `prefix`
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += 256) {
+      const unsigned key = score_key(x[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned above = 0;
+      int d = 255;
+      for (; d > 0; --d) {
+        if (above + hist[d] >= need) break;
+        above += hist[d];
+      }
+      s_prefix = prefix | ((unsigned)d << shift);
+      s_need = need - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  // prefix = the k-th largest key; `need` of the keys equal to it are taken
+  if (tid == 0) s_count = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += 256)
+    if (score_key(x[i]) > prefix) out[atomicAdd(&s_count, 1u)] = i;
+  __syncthreads();
+  const unsigned base = s_count;  // = k - need
+  unsigned taken = 0;
+  for (int i0 = 0; i0 < n && taken < need; i0 += 256) {
+    const int i = i0 + tid;
+    const bool eq = i < n && score_key(x[i]) == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) wsum[wid] = __popc(bal);
+    __syncthreads();
+    unsigned before = 0, total = 0;
+    for (int w = 0; w < 8; ++w) {
+      if (w < wid) before += wsum[w];
+      total += wsum[w];
+    }
+    const unsigned rank = taken + before + __popc(bal & ((1u << lane) - 1u));
+    if (eq && rank < need) out[base + rank] = i;
+    taken += total;
+    __syncthreads();
+  }
+}
+
+void launch_topk(int R, int n, int k, const float* score, int* cand, cudaStream_t s) {
+  launch_pdl(topk_kernel, dim3(R), dim3(256), 0, s, n, k, score, cand);
+}
+
+// Exact logits of the candidates: one warp per (row, candidate), the dot product of the
+// head row with the head input (hi + lo parts, fp32 sums), an argmax key per row (ties:
+// lower index) and, when asked, the logit.
+template <typename T>
+__global__ void __launch_bounds__(256) cand_head_kernel(int R, int H, int k,
+                                                        const int* __restrict__ cand,
+                                                        const T* __restrict__ head,
+                                                        const T* __restrict__ y, int split,
+                                                        unsigned long long* keys, float* logits,
+                                                        int Vd) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int wg = blockIdx.x * 8 + (threadIdx.x >> 5);  // (row, candidate) pair
+  if (wg >= R * k) return;
+  const int r = wg / k;
+  const int c = cand[wg];
+  const T* hr = head + (size_t)c * H;
+  const T* yh = y + (size_t)r * H;
+  const T* yl = y + (size_t)(r + R) * H;
+  float acc = 0.f;
+  for (int i = lane; i < H; i += 32) {
+    float yi = to_f32(yh[i]);
+    if (split) yi += to_f32(yl[i]);
+    acc = fmaf(to_f32(hr[i]), yi, acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    atomicMax(keys + r, argmax_key(acc, c));
+    if (logits) logits[(size_t)r * Vd + c] = acc;
+  }
+}
+
+__global__ void fill_kernel(size_t n, float v, float* p) {
+  pdl_enter();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
+void launch_cand_head(bool bf16m, int R, int H, int k, const int* cand, const void* head,
+                      const void* y, int split, unsigned long long* keys, float* logits, int Vd,
+                      cudaStream_t s) {
+  if (logits) {
+    const size_t n = (size_t)R * Vd;
+    const size_t nb = (n + 255) / 256;
+    launch_pdl(fill_kernel, dim3(nb < 1024 ? (unsigned)nb : 1024u), dim3(256), 0, s, n,
+               -INFINITY, logits);
+  }
+  const int blocks = cdiv(R * k, 8);
+  if (bf16m)
+    launch_pdl(cand_head_kernel<bf16>, dim3(blocks), dim3(256), 0, s, R, H, k, cand,
+               (const bf16*)head, (const bf16*)y, split, keys, logits, Vd);
+  else
+    launch_pdl(cand_head_kernel<float>, dim3(blocks), dim3(256), 0, s, R, H, k, cand,
+               (const float*)head, (const float*)y, 0, keys, logits, Vd);
+}
+
+// =====================================================================================
 // Greedy verification ("EAGLE-4 overview"): longest agreeing prefix + bonus token.
 // =====================================================================================
 __global__ void verify_kernel(int B, int K, const int* __restrict__ draft,

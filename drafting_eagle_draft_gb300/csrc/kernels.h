@@ -63,6 +63,14 @@ void launch_masked_attention(bool bf16, const MaskedAttnArgs& a, cudaStream_t s)
 struct TcGemmPlan;
 int masked_attn_tc_launch(TcGemmPlan* plan, const MaskedAttnArgs& a, cudaStream_t s);
 
+// Efficient LM head: fixed-point rows -> projection operand; per-row top-k of a score
+// matrix [R][n] -> cand [R][k]; exact logits of the candidates -> argmax keys (+ logits,
+// -inf elsewhere, when `logits` is given).
+void launch_fx_to_act(bool bf16, int R, int n, fx_t* src, int split, void* dst, cudaStream_t s);
+void launch_topk(int R, int n, int k, const float* score, int* cand, cudaStream_t s);
+void launch_cand_head(bool bf16, int R, int H, int k, const int* cand, const void* head,
+                      const void* y, int split, unsigned long long* keys, float* logits, int Vd,
+                      cudaStream_t s);
 void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* out_tokens,
                           cudaStream_t s);
 

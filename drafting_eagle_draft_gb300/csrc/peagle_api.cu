@@ -28,6 +28,13 @@ struct peagle_ctx {
   int num_sms;
   // weights (library-owned device memory)
   void *embed, *emb_mask, *h_shared, *fc, *input_norm, *hidden_norm, *final_norm, *lm_head;
+  // efficient LM head (dims.lm_rank > 0): weights and per-pass buffers
+  void *lm_proj, *lm_score;
+  fx_t* lm_zfx;             // [rows][rank] fixed-point projection
+  void* lm_z;               // [2 rows][rank] projection as the next operand (hi / lo)
+  float* lm_approx;         // [rows][Vd] rank-r scores
+  int* lm_cand;             // [rows][k] candidates
+  unsigned long long* lm_kscr;  // argmax keys of the score GEMM's epilogue (unused)
   int* d2t;
   std::vector<void*> qkv, o, attn_norm, post_norm, gate_up, down;
   float2* rope;
@@ -158,6 +165,10 @@ static int validate_dims(const peagle_dims* d) {
   if (d->max_K * (d->n_q_heads / d->n_kv_heads) > 128) return PEAGLE_ERR_UNSUPPORTED;
   if (d->max_rows > 0 && d->max_seq <= 0) return PEAGLE_ERR_INVALID;
   if (d->attn_window < 0) return PEAGLE_ERR_INVALID;
+  if (d->lm_rank < 0 || d->lm_topk < 0) return PEAGLE_ERR_INVALID;
+  if (d->lm_rank > 0 && (d->lm_rank % 64 || d->lm_rank > 512 || d->lm_topk < 1 ||
+                         d->lm_topk > 1024))
+    return PEAGLE_ERR_UNSUPPORTED;
   // the masked attention tile holds 64 (row, q head) pairs of one kv head
   if (d->max_rows > 0 && d->n_q_heads / d->n_kv_heads > 64) return PEAGLE_ERR_UNSUPPORTED;
   return PEAGLE_OK;
@@ -209,6 +220,7 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
       !w->hidden_norm || !w->qkv || !w->o || !w->post_norm || !w->gate || !w->up || !w->down ||
       !w->final_norm || !w->lm_head || !w->d2t)
     return PEAGLE_ERR_INVALID;
+  if (dims->lm_rank > 0 && (!w->lm_proj || !w->lm_score)) return PEAGLE_ERR_INVALID;
   const peagle_dims& d = *dims;
   for (int l = 0; l < d.n_layers; ++l)
     if (!w->qkv[l] || !w->o[l] || !w->post_norm[l] || !w->gate[l] || !w->up[l] || !w->down[l] ||
@@ -250,6 +262,10 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   TRY(copy_in(c, &c->final_norm, w->final_norm, (size_t)H * es));
   TRY(copy_in(c, &c->lm_head, w->lm_head, (size_t)d.draft_vocab * H * es));
   TRY(copy_in(c, (void**)&c->d2t, w->d2t, (size_t)d.draft_vocab * 4));
+  if (d.lm_rank > 0) {
+    TRY(copy_in(c, &c->lm_proj, w->lm_proj, (size_t)d.lm_rank * H * es));
+    TRY(copy_in(c, &c->lm_score, w->lm_score, (size_t)d.draft_vocab * d.lm_rank * es));
+  }
   c->qkv.resize(d.n_layers);
   c->o.resize(d.n_layers);
   c->attn_norm.assign(d.n_layers, nullptr);
@@ -321,6 +337,15 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     TRY(dalloc(c, &c->K1, (size_t)d.max_seq * nkv * hd * es));
     TRY(dalloc(c, &c->V1, (size_t)d.max_seq * nkv * hd * es));
     TRY(dalloc(c, (void**)&c->row_index, (size_t)d.max_seq * 17 * 4));
+  }
+  if (d.lm_rank > 0) {
+    const int dr = d.max_batch * d.max_K;  // draft rows
+    const int k = d.lm_topk < d.draft_vocab ? d.lm_topk : d.draft_vocab;
+    TRY(dalloc(c, (void**)&c->lm_zfx, (size_t)dr * d.lm_rank * 8));
+    TRY(dalloc(c, &c->lm_z, (size_t)2 * dr * d.lm_rank * es));
+    TRY(dalloc(c, (void**)&c->lm_approx, (size_t)dr * d.draft_vocab * 4));
+    TRY(dalloc(c, (void**)&c->lm_cand, (size_t)dr * k * 4));
+    TRY(dalloc(c, (void**)&c->lm_kscr, (size_t)2 * dr * 8));
   }
   if (c->bf) TRY(tc_create(&c->tc, c->num_sms, R, max_out > 3 * H ? max_out : 3 * H, c->err));
   // fc(h_shared): constant for every MTP row, computed once with the pass's own GEMM
@@ -646,6 +671,39 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
 
 // The draft pass (all_ntp = false: row 0 of each request NTP, rows 1.. MTP) and the
 // catch-up pass (all_ntp: every row takes its own token and hidden state).
+// Efficient LM head over the R draft rows whose final residual is in c->res: final norm,
+// rank-r projection (fixed point, then the next operand), scores of the whole draft
+// vocabulary, per-row top-k candidates, the full head on the candidates, argmax + d2t.
+static int efficient_head(peagle_ctx* c, int R, int split, int32_t* out_tokens,
+                          float* out_logits, cudaStream_t s) {
+  const peagle_dims& d = c->d;
+  const int H = d.hidden, r = d.lm_rank, Vd = d.draft_vocab;
+  const int k = d.lm_topk < Vd ? d.lm_topk : Vd;
+  TIMED(PEAGLE_STAGE_NORM,
+        launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, split, c->Xn, s));
+  {
+    EpiArgs e = epi_base(c, EPI_STORE, R, r);
+    e.in_split = split;
+    e.out_fx = c->lm_zfx;
+    e.out_ld = r;
+    GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_proj, c->Xn, H, r, H, R, e, s);
+  }
+  TIMED(PEAGLE_STAGE_LMHEAD, launch_fx_to_act(c->bf, R, r, c->lm_zfx, split, c->lm_z, s));
+  {
+    EpiArgs e = epi_base(c, EPI_LMHEAD, R, Vd);
+    e.in_split = split;
+    e.logits = c->lm_approx;
+    e.keys = c->lm_kscr;
+    GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_score, c->lm_z, r, Vd, r, R, e, s);
+  }
+  TIMED(PEAGLE_STAGE_LMHEAD, launch_topk(R, Vd, k, c->lm_approx, c->lm_cand, s));
+  TIMED(PEAGLE_STAGE_LMHEAD, launch_cand_head(c->bf, R, H, k, c->lm_cand, c->lm_head, c->Xn,
+                                              split, c->keys, out_logits, Vd, s));
+  TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, out_tokens, s));
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "efficient LM head launch");
+}
+
 static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
                       const int32_t* seq_lens, const void* target_hidden,
                       const int32_t* new_token, int32_t K, bool all_ntp,
@@ -666,10 +724,16 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   // long ragged contexts, the spread norm steps), and the multi-kernel path, whose
   // attention runs several CTAs per SM, is faster: decode_b1 (8 rows) 431 vs 448 us,
   // decode_b2 (16 rows) 613 vs 609 us, ragged_b16 (80 rows) 1927 vs 1465 us.
+  const bool eff_head = d.lm_rank > 0 && (out_draft_tokens || out_logits);
   if (c->pass_on && (c->pass_force || R <= 16)) {
+    // with the efficient LM head the pass kernel stops at the last layer's residual
     const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K, all_ntp,
-                             out_draft_tokens, out_logits, s);
-    if (r != PEAGLE_ERR_UNSUPPORTED) return r;
+                             eff_head ? nullptr : out_draft_tokens,
+                             eff_head ? nullptr : out_logits, s);
+    if (r != PEAGLE_ERR_UNSUPPORTED)
+      return (r == PEAGLE_OK && eff_head)
+                 ? efficient_head(c, R, split, out_draft_tokens, out_logits, s)
+                 : r;
   }
 
   // S1: fc over the NTP rows' target hidden states, then the fused input rows
@@ -765,6 +829,7 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
     cudaError_t ce = cudaGetLastError();
     return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_catch_up launch");
   }
+  if (eff_head) return efficient_head(c, R, split, out_draft_tokens, out_logits, s);
   TIMED(PEAGLE_STAGE_NORM,
         launch_rmsnorm(c->bf, R, H, c->res, c->final_norm, d.rms_eps, split, c->Xn, s));
   {
@@ -844,7 +909,8 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   if (n < 1 || K < 1 || M < 1) return PEAGLE_ERR_INVALID;
   if (d.max_rows <= 0 || M > d.max_rows || n > d.max_seq || K > 16) return PEAGLE_ERR_CAPACITY;
   if (n > d.max_positions) return PEAGLE_ERR_CAPACITY;
-  if (d.attn_window > 0) return PEAGLE_ERR_UNSUPPORTED;  // the training mask has no window
+  // the training mask has no window; the training forward scores the full head
+  if (d.attn_window > 0 || d.lm_rank > 0) return PEAGLE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   const int H = d.hidden, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
   const int qkv_out = (nq + 2 * nkv) * hd;

@@ -83,6 +83,16 @@ typedef struct peagle_dims {
                             .. pos.  0 = the whole context.  Draft and catch-up
                             passes only; peagle_forward_parallel rejects a window
                             with PEAGLE_ERR_UNSUPPORTED.                         */
+  int32_t lm_rank;       /* efficient LM head ("EAGLE-4", "EAGLE-4 overview": a
+                            rank-128 projection scores the whole vocabulary, the
+                            full head scores only the best candidates): 0 = the
+                            full head; else a multiple of 64 (<= 512), with
+                            weights lm_proj / lm_score.  Draft and catch-up passes
+                            only (peagle_forward_parallel: UNSUPPORTED).          */
+  int32_t lm_topk;       /* candidates the full head scores (1 .. 1024; more than
+                            the draft vocabulary means all of it).  With the
+                            efficient head, out_logits holds the exact logits of
+                            the candidates and -inf elsewhere.                   */
 } peagle_dims;
 
 /* Drafter weights (host or device pointers; dtype = dims.dtype for every float
@@ -106,6 +116,10 @@ typedef struct peagle_weights {
   const void* final_norm;        /* [H]                                             */
   const void* lm_head;           /* [Vd, H]                                         */
   const int32_t* d2t;            /* [Vd] draft->target offsets: id = i + d2t[i]     */
+  /* Efficient LM head ("EAGLE-4", "EAGLE-4 overview"), used when dims.lm_rank > 0,
+   * else ignored (may be NULL): */
+  const void* lm_proj;           /* [rank, H]  projection of the LM-head input        */
+  const void* lm_score;          /* [Vd, rank] scores of the projected input           */
 } peagle_weights;
 
 /* Caller-owned drafter KV cache (device).  Layout of k and v:

@@ -45,11 +45,12 @@ def test_exports_every_declared_symbol(pk):
 
 
 def test_struct_layout_matches_header(pk):
-    # peagle_dims: 14 int32 + 2 float + attn_window; peagle_weights: 16 pointers;
-    # peagle_kv: 2 ptr + 2 int
-    assert ctypes.sizeof(pk.PeagleDims) == 68
+    # peagle_dims: 14 int32 + 2 float + attn_window, lm_rank, lm_topk;
+    # peagle_weights: 18 pointers; peagle_kv: 2 ptr + 2 int
+    assert ctypes.sizeof(pk.PeagleDims) == 76
     assert pk.PeagleDims.attn_window.offset == 64
-    assert ctypes.sizeof(pk.PeagleWeights) == 16 * 8
+    assert pk.PeagleDims.lm_topk.offset == 72
+    assert ctypes.sizeof(pk.PeagleWeights) == 18 * 8
     assert ctypes.sizeof(pk.PeagleKV) == 24
 
 

@@ -1,0 +1,109 @@
+"""Efficient LM head ("EAGLE-4", "EAGLE-4 overview": a rank-128 projection scores the whole
+vocabulary and the full head scores only the best candidates) on the GPU against the fp64
+oracle, on the fp32 path and both bf16 paths.
+
+Several answers can be right where two rank-r scores tie at the candidate boundary, so a
+row's candidate set must equal the oracle's up to scores within the tolerance of the
+boundary score; the candidates' exact logits must match; the token must match wherever
+the candidate sets agree and the oracle's top-1 margin among them is clear, and must be
+the best of its own candidates everywhere."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from pe_helpers import LOGIT_TOL, MARGIN, make_ctx, oracle_draft, run_draft
+
+pytestmark = pytest.mark.gpu
+
+SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_dim=64,
+                        intermediate=320, draft_vocab=1000, target_vocab=1500,
+                        rope_theta=10000.0, rms_eps=1e-5, dtype="bf16", d2t="monotone",
+                        lm_rank=64, lm_topk=32)
+
+
+def _case(dims, lens, K, seed):
+    wl = synth.Workload("e", dims, len(lens), K, tuple(lens))
+    w = synth.make_weights(dims, seed)
+    inp = synth.make_decode_inputs(wl, seed + 1)
+    return w, inp
+
+
+def _check(dims, w, ref, toks, lg, what):
+    tol = LOGIT_TOL[dims.dtype]
+    B, K, Vd = lg.shape
+    k = min(dims.lm_topk, Vd)
+    agree = 0
+    for b in range(B):
+        for j in range(K):
+            cg = set(np.nonzero(np.isfinite(lg[b, j]))[0].tolist())
+            co = set(np.nonzero(np.isfinite(ref.logits[b, j]))[0].tolist())
+            assert len(cg) == k, f"{what}: row {b},{j} has {len(cg)} candidates"
+            kth = np.sort(ref.approx[b, j])[::-1][k - 1]
+            for i in cg ^ co:
+                assert abs(ref.approx[b, j, i] - kth) <= tol, \
+                    f"{what}: row {b},{j} candidate {i} far from the boundary"
+            both = sorted(cg & co)
+            err = np.max(np.abs(lg[b, j, both] - ref.logits[b, j, both]))
+            assert err <= tol, f"{what}: candidate logits err {err:.3e}"
+            own = max(cg, key=lambda i: (lg[b, j, i], -i))
+            assert toks[b, j] == own + int(w["d2t"][own]), f"{what}: token not its best"
+            if cg == co and ref.margin[b, j] > MARGIN:
+                agree += 1
+                assert toks[b, j] == ref.tokens[b, j], f"{what}: row {b},{j} token differs"
+    assert agree > 0.5 * B * K, f"{what}: too few rows with a clear answer ({agree})"
+
+
+def test_tiny_f32_efficient_head():
+    dims = synth.shrink(synth.DIMS_TINY, lm_rank=64, lm_topk=16)
+    w, inp = _case(dims, [0, 50, 128], 4, 71)
+    ctx = make_ctx(dims, w, 3, 4, inp["capacity"] + 1)
+    toks, lg, _ = run_draft(ctx, dims, inp, 4)
+    _check(dims, w, oracle_draft(dims, w, inp, 4), toks, lg, "tiny f32 efficient head")
+    ctx.close()
+
+
+@pytest.mark.parametrize("pass_kernel", [True, False])
+@pytest.mark.parametrize("lens,K,topk", [([40, 300], 5, 32), ([129], 8, 1), ([7, 64, 90], 3, 200)])
+def test_small_bf16_efficient_head(pass_kernel, lens, K, topk):
+    dims = synth.shrink(SMALL_BF16, lm_topk=topk)
+    w, inp = _case(dims, lens, K, 31 + K)
+    ctx = make_ctx(dims, w, len(lens), K, inp["capacity"] + 1, pass_kernel=pass_kernel)
+    toks, lg, _ = run_draft(ctx, dims, inp, K)
+    _check(dims, w, oracle_draft(dims, w, inp, K), toks, lg,
+           f"bf16 efficient head {lens} K={K} top{topk} {'pass' if pass_kernel else 'multi'}")
+    ctx.close()
+
+
+def test_every_candidate_is_the_full_head():
+    """lm_topk >= the draft vocabulary: the same tokens as the full head, and logits equal
+    to the full head's within the tolerance (the same rows, scored by another kernel)."""
+    lens, K = [33, 90], 4
+    dims = synth.shrink(SMALL_BF16, lm_topk=1024)
+    w, inp = _case(dims, lens, K, 9)
+    out = []
+    for dd in (synth.shrink(dims, lm_rank=0, lm_topk=0), dims):
+        ctx = make_ctx(dd, w, 2, K, inp["capacity"] + 1)
+        toks, lg, _ = run_draft(ctx, dd, inp, K)
+        out.append((toks, lg))
+        ctx.close()
+    assert np.array_equal(out[0][0], out[1][0])
+    assert np.max(np.abs(out[0][1] - out[1][1])) < 1e-3
+
+
+def test_forward_parallel_rejects_the_efficient_head():
+    import drafting_eagle_draft_gb300 as m
+
+    dims = SMALL_BF16
+    w = synth.make_weights(dims, 3)
+    ctx = make_ctx(dims, w, 1, 4, 64, max_rows=64, max_seq=16)
+    n, K = 8, 2
+    rp, rd = m.peagle_cod_rows(n, K, 1.0, np.zeros((n, K)))
+    tok = torch.zeros(n, dtype=torch.int32, device="cuda")
+    hid = torch.zeros(n, 3 * dims.hidden, dtype=torch.bfloat16, device="cuda")
+    am = torch.empty(len(rp), dtype=torch.int32, device="cuda")
+    with pytest.raises(m.PeagleError) as e:
+        m.peagle_forward_parallel(ctx, n, K, tok, hid, torch.from_numpy(rp).cuda(),
+                                  torch.from_numpy(rd).cuda(), len(rp), am, None)
+    assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
+    ctx.close()
