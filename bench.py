@@ -12,9 +12,11 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode_b1|decode_b2|ragged_b16]
 
-Two extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
-COD 0.8) and sliding_window (the concurrency-2 workload with and without a 4096-position
-drafter attention window); --no-train-fwd / --no-window skip them.
+Three extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
+COD 0.8), sliding_window (the concurrency-2 workload with and without a 4096-position
+drafter attention window) and efficient_head (the headline workload with the rank-128 /
+top-128 LM head and with the full head, on the 32000-entry draft vocabulary and on the
+whole 201088-entry vocabulary); --no-train-fwd / --no-window / --no-head skip them.
 
 --impl reference times the fp64 oracle on the host cores instead (a deliberately slow
 plain program; see the cpu_baseline object).  Under torchrun each rank runs an
@@ -54,6 +56,8 @@ def parse():
                     help="skip the training-style masked forward measurement")
     ap.add_argument("--no-window", action="store_true",
                     help="skip the sliding-window attention measurement")
+    ap.add_argument("--no-head", action="store_true",
+                    help="skip the efficient LM head measurement")
     return ap.parse_args()
 
 
@@ -382,52 +386,60 @@ def run_ours(args, rank, world, dist):
         out["train_fwd"] = train_fwd_measure(dev)
     if rank == 0 and world == 1 and not args.no_window:
         out["sliding_window"] = window_measure(dev)
+    if rank == 0 and world == 1 and not args.no_head:
+        out["efficient_head"] = head_measure(dev)
     return out
 
 
-def window_measure(dev, window=4096, reps=20):
-    """Sliding-window drafter attention on the concurrency-2 workload (contexts 8192 and
-    10240, K=8): draft-pass time as a CUDA graph with a 4096-position window and with full
-    attention on the same inputs, and the cached keys / values each pass reads."""
+def _pass_us(dev, wl, dims, w, inp, reps=20):
+    """Draft-pass time of one context on `inp`, replayed as a CUDA graph (microseconds)."""
     import torch
 
     import drafting_eagle_draft_gb300 as pk
 
-    wl = synth.WORKLOADS["decode_b2"]
-    w = synth.make_weights(wl.dims, 1234)
-    inp = synth.make_decode_inputs(wl, 99)
     B, K, cap = wl.batch, wl.K, inp["capacity"]
     ck, cv = inp["cache_k"].to(dev), inp["cache_v"].to(dev)
     kv = pk.kv_struct(ck, cv, cap, B)
     sl = torch.from_numpy(inp["seq_lens"]).to(dev)
     th = inp["target_hidden"].to(dev)
     nt = torch.from_numpy(inp["new_token"]).to(dev)
-    res = {}
-    for name, W in (("window", window), ("full", 0)):
-        dims = synth.shrink(wl.dims, attn_window=W)
-        ctx = pk.peagle_create(w, pk.make_dims(dims, B, K, cap))
-        toks = torch.zeros(B, K, dtype=torch.int32, device=dev)
-        s = torch.cuda.Stream(device=dev)
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, s)
-        s.synchronize()
-        assert pk.peagle_status(ctx) == pk.PEAGLE_OK
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
+    ctx = pk.peagle_create(w, pk.make_dims(dims, B, K, cap))
+    toks = torch.zeros(B, K, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
             pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, s)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                g.replay()
-            e0.record(s)
-            for _ in range(reps):
-                g.replay()
-            e1.record(s)
-        e1.synchronize()
-        res[name] = e0.elapsed_time(e1) / reps * 1e3
-        ctx.close()
+    s.synchronize()
+    assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, s)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    out = toks.cpu().numpy()
+    ctx.close()
+    return us, out
+
+
+def window_measure(dev, window=4096):
+    """Sliding-window drafter attention on the concurrency-2 workload (contexts 8192 and
+    10240, K=8): draft-pass time as a CUDA graph with a 4096-position window and with full
+    attention on the same inputs, and the cached keys / values each pass reads."""
+    wl = synth.WORKLOADS["decode_b2"]
+    w = synth.make_weights(wl.dims, 1234)
+    inp = synth.make_decode_inputs(wl, 99)
+    K = wl.K
+    res = {name: _pass_us(dev, wl, synth.shrink(wl.dims, attn_window=W), w, inp)[0]
+           for name, W in (("window", window), ("full", 0))}
     lens = [int(x) for x in inp["seq_lens"]]
     kvb = lambda span: sum(span(L) for L in lens) * wl.dims.n_kv_heads * wl.dims.head_dim * 2 * 2 \
         * wl.dims.n_layers
@@ -436,6 +448,35 @@ def window_measure(dev, window=4096, reps=20):
             "us_per_pass_full": round(res["full"], 2),
             "kv_bytes_per_pass": kvb(lambda L: min(L + K, window + K - 1)),
             "kv_bytes_per_pass_full": kvb(lambda L: L + K)}
+
+
+def head_measure(dev, rank=128, topk=128):
+    """Efficient LM head on the headline workload (batch 1, 4096 cached positions, K=8):
+    draft-pass time as a CUDA graph with the rank-128 scoring projection and the full head
+    on its 128 best candidates, against the full head on the same weights and inputs, the
+    head bytes each pass reads (candidate rows counted once per draft row), and how many
+    of the K drafted tokens the two agree on.  Measured on the 32000-entry draft vocabulary
+    and on the whole 201088-entry target vocabulary as the draft vocabulary (no d2t), the
+    setting the efficient head is meant for."""
+    wl = synth.WORKLOADS["decode_b1"]
+    inp = synth.make_decode_inputs(wl, 99)
+    out = {}
+    for name, vocab in (("draft_vocab", None), ("full_vocab", wl.dims.target_vocab)):
+        d = synth.shrink(wl.dims, lm_rank=rank, lm_topk=topk)
+        if vocab:
+            d = synth.shrink(d, draft_vocab=vocab, d2t="identity")
+        w = synth.make_weights(d, 1234)
+        eff, t_eff = _pass_us(dev, wl, d, w, inp)
+        full, t_full = _pass_us(dev, wl, synth.shrink(d, lm_rank=0, lm_topk=0), w, inp)
+        H, Vd, R = d.hidden, d.draft_vocab, wl.batch * wl.K
+        out[name] = {
+            "workload": "decode_b1 (context 4096, K=8), Vd %d, rank %d, top %d" % (Vd, rank, topk),
+            "us_per_pass": round(eff, 2), "us_per_pass_full_head": round(full, 2),
+            "head_bytes_per_pass": 2 * (rank * H + Vd * rank + R * topk * H),
+            "head_bytes_per_pass_full_head": 2 * Vd * H,
+            "tokens_equal_full_head": int((t_eff == t_full).sum()), "tokens": int(t_eff.size)}
+        del w
+    return out
 
 
 def train_fwd_measure(dev, reps=3):

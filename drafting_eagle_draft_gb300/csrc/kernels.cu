@@ -10,6 +10,7 @@
 
 #include "kernels.h"
 #include "attn_decode.cuh"
+#include "tc_ptx.cuh"
 
 namespace peagle {
 
@@ -30,6 +31,24 @@ __device__ __forceinline__ void load4<bf16>(const bf16* p, float* v) {
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&t.y);
   float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+
+// A 16-byte piece as fp32: 8 bf16 or 4 floats.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& q, float* v);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& q, float* v) {
+  v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+  v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<bf16>(const uint4& q, float* v) {
+  const unsigned w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
 }
 
 template <typename T>
@@ -991,133 +1010,610 @@ void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* 
 // Efficient LM head ("EAGLE-4", "EAGLE-4 overview": a rank-128 projection scores the
 // vocabulary, the full head scores the best candidates).
 // =====================================================================================
-// Fixed-point rows [R][n] -> the next projection's operand ([2R][n] bf16 hi / lo, or
-// [R][n] fp32); the fixed-point rows are cleared for the next pass.
-template <typename T>
-__global__ void fx_to_act_kernel(int R, int n, fx_t* __restrict__ src, int split,
-                                 T* __restrict__ dst) {
-  pdl_enter();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R * n; i += gridDim.x * blockDim.x) {
-    const int r = i / n, col = i - r * n;
-    store_act<T>(dst, n, r, R, split, col, from_fx(src[i]));
-    src[i] = 0;
-  }
-}
-
-void launch_fx_to_act(bool bf16m, int R, int n, fx_t* src, int split, void* dst,
-                      cudaStream_t s) {
-  const int blocks = cdiv(R * n, 256) < 1024 ? cdiv(R * n, 256) : 1024;
-  if (bf16m)
-    launch_pdl(fx_to_act_kernel<bf16>, dim3(blocks), dim3(256), 0, s, R, n, src, split,
-               (bf16*)dst);
-  else
-    launch_pdl(fx_to_act_kernel<float>, dim3(blocks), dim3(256), 0, s, R, n, src, 0,
-               (float*)dst);
-}
-
-// Top-k of one row of scores per CTA (256 threads): radix selection of the k-th largest
-// orderable key (four passes of 8 bits), then the keys above it and, in index order,
-// enough of the keys equal to it.  cand[r][0 .. k) = the chosen indices (any order).
+// Orderable 32-bit image of a score: larger score, larger key; +0 and -0 map together.
 __device__ __forceinline__ unsigned score_key(float v) {
   if (v == 0.f) v = 0.f;
   const unsigned u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(int n, int k, const float* __restrict__ score,
-                                                   int* __restrict__ cand) {
-  __shared__ unsigned hist[256];
-  __shared__ unsigned s_prefix, s_need, s_count;
-  __shared__ unsigned wsum[8];
+// Histogram of the scores' first radix digit (key bits 31..21, 2048 buckets) per draft
+// row, counted in shared memory by the scoring kernels (two 16-bit counters per word, so
+// 8 draft rows fit in 32 KB) and added into the global [R][2048] histogram that the top-k
+// selection starts from.
+constexpr int HS_ROWS = 8;
+__device__ __forceinline__ void hs_add(unsigned* sh, int rr, float v) {
+  const unsigned b = score_key(v) >> 21;
+  atomicAdd(&sh[rr * 1024 + (b >> 1)], (b & 1u) ? 65536u : 1u);
+}
+__device__ __forceinline__ void hs_clear(unsigned* sh) {
+  for (int i = threadIdx.x; i < HS_ROWS * 1024; i += blockDim.x) sh[i] = 0u;
+}
+__device__ __forceinline__ void hs_flush(const unsigned* sh, int r0, int R, unsigned* hist) {
+  for (int i = threadIdx.x; i < HS_ROWS * 1024; i += blockDim.x) {
+    const unsigned w = sh[i];
+    const int rr = i >> 10;
+    if (w == 0u || r0 + rr >= R) continue;
+    unsigned* h = hist + (size_t)(r0 + rr) * 2048 + 2 * (i & 1023);
+    if (w & 0xFFFFu) atomicAdd(h, w & 0xFFFFu);
+    if (w >> 16) atomicAdd(h + 1, w >> 16);
+  }
+}
+
+// Rank-r scores of the whole draft vocabulary, fp32 weights, on the CUDA cores:
+//   approx[row][v] = lm_score[v] . z[row],  z = the fixed-point rank-r projection [R][r].
+// A vocabulary row is r elements in 16-byte pieces; a group of LPR lanes holds one row
+// (CPL pieces per lane), so a warp scores 32 / LPR rows per step.  Draft rows are taken
+// RC at a time with their z pieces in registers.  The group's partial sums are combined
+// by a reduce-scatter over shuffles: each halving step trades half of the RC sums with
+// the partner lane, so after log2(RC) steps a lane holds one draft row's sum, and plain
+// shuffle adds finish it.
+template <int RANK>
+__global__ void __launch_bounds__(256) head_score_f32_kernel(int R, int Vd,
+                                                             const fx_t* __restrict__ zfx,
+                                                             const float* __restrict__ score,
+                                                             float* __restrict__ approx,
+                                                             unsigned* __restrict__ hist) {
+  constexpr int E = 4;                         // elements per piece
+  constexpr int P = RANK / E;                  // pieces per vocabulary row
+  constexpr int CPL = P > 32 ? P / 32 : 1;     // pieces per lane
+  constexpr int LPR = P / CPL;                 // lanes per vocabulary row (16 or 32)
+  constexpr int RPW = 32 / LPR;                // vocabulary rows per warp step
+  constexpr int RC = HS_ROWS / CPL;            // draft rows per sweep (<= LPR)
+  static_assert(RC <= LPR, "reduce-scatter needs a lane per draft row");
+  __shared__ unsigned sh[HS_ROWS * 1024];
   pdl_enter();
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const float* x = score + (size_t)r * n;
-  int* out = cand + (size_t)r * k;
-  unsigned prefix = 0, mask = 0, need = (unsigned)k;  // the k-th largest key has `prefix`
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += 256) {
-      const unsigned key = score_key(x[i]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      unsigned above = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (above + hist[d] >= need) break;
-        above += hist[d];
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, pl = lane % LPR;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int stride = gridDim.x * 8 * RPW;
+  // the draft row whose sum this lane ends with, and whether it stores it
+  int mine = 0;
+#pragma unroll
+  for (int o = LPR / 2, cnt = RC; cnt > 1; o >>= 1, cnt >>= 1) mine += (pl & o) ? cnt / 2 : 0;
+  const bool writer = (pl & (LPR / RC - 1)) == 0;
+  for (int r0 = 0; r0 < R; r0 += RC) {
+    hs_clear(sh);
+    float z[RC][CPL][E];
+#pragma unroll
+    for (int rr = 0; rr < RC; ++rr)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const fx_t* zp = zfx + (size_t)(r0 + rr) * RANK + (pl + c * LPR) * E;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          longlong2 q = make_longlong2(0, 0);
+          if (r0 + rr < R) q = *reinterpret_cast<const longlong2*>(zp + e);
+          z[rr][c][e] = from_fx(q.x);
+          z[rr][c][e + 1] = from_fx(q.y);
+        }
       }
-      s_prefix = prefix | ((unsigned)d << shift);
-      s_need = need - above;
+    __syncthreads();
+    // the loop bound is the warp's first row, so every lane takes the same steps
+    for (int w0 = gw * RPW; w0 < Vd; w0 += stride) {
+      const int v = w0 + sub;
+      float w[CPL][E];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const float4 q = v < Vd ? *reinterpret_cast<const float4*>(score + (size_t)v * RANK +
+                                                                   (pl + c * LPR) * E)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[c][0] = q.x; w[c][1] = q.y; w[c][2] = q.z; w[c][3] = q.w;
+      }
+      float acc[RC];
+#pragma unroll
+      for (int rr = 0; rr < RC; ++rr) {
+        float a = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+#pragma unroll
+          for (int e = 0; e < E; ++e) a = fmaf(w[c][e], z[rr][c][e], a);
+        acc[rr] = a;
+      }
+#pragma unroll
+      for (int o = LPR / 2, cnt = RC; o > 0; o >>= 1, cnt = cnt > 1 ? cnt >> 1 : 1) {
+        const bool upper = (pl & o) != 0;
+#pragma unroll
+        for (int i = 0; i < (cnt > 1 ? cnt / 2 : 1); ++i) {
+          const float send = cnt > 1 ? (upper ? acc[i] : acc[i + cnt / 2]) : acc[0];
+          const float keep = cnt > 1 ? (upper ? acc[i + cnt / 2] : acc[i]) : acc[0];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      if (writer && v < Vd && r0 + mine < R) {
+        approx[(size_t)(r0 + mine) * Vd + v] = acc[0];
+        hs_add(sh, mine, acc[0]);
+      }
     }
     __syncthreads();
-    prefix = s_prefix;
-    need = s_need;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  // prefix = the k-th largest key; `need` of the keys equal to it are taken
-  if (tid == 0) s_count = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += 256)
-    if (score_key(x[i]) > prefix) out[atomicAdd(&s_count, 1u)] = i;
-  __syncthreads();
-  const unsigned base = s_count;  // = k - need
-  unsigned taken = 0;
-  for (int i0 = 0; i0 < n && taken < need; i0 += 256) {
-    const int i = i0 + tid;
-    const bool eq = i < n && score_key(x[i]) == prefix;
-    const unsigned bal = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) wsum[wid] = __popc(bal);
-    __syncthreads();
-    unsigned before = 0, total = 0;
-    for (int w = 0; w < 8; ++w) {
-      if (w < wid) before += wsum[w];
-      total += wsum[w];
-    }
-    const unsigned rank = taken + before + __popc(bal & ((1u << lane) - 1u));
-    if (eq && rank < need) out[base + rank] = i;
-    taken += total;
+    hs_flush(sh, r0, R, hist);
     __syncthreads();
   }
 }
 
-void launch_topk(int R, int n, int k, const float* score, int* cand, cudaStream_t s) {
-  launch_pdl(topk_kernel, dim3(R), dim3(256), 0, s, n, k, score, cand);
+// Rank-r scores, bf16 weights, on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
+// A = 16 vocabulary rows of lm_score, B = 8 draft rows of z as bf16 hi + lo parts (z to
+// about 16 significant bits), C = the 16 x 8 scores.  A dot product may run over k in any
+// order that A and B share, so each lane takes 16 contiguous bytes of its two A rows per
+// 32-wide k chunk (two MMA k-steps) and z at the same k.
+// Each CTA streams lm_score through a ring of HS_STAGES shared-memory stages of 32 KB
+// (stages dealt to the CTAs in turn): one producer thread issues a bulk copy per stage
+// (completion on the stage's `full` mbarrier, L2 evict-last), eight consumer warps take
+// one 16-row tile each per turn and release it on the stage's `empty` mbarrier.  Waits
+// are bounded: a wait that gives up raises PEAGLE_DEV_TIMEOUT and every role leaves its
+// loop.
+constexpr int HS_WARPS = 8;
+constexpr int HS_THREADS = 32 * (HS_WARPS + 1);
+constexpr int HS_STAGES = 4;
+constexpr int HS_STAGE_BYTES = 32 * 1024;
+
+template <int RANK>
+__global__ void __launch_bounds__(HS_THREADS, 1) head_score_mma_kernel(
+    int R, int Vd, const fx_t* __restrict__ zfx, const bf16* __restrict__ score,
+    float* __restrict__ approx, unsigned* __restrict__ hist, unsigned* err) {
+  constexpr int KC = RANK / 32;                // 32-wide k chunks
+  constexpr int AG = KC < 4 ? KC : 4;          // chunks of A read together
+  constexpr int ROW_B = RANK * 2;
+  constexpr int TILE_B = 16 * ROW_B;
+  constexpr int TPS = HS_STAGE_BYTES / TILE_B; // tiles per stage
+  static_assert(TPS >= 1, "a stage holds a tile");
+  extern __shared__ __align__(128) uint8_t hs_ring[];
+  __shared__ unsigned sh[HS_ROWS * 1024];
+  __shared__ uint64_t full[HS_STAGES], empty[HS_STAGES];
+  __shared__ int abort_flag;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
+  // fills of TPS tiles are dealt to the CTAs in turn, so at any moment the grid reads one
+  // contiguous window of lm_score (spread over every memory channel)
+  const int tiles = (Vd + 15) / 16;
+  const int fills = (tiles + TPS - 1) / TPS;
+  const int nfill = fills > (int)blockIdx.x ? (fills - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int nt = nfill * TPS;  // CTA-local tile slots (slots past the vocabulary are skipped)
+  if (t == 0) {
+    for (int i = 0; i < HS_STAGES; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], TPS);
+    }
+    abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_enter();
+  for (int r0 = 0, sweep = 0; r0 < R; r0 += HS_ROWS, ++sweep) {
+    const int fbase = sweep * nfill;  // fills of earlier sweeps (barrier phases run on)
+    hs_clear(sh);
+    __syncthreads();
+    if (warp == HS_WARPS) {
+      if (lane == 0) {
+        // the scoring factor is small next to the pass's weights, which stream through L2
+        // with evict-first: keep it resident from one pass to the next
+        const uint64_t pol = tc::policy_evict_last();
+        int issued = 0;
+        for (int f = 0; f < nfill && !abort_flag; ++f) {
+          const int F = fbase + f, st = F % HS_STAGES;
+          if (F >= HS_STAGES && !tc::mbar_wait(&empty[st], ((F / HS_STAGES) - 1) & 1, &abort_flag)) {
+            raise_error(err, PEAGLE_DEV_TIMEOUT);
+            abort_flag = 1;
+            break;
+          }
+          const int t0 = (f * (int)gridDim.x + (int)blockIdx.x) * TPS;
+          const int ft = tiles - t0 < TPS ? tiles - t0 : TPS;  // tiles in this fill
+          const int rows = (Vd - 16 * t0) < 16 * ft ? Vd - 16 * t0 : 16 * ft;
+          const uint32_t bytes = (uint32_t)rows * ROW_B;
+          tc::mbar_expect_tx(&full[st], bytes);
+          tc::bulk_load(hs_ring + (size_t)st * HS_STAGE_BYTES, score + (size_t)t0 * 16 * RANK, bytes,
+                        &full[st], pol);
+          ++issued;
+          // slots of a short last fill are released at once
+          for (int i = ft; i < TPS; ++i) tc::mbar_arrive(&empty[st]);
+        }
+        if (abort_flag) {  // let the copies in flight land before the CTA exits
+          for (int f = issued > HS_STAGES ? issued - HS_STAGES : 0; f < issued; ++f) {
+            const int F = fbase + f;
+            tc::mbar_wait(&full[F % HS_STAGES], (F / HS_STAGES) & 1, &abort_flag, 100000000ull);
+          }
+        }
+      }
+    } else {
+      // B fragments: k-step s of chunk c takes k = 32c + 8q + 4s + {0,1} (b0), {2,3} (b1)
+      uint32_t bh[KC][2][2], bl[KC][2][2];
+#pragma unroll
+      for (int c = 0; c < KC; ++c)
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float z0 = 0.f, z1 = 0.f;
+            if (r0 + g < R) {
+              const longlong2 zz = *reinterpret_cast<const longlong2*>(
+                  zfx + (size_t)(r0 + g) * RANK + 32 * c + 8 * q + 4 * s2 + 2 * j);
+              z0 = from_fx(zz.x);
+              z1 = from_fx(zz.y);
+            }
+            split2(z0, z1, bh[c][s2][j], bl[c][s2][j]);
+          }
+      for (int j = warp; j < nt; j += HS_WARPS) {
+        const int tg = ((j / TPS) * (int)gridDim.x + (int)blockIdx.x) * TPS + j % TPS;
+        if (tg >= tiles) continue;  // released by the producer
+        const int F = fbase + j / TPS, st = F % HS_STAGES;
+        if (!tc::mbar_wait(&full[st], (F / HS_STAGES) & 1, &abort_flag)) {
+          raise_error(err, PEAGLE_DEV_TIMEOUT);
+          abort_flag = 1;
+          break;
+        }
+        const uint8_t* tile = hs_ring + (size_t)st * HS_STAGE_BYTES + (size_t)(j % TPS) * TILE_B;
+        const int va = tg * 16 + g, vb = va + 8;
+        // hi and lo products and the two k-steps of a chunk accumulate separately
+        float acc[2][2][4] = {};
+#pragma unroll
+        for (int c0 = 0; c0 < KC; c0 += AG) {
+          uint4 qa[AG], qb[AG];
+#pragma unroll
+          for (int c = 0; c < AG; ++c) {
+            const int off = 64 * (c0 + c) + 16 * q;
+            qa[c] = va < Vd ? *reinterpret_cast<const uint4*>(tile + g * ROW_B + off)
+                            : make_uint4(0u, 0u, 0u, 0u);
+            qb[c] = vb < Vd ? *reinterpret_cast<const uint4*>(tile + (g + 8) * ROW_B + off)
+                            : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int c = 0; c < AG; ++c) {
+            const uint32_t wa[4] = {qa[c].x, qa[c].y, qa[c].z, qa[c].w};
+            const uint32_t wb[4] = {qb[c].x, qb[c].y, qb[c].z, qb[c].w};
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+              // A: (row g, k 2q, 2q+1) = elements 4s, 4s+1 of the piece; (row g, k 2q+8,
+              // 2q+9) = elements 4s+2, 4s+3; rows g+8 likewise from the second row
+              const uint32_t af[4] = {wa[2 * s2], wb[2 * s2], wa[2 * s2 + 1], wb[2 * s2 + 1]};
+              mma16816(acc[0][s2], af, bh[c0 + c][s2][0], bh[c0 + c][s2][1]);
+              mma16816(acc[1][s2], af, bl[c0 + c][s2][0], bl[c0 + c][s2][1]);
+            }
+          }
+        }
+        // the products depend on every shared-memory read of the tile: release it
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[st]);
+        // acc[.][.] = (va, draft 2q), (va, 2q + 1), (vb, 2q), (vb, 2q + 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int rr = 2 * q + (e & 1), v = (e < 2) ? va : vb;
+          const float x = (acc[0][0][e] + acc[0][1][e]) + (acc[1][0][e] + acc[1][1][e]);
+          if (r0 + rr < R && v < Vd) {
+            approx[(size_t)(r0 + rr) * Vd + v] = x;
+            hs_add(sh, rr, x);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (abort_flag) return;
+    hs_flush(sh, r0, R, hist);
+  }
 }
 
-// Exact logits of the candidates: one warp per (row, candidate), the dot product of the
-// head row with the head input (hi + lo parts, fp32 sums), an argmax key per row (ties:
-// lower index) and, when asked, the logit.
+template <int RANK>
+static void head_score_mma_launch(int blocks, cudaStream_t s, int R, int Vd, const fx_t* zfx,
+                                  const bf16* score, float* approx, unsigned* hist,
+                                  unsigned* err) {
+  const size_t smem = (size_t)HS_STAGES * HS_STAGE_BYTES;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(head_score_mma_kernel<RANK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    attr_set = true;
+  }
+  launch_pdl(head_score_mma_kernel<RANK>, dim3(blocks), dim3(HS_THREADS), smem, s, R, Vd, zfx,
+             score, approx, hist, err);
+}
+
+template <typename KernelT, typename T>
+static void head_score_go(KernelT kern, int blocks, cudaStream_t s, int R, int Vd,
+                          const fx_t* zfx, const T* score, float* approx, unsigned* hist) {
+  launch_pdl(kern, dim3(blocks), dim3(256), 0, s, R, Vd, zfx, score, approx, hist);
+}
+
+void launch_head_score(bool bf16m, int R, int r, int Vd, const fx_t* zfx, const void* score,
+                       float* approx, unsigned* hist, unsigned* err, int num_sms, cudaStream_t s) {
+  if (bf16m) {
+    // one CTA per SM
+    int blocks = cdiv(Vd, 16 * 8);
+    if (blocks > num_sms) blocks = num_sms;
+    const bf16* w = (const bf16*)score;
+    if (r == 64) head_score_mma_launch<64>(blocks, s, R, Vd, zfx, w, approx, hist, err);
+    else if (r == 128) head_score_mma_launch<128>(blocks, s, R, Vd, zfx, w, approx, hist, err);
+    else if (r == 256) head_score_mma_launch<256>(blocks, s, R, Vd, zfx, w, approx, hist, err);
+    else head_score_mma_launch<512>(blocks, s, R, Vd, zfx, w, approx, hist, err);
+    return;
+  }
+  // CUDA cores: vocabulary rows a CTA scores per step: 8 warps x (512 bytes / row bytes)
+  const int per_cta = 8 * (r * 4 < 512 ? 512 / (r * 4) : 1);
+  int blocks = cdiv(Vd, per_cta * 2);
+  if (blocks > 2 * num_sms) blocks = 2 * num_sms;
+  const float* w = (const float*)score;
+  if (r == 64) head_score_go(head_score_f32_kernel<64>, blocks, s, R, Vd, zfx, w, approx, hist);
+  else if (r == 128) head_score_go(head_score_f32_kernel<128>, blocks, s, R, Vd, zfx, w, approx, hist);
+  else if (r == 256) head_score_go(head_score_f32_kernel<256>, blocks, s, R, Vd, zfx, w, approx, hist);
+  else head_score_go(head_score_f32_kernel<512>, blocks, s, R, Vd, zfx, w, approx, hist);
+}
+
+// Top-k of each row of scores [R][n], largest first, ties to the lower index, from the
+// first-digit histograms the scoring kernel left.  Keys are the scores' orderable 32-bit
+// images, selected by radix digits of 11, 11 and 10 bits.  A grid of S slices per row:
+// every CTA finds the boundary bucket of the first digit (the one holding the k-th
+// largest key) and gathers its slice's keys at or above it (a few hundred per row for
+// smooth scores) into a global list; the last CTA of the row to finish loads the list
+// into shared memory and resolves the other two digits and the ties there.  Rows whose
+// list does not fit are resolved by that CTA over global memory instead, with the ties
+// taken in index order.  cand[row][0 .. k) = the chosen indices (any order).  The last
+// CTA also clears the row's histogram, list counters and fixed-point projection for the
+// next pass.
+constexpr int TS_THREADS = 512;
+constexpr int TK_CAP = 4096;
+
+struct TopkSmem {
+  unsigned hist[2048];
+  unsigned lkey[TK_CAP];
+  int lidx[TK_CAP];
+  unsigned wsum[32];
+  unsigned digit, above, nout;
+  int last;
+};
+
+// The bucket of h[2048] holding the need-th largest key (counted from the top) ->
+// S.digit, and the number of keys in the buckets above it -> S.above.
+__device__ void tk_find(TopkSmem& S, const unsigned* h, unsigned need) {
+  constexpr int BPT = 2048 / TS_THREADS;
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  unsigned c[BPT], sum = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    c[j] = h[2047 - BPT * t - j];
+    sum += c[j];
+  }
+  unsigned inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) S.wsum[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const unsigned w = lane < TS_THREADS / 32 ? S.wsum[lane] : 0u;
+    unsigned winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
+    }
+    if (lane < TS_THREADS / 32) S.wsum[lane] = winc - w;
+  }
+  __syncthreads();
+  unsigned run = S.wsum[wid] + inc - sum;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    if (run < need && run + c[j] >= need) {
+      S.digit = (unsigned)(2047 - BPT * t - j);
+      S.above = run;
+    }
+    run += c[j];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void tk_clear(TopkSmem& S) {
+  for (int i = threadIdx.x; i < 2048; i += TS_THREADS) S.hist[i] = 0u;
+  __syncthreads();
+}
+
+// f(key, index) over scores x[beg, end) in global memory
+template <typename F>
+__device__ __forceinline__ void tk_row(const float* __restrict__ x, int beg, int end, F f) {
+  for (int i = beg + threadIdx.x; i < end; i += TS_THREADS) f(score_key(x[i]), i);
+}
+
+// Refine the boundary digit d1 (bits 31..21, need1 keys still wanted in it) to the k-th
+// key over `each` (a source of (key, index)); returns the key, *need = how many of the
+// keys equal to it are taken, *ties = how many there are.
+template <typename Each>
+__device__ unsigned tk_refine(TopkSmem& S, Each each, unsigned d1, unsigned need1,
+                              unsigned* need, unsigned* ties) {
+  tk_clear(S);
+  each([&](unsigned u, int) {
+    if ((u >> 21) == d1) atomicAdd(&S.hist[(u >> 10) & 2047u], 1u);
+  });
+  __syncthreads();
+  tk_find(S, S.hist, need1);
+  const unsigned d2 = S.digit, need2 = need1 - S.above;
+  const unsigned p22 = (d1 << 11) | d2;
+  __syncthreads();
+  tk_clear(S);
+  each([&](unsigned u, int) {
+    if ((u >> 10) == p22) atomicAdd(&S.hist[u & 1023u], 1u);
+  });
+  __syncthreads();
+  tk_find(S, S.hist, need2);
+  const unsigned d3 = S.digit;
+  *need = need2 - S.above;
+  *ties = S.hist[d3];
+  return (p22 << 10) | d3;
+}
+
+__global__ void __launch_bounds__(TS_THREADS) topk_select_kernel(
+    int n, int k, const float* __restrict__ score, unsigned* __restrict__ hist,
+    unsigned* __restrict__ gcount, unsigned* __restrict__ gdone, unsigned* __restrict__ gkey,
+    int* __restrict__ gidx, int* __restrict__ cand, fx_t* __restrict__ zfx, int zn) {
+  __shared__ TopkSmem S;
+  pdl_enter();
+  const int row = blockIdx.y, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const float* x = score + (size_t)row * n;
+  unsigned* hrow = hist + (size_t)row * 2048;
+  for (int i = t; i < 2048; i += TS_THREADS) S.hist[i] = __ldcg(hrow + i);
+  if (t == 0) S.nout = 0;
+  __syncthreads();
+  tk_find(S, S.hist, (unsigned)k);
+  const unsigned d1 = S.digit, above1 = S.above;
+  const unsigned m = above1 + S.hist[d1];  // keys with digit >= d1
+  const unsigned need1 = (unsigned)k - above1;
+  {
+    const int chunk = cdiv(n, gridDim.x);
+    const int beg = blockIdx.x * chunk, end = min(n, beg + chunk);
+    unsigned* lk = gkey + (size_t)row * TK_CAP;
+    int* li = gidx + (size_t)row * TK_CAP;
+    tk_row(x, beg, end, [&](unsigned u, int i) {
+      if ((u >> 21) >= d1) {
+        const unsigned p = atomicAdd(gcount + row, 1u);
+        if (p < (unsigned)TK_CAP) {
+          lk[p] = u;
+          li[p] = i;
+        }
+      }
+    });
+  }
+  __syncthreads();
+  if (t == 0) S.last = atom_add_acq_rel(gdone + row, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!S.last) return;
+  // the last CTA of the row: every slice's keys are in the list
+  for (int i = t; i < 2048; i += TS_THREADS) hrow[i] = 0u;
+  if (zfx)
+    for (int i = t; i < zn; i += TS_THREADS) zfx[(size_t)row * zn + i] = 0;
+  int* out = cand + (size_t)row * k;
+  unsigned need, ties, kth;
+  if (m <= (unsigned)TK_CAP) {
+    for (int i = t; i < (int)m; i += TS_THREADS) {
+      S.lkey[i] = __ldcg(gkey + (size_t)row * TK_CAP + i);
+      S.lidx[i] = __ldcg(gidx + (size_t)row * TK_CAP + i);
+    }
+    __syncthreads();
+    auto each = [&](auto f) {
+      for (int i = threadIdx.x; i < (int)m; i += TS_THREADS) f(S.lkey[i], S.lidx[i]);
+    };
+    kth = tk_refine(S, each, d1, need1, &need, &ties);
+    for (int i = t; i < (int)m; i += TS_THREADS) {
+      const unsigned u = S.lkey[i];
+      bool take = u > kth;
+      if (u == kth) {
+        if (need == ties) {
+          take = true;
+        } else {  // the `need` lowest indices among the ties
+          const int me = S.lidx[i];
+          unsigned rank = 0;
+          for (int j = 0; j < (int)m; ++j) rank += (S.lkey[j] == kth && S.lidx[j] < me);
+          take = rank < need;
+        }
+      }
+      if (take) out[atomicAdd(&S.nout, 1u)] = S.lidx[i];
+    }
+  } else {
+    auto each = [&](auto f) { tk_row(x, 0, n, f); };
+    kth = tk_refine(S, each, d1, need1, &need, &ties);
+    tk_row(x, 0, n, [&](unsigned u, int i) {
+      if (u > kth || (u == kth && need == ties)) out[atomicAdd(&S.nout, 1u)] = i;
+    });
+    if (need != ties) {
+      __syncthreads();
+      const unsigned base = S.nout;  // = k - need
+      unsigned taken = 0;
+      for (int i0 = 0; i0 < n && taken < need; i0 += TS_THREADS) {
+        const int i = i0 + t;
+        const bool eq = i < n && score_key(x[i]) == kth;
+        const unsigned bal = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) S.wsum[wid] = __popc(bal);
+        __syncthreads();
+        unsigned before = 0, total = 0;
+        for (int w = 0; w < TS_THREADS / 32; ++w) {
+          const unsigned c = S.wsum[w];
+          if (w < wid) before += c;
+          total += c;
+        }
+        const unsigned rank = taken + before + __popc(bal & ((1u << lane) - 1u));
+        if (eq && rank < need) out[base + rank] = i;
+        taken += total;
+        __syncthreads();
+      }
+    }
+  }
+  if (t == 0) {
+    gcount[row] = 0u;
+    gdone[row] = 0u;
+  }
+}
+
+void launch_topk(int R, int n, int k, const float* score, unsigned* hist, unsigned* gcount,
+                 unsigned* gdone, unsigned* gkey, int* gidx, int* cand, fx_t* zfx, int zn,
+                 int num_sms, cudaStream_t s) {
+  // slices per row: about two CTAs per SM over all rows, at least 512 keys a slice
+  int S = 2 * num_sms / R;
+  if (S > cdiv(n, 512)) S = cdiv(n, 512);
+  if (S > 64) S = 64;
+  if (S < 1) S = 1;
+  launch_pdl(topk_select_kernel, dim3(S, R), dim3(TS_THREADS), 0, s, n, k, score, hist, gcount,
+             gdone, gkey, gidx, cand, zfx, zn);
+}
+
+// Exact logits of the candidates: a CTA per (row, 8 candidates), the row's head input
+// (hi + lo parts) staged once in shared memory as fp32, a warp per candidate streaming
+// its head row in 16-byte pieces, an argmax key per row (ties: lower index) and, when
+// asked, the logit.  The last CTA to finish decodes every row's argmax (token id through
+// d2t) and clears the keys and its counter for the next pass.
 template <typename T>
 __global__ void __launch_bounds__(256) cand_head_kernel(int R, int H, int k,
                                                         const int* __restrict__ cand,
                                                         const T* __restrict__ head,
                                                         const T* __restrict__ y, int split,
                                                         unsigned long long* keys, float* logits,
-                                                        int Vd) {
+                                                        int Vd, const int* __restrict__ d2t,
+                                                        int* __restrict__ out,
+                                                        unsigned* done) {
+  constexpr int E = 16 / sizeof(T);
+  extern __shared__ float ys[];
+  __shared__ bool s_last;
   pdl_enter();
-  const int lane = threadIdx.x & 31;
-  const int wg = blockIdx.x * 8 + (threadIdx.x >> 5);  // (row, candidate) pair
-  if (wg >= R * k) return;
-  const int r = wg / k;
-  const int c = cand[wg];
-  const T* hr = head + (size_t)c * H;
-  const T* yh = y + (size_t)r * H;
-  const T* yl = y + (size_t)(r + R) * H;
-  float acc = 0.f;
-  for (int i = lane; i < H; i += 32) {
-    float yi = to_f32(yh[i]);
-    if (split) yi += to_f32(yl[i]);
-    acc = fmaf(to_f32(hr[i]), yi, acc);
+  const int t = threadIdx.x, lane = t & 31;
+  const int row = blockIdx.y;
+  const T* yh = y + (size_t)row * H;
+  const T* yl = y + (size_t)(row + R) * H;
+  for (int i = t; i < H; i += 256) ys[i] = to_f32(yh[i]) + (split ? to_f32(yl[i]) : 0.f);
+  __syncthreads();
+  const int j = blockIdx.x * 8 + (t >> 5);
+  if (j < k) {
+    const int c = cand[(size_t)row * k + j];
+    const uint4* hr = reinterpret_cast<const uint4*>(head + (size_t)c * H);
+    const int np = H / E;
+    constexpr int NB = 12;  // pieces in flight per lane (a 2880-wide bf16 row in one batch)
+    float acc = 0.f;
+    for (int p0 = lane; p0 < np; p0 += 32 * NB) {
+      uint4 q[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        q[b] = p0 + 32 * b < np ? hr[p0 + 32 * b] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const int p = p0 + 32 * b;
+        if (p < np) {
+          float w[E];
+          unpack16<T>(q[b], w);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc = fmaf(w[e], ys[p * E + e], acc);
+        }
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      atomicMax(keys + row, argmax_key(acc, c));
+      if (logits) logits[(size_t)row * Vd + c] = acc;
+    }
   }
-  acc = warp_sum(acc);
-  if (lane == 0) {
-    atomicMax(keys + r, argmax_key(acc, c));
-    if (logits) logits[(size_t)r * Vd + c] = acc;
+  __syncthreads();
+  if (t == 0) s_last = atom_add_acq_rel(done, 1u) == gridDim.x * gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  for (int rr = t; rr < R; rr += 256) {
+    const int idx = argmax_key_index(__ldcg(keys + rr));
+    if (out) out[rr] = d2t ? idx + d2t[idx] : idx;
+    keys[rr] = 0ull;
   }
+  if (t == 0) *done = 0u;
 }
 
 __global__ void fill_kernel(size_t n, float v, float* p) {
@@ -1129,20 +1625,21 @@ __global__ void fill_kernel(size_t n, float v, float* p) {
 
 void launch_cand_head(bool bf16m, int R, int H, int k, const int* cand, const void* head,
                       const void* y, int split, unsigned long long* keys, float* logits, int Vd,
-                      cudaStream_t s) {
+                      const int* d2t, int* out, unsigned* done, cudaStream_t s) {
   if (logits) {
     const size_t n = (size_t)R * Vd;
     const size_t nb = (n + 255) / 256;
     launch_pdl(fill_kernel, dim3(nb < 1024 ? (unsigned)nb : 1024u), dim3(256), 0, s, n,
                -INFINITY, logits);
   }
-  const int blocks = cdiv(R * k, 8);
+  const dim3 grid(cdiv(k, 8), R);
+  const size_t smem = (size_t)H * 4;
   if (bf16m)
-    launch_pdl(cand_head_kernel<bf16>, dim3(blocks), dim3(256), 0, s, R, H, k, cand,
-               (const bf16*)head, (const bf16*)y, split, keys, logits, Vd);
+    launch_pdl(cand_head_kernel<bf16>, grid, dim3(256), smem, s, R, H, k, cand,
+               (const bf16*)head, (const bf16*)y, split, keys, logits, Vd, d2t, out, done);
   else
-    launch_pdl(cand_head_kernel<float>, dim3(blocks), dim3(256), 0, s, R, H, k, cand,
-               (const float*)head, (const float*)y, 0, keys, logits, Vd);
+    launch_pdl(cand_head_kernel<float>, grid, dim3(256), smem, s, R, H, k, cand,
+               (const float*)head, (const float*)y, 0, keys, logits, Vd, d2t, out, done);
 }
 
 // =====================================================================================

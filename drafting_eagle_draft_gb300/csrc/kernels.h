@@ -63,14 +63,21 @@ void launch_masked_attention(bool bf16, const MaskedAttnArgs& a, cudaStream_t s)
 struct TcGemmPlan;
 int masked_attn_tc_launch(TcGemmPlan* plan, const MaskedAttnArgs& a, cudaStream_t s);
 
-// Efficient LM head: fixed-point rows -> projection operand; per-row top-k of a score
-// matrix [R][n] -> cand [R][k]; exact logits of the candidates -> argmax keys (+ logits,
-// -inf elsewhere, when `logits` is given).
-void launch_fx_to_act(bool bf16, int R, int n, fx_t* src, int split, void* dst, cudaStream_t s);
-void launch_topk(int R, int n, int k, const float* score, int* cand, cudaStream_t s);
+// Efficient LM head: rank-r scores approx [R][Vd] of the fixed-point projection zfx [R][r]
+// (r = 64, 128, 256 or 512) and their first-digit histogram, added into hist [R][2048];
+// per-row top-k of approx -> cand [R][k] through the list gkey / gidx [R][4096] and the
+// counters gcount / gdone [R] (the top-k launch clears hist, the counters and zfx); exact
+// logits of the candidates -> argmax keys (+ logits, -inf elsewhere, when `logits` is
+// given), decoded into out (token ids through d2t) by the last CTA, which also clears keys
+// and the `done` counter.  H * 4 bytes of shared memory.
+void launch_head_score(bool bf16, int R, int r, int Vd, const fx_t* zfx, const void* score,
+                       float* approx, unsigned* hist, unsigned* err, int num_sms, cudaStream_t s);
+void launch_topk(int R, int n, int k, const float* score, unsigned* hist, unsigned* gcount,
+                 unsigned* gdone, unsigned* gkey, int* gidx, int* cand, fx_t* zfx, int zn,
+                 int num_sms, cudaStream_t s);
 void launch_cand_head(bool bf16, int R, int H, int k, const int* cand, const void* head,
                       const void* y, int split, unsigned long long* keys, float* logits, int Vd,
-                      cudaStream_t s);
+                      const int* d2t, int* out, unsigned* done, cudaStream_t s);
 void launch_argmax_decode(int R, unsigned long long* keys, const int* d2t, int* out_tokens,
                           cudaStream_t s);
 

@@ -31,10 +31,13 @@ struct peagle_ctx {
   // efficient LM head (dims.lm_rank > 0): weights and per-pass buffers
   void *lm_proj, *lm_score;
   fx_t* lm_zfx;             // [rows][rank] fixed-point projection
-  void* lm_z;               // [2 rows][rank] projection as the next operand (hi / lo)
   float* lm_approx;         // [rows][Vd] rank-r scores
   int* lm_cand;             // [rows][k] candidates
-  unsigned long long* lm_kscr;  // argmax keys of the score GEMM's epilogue (unused)
+  unsigned* lm_hist;        // [rows][2048] first-digit histogram of the scores
+  unsigned *lm_gcount, *lm_gdone;  // [rows] gathered keys / finished slices of the top-k
+  unsigned* lm_gkey;        // [rows][4096] gathered keys and their indices
+  int* lm_gidx;
+  unsigned* lm_done;        // CTAs of the candidate head that have finished
   int* d2t;
   std::vector<void*> qkv, o, attn_norm, post_norm, gate_up, down;
   float2* rope;
@@ -166,8 +169,10 @@ static int validate_dims(const peagle_dims* d) {
   if (d->max_rows > 0 && d->max_seq <= 0) return PEAGLE_ERR_INVALID;
   if (d->attn_window < 0) return PEAGLE_ERR_INVALID;
   if (d->lm_rank < 0 || d->lm_topk < 0) return PEAGLE_ERR_INVALID;
-  if (d->lm_rank > 0 && (d->lm_rank % 64 || d->lm_rank > 512 || d->lm_topk < 1 ||
-                         d->lm_topk > 1024))
+  if (d->lm_rank > 0 &&
+      ((d->lm_rank != 64 && d->lm_rank != 128 && d->lm_rank != 256 && d->lm_rank != 512) ||
+       d->lm_topk < 1 || d->lm_topk > 1024 || d->hidden > 12288 ||
+       d->draft_vocab > (1 << 24)))
     return PEAGLE_ERR_UNSUPPORTED;
   // the masked attention tile holds 64 (row, q head) pairs of one kv head
   if (d->max_rows > 0 && d->n_q_heads / d->n_kv_heads > 64) return PEAGLE_ERR_UNSUPPORTED;
@@ -342,10 +347,14 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     const int dr = d.max_batch * d.max_K;  // draft rows
     const int k = d.lm_topk < d.draft_vocab ? d.lm_topk : d.draft_vocab;
     TRY(dalloc(c, (void**)&c->lm_zfx, (size_t)dr * d.lm_rank * 8));
-    TRY(dalloc(c, &c->lm_z, (size_t)2 * dr * d.lm_rank * es));
     TRY(dalloc(c, (void**)&c->lm_approx, (size_t)dr * d.draft_vocab * 4));
     TRY(dalloc(c, (void**)&c->lm_cand, (size_t)dr * k * 4));
-    TRY(dalloc(c, (void**)&c->lm_kscr, (size_t)2 * dr * 8));
+    TRY(dalloc(c, (void**)&c->lm_done, 4));
+    TRY(dalloc(c, (void**)&c->lm_hist, (size_t)dr * 2048 * 4));
+    TRY(dalloc(c, (void**)&c->lm_gcount, (size_t)dr * 4));
+    TRY(dalloc(c, (void**)&c->lm_gdone, (size_t)dr * 4));
+    TRY(dalloc(c, (void**)&c->lm_gkey, (size_t)dr * 4096 * 4));
+    TRY(dalloc(c, (void**)&c->lm_gidx, (size_t)dr * 4096 * 4));
   }
   if (c->bf) TRY(tc_create(&c->tc, c->num_sms, R, max_out > 3 * H ? max_out : 3 * H, c->err));
   // fc(h_shared): constant for every MTP row, computed once with the pass's own GEMM
@@ -672,8 +681,8 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
 // The draft pass (all_ntp = false: row 0 of each request NTP, rows 1.. MTP) and the
 // catch-up pass (all_ntp: every row takes its own token and hidden state).
 // Efficient LM head over the R draft rows whose final residual is in c->res: final norm,
-// rank-r projection (fixed point, then the next operand), scores of the whole draft
-// vocabulary, per-row top-k candidates, the full head on the candidates, argmax + d2t.
+// rank-r projection (fixed point), scores of the whole draft vocabulary, per-row top-k
+// candidates, the full head on the candidates, argmax + d2t.
 static int efficient_head(peagle_ctx* c, int R, int split, int32_t* out_tokens,
                           float* out_logits, cudaStream_t s) {
   const peagle_dims& d = c->d;
@@ -688,18 +697,15 @@ static int efficient_head(peagle_ctx* c, int R, int split, int32_t* out_tokens,
     e.out_ld = r;
     GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_proj, c->Xn, H, r, H, R, e, s);
   }
-  TIMED(PEAGLE_STAGE_LMHEAD, launch_fx_to_act(c->bf, R, r, c->lm_zfx, split, c->lm_z, s));
-  {
-    EpiArgs e = epi_base(c, EPI_LMHEAD, R, Vd);
-    e.in_split = split;
-    e.logits = c->lm_approx;
-    e.keys = c->lm_kscr;
-    GEMM(PEAGLE_STAGE_LMHEAD, c, c->lm_score, c->lm_z, r, Vd, r, R, e, s);
-  }
-  TIMED(PEAGLE_STAGE_LMHEAD, launch_topk(R, Vd, k, c->lm_approx, c->lm_cand, s));
+  TIMED(PEAGLE_STAGE_LMHEAD, launch_head_score(c->bf, R, r, Vd, c->lm_zfx, c->lm_score,
+                                               c->lm_approx, c->lm_hist, c->err, c->num_sms,
+                                               s));
+  TIMED(PEAGLE_STAGE_LMHEAD,
+        launch_topk(R, Vd, k, c->lm_approx, c->lm_hist, c->lm_gcount, c->lm_gdone, c->lm_gkey,
+                    c->lm_gidx, c->lm_cand, c->lm_zfx, r, c->num_sms, s));
   TIMED(PEAGLE_STAGE_LMHEAD, launch_cand_head(c->bf, R, H, k, c->lm_cand, c->lm_head, c->Xn,
-                                              split, c->keys, out_logits, Vd, s));
-  TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(R, c->keys, c->d2t, out_tokens, s));
+                                              split, c->keys, out_logits, Vd, c->d2t,
+                                              out_tokens, c->lm_done, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "efficient LM head launch");
 }

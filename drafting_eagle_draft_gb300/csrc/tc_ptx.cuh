@@ -63,6 +63,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
 }
+// Plain bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory, completion on `bar`, with an L2 eviction policy.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 // 2D tiled load of box {x .. x+bx, y .. y+by} into shared memory, completion on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y,
                                             uint64_t* bar, uint64_t policy) {

@@ -86,9 +86,11 @@ typedef struct peagle_dims {
   int32_t lm_rank;       /* efficient LM head ("EAGLE-4", "EAGLE-4 overview": a
                             rank-128 projection scores the whole vocabulary, the
                             full head scores only the best candidates): 0 = the
-                            full head; else a multiple of 64 (<= 512), with
-                            weights lm_proj / lm_score.  Draft and catch-up passes
-                            only (peagle_forward_parallel: UNSUPPORTED).          */
+                            full head; else 64, 128, 256 or 512, with weights
+                            lm_proj / lm_score, hidden <= 12288 and a draft
+                            vocabulary of at most 2^24 entries.  Draft and
+                            catch-up passes only (peagle_forward_parallel:
+                            UNSUPPORTED).                                         */
   int32_t lm_topk;       /* candidates the full head scores (1 .. 1024; more than
                             the draft vocabulary means all of it).  With the
                             efficient head, out_logits holds the exact logits of

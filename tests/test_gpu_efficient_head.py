@@ -75,6 +75,40 @@ def test_small_bf16_efficient_head(pass_kernel, lens, K, topk):
     ctx.close()
 
 
+@pytest.mark.parametrize("rank,vocab", [(128, 1000), (256, 1000), (512, 1000), (128, 20000)])
+def test_bf16_efficient_head_ranks(rank, vocab):
+    """The pages' rank 128 and the other supported ranks; a 20000-entry vocabulary splits
+    each row's top-k over several slices."""
+    lens, K = [60, 200], 4
+    dims = synth.shrink(SMALL_BF16, lm_rank=rank, lm_topk=128, draft_vocab=vocab,
+                        target_vocab=max(1500, vocab + 500))
+    w, inp = _case(dims, lens, K, 3 + rank)
+    ctx = make_ctx(dims, w, len(lens), K, inp["capacity"] + 1)
+    toks, lg, _ = run_draft(ctx, dims, inp, K)
+    _check(dims, w, oracle_draft(dims, w, inp, K), toks, lg, f"bf16 rank {rank} vocab {vocab}")
+    ctx.close()
+
+
+@pytest.mark.parametrize("vocab", [1000, 20000])
+def test_all_scores_tied(vocab):
+    """A zero scoring factor ties every rank-r score: the candidates are the k lowest
+    indices (the gathered list resolves 1000 ties by index; 20000 do not fit it and take
+    the global-memory path)."""
+    lens, K, k = [30], 3, 64
+    dims = synth.shrink(SMALL_BF16, lm_topk=k, draft_vocab=vocab, target_vocab=vocab + 500)
+    w, inp = _case(dims, lens, K, 5)
+    w["lm_score"] = torch.zeros_like(w["lm_score"])
+    ctx = make_ctx(dims, w, 1, K, inp["capacity"] + 1)
+    toks, lg, _ = run_draft(ctx, dims, inp, K)
+    ref = oracle_draft(dims, w, inp, K)
+    for j in range(K):
+        cg = np.nonzero(np.isfinite(lg[0, j]))[0]
+        assert np.array_equal(cg, np.arange(k)), f"row {j}: {cg[:8]}..."
+        assert np.array_equal(np.nonzero(np.isfinite(ref.logits[0, j]))[0], np.arange(k))
+        assert np.max(np.abs(lg[0, j, :k] - ref.logits[0, j, :k])) <= LOGIT_TOL["bf16"]
+    ctx.close()
+
+
 def test_every_candidate_is_the_full_head():
     """lm_topk >= the draft vocabulary: the same tokens as the full head, and logits equal
     to the full head's within the tolerance (the same rows, scored by another kernel)."""
