@@ -16,7 +16,8 @@ Three extra objects on the line: train_fwd (the training-style masked forward, n
 COD 0.8), sliding_window (the concurrency-2 workload with and without a 4096-position
 drafter attention window) and efficient_head (the headline workload with the rank-128 /
 top-128 LM head and with the full head, on the 32000-entry draft vocabulary and on the
-whole 201088-entry vocabulary); --no-train-fwd / --no-window / --no-head skip them.
+whole 201088-entry vocabulary); --no-train-fwd / --no-window / --no-head skip them, and
+--only NAME runs one of them alone (a short driver for profilers).
 
 --impl reference times the fp64 oracle on the host cores instead (a deliberately slow
 plain program; see the cpu_baseline object).  Under torchrun each rank runs an
@@ -58,6 +59,10 @@ def parse():
                     help="skip the sliding-window attention measurement")
     ap.add_argument("--no-head", action="store_true",
                     help="skip the efficient LM head measurement")
+    ap.add_argument("--only", choices=["train_fwd", "window", "head_draft_vocab",
+                                       "head_full_vocab"],
+                    help="run one of the extra measurements alone and print its object "
+                         "(a short driver for profilers)")
     return ap.parse_args()
 
 
@@ -450,7 +455,7 @@ def window_measure(dev, window=4096):
             "kv_bytes_per_pass_full": kvb(lambda L: L + K)}
 
 
-def head_measure(dev, rank=128, topk=128):
+def head_measure(dev, rank=128, topk=128, vocabs=("draft_vocab", "full_vocab")):
     """Efficient LM head on the headline workload (batch 1, 4096 cached positions, K=8):
     draft-pass time as a CUDA graph with the rank-128 scoring projection and the full head
     on its 128 best candidates, against the full head on the same weights and inputs, the
@@ -462,6 +467,8 @@ def head_measure(dev, rank=128, topk=128):
     inp = synth.make_decode_inputs(wl, 99)
     out = {}
     for name, vocab in (("draft_vocab", None), ("full_vocab", wl.dims.target_vocab)):
+        if name not in vocabs:
+            continue
         d = synth.shrink(wl.dims, lm_rank=rank, lm_topk=topk)
         if vocab:
             d = synth.shrink(d, draft_vocab=vocab, d2t="identity")
@@ -619,6 +626,17 @@ def main():
     dist = None
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.only:
+        import torch
+
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        if args.only == "train_fwd":
+            out = {"train_fwd": train_fwd_measure(dev)}
+        elif args.only == "window":
+            out = {"sliding_window": window_measure(dev)}
+        else:
+            out = {"efficient_head": head_measure(dev, vocabs=(args.only[5:],))}
     else:
         if world > 1:
             import torch
