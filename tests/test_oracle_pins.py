@@ -701,3 +701,91 @@ def test_efficient_head_candidates_and_winner_by_brute_force():
             best = max(cand, key=lambda i: (full.logits[b, j, i], -i))
             assert r.argmax[b, j] == best
             assert r.tokens[b, j] == best + int(w["d2t"][best])
+
+
+# ---------------------------------------------------------------- training step
+from oracle import peagle_train_oracle as T  # noqa: E402
+
+
+def _train_case(seed=11, n=6, K=3, cod=None):
+    """Tiny drafter (two layers, GQA 2:1) with norm gains, emb(mask) and h_shared drawn
+    away from their initial values, so that no gradient pin passes on a unit gain."""
+    dims = synth.Dims(hidden=8, n_layers=2, n_q_heads=2, n_kv_heads=1, head_dim=4,
+                      intermediate=12, draft_vocab=11, target_vocab=13, rope_theta=10000.0,
+                      rms_eps=1e-5, dtype="f32", d2t="identity")
+    W = O.Weights64.from_synth(synth.make_weights(dims, seed))
+    rng = np.random.default_rng(seed)
+    W.embed = O.to64(W.embed)
+    W.fc, W.lm_head = W.fc * 8.0, W.lm_head * 8.0
+    for name in ("input_norm", "hidden_norm", "final_norm"):
+        setattr(W, name, 1.0 + 0.3 * rng.standard_normal(dims.hidden))
+    for L in W.layers:
+        for k in list(L):
+            L[k] = (1.0 + 0.3 * rng.standard_normal(L[k].shape)) if k.endswith("norm") \
+                else L[k] * 8.0
+    tokens = rng.integers(0, dims.target_vocab, n)
+    hidden = rng.standard_normal((n, 3 * dims.hidden))
+    rows = np.array([(p, d) for p in range(n) for d in range(1, K + 1) if p - d + 1 >= 0])
+    if cod is not None:
+        rows = O.cod_retained(n, K, cod, rng.random((n, K)))
+    labels = rng.integers(0, dims.draft_vocab, len(rows))
+    return dims, W, tokens, hidden, rows, labels
+
+
+def _params(W):
+    out = {"embed": W.embed, "emb_mask": W.emb_mask, "h_shared": W.h_shared, "fc": W.fc,
+           "input_norm": W.input_norm, "hidden_norm": W.hidden_norm,
+           "final_norm": W.final_norm, "lm_head": W.lm_head}
+    for li, L in enumerate(W.layers):
+        for k, v in L.items():
+            out[f"layers.{li}.{k}"] = v
+    return out
+
+
+def _grad(g, name):
+    if name.startswith("layers."):
+        _, li, k = name.split(".")
+        return g["layers"][int(li)][k]
+    return g[name]
+
+
+def test_train_step_forward_is_the_training_forward():
+    dims, W, tokens, hidden, rows, labels = _train_case(cod=0.8)
+    loss, logits, _ = T.train_step(W, dims, tokens, hidden, rows, labels)
+    ref, _, _ = O.forward_parallel(W, dims, tokens, hidden, rows, bf16=False)
+    assert np.allclose(logits, ref, rtol=0, atol=1e-12)
+    # mean cross-entropy, from scipy's logsumexp
+    ce = scipy.special.logsumexp(ref, axis=1) - ref[np.arange(len(rows)), labels]
+    assert abs(loss - ce.mean()) < 1e-12
+
+
+@pytest.mark.parametrize("cod", [None, 0.7])
+def test_train_step_gradients_match_finite_differences(cod):
+    """Every parameter tensor, several entries each: the hand-written chain rule against
+    central differences of the loss (h = 1e-5, fp64)."""
+    dims, W, tokens, hidden, rows, labels = _train_case(cod=cod, seed=5 if cod else 11)
+    loss, _, g = T.train_step(W, dims, tokens, hidden, rows, labels)
+    rng = np.random.default_rng(1)
+    used = sorted({int(tokens[p]) for p, d in rows if d == 1})
+    h = 1e-5
+    for name, arr in _params(W).items():
+        if name.endswith("attn_norm") and name.startswith("layers.0."):
+            assert not np.any(_grad(g, name))  # layer 1 reads x0, not a norm of res
+            continue
+        for _ in range(4):
+            if name == "embed":
+                idx = (used[rng.integers(len(used))], int(rng.integers(arr.shape[1])))
+            else:
+                idx = tuple(int(rng.integers(s)) for s in arr.shape)
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = T.train_step(W, dims, tokens, hidden, rows, labels)[0]
+            arr[idx] = old - h
+            lm = T.train_step(W, dims, tokens, hidden, rows, labels)[0]
+            arr[idx] = old
+            fd = (lp - lm) / (2 * h)
+            an = _grad(g, name)[idx]
+            assert abs(fd - an) <= 1e-7 + 1e-5 * abs(fd), (name, idx, fd, an)
+    # rows of the embedding that no depth-1 row reads get no gradient
+    unused = [t for t in range(dims.target_vocab) if t not in used]
+    assert not np.any(g["embed"][unused])
