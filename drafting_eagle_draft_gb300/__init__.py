@@ -32,7 +32,8 @@ PEAGLE_BF16 = 1
 # every entry point declared in include/peagle.h
 EXPORTS = ("peagle_create", "peagle_draft", "peagle_catch_up", "peagle_verify_greedy",
            "peagle_append_kv",
-           "peagle_forward_parallel", "peagle_cod_rows", "peagle_sequence_partition",
+           "peagle_forward_parallel", "peagle_train_step", "peagle_cod_rows",
+           "peagle_sequence_partition",
            "peagle_status",
            "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
            "peagle_decode_attention_static",
@@ -60,6 +61,15 @@ class PeagleWeights(ctypes.Structure):
                 ("up", ctypes.POINTER(_vp)), ("down", ctypes.POINTER(_vp)),
                 ("final_norm", _vp), ("lm_head", _vp), ("d2t", _vp), ("lm_proj", _vp),
                 ("lm_score", _vp)]
+
+
+class PeagleGrads(ctypes.Structure):
+    _fields_ = [("embed", _vp), ("emb_mask", _vp), ("h_shared", _vp), ("fc", _vp),
+                ("input_norm", _vp), ("hidden_norm", _vp), ("qkv", ctypes.POINTER(_vp)),
+                ("o", ctypes.POINTER(_vp)), ("attn_norm", ctypes.POINTER(_vp)),
+                ("post_norm", ctypes.POINTER(_vp)), ("gate", ctypes.POINTER(_vp)),
+                ("up", ctypes.POINTER(_vp)), ("down", ctypes.POINTER(_vp)),
+                ("final_norm", _vp), ("lm_head", _vp)]
 
 
 class PeagleKV(ctypes.Structure):
@@ -95,6 +105,8 @@ def lib():
                                        _vp, _vp, _i32, _vp]
         L.peagle_forward_parallel.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp,
                                               _vp, _vp]
+        L.peagle_train_step.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                        ctypes.POINTER(PeagleGrads), _vp]
         L.peagle_cod_rows.argtypes = [_i32, _i32, ctypes.c_double, _vp, _vp, _vp, _i32]
         L.peagle_sequence_partition.argtypes = [_i32, _vp, _vp, _i32, _vp, _vp]
         L.peagle_status.argtypes = [_vp]
@@ -255,6 +267,37 @@ def peagle_forward_parallel(ctx: Context, n, K, tokens, hidden, row_p, row_d, M,
                                          _ptr(out_argmax), _ptr(out_logits),
                                          _stream_ptr(stream)),
            "peagle_forward_parallel")
+
+
+def grads_struct(g, n_layers):
+    """PeagleGrads over a dict of fp32 device tensors named like the weights (embed and
+    attn_norm optional); the per-layer pointer arrays are kept on the struct."""
+    def arr(name):
+        if name not in g or g[name] is None:
+            return None
+        a = (_vp * n_layers)(*[_ptr(t) for t in g[name]])
+        return a
+    st = PeagleGrads()
+    for k in ("embed", "emb_mask", "h_shared", "fc", "input_norm", "hidden_norm",
+              "final_norm", "lm_head"):
+        setattr(st, k, _ptr(g.get(k)))
+    st._keep = []
+    for k in ("qkv", "o", "attn_norm", "post_norm", "gate", "up", "down"):
+        a = arr(k)
+        st._keep.append(a)
+        setattr(st, k, ctypes.cast(a, ctypes.POINTER(_vp)) if a is not None else None)
+    return st
+
+
+def peagle_train_step(ctx: Context, n, K, tokens, hidden, row_p, row_d, M, labels, out_loss,
+                      grads, stream=None):
+    """One training step (loss + every parameter gradient); grads: PeagleGrads or a dict
+    for grads_struct."""
+    st = grads if isinstance(grads, PeagleGrads) else grads_struct(grads, ctx.cdims.n_layers)
+    _check(lib().peagle_train_step(ctx.handle, int(n), int(K), _ptr(tokens), _ptr(hidden),
+                                   _ptr(row_p), _ptr(row_d), int(M), _ptr(labels),
+                                   _ptr(out_loss), ctypes.byref(st), _stream_ptr(stream)),
+           "peagle_train_step")
 
 
 def peagle_cod_rows(n, K, ratio, uniforms):

@@ -8,17 +8,40 @@
 #include <string.h>
 
 #include <algorithm>
+#include <memory>
 #include <vector>
+
+#include <cublas_v2.h>
 
 #include "gemm_tc.h"
 #include "kernels.h"
 #include "pass_kernel.h"
 #include "tc_ptx.cuh"
+#include "train_kernels.h"
 
 using namespace peagle;
 
 // pass-kernel calls whose phase times one timing read can report
 constexpr int PASS_TRACE_SLOTS = 64;
+
+// Training-step workspace, allocated by the first peagle_train_step for max_rows rows and
+// max_seq positions: fp32 copies of the weights (bf16 contexts), the forward's saved
+// activations per layer and the backward's buffers.
+struct TrainWs {
+  int Mmax = 0, nmax = 0;
+  // fp32 weights (the context's own buffers on fp32 contexts); gate / up interleaved
+  float *fc, *lm, *in_norm, *hid_norm, *fin_norm;
+  std::vector<float*> qkv, o, gu, down, attn_norm, post_norm;
+  // forward (saved)
+  int* chain;
+  float *E, *Hin, *f, *r1, *r2, *x0, *y, *ry, *logits, *row_loss, *resL;
+  std::vector<float*> res_in, a, ra, Qh, Kr, Vr, K1, V1, Pc, lse, O, res_mid, u, ru, GU, act;
+  // scratch
+  float *qkvb, *S1, *dP1, *Oh;
+  // backward
+  float *bufA, *bufB, *dact, *dGU, *du, *dO, *dOh, *Dv, *dQh, *dKr, *dVr, *dK1, *dV1, *dqkv,
+      *da, *dgu_w, *dE, *df, *dHin, *dy;
+};
 
 struct peagle_ctx {
   peagle_dims d;
@@ -80,6 +103,8 @@ struct peagle_ctx {
   unsigned long long* pass_trace_cta;  // per-CTA signal times of the latest traced pass
   int trace_cta_phases;
   std::vector<void*> allocs;
+  TrainWs* tw = nullptr;
+  cublasHandle_t blas = nullptr;
   // optional per-stage timing: CUDA events recorded around each launch on its stream
   bool timing;
   std::vector<cudaEvent_t> ev;
@@ -147,6 +172,8 @@ static void free_ctx(peagle_ctx* c) {
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->tc) tc_destroy(c->tc);
+  if (c->blas) cublasDestroy(c->blas);
+  delete c->tw;
   delete c->pp;
   delete c;
 }
@@ -1028,6 +1055,315 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   TIMED(PEAGLE_STAGE_SMALL, launch_argmax_decode(M, c->keys, nullptr, out_argmax, s));
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "peagle_forward_parallel launch");
+}
+
+// ---- training step ("P-EAGLE: Parallel-Drafting EAGLE with Scalable Training", A2 section
+// 2 and section 3): the training-style forward with its activations kept, the mean
+// cross-entropy over the retained rows, and the gradient of every parameter.  fp32
+// activations; the plain GEMMs (projections, the attention's depth-1 prefix products) run
+// on cuBLAS, TF32 tensor cores for bf16 drafters and fp32 for fp32 drafters.
+
+// row-major C[m x n] = alpha op(A) op(B) + beta C, with op(A) m x k and op(B) k x n
+#define TRY_RET(x)  \
+  do {              \
+    int _r = (x);   \
+    if (_r) return _r; \
+  } while (0)
+
+static bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int m, int n, int k, float alpha,
+                    const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                    int ldc) {
+  return cublasSgemm(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, n, m, k,
+                     &alpha, B, ldb, A, lda, &beta, C, ldc) == CUBLAS_STATUS_SUCCESS;
+}
+
+static int train_ws(peagle_ctx* c) {
+  if (c->tw) return PEAGLE_OK;
+  const peagle_dims& d = c->d;
+  const int M = d.max_rows, n = d.max_seq, H = d.hidden, I = d.intermediate;
+  const int nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, G = nq / nkv;
+  const int qkv_out = (nq + 2 * nkv) * hd, N = d.n_layers, Vd = d.draft_vocab;
+  // built aside and attached only when complete (a failed call leaves no half workspace;
+  // what it allocated stays on the context's list and is freed with it)
+  std::unique_ptr<TrainWs> hold(new TrainWs());
+  TrainWs* w = hold.get();
+  w->Mmax = M;
+  w->nmax = n;
+  auto fl = [&](float** p, size_t count) { return dalloc(c, (void**)p, count * 4); };
+  // fp32 weights
+  auto wcopy = [&](float** dst, void* src, size_t count) -> int {
+    if (!c->bf) {
+      *dst = (float*)src;
+      return PEAGLE_OK;
+    }
+    TRY_RET(fl(dst, count));
+    launch_to_f32(count, src, *dst, 0);
+    return PEAGLE_OK;
+  };
+  TRY_RET(wcopy(&w->fc, c->fc, (size_t)H * 3 * H));
+  TRY_RET(wcopy(&w->lm, c->lm_head, (size_t)Vd * H));
+  TRY_RET(wcopy(&w->in_norm, c->input_norm, H));
+  TRY_RET(wcopy(&w->hid_norm, c->hidden_norm, H));
+  TRY_RET(wcopy(&w->fin_norm, c->final_norm, H));
+  w->qkv.resize(N);
+  w->o.resize(N);
+  w->gu.resize(N);
+  w->down.resize(N);
+  w->attn_norm.assign(N, nullptr);
+  w->post_norm.resize(N);
+  for (int l = 0; l < N; ++l) {
+    const int din = l == 0 ? 2 * H : H;
+    TRY_RET(wcopy(&w->qkv[l], c->qkv[l], (size_t)qkv_out * din));
+    TRY_RET(wcopy(&w->o[l], c->o[l], (size_t)H * nq * hd));
+    TRY_RET(wcopy(&w->gu[l], c->gate_up[l], (size_t)2 * I * H));
+    TRY_RET(wcopy(&w->down[l], c->down[l], (size_t)H * I));
+    if (l > 0) TRY_RET(wcopy(&w->attn_norm[l], c->attn_norm[l], H));
+    TRY_RET(wcopy(&w->post_norm[l], c->post_norm[l], H));
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return PEAGLE_ERR_CUDA;
+  // forward, kept for the backward
+  TRY_RET(dalloc(c, (void**)&w->chain, (size_t)M * 15 * 4));
+  TRY_RET(fl(&w->E, (size_t)M * H));
+  TRY_RET(fl(&w->Hin, (size_t)M * 3 * H));
+  TRY_RET(fl(&w->f, (size_t)M * H));
+  TRY_RET(fl(&w->r1, M));
+  TRY_RET(fl(&w->r2, M));
+  TRY_RET(fl(&w->x0, (size_t)M * 2 * H));
+  TRY_RET(fl(&w->y, (size_t)M * H));
+  TRY_RET(fl(&w->ry, M));
+  TRY_RET(fl(&w->logits, (size_t)M * Vd));
+  TRY_RET(fl(&w->row_loss, M));
+  TRY_RET(fl(&w->resL, (size_t)M * H));
+  for (auto* v : {&w->res_in, &w->a, &w->ra, &w->Qh, &w->Kr, &w->Vr, &w->K1, &w->V1, &w->Pc,
+                  &w->lse, &w->O, &w->res_mid, &w->u, &w->ru, &w->GU, &w->act})
+    v->assign(N, nullptr);
+  for (int l = 0; l < N; ++l) {
+    if (l > 0) {
+      TRY_RET(fl(&w->res_in[l], (size_t)M * H));
+      TRY_RET(fl(&w->a[l], (size_t)M * H));
+      TRY_RET(fl(&w->ra[l], M));
+    }
+    TRY_RET(fl(&w->Qh[l], (size_t)nq * M * hd));
+    TRY_RET(fl(&w->Kr[l], (size_t)M * nkv * hd));
+    TRY_RET(fl(&w->Vr[l], (size_t)M * nkv * hd));
+    TRY_RET(fl(&w->K1[l], (size_t)nkv * n * hd));
+    TRY_RET(fl(&w->V1[l], (size_t)nkv * n * hd));
+    TRY_RET(fl(&w->Pc[l], (size_t)nq * M * 15));
+    TRY_RET(fl(&w->lse[l], (size_t)nq * M));
+    TRY_RET(fl(&w->O[l], (size_t)M * nq * hd));
+    TRY_RET(fl(&w->res_mid[l], (size_t)M * H));
+    TRY_RET(fl(&w->u[l], (size_t)M * H));
+    TRY_RET(fl(&w->ru[l], M));
+    TRY_RET(fl(&w->GU[l], (size_t)M * 2 * I));
+    TRY_RET(fl(&w->act[l], (size_t)M * I));
+  }
+  w->res_in[0] = w->f;
+  w->a[0] = w->x0;
+  TRY_RET(fl(&w->qkvb, (size_t)M * qkv_out));
+  TRY_RET(fl(&w->S1, (size_t)G * M * n));
+  TRY_RET(fl(&w->dP1, (size_t)G * M * n));
+  TRY_RET(fl(&w->Oh, (size_t)nq * M * hd));
+  // backward
+  TRY_RET(fl(&w->bufA, (size_t)M * H));
+  TRY_RET(fl(&w->bufB, (size_t)M * H));
+  TRY_RET(fl(&w->dact, (size_t)M * I));
+  TRY_RET(fl(&w->dGU, (size_t)M * 2 * I));
+  TRY_RET(fl(&w->du, (size_t)M * H));
+  TRY_RET(fl(&w->dO, (size_t)M * nq * hd));
+  TRY_RET(fl(&w->dOh, (size_t)nq * M * hd));
+  TRY_RET(fl(&w->Dv, (size_t)nq * M));
+  TRY_RET(fl(&w->dQh, (size_t)nq * M * hd));
+  TRY_RET(fl(&w->dKr, (size_t)M * nkv * hd));
+  TRY_RET(fl(&w->dVr, (size_t)M * nkv * hd));
+  TRY_RET(fl(&w->dK1, (size_t)nkv * n * hd));
+  TRY_RET(fl(&w->dV1, (size_t)nkv * n * hd));
+  TRY_RET(fl(&w->dqkv, (size_t)M * qkv_out));
+  TRY_RET(fl(&w->da, (size_t)M * 2 * H));
+  TRY_RET(fl(&w->dgu_w, (size_t)2 * I * H));
+  TRY_RET(fl(&w->dE, (size_t)M * H));
+  TRY_RET(fl(&w->df, (size_t)M * H));
+  TRY_RET(fl(&w->dHin, (size_t)M * 3 * H));
+  TRY_RET(fl(&w->dy, (size_t)M * H));
+  if (!c->blas && cublasCreate(&c->blas) != CUBLAS_STATUS_SUCCESS) return PEAGLE_ERR_CUDA;
+  cublasSetMathMode(c->blas, c->bf ? CUBLAS_TF32_TENSOR_OP_MATH : CUBLAS_DEFAULT_MATH);
+  c->tw = hold.release();
+  return PEAGLE_OK;
+}
+
+static int zero(float* p, size_t count, cudaStream_t s) {
+  return cudaMemsetAsync(p, 0, count * 4, s) == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+}
+
+extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int32_t* tokens,
+                                 const void* hidden, const int32_t* row_p, const int32_t* row_d,
+                                 int32_t M, const int32_t* labels, float* out_loss,
+                                 const peagle_grads* gr, void* stream) {
+  if (!c || !tokens || !hidden || !row_p || !row_d || !labels || !out_loss || !gr)
+    return PEAGLE_ERR_INVALID;
+  if (!gr->emb_mask || !gr->h_shared || !gr->fc || !gr->input_norm || !gr->hidden_norm ||
+      !gr->qkv || !gr->o || !gr->post_norm || !gr->gate || !gr->up || !gr->down ||
+      !gr->final_norm || !gr->lm_head)
+    return PEAGLE_ERR_INVALID;
+  const peagle_dims& d = c->d;
+  if (n < 1 || K < 1 || M < 1) return PEAGLE_ERR_INVALID;
+  if (d.max_rows <= 0 || M > d.max_rows || n > d.max_seq || K > 16) return PEAGLE_ERR_CAPACITY;
+  if (n > d.max_positions) return PEAGLE_ERR_CAPACITY;
+  if (d.attn_window > 0 || d.lm_rank > 0) return PEAGLE_ERR_UNSUPPORTED;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!gr->qkv[l] || !gr->o[l] || !gr->post_norm[l] || !gr->gate[l] || !gr->up[l] ||
+        !gr->down[l])
+      return PEAGLE_ERR_INVALID;
+  TRY_RET(train_ws(c));
+  TrainWs* w = c->tw;
+  cudaStream_t s = (cudaStream_t)stream;
+  cublasHandle_t hb = c->blas;
+  if (cublasSetStream(hb, s) != CUBLAS_STATUS_SUCCESS) return PEAGLE_ERR_CUDA;
+  const int H = d.hidden, I = d.intermediate, Vd = d.draft_vocab, Vt = d.target_vocab;
+  const int nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, G = nq / nkv;
+  const int qkv_out = (nq + 2 * nkv) * hd, N = d.n_layers, nqhd = nq * hd;
+  const float eps = d.rms_eps, scale = 1.f / sqrtf((float)hd);
+  const int Kmax = 16;
+  bool ok = true;
+  auto GM = [&](bool ta, bool tb, int m, int nn, int k, float alpha, const float* A, int lda,
+                const float* B, int ldb, float beta, float* C, int ldc) {
+    ok = ok && gemm_rm(hb, ta, tb, m, nn, k, alpha, A, lda, B, ldb, beta, C, ldc);
+  };
+  launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s);
+  launch_chain(M, n, K, Kmax, row_p, row_d, c->row_index, w->chain, s);
+  TrainAttn ta;
+  ta.M = M;
+  ta.n = n;
+  ta.K = K;
+  ta.nq = nq;
+  ta.nkv = nkv;
+  ta.hd = hd;
+  ta.scale = scale;
+  ta.row_p = row_p;
+  ta.row_d = row_d;
+  ta.chain = w->chain;
+
+  // ---- forward
+  launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
+                      c->h_shared, w->E, w->Hin, c->err, s);
+  GM(false, true, M, H, 3 * H, 1.f, w->Hin, 3 * H, w->fc, 3 * H, 0.f, w->f, H);
+  launch_rms_fwd(M, H, w->E, H, w->in_norm, eps, w->x0, 2 * H, w->r1, s);
+  launch_rms_fwd(M, H, w->f, H, w->hid_norm, eps, w->x0 + H, 2 * H, w->r2, s);
+  const float* res = w->f;
+  for (int l = 0; l < N; ++l) {
+    const int din = l == 0 ? 2 * H : H;
+    if (l > 0) launch_rms_fwd(M, H, w->res_in[l], H, w->attn_norm[l], eps, w->a[l], H, w->ra[l], s);
+    GM(false, true, M, qkv_out, din, 1.f, w->a[l], din, w->qkv[l], din, 0.f, w->qkvb, qkv_out);
+    TRY_RET(zero(w->K1[l], (size_t)nkv * n * hd, s));
+    TRY_RET(zero(w->V1[l], (size_t)nkv * n * hd, s));
+    launch_train_rope(M, n, K, nq, nkv, hd, w->qkvb, row_p, row_d, c->rope, w->Qh[l], w->Kr[l],
+                      w->Vr[l], w->K1[l], w->V1[l], s);
+    for (int g = 0; g < nkv; ++g) {
+      const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;
+      const float* K1g = w->K1[l] + (size_t)g * n * hd;
+      const float* V1g = w->V1[l] + (size_t)g * n * hd;
+      GM(false, true, G * M, n, hd, scale, Qg, hd, K1g, hd, 0.f, w->S1, n);
+      launch_attn_fwd_softmax(ta, g, w->S1, w->Qh[l], w->Kr[l], w->Pc[l], w->lse[l], s);
+      GM(false, false, G * M, hd, n, 1.f, w->S1, n, V1g, hd, 0.f, w->Oh + (size_t)g * G * M * hd,
+         hd);
+      launch_attn_fwd_out(ta, g, w->Oh, w->Pc[l], w->Vr[l], w->O[l], s);
+    }
+    if (cudaMemcpyAsync(w->res_mid[l], res, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    GM(false, true, M, H, nqhd, 1.f, w->O[l], nqhd, w->o[l], nqhd, 1.f, w->res_mid[l], H);
+    launch_rms_fwd(M, H, w->res_mid[l], H, w->post_norm[l], eps, w->u[l], H, w->ru[l], s);
+    GM(false, true, M, 2 * I, H, 1.f, w->u[l], H, w->gu[l], H, 0.f, w->GU[l], 2 * I);
+    launch_swiglu_fwd(M, I, w->GU[l], w->act[l], s);
+    float* res_out = l + 1 < N ? w->res_in[l + 1] : w->resL;
+    if (cudaMemcpyAsync(res_out, w->res_mid[l], (size_t)M * H * 4, cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    GM(false, true, M, H, I, 1.f, w->act[l], I, w->down[l], I, 1.f, res_out, H);
+    res = res_out;
+  }
+  launch_rms_fwd(M, H, w->resL, H, w->fin_norm, eps, w->y, H, w->ry, s);
+  GM(false, true, M, Vd, H, 1.f, w->y, H, w->lm, H, 0.f, w->logits, Vd);
+  launch_ce(M, Vd, w->logits, labels, w->row_loss, out_loss, c->err, s);  // logits -> dlogits
+
+  // ---- backward
+  GM(true, false, Vd, H, M, 1.f, w->logits, Vd, w->y, H, 0.f, gr->lm_head, H);
+  GM(false, false, M, H, Vd, 1.f, w->logits, Vd, w->lm, H, 0.f, w->dy, H);
+  float* dres = w->bufA;
+  float* dmid = w->bufB;
+  launch_rms_bwd(M, H, w->resL, H, w->ry, w->fin_norm, w->dy, H, dres, H, false, s);
+  TRY_RET(zero(gr->final_norm, H, s));
+  launch_colsum(M, H, w->dy, H, w->resL, H, w->ry, nullptr, gr->final_norm, s);
+  for (int l = N - 1; l >= 0; --l) {
+    const int din = l == 0 ? 2 * H : H;
+    // MLP
+    GM(true, false, H, I, M, 1.f, dres, H, w->act[l], I, 0.f, gr->down[l], I);
+    GM(false, false, M, I, H, 1.f, dres, H, w->down[l], I, 0.f, w->dact, I);
+    launch_swiglu_bwd(M, I, w->GU[l], w->dact, w->dGU, s);
+    GM(true, false, 2 * I, H, M, 1.f, w->dGU, 2 * I, w->u[l], H, 0.f, w->dgu_w, H);
+    launch_gu_split(I, H, w->dgu_w, gr->gate[l], gr->up[l], s);
+    GM(false, false, M, H, 2 * I, 1.f, w->dGU, 2 * I, w->gu[l], H, 0.f, w->du, H);
+    if (cudaMemcpyAsync(dmid, dres, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    launch_rms_bwd(M, H, w->res_mid[l], H, w->ru[l], w->post_norm[l], w->du, H, dmid, H, true, s);
+    TRY_RET(zero(gr->post_norm[l], H, s));
+    launch_colsum(M, H, w->du, H, w->res_mid[l], H, w->ru[l], nullptr, gr->post_norm[l], s);
+    // attention
+    GM(true, false, H, nqhd, M, 1.f, dmid, H, w->O[l], nqhd, 0.f, gr->o[l], nqhd);
+    GM(false, false, M, nqhd, H, 1.f, dmid, H, w->o[l], nqhd, 0.f, w->dO, nqhd);
+    launch_attn_bwd_prep(ta, w->dO, w->O[l], w->dOh, w->Dv, s);
+    TRY_RET(zero(w->dKr, (size_t)M * nkv * hd, s));
+    TRY_RET(zero(w->dVr, (size_t)M * nkv * hd, s));
+    for (int g = 0; g < nkv; ++g) {
+      const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;
+      const float* K1g = w->K1[l] + (size_t)g * n * hd;
+      const float* V1g = w->V1[l] + (size_t)g * n * hd;
+      const float* dOg = w->dOh + (size_t)g * G * M * hd;
+      float* dQg = w->dQh + (size_t)g * G * M * hd;
+      GM(false, true, G * M, n, hd, scale, Qg, hd, K1g, hd, 0.f, w->S1, n);
+      GM(false, true, G * M, n, hd, 1.f, dOg, hd, V1g, hd, 0.f, w->dP1, n);
+      launch_attn_bwd_ds(ta, g, w->S1, w->dP1, w->lse[l], w->Dv, w->Qh[l], w->Kr[l], w->Vr[l],
+                         w->dOh, w->dQh, w->dKr, w->dVr, s);
+      GM(false, false, G * M, hd, n, 1.f, w->dP1, n, K1g, hd, 1.f, dQg, hd);
+      GM(true, false, n, hd, G * M, 1.f, w->dP1, n, Qg, hd, 0.f, w->dK1 + (size_t)g * n * hd, hd);
+      GM(true, false, n, hd, G * M, 1.f, w->S1, n, dOg, hd, 0.f, w->dV1 + (size_t)g * n * hd, hd);
+    }
+    launch_kv1_scatter(M, n, K, nkv, hd, row_p, row_d, w->dK1, w->dV1, w->dKr, w->dVr, s);
+    launch_train_rope_bwd(M, n, K, nq, nkv, hd, w->dQh, w->dKr, w->dVr, row_p, row_d, c->rope,
+                          w->dqkv, s);
+    GM(true, false, qkv_out, din, M, 1.f, w->dqkv, qkv_out, w->a[l], din, 0.f, gr->qkv[l], din);
+    GM(false, false, M, din, qkv_out, 1.f, w->dqkv, qkv_out, w->qkv[l], din, 0.f, w->da, din);
+    if (l > 0) {
+      launch_rms_bwd(M, H, w->res_in[l], H, w->ra[l], w->attn_norm[l], w->da, H, dmid, H, true, s);
+      if (gr->attn_norm && gr->attn_norm[l]) {
+        TRY_RET(zero(gr->attn_norm[l], H, s));
+        launch_colsum(M, H, w->da, H, w->res_in[l], H, w->ra[l], nullptr, gr->attn_norm[l], s);
+      }
+    } else if (gr->attn_norm && gr->attn_norm[0]) {
+      TRY_RET(zero(gr->attn_norm[0], H, s));  // layer 1 reads x0, not a norm of the residual
+    }
+    std::swap(dres, dmid);  // dres = the residual stream's gradient at the layer's input
+  }
+  // first-layer input x0 = [rms_in(E) || rms_hid(f)]; the residual stream starts at f
+  launch_rms_bwd(M, H, w->E, H, w->r1, w->in_norm, w->da, 2 * H, w->dE, H, false, s);
+  TRY_RET(zero(gr->input_norm, H, s));
+  launch_colsum(M, H, w->da, 2 * H, w->E, H, w->r1, nullptr, gr->input_norm, s);
+  launch_rms_bwd(M, H, w->f, H, w->r2, w->hid_norm, w->da + H, 2 * H, w->df, H, false, s);
+  TRY_RET(zero(gr->hidden_norm, H, s));
+  launch_colsum(M, H, w->da + H, 2 * H, w->f, H, w->r2, nullptr, gr->hidden_norm, s);
+  launch_add((size_t)M * H, dres, w->df, s);
+  GM(true, false, H, 3 * H, M, 1.f, w->df, H, w->Hin, 3 * H, 0.f, gr->fc, 3 * H);
+  GM(false, false, M, 3 * H, H, 1.f, w->df, H, w->fc, 3 * H, 0.f, w->dHin, 3 * H);
+  TRY_RET(zero(gr->emb_mask, H, s));
+  launch_colsum(M, H, w->dE, H, nullptr, 0, nullptr, row_d, gr->emb_mask, s);
+  TRY_RET(zero(gr->h_shared, (size_t)3 * H, s));
+  launch_colsum(M, 3 * H, w->dHin, 3 * H, nullptr, 0, nullptr, row_d, gr->h_shared, s);
+  if (gr->embed) {
+    TRY_RET(zero(gr->embed, (size_t)Vt * H, s));
+    launch_embed_grad(M, n, K, H, Vt, row_p, row_d, tokens, w->dE, gr->embed, s);
+  }
+  if (!ok) return PEAGLE_ERR_CUDA;
+  cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "training step launch");
 }
 
 extern "C" int peagle_cod_rows(int32_t n, int32_t K, double ratio, const double* uniforms,

@@ -221,6 +221,48 @@ int peagle_forward_parallel(peagle_ctx* ctx, int32_t n, int32_t K, const int32_t
                             const void* hidden, const int32_t* row_p, const int32_t* row_d,
                             int32_t M, int32_t* out_argmax, float* out_logits, void* stream);
 
+/* Gradients written by peagle_train_step: fp32 device buffers shaped like the weights of
+ * peagle_weights (gate and up separate, [I, H] each), owned by the caller and overwritten
+ * by the call.  Per-layer entries are host arrays of n_layers device pointers.  embed
+ * ([Vt, H]) and attn_norm (and any of its entries) may be NULL: those gradients are then
+ * skipped (attn_norm[0] is written as zeros: layer 1 reads the 2H input, not a norm of
+ * the residual). */
+typedef struct peagle_grads {
+  float* embed;
+  float* emb_mask;
+  float* h_shared;
+  float* fc;
+  float* input_norm;
+  float* hidden_norm;
+  float* const* qkv;
+  float* const* o;
+  float* const* attn_norm;
+  float* const* post_norm;
+  float* const* gate;
+  float* const* up;
+  float* const* down;
+  float* final_norm;
+  float* lm_head;
+} peagle_grads;
+
+/* One training step without optimizer ("P-EAGLE: Parallel-Drafting EAGLE with Scalable
+ * Training", A2 section 2 and section 3): the training-style forward of
+ * peagle_forward_parallel over the rows (row_p, row_d) -- same arguments and the same row
+ * contract -- then loss = the mean over the M rows of the cross-entropy of the row's
+ * draft-vocabulary logits against labels[i] (device int32 [M], in [0, Vd)), and the
+ * gradient of the loss with respect to every parameter into `grads`.
+ *   out_loss  device fp32 scalar.
+ * Arithmetic: fp32 activations; projections and the attention's depth-1 products on
+ * cuBLAS (TF32 tensor cores for bf16 drafters, fp32 for fp32 drafters).  Needs
+ * dims.max_rows > 0; the first call allocates the step's workspaces (fp32 weight copies
+ * for bf16 drafters and every layer's kept activations), so it is not capturable in a
+ * CUDA graph.  UNSUPPORTED with attn_window or lm_rank set.  Device checks: BAD_ROW for
+ * rows outside the contract, BAD_TOKEN for tokens or labels out of range. */
+int peagle_train_step(peagle_ctx* ctx, int32_t n, int32_t K, const int32_t* tokens,
+                      const void* hidden, const int32_t* row_p, const int32_t* row_d, int32_t M,
+                      const int32_t* labels, float* out_loss, const peagle_grads* grads,
+                      void* stream);
+
 /* Host-side COD sampling ("COD sampling"; 3.2): depth 1 keeps every position; row
  * (p, d >= 2) exists when p - d + 1 >= 0 and is kept when its dependency (p-1, d-1)
  * was kept and uniforms[p*K + d-1] < ratio.  Writes the retained rows p-major into

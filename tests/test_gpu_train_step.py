@@ -1,0 +1,131 @@
+"""Training step (mean cross-entropy over retained rows, every parameter gradient; "P-EAGLE:
+Parallel-Drafting EAGLE with Scalable Training", A2 section 2 and section 3) on the GPU
+against the fp64 oracle ``peagle_train_step``'s counterpart in oracle/peagle_train_oracle.
+
+Tolerances, from the arithmetic: fp32 drafters run every product in fp32 (relative error
+of a gradient tensor about 1e-6, bound 1e-4); bf16 drafters run the GEMMs on TF32 tensor
+cores (operands rounded to 11 significant bits, 2^-11 = 4.9e-4 per element), bound 1e-2
+on each tensor's relative Frobenius error and 1e-3 on the loss."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import peagle_oracle as O
+from oracle import peagle_train_oracle as T
+from pe_helpers import make_ctx, pk
+
+pytestmark = pytest.mark.gpu
+
+SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_dim=64,
+                        intermediate=320, draft_vocab=1000, target_vocab=1500,
+                        rope_theta=10000.0, rms_eps=1e-5, dtype="bf16", d2t="monotone")
+
+
+def _weights(dims, seed):
+    """Synthetic weights with norm gains, emb(mask) and h_shared away from their initial
+    values (a unit gain would hide a missing factor)."""
+    w = synth.make_weights(dims, seed)
+    g = torch.Generator().manual_seed(seed)
+    dt = w["fc"].dtype
+    for k in ("input_norm", "hidden_norm", "final_norm"):
+        w[k] = (1.0 + 0.3 * torch.randn(dims.hidden, generator=g)).to(dt)
+    for L in w["layers"]:
+        for k in ("attn_norm", "post_norm"):
+            L[k] = (1.0 + 0.3 * torch.randn(dims.hidden, generator=g)).to(dt)
+    return w
+
+
+def _grad_buffers(dims):
+    H, I, nq, nkv, hd = (dims.hidden, dims.intermediate, dims.n_q_heads, dims.n_kv_heads,
+                         dims.head_dim)
+    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")  # noqa: E731
+    q = (nq + 2 * nkv) * hd
+    return {"embed": z(dims.target_vocab, H), "emb_mask": z(H), "h_shared": z(3 * H),
+            "fc": z(H, 3 * H), "input_norm": z(H), "hidden_norm": z(H), "final_norm": z(H),
+            "lm_head": z(dims.draft_vocab, H),
+            "qkv": [z(q, 2 * H if l == 0 else H) for l in range(dims.n_layers)],
+            "o": [z(H, nq * hd) for _ in range(dims.n_layers)],
+            "attn_norm": [z(H) for _ in range(dims.n_layers)],
+            "post_norm": [z(H) for _ in range(dims.n_layers)],
+            "gate": [z(I, H) for _ in range(dims.n_layers)],
+            "up": [z(I, H) for _ in range(dims.n_layers)],
+            "down": [z(H, I) for _ in range(dims.n_layers)]}
+
+
+def _run(dims, seed, n, K, cod):
+    w = _weights(dims, seed)
+    rng = np.random.default_rng(seed)
+    tokens = rng.integers(0, dims.target_vocab, n).astype(np.int32)
+    hidden = synth.normal((n, 3 * dims.hidden), np.random.SeedSequence(seed + 1), 1.0,
+                          dims.torch_dtype)
+    u = rng.random((n, K)) if cod else np.zeros((n, K))
+    rp, rd = pk().peagle_cod_rows(n, K, cod if cod else 1.0, u)
+    M = len(rp)
+    labels = rng.integers(0, dims.draft_vocab, M).astype(np.int32)
+    m = pk()
+    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=M, max_seq=n)
+    g = _grad_buffers(dims)
+    loss = torch.full((1,), float("nan"), device="cuda")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    m.peagle_train_step(ctx, n, K, dev(tokens), hidden.cuda(), dev(rp), dev(rd), M, dev(labels),
+                        loss, g)
+    torch.cuda.synchronize()
+    assert m.peagle_status(ctx) == m.PEAGLE_OK
+    ctx.close()
+    W = O.Weights64.from_synth(w)
+    W.embed = O.to64(W.embed)
+    rows = np.stack([rp, rd], 1).astype(np.int64)
+    ref_loss, _, ref = T.train_step(W, dims, tokens, O.to64(hidden), rows, labels)
+    return float(loss.item()), g, ref_loss, ref
+
+
+def _flat(g, ref, n_layers):
+    for k in ("embed", "emb_mask", "h_shared", "fc", "input_norm", "hidden_norm", "final_norm",
+              "lm_head"):
+        yield k, g[k], ref[k]
+    for l in range(n_layers):
+        for k in ("qkv", "o", "attn_norm", "post_norm", "gate", "up", "down"):
+            yield f"layers.{l}.{k}", g[k][l], ref["layers"][l][k]
+
+
+def _compare(dims, out, tol, loss_tol):
+    loss, g, ref_loss, ref = out
+    assert abs(loss - ref_loss) <= loss_tol * abs(ref_loss), (loss, ref_loss)
+    for name, got, want in _flat(g, ref, dims.n_layers):
+        got = got.cpu().double().numpy()
+        assert np.all(np.isfinite(got)), name
+        den = np.linalg.norm(want)
+        err = np.linalg.norm(got - want)
+        if den == 0:
+            assert err == 0, name
+        else:
+            assert err <= tol * den, f"{name}: relative error {err / den:.3e}"
+
+
+@pytest.mark.parametrize("n,K,cod", [(24, 4, 0.8), (16, 1, None), (12, 8, None)])
+def test_tiny_f32_train_step(n, K, cod):
+    dims = synth.DIMS_TINY
+    _compare(dims, _run(dims, 3 + K, n, K, cod), 1e-4, 1e-5)
+
+
+@pytest.mark.parametrize("n,K,cod", [(40, 8, 0.8), (33, 3, 0.6)])
+def test_small_bf16_train_step(n, K, cod):
+    dims = SMALL_BF16
+    _compare(dims, _run(dims, 7 + K, n, K, cod), 1e-2, 1e-3)
+
+
+def test_train_step_rejects_a_window():
+    m = pk()
+    dims = synth.shrink(SMALL_BF16, attn_window=8)
+    w = synth.make_weights(dims, 1)
+    ctx = make_ctx(dims, w, 1, 2, 32, max_rows=16, max_seq=8)
+    z = torch.zeros(16, dtype=torch.int32, device="cuda")
+    g = _grad_buffers(dims)
+    loss = torch.zeros(1, device="cuda")
+    with pytest.raises(m.PeagleError) as e:
+        m.peagle_train_step(ctx, 8, 2, z, torch.zeros(8, 3 * dims.hidden, device="cuda",
+                                                      dtype=torch.bfloat16),
+                            z, z, 8, z, loss, g)
+    assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
+    ctx.close()
