@@ -12,12 +12,13 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode_b1|decode_b2|ragged_b16]
 
-Three extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
-COD 0.8), sliding_window (the concurrency-2 workload with and without a 4096-position
+Four extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
+COD 0.8), train_step (the same rows: forward, mean cross-entropy and every parameter
+gradient), sliding_window (the concurrency-2 workload with and without a 4096-position
 drafter attention window) and efficient_head (the headline workload with the rank-128 /
 top-128 LM head and with the full head, on the 32000-entry draft vocabulary and on the
-whole 201088-entry vocabulary); --no-train-fwd / --no-window / --no-head skip them, and
---only NAME runs one of them alone (a short driver for profilers).
+whole 201088-entry vocabulary); --no-train-fwd / --no-train-step / --no-window / --no-head
+skip them, and --only NAME runs one of them alone (a short driver for profilers).
 
 --impl reference times the fp64 oracle on the host cores instead (a deliberately slow
 plain program; see the cpu_baseline object).  Under torchrun each rank runs an
@@ -59,7 +60,9 @@ def parse():
                     help="skip the sliding-window attention measurement")
     ap.add_argument("--no-head", action="store_true",
                     help="skip the efficient LM head measurement")
-    ap.add_argument("--only", choices=["train_fwd", "window", "head_draft_vocab",
+    ap.add_argument("--no-train-step", action="store_true",
+                    help="skip the training step measurement")
+    ap.add_argument("--only", choices=["train_fwd", "train_step", "window", "head_draft_vocab",
                                        "head_full_vocab"],
                     help="run one of the extra measurements alone and print its object "
                          "(a short driver for profilers)")
@@ -393,6 +396,8 @@ def run_ours(args, rank, world, dist):
         out["sliding_window"] = window_measure(dev)
     if rank == 0 and world == 1 and not args.no_head:
         out["efficient_head"] = head_measure(dev)
+    if rank == 0 and world == 1 and not args.no_train_step:
+        out["train_step"] = train_step_measure(dev)
     return out
 
 
@@ -547,6 +552,79 @@ def train_fwd_measure(dev, reps=3):
             "stages_ms": {k: round(v[0], 3) for k, v in st.items()}}
 
 
+def train_step_measure(dev, reps=3):
+    """Training step without optimizer on the training workload (decode drafter, n=2048,
+    K=8, COD 0.8): ms per step (forward with kept activations, mean cross-entropy, every
+    parameter gradient) with CUDA events, and its algorithmic FLOPs against the TF32 peak
+    (the GEMMs run on TF32 tensor cores): projections 6*M*params (forward, dX, dW) plus
+    attention 12*nq*hd*(allowed pairs) (forward 2 products, backward 4)."""
+    import numpy as np
+    import torch
+
+    import drafting_eagle_draft_gb300 as pk
+
+    wl = synth.WORKLOADS["train_fwd"]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    ti = synth.make_train_inputs(wl, 21)
+    n, K = wl.n_seq, wl.K
+    rp, rd = pk.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
+    M = len(rp)
+    ctx = pk.peagle_create(w, pk.make_dims(dims, 1, K, n, max_rows=M, max_seq=n))
+    del w
+    H, I, nq, nkv, hd, L = (dims.hidden, dims.intermediate, dims.n_q_heads, dims.n_kv_heads,
+                            dims.head_dim, dims.n_layers)
+    z = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)  # noqa: E731
+    qo = (nq + 2 * nkv) * hd
+    g = {"embed": None, "emb_mask": z(H), "h_shared": z(3 * H), "fc": z(H, 3 * H),
+         "input_norm": z(H), "hidden_norm": z(H), "final_norm": z(H),
+         "lm_head": z(dims.draft_vocab, H),
+         "qkv": [z(qo, 2 * H if l == 0 else H) for l in range(L)],
+         "o": [z(H, nq * hd) for _ in range(L)], "attn_norm": [z(H) for _ in range(L)],
+         "post_norm": [z(H) for _ in range(L)], "gate": [z(I, H) for _ in range(L)],
+         "up": [z(I, H) for _ in range(L)], "down": [z(H, I) for _ in range(L)]}
+    gs = pk.grads_struct(g, L)
+    tok = torch.from_numpy(ti["tokens"]).to(dev)
+    hid = ti["hidden"].to(dev)
+    rpd = torch.from_numpy(rp).to(dev)
+    rdd = torch.from_numpy(rd).to(dev)
+    lab = torch.from_numpy(
+        np.random.default_rng(5).integers(0, dims.draft_vocab, M).astype(np.int32)).to(dev)
+    loss = torch.zeros(1, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step():
+        pk.peagle_train_step(ctx, n, K, tok, hid, rpd, rdd, M, lab, loss, gs, s)
+
+    with torch.cuda.stream(s):
+        step()
+        step()
+    s.synchronize()
+    assert pk.peagle_status(ctx) == pk.PEAGLE_OK
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            step()
+        e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    ctx.close()
+    params = gemm_weight_bytes(dims) // 2
+    p_np, d_np = rp.astype("int64"), rd.astype("int64")
+    pairs = int(((p_np - d_np + 1) + 1).sum() + (d_np - 1).sum())
+    flops = 6.0 * M * params + 12.0 * nq * hd * pairs
+    pk_ = peaks()
+    # TF32 peak: the measured sustained bf16 peak times the nominal dense ratio 1.1 / 2.25
+    peak = pk_["bf16_tflops_sustained"] * 1.1 / 2.25
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"workload": wl.name, "rows": M, "ms": round(ms, 3), "loss": round(loss.item(), 5),
+            "tflops": round(tflops, 1), "peak_tflops": round(peak, 1),
+            "peak_source": "measured bf16 sustained x nominal TF32/bf16 ratio (1.1/2.25)",
+            "frac": round(tflops / peak, 4), "algorithmic_tflop": round(flops / 1e12, 3)}
+
+
 # ---------------------------------------------------------------------------- oracle arm
 
 
@@ -633,6 +711,8 @@ def main():
         torch.cuda.set_device(dev)
         if args.only == "train_fwd":
             out = {"train_fwd": train_fwd_measure(dev)}
+        elif args.only == "train_step":
+            out = {"train_step": train_step_measure(dev)}
         elif args.only == "window":
             out = {"sliding_window": window_measure(dev)}
         else:

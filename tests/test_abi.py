@@ -52,6 +52,8 @@ def test_struct_layout_matches_header(pk):
     assert pk.PeagleDims.lm_topk.offset == 72
     assert ctypes.sizeof(pk.PeagleWeights) == 18 * 8
     assert ctypes.sizeof(pk.PeagleKV) == 24
+    assert ctypes.sizeof(pk.PeagleGrads) == 15 * 8
+    assert pk.PeagleGrads.qkv.offset == 6 * 8 and pk.PeagleGrads.lm_head.offset == 14 * 8
 
 
 def test_host_argument_errors(pk):

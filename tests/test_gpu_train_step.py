@@ -129,3 +129,39 @@ def test_train_step_rejects_a_window():
                             z, z, 8, z, loss, g)
     assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
     ctx.close()
+
+
+def test_train_step_loss_at_full_size_is_the_forward_cross_entropy():
+    """The training workload (decode drafter, n = 2048, K = 8, COD 0.8; 8,407 rows): the
+    step's loss equals the mean cross-entropy of the bf16 training forward's logits on the
+    same rows (two independent paths: TF32 fp32-activation GEMMs against tcgen05 bf16 hi/lo
+    GEMMs), and every gradient is finite."""
+    m = pk()
+    wl = synth.WORKLOADS["train_fwd"]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    ti = synth.make_train_inputs(wl, 21)
+    n, K = wl.n_seq, wl.K
+    rp, rd = m.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
+    M = len(rp)
+    labels = np.random.default_rng(5).integers(0, dims.draft_vocab, M).astype(np.int32)
+    ctx = make_ctx(dims, w, 1, K, n, max_rows=M, max_seq=n)
+    del w
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    tok, hid, rpd, rdd, lab = dev(ti["tokens"]), ti["hidden"].cuda(), dev(rp), dev(rd), dev(labels)
+    lg = torch.empty(M, dims.draft_vocab, device="cuda")
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    m.peagle_forward_parallel(ctx, n, K, tok, hid, rpd, rdd, M, am, lg)
+    ce = (torch.logsumexp(lg.double(), 1) - lg.double()[torch.arange(M), lab.long()]).mean()
+    g = _grad_buffers(dims)
+    g["embed"] = None
+    loss = torch.zeros(1, device="cuda")
+    m.peagle_train_step(ctx, n, K, tok, hid, rpd, rdd, M, lab, loss, g)
+    torch.cuda.synchronize()
+    assert m.peagle_status(ctx) == m.PEAGLE_OK
+    ctx.close()
+    assert abs(loss.item() - ce.item()) <= 1e-3 * abs(ce.item()), (loss.item(), ce.item())
+    for name, t in g.items():
+        for x in (t if isinstance(t, list) else [t]):
+            if x is not None:
+                assert torch.isfinite(x).all(), name
