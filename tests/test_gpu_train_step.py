@@ -165,3 +165,40 @@ def test_train_step_loss_at_full_size_is_the_forward_cross_entropy():
         for x in (t if isinstance(t, list) else [t]):
             if x is not None:
                 assert torch.isfinite(x).all(), name
+
+
+def test_train_step_flags_rows_outside_the_contract():
+    """A row set that is not closed under the mask's dependencies (a depth-1 row missing)
+    and a label outside the vocabulary are reported through the device error word; the
+    calls complete with finite gradients, and a valid call afterwards is clean."""
+    m = pk()
+    dims = synth.DIMS_TINY
+    w = synth.make_weights(dims, 2)
+    n, K = 8, 3
+    rp, rd = m.peagle_cod_rows(n, K, 1.0, np.zeros((n, K)))
+    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=len(rp), max_seq=n)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    tok = dev(np.arange(n, dtype=np.int32))
+    hid = torch.randn(n, 3 * dims.hidden, device="cuda")
+
+    def run(p, d, labels):
+        g = _grad_buffers(dims)
+        loss = torch.zeros(1, device="cuda")
+        m.peagle_train_step(ctx, n, K, tok, hid, dev(p), dev(d), len(p), dev(labels), loss, g)
+        st = m.peagle_status(ctx)
+        bits = m.peagle_device_error_bits(ctx)
+        assert np.isfinite(loss.item())
+        for t in g.values():
+            for x in (t if isinstance(t, list) else [t]):
+                assert torch.isfinite(x).all()
+        return st, bits
+
+    keep = ~((rp == 4) & (rd == 1))  # (5, 1) then misses its dependency (4, 1)
+    st, bits = run(rp[keep], rd[keep], np.zeros(int(keep.sum()), np.int32))
+    assert st == m.PEAGLE_ERR_DEVICE and bits & m.PEAGLE_DEV_BAD_ROW
+    lab = np.zeros(len(rp), np.int32)
+    lab[3] = dims.draft_vocab
+    st, bits = run(rp, rd, lab)
+    assert st == m.PEAGLE_ERR_DEVICE and bits & m.PEAGLE_DEV_BAD_TOKEN
+    assert run(rp, rd, np.zeros(len(rp), np.int32))[0] == m.PEAGLE_OK
+    ctx.close()
