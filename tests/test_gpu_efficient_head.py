@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import synth
-from pe_helpers import LOGIT_TOL, MARGIN, make_ctx, oracle_draft, run_draft
+from oracle import peagle_oracle as O
+from pe_helpers import LOGIT_TOL, MARGIN, make_ctx, oracle_draft, pk, run_draft
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +30,7 @@ def _case(dims, lens, K, seed):
     return w, inp
 
 
-def _check(dims, w, ref, toks, lg, what):
+def _check(dims, w, ref, toks, lg, what, quota=True):
     tol = LOGIT_TOL[dims.dtype]
     B, K, Vd = lg.shape
     k = min(dims.lm_topk, Vd)
@@ -51,7 +52,8 @@ def _check(dims, w, ref, toks, lg, what):
             if cg == co and ref.margin[b, j] > MARGIN:
                 agree += 1
                 assert toks[b, j] == ref.tokens[b, j], f"{what}: row {b},{j} token differs"
-    assert agree > 0.5 * B * K, f"{what}: too few rows with a clear answer ({agree})"
+    if quota:
+        assert agree > 0.5 * B * K, f"{what}: too few rows with a clear answer ({agree})"
 
 
 def test_tiny_f32_efficient_head():
@@ -141,3 +143,60 @@ def test_forward_parallel_rejects_the_efficient_head():
                                   torch.from_numpy(rd).cuda(), len(rp), am, None)
     assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
     ctx.close()
+
+
+@pytest.mark.parametrize("pass_kernel", [True, False])
+def test_efficient_head_with_a_sliding_window(pass_kernel):
+    """Both EAGLE-4 drafter variants at once: a 64-position window and the rank-128 head."""
+    lens, K = [300, 20, 130], 5
+    dims = synth.shrink(SMALL_BF16, lm_rank=128, lm_topk=64, attn_window=64)
+    w, inp = _case(dims, lens, K, 41)
+    ctx = make_ctx(dims, w, len(lens), K, inp["capacity"] + 1, pass_kernel=pass_kernel)
+    toks, lg, _ = run_draft(ctx, dims, inp, K)
+    _check(dims, w, oracle_draft(dims, w, inp, K), toks, lg,
+           f"window + efficient head {'pass' if pass_kernel else 'multi'}")
+    ctx.close()
+
+
+def test_efficient_head_at_the_largest_candidate_count():
+    """lm_topk = 1024 (the largest accepted) over a 20000-entry vocabulary."""
+    lens, K = [50, 200], 4
+    dims = synth.shrink(SMALL_BF16, lm_rank=128, lm_topk=1024, draft_vocab=20000,
+                        target_vocab=20500)
+    w, inp = _case(dims, lens, K, 43)
+    ctx = make_ctx(dims, w, len(lens), K, inp["capacity"] + 1)
+    toks, lg, _ = run_draft(ctx, dims, inp, K)
+    # with 1024 candidates a row's set often differs from the oracle's by near-boundary
+    # ties (allowed, checked), so no quota of identical sets is asked for
+    _check(dims, w, oracle_draft(dims, w, inp, K), toks, lg, "top 1024", quota=False)
+    ctx.close()
+
+
+@pytest.mark.parametrize("pass_kernel", [True, False])
+def test_catch_up_with_the_efficient_head(pass_kernel):
+    """The catch-up pass (accepted tokens as depth-1 rows) through the efficient head."""
+    import pe_helpers as H
+
+    m = pk()
+    lens, T = [0, 37, 100], 5
+    dims = synth.shrink(SMALL_BF16, lm_rank=128, lm_topk=48)
+    w = synth.make_weights(dims, 29)
+    wl = synth.Workload("c", dims, len(lens), T, tuple(lens))
+    inp = synth.make_decode_inputs(wl, 30, capacity=max(lens) + T + 8)
+    hid = synth.normal((len(lens), T, 3 * dims.hidden), 31, 1.0, dims.torch_dtype)
+    tok = synth.uniform_ints(len(lens) * T, 0, dims.target_vocab, 32).reshape(len(lens), T)
+    ctx = make_ctx(dims, w, len(lens), 8, inp["capacity"], pass_kernel=pass_kernel)
+    d = H.to_dev(inp)
+    B = len(lens)
+    kv = m.kv_struct(d["ck"], d["cv"], d["ck"].shape[3], d["ck"].shape[1])
+    out = torch.full((B, T), -7, dtype=torch.int32, device="cuda")
+    lg = torch.full((B, T, dims.draft_vocab), float("nan"), device="cuda")
+    m.peagle_catch_up(ctx, B, kv, d["sl"], hid.cuda(), torch.from_numpy(tok).int().cuda(), T,
+                      out, lg)
+    assert m.peagle_status(ctx) == m.PEAGLE_OK
+    ctx.close()
+    W = O.Weights64.from_synth(w, lazy=True)
+    ref = O.catch_up(W, dims, inp["cache_k"], inp["cache_v"], inp["seq_lens"], hid, tok,
+                     bf16=O.DRAFT_BF16_CASTS)
+    _check(dims, w, ref, out.cpu().numpy(), lg.cpu().numpy(),
+           f"catch-up efficient head {'pass' if pass_kernel else 'multi'}", quota=False)
