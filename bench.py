@@ -166,6 +166,20 @@ def kv_bytes(dims, lens, K) -> int:
     return int(sum(int(L) + K for L in lens)) * per_pos
 
 
+def whole_job(dist, ms_step, units_per_rank, world, device):
+    """Whole-job throughput of `world` independent replicas (weak scaling): the units all
+    ranks processed over the slowest rank's step time, the max taken over ranks by a
+    collective when `dist` is given.  Returns (max ms per step, units per second)."""
+    import torch
+
+    ms_max = float(ms_step)
+    if dist:
+        t = torch.tensor([ms_max], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, world * units_per_rank / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------- our arm
 
 
@@ -345,13 +359,7 @@ def run_ours(args, rank, world, dist):
     achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
 
     # whole job: tokens of all ranks / max time over ranks
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    else:
-        ms_max = ms_step
-    total_tok_s = world * R / (ms_max * 1e-3)
+    ms_max, total_tok_s = whole_job(dist, ms_step, R, world, dev)
 
     out = None
     if rank == 0:
