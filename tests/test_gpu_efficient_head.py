@@ -200,3 +200,20 @@ def test_catch_up_with_the_efficient_head(pass_kernel):
                      bf16=O.DRAFT_BF16_CASTS)
     _check(dims, w, ref, out.cpu().numpy(), lg.cpu().numpy(),
            f"catch-up efficient head {'pass' if pass_kernel else 'multi'}", quota=False)
+
+
+@pytest.mark.parametrize("vocab", [None, 201088])
+def test_efficient_head_at_full_size(vocab):
+    """The headline workload (decode drafter, context 4096, K = 8) with the rank-128 /
+    top-128 head, on the 32000-entry draft vocabulary and on the whole 201088-entry
+    vocabulary (no d2t): against the fp64 oracle on every row."""
+    wl = synth.WORKLOADS["decode_b1"]
+    dims = synth.shrink(wl.dims, lm_rank=128, lm_topk=128)
+    if vocab:
+        dims = synth.shrink(dims, draft_vocab=vocab, d2t="identity")
+    w = synth.make_weights(dims, 1234)
+    inp = synth.make_decode_inputs(wl, 99)
+    ctx = make_ctx(dims, w, wl.batch, wl.K, inp["capacity"])
+    toks, lg, _ = run_draft(ctx, dims, inp, wl.K)
+    ctx.close()
+    _check(dims, w, oracle_draft(dims, w, inp, wl.K), toks, lg, f"decode_b1 vocab {dims.draft_vocab}")
