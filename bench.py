@@ -305,26 +305,32 @@ def run_ours(args, rank, world, dist):
     else:
         launches_per_step = sum(stage_n.values()) + 1  # + verify (context-free)
 
-    # end to end through the public API with host buffers (pinned), copies in the region
-    th_h = inp["target_hidden"].pin_memory()
-    nt_h = torch.from_numpy(inp["new_token"]).pin_memory()
-    sl_h = torch.from_numpy(inp["seq_lens"]).pin_memory()
-    toks_h = torch.empty(B, K, dtype=torch.int32).pin_memory()
-    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    bonus_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    h2d = th_h.numel() * th_h.element_size() + nt_h.numel() * 4 + sl_h.numel() * 4
-    d2h = toks_h.numel() * 4 + acc_h.numel() * 4 + bonus_h.numel() * 4
+    # end to end through the public API with host buffers (pinned), copies in the region:
+    # one packed host->device copy of the step's inputs (target hidden states, new tokens,
+    # seq_lens) and one packed device->host copy of its results (draft tokens, accepted
+    # lengths, bonus tokens)
+    th_b = inp["target_hidden"].numel() * inp["target_hidden"].element_size()
+    h2d = th_b + 4 * B + 4 * B
+    in_h = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    in_h[:th_b].copy_(inp["target_hidden"].contiguous().view(-1).view(torch.uint8))
+    in_h[th_b:th_b + 4 * B].copy_(torch.from_numpy(inp["new_token"]).view(torch.uint8))
+    in_h[th_b + 4 * B:].copy_(torch.from_numpy(inp["seq_lens"]).view(torch.uint8))
+    in_d = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    th_e = in_d[:th_b].view(th.dtype).view(th.shape)
+    nt_e = in_d[th_b:th_b + 4 * B].view(torch.int32)
+    sl_e = in_d[th_b + 4 * B:].view(torch.int32)
+    out_d = torch.empty(B * K + 2 * B, dtype=torch.int32, device=dev)
+    toks_e = out_d[:B * K].view(B, K)
+    acc_e, bonus_e = out_d[B * K:B * K + B], out_d[B * K + B:]
+    out_h = torch.empty(B * K + 2 * B, dtype=torch.int32).pin_memory()
+    d2h = out_h.numel() * 4
 
     def e2e_step():
-        th.copy_(th_h, non_blocking=True)
-        nt.copy_(nt_h, non_blocking=True)
-        sl.copy_(sl_h, non_blocking=True)
-        pk.peagle_draft(ctx, B, kv, sl, th, nt, K, toks, None, stream)
-        pk.peagle_verify_greedy(B, K, toks, tgt, acc, bonus, stream)
-        pk.peagle_append_kv(ctx, B, kv, sl, ntp_only, stream=stream, n_extra=1)
-        toks_h.copy_(toks, non_blocking=True)
-        acc_h.copy_(acc, non_blocking=True)
-        bonus_h.copy_(bonus, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
+        pk.peagle_draft(ctx, B, kv, sl_e, th_e, nt_e, K, toks_e, None, stream)
+        pk.peagle_verify_greedy(B, K, toks_e, tgt, acc_e, bonus_e, stream)
+        pk.peagle_append_kv(ctx, B, kv, sl_e, ntp_only, stream=stream, n_extra=1)
+        out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
