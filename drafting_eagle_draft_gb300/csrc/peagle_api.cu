@@ -1241,6 +1241,10 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   ta.row_p = row_p;
   ta.row_d = row_d;
   ta.chain = w->chain;
+  // bf16 drafters take the fused TF32 attention backward (fp32 drafters keep fp32 GEMMs);
+  // PEAGLE_TRAIN_FUSED_ATTN=0 selects the dense score matrices for them too
+  const char* fa_env = getenv("PEAGLE_TRAIN_FUSED_ATTN");
+  const bool fused_attn = c->bf && attn_bwd_fused_ok(ta) && !(fa_env && fa_env[0] == '0');
 
   // ---- forward
   launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
@@ -1313,7 +1317,18 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     launch_attn_bwd_prep(ta, w->dO, w->O[l], w->dOh, w->Dv, s);
     TRY_RET(zero(w->dKr, (size_t)M * nkv * hd, s));
     TRY_RET(zero(w->dVr, (size_t)M * nkv * hd, s));
-    for (int g = 0; g < nkv; ++g) {
+    if (fused_attn) {
+      // chain part per row, then the prefix part on TF32 tensor cores without the dense
+      // score matrices
+      for (int g = 0; g < nkv; ++g)
+        launch_attn_bwd_ds(ta, g, nullptr, nullptr, w->lse[l], w->Dv, w->Qh[l], w->Kr[l],
+                           w->Vr[l], w->dOh, w->dQh, w->dKr, w->dVr, s);
+      TRY_RET(zero(w->dK1, (size_t)nkv * n * hd, s));
+      TRY_RET(zero(w->dV1, (size_t)nkv * n * hd, s));
+      launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l], w->V1[l],
+                            w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, s);
+    }
+    for (int g = 0; g < nkv && !fused_attn; ++g) {
       const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;
       const float* K1g = w->K1[l] + (size_t)g * n * hd;
       const float* V1g = w->V1[l] + (size_t)g * n * hd;

@@ -308,9 +308,10 @@ __global__ void attn_bwd_prep_kernel(TrainAttn a, const float* dO, const float* 
 }
 
 // One warp per (head of group g, row): the prefix probabilities P1 = exp(S1 - lse) (in
-// place over the recomputed scores) and dS1 = P1 (dP1 - D) scale (in place over dP1);
-// the chain's scores, probabilities and dS give dQh's initial value (the GEMM dS1 K1 adds
-// the prefix part) and are added into the chain rows' dK / dV.
+// place over the recomputed scores) and dS1 = P1 (dP1 - D) scale (in place over dP1),
+// unless S1 is null; the chain's scores, probabilities and dS give dQh's initial value
+// (the prefix part is added after: the GEMM dS1 K1 or the fused dQ kernel) and are added
+// into the chain rows' dK / dV.
 __global__ void attn_bwd_ds_kernel(TrainAttn a, int g, float* S1, float* dP1, const float* lse,
                                    const float* Dv, const float* Qh, const float* Kr,
                                    const float* Vr, const float* dOh, float* dQh, float* dKr,
@@ -321,16 +322,18 @@ __global__ void attn_bwd_ds_kernel(TrainAttn a, int g, float* S1, float* dP1, co
   const int hl = w / a.M, i = w % a.M, h = g * G + hl;
   const int anc = anchor_of(a.row_p[i], a.row_d[i], a.n, a.K);
   const float L = lse[(size_t)h * a.M + i], D = Dv[(size_t)h * a.M + i];
-  float* srow = S1 + ((size_t)hl * a.M + i) * a.n;
-  float* drow = dP1 + ((size_t)hl * a.M + i) * a.n;
-  for (int j = lane; j < a.n; j += 32) {
-    float pr = 0.f, ds = 0.f;
-    if (j <= anc) {
-      pr = expf(srow[j] - L);
-      ds = pr * (drow[j] - D) * a.scale;
+  if (S1) {  // without the dense matrices the fused kernels handle the prefix
+    float* srow = S1 + ((size_t)hl * a.M + i) * a.n;
+    float* drow = dP1 + ((size_t)hl * a.M + i) * a.n;
+    for (int j = lane; j < a.n; j += 32) {
+      float pr = 0.f, ds = 0.f;
+      if (j <= anc) {
+        pr = expf(srow[j] - L);
+        ds = pr * (drow[j] - D) * a.scale;
+      }
+      srow[j] = pr;
+      drow[j] = ds;
     }
-    srow[j] = pr;
-    drow[j] = ds;
   }
   const float* q = Qh + ((size_t)h * a.M + i) * a.hd;
   const float* dO = dOh + ((size_t)h * a.M + i) * a.hd;

@@ -54,6 +54,15 @@ void launch_attn_bwd_ds(const TrainAttn& a, int g, float* S1, float* dP1, const 
 void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, const int* row_d,
                         const float* dK1, const float* dV1, float* dKr, float* dVr,
                         cudaStream_t s);
+// Fused prefix-attention backward on TF32 tensor cores (train_attn_mma.cu), for head_dim
+// 64 and at most 8 q heads per kv head: dQh += dS K1 (dQh holds the chain part) and
+// dK1 / dV1 (zero beforehand) += dS^T Q / P^T dO; row_index as from rows-prepare.  Qh,
+// dOh, K1 and V1 are rounded to TF32 in place first.
+bool attn_bwd_fused_ok(const TrainAttn& a);
+void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
+                           const float* dOh, const float* K1, const float* V1,
+                           const float* lse, const float* Dv, float* dQh, float* dK1,
+                           float* dV1, cudaStream_t s);
 void launch_ce(int M, int V, float* logits, const int* labels, float* row_loss, float* loss,
                unsigned* err, cudaStream_t s);
 void launch_embed_grad(int M, int n, int K, int H, int Vt, const int* row_p, const int* row_d,
