@@ -253,7 +253,9 @@ typedef struct peagle_grads {
  * gradient of the loss with respect to every parameter into `grads`.
  *   out_loss  device fp32 scalar.
  * Arithmetic: fp32 activations; projections and the attention's depth-1 products on
- * cuBLAS (TF32 tensor cores for bf16 drafters, fp32 for fp32 drafters).  Needs
+ * cuBLAS (TF32 tensor cores for bf16 drafters, fp32 for fp32 drafters); for bf16
+ * drafters with head_dim 64 the attention backward's depth-1 part runs on the library's
+ * own TF32 tensor-core kernels.  Needs
  * dims.max_rows > 0; the first call allocates the step's workspaces (fp32 weight copies
  * for bf16 drafters and every layer's kept activations), so it is not capturable in a
  * CUDA graph.  UNSUPPORTED with attn_window or lm_rank set.  Device checks: BAD_ROW for
