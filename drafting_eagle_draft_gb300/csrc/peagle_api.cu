@@ -37,7 +37,7 @@ struct TrainWs {
   float *E, *Hin, *f, *r1, *r2, *x0, *y, *ry, *logits, *row_loss, *resL;
   std::vector<float*> res_in, a, ra, Qh, Kr, Vr, K1, V1, Pc, lse, O, res_mid, u, ru, GU, act;
   // scratch
-  float *qkvb, *S1, *dP1, *Oh;
+  float *qkvb, *S1, *dP1, *Oh, *lrow;
   // backward
   float *bufA, *bufB, *dact, *dGU, *du, *dO, *dOh, *Dv, *dQh, *dKr, *dVr, *dK1, *dV1, *dqkv,
       *da, *dgu_w, *dE, *df, *dHin, *dy;
@@ -1160,9 +1160,9 @@ static int train_ws(peagle_ctx* c) {
   w->res_in[0] = w->f;
   w->a[0] = w->x0;
   TRY_RET(fl(&w->qkvb, (size_t)M * qkv_out));
-  TRY_RET(fl(&w->S1, (size_t)G * M * n));
-  TRY_RET(fl(&w->dP1, (size_t)G * M * n));
+  w->S1 = w->dP1 = nullptr;  // the dense prefix score matrices: allocated when first used
   TRY_RET(fl(&w->Oh, (size_t)nq * M * hd));
+  TRY_RET(fl(&w->lrow, (size_t)nq * M));
   // backward
   TRY_RET(fl(&w->bufA, (size_t)M * H));
   TRY_RET(fl(&w->bufB, (size_t)M * H));
@@ -1245,6 +1245,11 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   // PEAGLE_TRAIN_FUSED_ATTN=0 selects the dense score matrices for them too
   const char* fa_env = getenv("PEAGLE_TRAIN_FUSED_ATTN");
   const bool fused_attn = c->bf && attn_bwd_fused_ok(ta) && !(fa_env && fa_env[0] == '0');
+  if (!fused_attn && !w->S1) {
+    const size_t count = (size_t)G * w->Mmax * w->nmax;
+    TRY_RET(dalloc(c, (void**)&w->S1, count * 4));
+    TRY_RET(dalloc(c, (void**)&w->dP1, count * 4));
+  }
 
   // ---- forward
   launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
@@ -1261,7 +1266,10 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     TRY_RET(zero(w->V1[l], (size_t)nkv * n * hd, s));
     launch_train_rope(M, n, K, nq, nkv, hd, w->qkvb, row_p, row_d, c->rope, w->Qh[l], w->Kr[l],
                       w->Vr[l], w->K1[l], w->V1[l], s);
-    for (int g = 0; g < nkv; ++g) {
+    if (fused_attn)  // online softmax over the prefix, then the chain keys per row
+      launch_attn_fwd_fused(ta, w->Qh[l], w->Kr[l], w->Vr[l], w->K1[l], w->V1[l], w->Oh, w->Dv,
+                            w->lrow, w->Pc[l], w->lse[l], w->O[l], s);
+    for (int g = 0; g < nkv && !fused_attn; ++g) {
       const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;
       const float* K1g = w->K1[l] + (size_t)g * n * hd;
       const float* V1g = w->V1[l] + (size_t)g * n * hd;
@@ -1326,7 +1334,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
       TRY_RET(zero(w->dK1, (size_t)nkv * n * hd, s));
       TRY_RET(zero(w->dV1, (size_t)nkv * n * hd, s));
       launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l], w->V1[l],
-                            w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, s);
+                            w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, true, s);
     }
     for (int g = 0; g < nkv && !fused_attn; ++g) {
       const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;

@@ -347,6 +347,195 @@ __global__ void __launch_bounds__(128, 3) attn_bwd_dkv_kernel(TrainAttn a, const
   }
 }
 
+// ---- forward: one CTA per (16 rows, kv group), one warp per head --------------------
+// Online softmax over the depth-1 prefix (K1 / V1 tiles of 64 keys staged as in the dQ
+// kernel): per tile the scores of the warp's 16 rows, the running row max m and sum l
+// (each row's four lanes reduce with shuffles), the accumulator O rescaled and P V added.
+// Writes the unnormalised prefix O (per-head rows) and m, l; attn_fwd_combine_kernel then
+// adds the chain keys and normalises.
+__global__ void __launch_bounds__(256) attn_fwd_prefix_kernel(TrainAttn a, const float* Qh,
+                                                              const float* K1, const float* V1,
+                                                              float* Op, float* mrow,
+                                                              float* lrow) {
+  extern __shared__ float smem[];  // [2 stages][K, V][64][FA_LD]
+  const int G = a.nq / a.nkv, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  const int i0 = blockIdx.x * 16;
+  const int r0 = i0 + gq, r1 = r0 + 8;
+  const int anc0 = anchor_row(a, r0), anc1 = anchor_row(a, r1);
+  int amax = max(anc0, anc1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const bool live = warp < G;
+  const int h = g * G + (live ? warp : 0);
+  const int ntiles = (amax + 64) / 64;  // 0 when no row sees a key
+  const float* K1g = K1 + (size_t)g * a.n * 64;
+  const float* V1g = V1 + (size_t)g * a.n * 64;
+  const int nthr = blockDim.x;
+  if (ntiles > 0) {
+    stage64(smem, K1g, 0, a.n, threadIdx.x, nthr);
+    stage64(smem + 64 * FA_LD, V1g, 0, a.n, threadIdx.x, nthr);
+    cp_commit();
+  }
+  uint32_t qa[8][4];
+  {
+    const float* q0 = Qh + ((size_t)h * a.M + min(r0, a.M - 1)) * 64;
+    const float* q1 = Qh + ((size_t)h * a.M + min(r1, a.M - 1)) * 64;
+    const bool v0 = r0 < a.M, v1 = r1 < a.M;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const float2 x0 = v0 ? *reinterpret_cast<const float2*>(q0 + 8 * s + 2 * tq) : make_float2(0.f, 0.f);
+      const float2 x1 = v1 ? *reinterpret_cast<const float2*>(q1 + 8 * s + 2 * tq) : make_float2(0.f, 0.f);
+      qa[s][0] = bits(x0.x); qa[s][1] = bits(x1.x); qa[s][2] = bits(x0.y); qa[s][3] = bits(x1.y);
+    }
+  }
+  float o[8][4];
+#pragma unroll
+  for (int nn = 0; nn < 8; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq, gq + 8
+  for (int kt = 0; kt < ntiles; ++kt) {
+    float* cur = smem + (size_t)(kt & 1) * 2 * 64 * FA_LD;
+    if (kt + 1 < ntiles) {
+      float* nxt = smem + (size_t)((kt + 1) & 1) * 2 * 64 * FA_LD;
+      stage64(nxt, K1g, (kt + 1) * 64, a.n, threadIdx.x, nthr);
+      stage64(nxt + 64 * FA_LD, V1g, (kt + 1) * 64, a.n, threadIdx.x, nthr);
+      cp_commit();
+      cp_wait1();
+    } else {
+      cp_wait0();
+    }
+    __syncthreads();
+    const float* Ks = cur;
+    const float* Vs = cur + 64 * FA_LD;
+    if (live) {
+      // scores of the tile's 64 keys: 8 groups of 8 (even / odd k steps apart)
+      float sc[8][4];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        float e[2][4] = {};
+        const float* kr = Ks + (kk * 8 + gq) * FA_LD + 2 * tq;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const float2 kb = *reinterpret_cast<const float2*>(kr + 8 * s2);
+          mma_tf32(e[s2 & 1], qa[s2][0], qa[s2][1], qa[s2][2], qa[s2][3], bits(kb.x), bits(kb.y));
+        }
+        const int k0 = kt * 64 + kk * 8 + 2 * tq, k1 = k0 + 1;
+        sc[kk][0] = k0 <= anc0 ? (e[0][0] + e[1][0]) * a.scale : -INFINITY;
+        sc[kk][1] = k1 <= anc0 ? (e[0][1] + e[1][1]) * a.scale : -INFINITY;
+        sc[kk][2] = k0 <= anc1 ? (e[0][2] + e[1][2]) * a.scale : -INFINITY;
+        sc[kk][3] = k1 <= anc1 ? (e[0][3] + e[1][3]) * a.scale : -INFINITY;
+      }
+      float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        t0 = fmaxf(t0, fmaxf(sc[kk][0], sc[kk][1]));
+        t1 = fmaxf(t1, fmaxf(sc[kk][2], sc[kk][3]));
+      }
+      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, 1));
+      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, 2));
+      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, 1));
+      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, 2));
+      const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+      // rescale what was accumulated (no key yet: nothing to rescale)
+      const float f0 = n0 == -INFINITY ? 1.f : expf(m0 - n0);
+      const float f1 = n1 == -INFINITY ? 1.f : expf(m1 - n1);
+#pragma unroll
+      for (int nn = 0; nn < 8; ++nn) {
+        o[nn][0] *= f0; o[nn][1] *= f0;
+        o[nn][2] *= f1; o[nn][3] *= f1;
+      }
+      l0 *= f0;
+      l1 *= f1;
+      m0 = n0;
+      m1 = n1;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const float p0 = sc[kk][0] == -INFINITY ? 0.f : expf(sc[kk][0] - n0);
+        const float p1 = sc[kk][1] == -INFINITY ? 0.f : expf(sc[kk][1] - n0);
+        const float p2 = sc[kk][2] == -INFINITY ? 0.f : expf(sc[kk][2] - n1);
+        const float p3 = sc[kk][3] == -INFINITY ? 0.f : expf(sc[kk][3] - n1);
+        s0 += p0 + p1;
+        s1 += p2 + p3;
+        // O += P V over these 8 keys: A = P (keys 2tq, 2tq + 1 as k positions tq, tq + 4)
+        const float* vc = Vs + (kk * 8 + 2 * tq) * FA_LD + gq;
+        const uint32_t P0 = tf32(p0), P1 = tf32(p1), P2 = tf32(p2), P3 = tf32(p3);
+#pragma unroll
+        for (int nn = 0; nn < 8; ++nn)
+          mma_tf32(o[nn], P0, P2, P1, P3, bits(vc[8 * nn]), bits(vc[FA_LD + 8 * nn]));
+      }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      l0 += s0;
+      l1 += s1;
+    }
+    __syncthreads();
+  }
+  if (!live) return;
+  float* g0 = Op + ((size_t)h * a.M + r0) * 64;
+  float* g1 = Op + ((size_t)h * a.M + r1) * 64;
+#pragma unroll
+  for (int nn = 0; nn < 8; ++nn) {
+    const int c = 8 * nn + 2 * tq;
+    if (r0 < a.M) { g0[c] = o[nn][0]; g0[c + 1] = o[nn][1]; }
+    if (r1 < a.M) { g1[c] = o[nn][2]; g1[c + 1] = o[nn][3]; }
+  }
+  if (tq == 0) {
+    if (r0 < a.M) { mrow[(size_t)h * a.M + r0] = m0; lrow[(size_t)h * a.M + r0] = l0; }
+    if (r1 < a.M) { mrow[(size_t)h * a.M + r1] = m1; lrow[(size_t)h * a.M + r1] = l1; }
+  }
+}
+
+// One warp per (head, row): the chain keys' scores join the prefix's running max and sum;
+// lse, the chain probabilities Pc and the normalised output row O [M][nq hd].
+__global__ void attn_fwd_combine_kernel(TrainAttn a, const float* Qh, const float* Kr,
+                                        const float* Vr, const float* Op, const float* mrow,
+                                        const float* lrow, float* Pc, float* lse, float* O) {
+  const int lane = threadIdx.x & 31, G = a.nq / a.nkv, K1n = a.K - 1;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= a.nq * a.M) return;
+  const int h = w / a.M, i = w % a.M, g = h / G;
+  const float* q = Qh + ((size_t)h * a.M + i) * 64;
+  float cs[16];
+  float m = mrow[(size_t)h * a.M + i];
+  const float mp = m;
+  for (int t = 0; t < K1n; ++t) {
+    const int r = a.chain[(size_t)i * K1n + t];
+    float sv = -INFINITY;
+    if (r >= 0) {
+      const float* kr = Kr + ((size_t)r * a.nkv + g) * 64;
+      float d = q[lane] * kr[lane] + q[lane + 32] * kr[lane + 32];
+      d = warp_sum(d);
+      sv = d * a.scale;
+    }
+    cs[t] = sv;
+    m = fmaxf(m, sv);
+  }
+  const float fp = (mp == -INFINITY) ? 0.f : expf(mp - m);
+  float l = lrow[(size_t)h * a.M + i] * fp;
+  for (int t = 0; t < K1n; ++t) l += cs[t] == -INFINITY ? 0.f : expf(cs[t] - m);
+  const float L = (l > 0.f) ? m + logf(l) : 0.f;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  float o0 = Op[((size_t)h * a.M + i) * 64 + lane] * fp;
+  float o1 = Op[((size_t)h * a.M + i) * 64 + lane + 32] * fp;
+  for (int t = 0; t < K1n; ++t) {
+    const int r = a.chain[(size_t)i * K1n + t];
+    if (r < 0) continue;
+    const float pw = expf(cs[t] - m);
+    const float* vr = Vr + ((size_t)r * a.nkv + g) * 64;
+    o0 += pw * vr[lane];
+    o1 += pw * vr[lane + 32];
+  }
+  float* orow = O + (size_t)i * a.nq * 64 + h * 64;
+  orow[lane] = o0 * inv;
+  orow[lane + 32] = o1 * inv;
+  if (lane < K1n)
+    Pc[((size_t)h * a.M + i) * K1n + lane] = cs[lane] == -INFINITY ? 0.f : expf(cs[lane] - L);
+  if (lane == 0) lse[(size_t)h * a.M + i] = L;
+}
+
 }  // namespace
 
 bool attn_bwd_fused_ok(const TrainAttn& a) {
@@ -354,10 +543,29 @@ bool attn_bwd_fused_ok(const TrainAttn& a) {
   return a.hd == 64 && G >= 1 && G <= 8;
 }
 
+void launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
+                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
+                           float* lse, float* O, cudaStream_t s) {
+  const int G = a.nq / a.nkv;
+  round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, Qh);
+  for (float* p : {K1, V1}) round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
+  const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(attn_fwd_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    attr_set = true;
+  }
+  attn_fwd_prefix_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, K1, V1, Op,
+                                                                           mrow, lrow);
+  attn_fwd_combine_kernel<<<(a.nq * a.M + 7) / 8, 256, 0, s>>>(a, Qh, Kr, Vr, Op, mrow, lrow, Pc,
+                                                              lse, O);
+}
+
 void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
                            const float* dOh, const float* K1, const float* V1,
                            const float* lse, const float* Dv, float* dQh, float* dK1,
-                           float* dV1, cudaStream_t s) {
+                           float* dV1, bool qkv_rounded, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
   static bool attr_set = false;
@@ -366,9 +574,14 @@ void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, c
                          (int)smem);
     attr_set = true;
   }
-  // the stored operands are rounded to TF32 once here, not per use in the products
-  for (float* p : {(float*)Qh, (float*)dOh}) round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, p);
-  for (float* p : {(float*)K1, (float*)V1}) round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
+  // the stored operands are rounded to TF32 once, not per use in the products (Q, K1 and
+  // V1 already are when the forward ran fused)
+  round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)dOh);
+  if (!qkv_rounded) {
+    round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)Qh);
+    for (float* p : {(float*)K1, (float*)V1})
+      round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
+  }
   attn_bwd_dq_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, dOh, K1, V1, lse,
                                                                        Dv, dQh);
   attn_bwd_dkv_kernel<<<dim3((a.n + 63) / 64, a.nkv, (a.M + DKV_CHUNK - 1) / DKV_CHUNK), 128, 0,

@@ -56,13 +56,19 @@ void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, 
                         cudaStream_t s);
 // Fused prefix-attention backward on TF32 tensor cores (train_attn_mma.cu), for head_dim
 // 64 and at most 8 q heads per kv head: dQh += dS K1 (dQh holds the chain part) and
-// dK1 / dV1 (zero beforehand) += dS^T Q / P^T dO; row_index as from rows-prepare.  Qh,
-// dOh, K1 and V1 are rounded to TF32 in place first.
+// dK1 / dV1 (zero beforehand) += dS^T Q / P^T dO; row_index as from rows-prepare.  dOh
+// (and Qh, K1, V1 unless qkv_rounded) are rounded to TF32 in place first.
 bool attn_bwd_fused_ok(const TrainAttn& a);
+// The forward the same way (Q, K1, V1 rounded to TF32 in place first): the prefix's unnormalised
+// output Op (per-head rows [nq][M][64]) with its row max / sum, then the chain keys joined
+// per row: lse, Pc and O [M][nq hd].
+void launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
+                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
+                           float* lse, float* O, cudaStream_t s);
 void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
                            const float* dOh, const float* K1, const float* V1,
                            const float* lse, const float* Dv, float* dQh, float* dK1,
-                           float* dV1, cudaStream_t s);
+                           float* dV1, bool qkv_rounded, cudaStream_t s);
 void launch_ce(int M, int V, float* logits, const int* labels, float* row_loss, float* loss,
                unsigned* err, cudaStream_t s);
 void launch_embed_grad(int M, int n, int K, int H, int Vt, const int* row_p, const int* row_d,
