@@ -1081,7 +1081,7 @@ static int train_ws(peagle_ctx* c) {
   if (c->tw) return PEAGLE_OK;
   const peagle_dims& d = c->d;
   const int M = d.max_rows, n = d.max_seq, H = d.hidden, I = d.intermediate;
-  const int nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, G = nq / nkv;
+  const int nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
   const int qkv_out = (nq + 2 * nkv) * hd, N = d.n_layers, Vd = d.draft_vocab;
   // built aside and attached only when complete (a failed call leaves no half workspace;
   // what it allocated stays on the context's list and is freed with it)
