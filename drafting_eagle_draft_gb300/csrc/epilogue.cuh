@@ -214,27 +214,32 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
     case EPI_QKV_FX: {
       // RoPE is a rotation and the row scale a constant, so each split-K partial can be
       // rotated, scaled and added on its own: the fixed-point sums are exact and the same
-      // for any order of arrival.  One output feature per thread; the RoPE factors of
-      // eight rows are fetched before any of them is used.
+      // for any order of arrival.  One output feature per thread; the positions of sixteen
+      // rows are fetched together, then their RoPE factors together, so a chunk of rows
+      // waits for two dependent loads rather than two per row.
       const int hd = a.hd, half = hd >> 1;
       const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd, kvw = a.nkv * hd;
+      constexpr int U = 16;
       for (int ml = tid; ml < mcount; ml += nthr) {
         const int m = m0 + ml;
         const int i = m % hd;
         const int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
         if (sec != 2 && i >= half) continue;  // handled together with its pair partner
-        for (int t0 = 0; t0 < rcount; t0 += 8) {
-          float2 cs[8];
+        for (int t0 = 0; t0 < rcount; t0 += U) {
+          int pos[U];
+          float2 cs[U];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < U; ++u) {
             const int ti = t0 + u;
-            int pos = -1;
-            if (sec != 2 && ti < rcount) pos = rpos ? rpos[ti] : __ldg(a.row_pos + r0 + ti);
-            cs[u] = (pos >= 0 && pos < a.max_pos) ? __ldg(a.rope + (size_t)pos * half + i)
-                                                  : make_float2(1.f, 0.f);
+            pos[u] = -1;
+            if (sec != 2 && ti < rcount) pos[u] = rpos ? rpos[ti] : __ldg(a.row_pos + r0 + ti);
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < U; ++u)
+            cs[u] = (pos[u] >= 0 && pos[u] < a.max_pos) ? __ldg(a.rope + (size_t)pos[u] * half + i)
+                                                        : make_float2(1.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
             const int ti = t0 + u;
             if (ti >= rcount) break;
             const int r = r0 + ti;

@@ -330,6 +330,51 @@ __global__ void __launch_bounds__(128) rmsnorm_v8_kernel(int H, const fx_t* __re
   }
 }
 
+// Fixed-point q / k / v of one layer (the additive QKV epilogue's sums) -> fp32 queries
+// [R][nq hd] and the bf16 KV cache slot row_pos[r] of request r / K; the accumulators are
+// cleared for the next layer.  A row without a cache slot raises KV_OVERFLOW and keeps
+// its query.
+__global__ void __launch_bounds__(256) qkv_finalize_kernel(int R, int K, int nq, int nkv, int hd,
+                                                           int cap, fx_t* q_fx, fx_t* kv_fx,
+                                                           float* Qf, bf16* kc, bf16* vc,
+                                                           const int* row_pos, unsigned* err) {
+  pdl_enter();
+  const int qw = nq * hd, kvw = nkv * hd;
+  const long long nQ = (long long)R * qw, nKV = (long long)R * 2 * kvw;
+  const long long nthr = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nQ + nKV; i += nthr) {
+    if (i < nQ) {
+      Qf[i] = from_fx(q_fx[i]);
+      q_fx[i] = 0;
+      continue;
+    }
+    const long long j = i - nQ;
+    const int r = (int)(j / (2 * kvw)), rem = (int)(j - (long long)r * 2 * kvw);
+    const int sec = rem / kvw, gk = rem - sec * kvw;
+    const int g = gk / hd, e = gk - g * hd;
+    const int pos = row_pos[r];
+    const float v = from_fx(kv_fx[j]);
+    kv_fx[j] = 0;
+    if (pos < 0 || pos >= cap) {
+      if (rem == 0) raise_error(err, PEAGLE_DEV_KV_OVERFLOW);
+      continue;
+    }
+    bf16* dst = sec == 0 ? kc : vc;
+    dst[(((size_t)(r / K) * nkv + g) * cap + pos) * hd + e] = __float2bfloat16_rn(v);
+  }
+}
+
+void launch_qkv_finalize(int R, int K, int nq, int nkv, int hd, int cap, fx_t* q_fx, fx_t* kv_fx,
+                         float* Qf, void* kc, void* vc, const int* row_pos, unsigned* err,
+                         int num_sms, cudaStream_t s) {
+  const long long n = (long long)R * (nq + 2 * nkv) * hd;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
+  if (blocks < 1) blocks = 1;
+  launch_pdl(qkv_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, s, R, K, nq, nkv, hd, cap,
+             q_fx, kv_fx, Qf, (bf16*)kc, (bf16*)vc, row_pos, err);
+}
+
 void launch_rmsnorm(bool bf16m, int R, int H, const fx_t* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s) {
   if (bf16m && H % 8 == 0 && H <= 16 * 128 * 8) {

@@ -55,6 +55,12 @@ void launch_input_fusion(bool bf16, int mode, int R, int K, int n_src, int H, co
 void launch_rmsnorm(bool bf16, int R, int H, const fx_t* res, const void* gamma, float eps,
                     int split, void* out, cudaStream_t s);
 
+// bf16 draft pass: fixed-point q / k,v sums of one layer -> fp32 queries and the KV cache
+// slots row_pos[r]; clears the sums
+void launch_qkv_finalize(int R, int K, int nq, int nkv, int hd, int cap, fx_t* q_fx, fx_t* kv_fx,
+                         float* Qf, void* kc, void* vc, const int* row_pos, unsigned* err,
+                         int num_sms, cudaStream_t s);
+
 void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);
 
 void launch_masked_attention(bool bf16, const MaskedAttnArgs& a, cudaStream_t s);

@@ -98,6 +98,8 @@ struct peagle_ctx {
   fx_t* pass_ss;    // [PASS_SS_SLOTS][PASS_MAX_ROWS] row sums of squares
   fx_t* pass_qfx;   // [PASS_MAX_ROWS, nq*hd] fixed-point queries
   fx_t* pass_kvfx;  // [PASS_MAX_ROWS][2][nkv*hd] fixed-point keys / values
+  fx_t* mk_qfx;     // bf16 multi-kernel pass: [max_batch*max_K, nq*hd] fixed-point queries
+  fx_t* mk_kvfx;    // and [max_batch*max_K][2][nkv*hd] keys / values (zero between layers)
   unsigned long long* pass_trace;
   std::vector<std::vector<int>> trace_stages;
   unsigned long long* pass_trace_cta;  // per-CTA signal times of the latest traced pass
@@ -349,6 +351,12 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   TRY(dalloc(c, &c->act, (size_t)R * I * es));
   TRY(dalloc(c, (void**)&c->keys, (size_t)R * 8));
   TRY(dalloc(c, (void**)&c->row_pos, (size_t)d.max_batch * d.max_K * 4));
+  c->mk_qfx = nullptr;
+  c->mk_kvfx = nullptr;
+  if (c->bf) {
+    TRY(dalloc(c, (void**)&c->mk_qfx, (size_t)d.max_batch * d.max_K * nq * hd * 8));
+    TRY(dalloc(c, (void**)&c->mk_kvfx, (size_t)d.max_batch * d.max_K * 2 * nkv * hd * 8));
+  }
   TRY(dalloc(c, (void**)&c->err, 64));
   int max_out = qkv_out;
   if (2 * I > max_out) max_out = 2 * I;
@@ -784,7 +792,10 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
                             c->hidden_norm, d.rms_eps, split, c->X0, c->res, c->keys, seq_lens,
                             c->row_pos, c->err, s));
   int chunk, nchunk;
-  attention_plan(c, batch, attention_span(c, kv->capacity, K), &chunk, &nchunk);
+  // about four items per SM: ragged contexts leave many items of a longer request than
+  // average, and finer chunks spread them (ragged_b16: 449 us of attention with two items
+  // per SM, 303 with four)
+  attention_plan(c, batch, attention_span(c, kv->capacity, K), &chunk, &nchunk, 4);
   for (int l = 0; l < d.n_layers; ++l) {
     const void* a_in = c->X0;
     int din = 2 * H;
@@ -794,8 +805,21 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       a_in = c->Xn;
       din = H;
     }
-    // S2: QKV projection + RoPE; k/v of row j go to cache slot seq_lens[b] + j
-    {
+    // S2: QKV projection + RoPE; k/v of row j go to cache slot seq_lens[b] + j.  bf16: the
+    // additive fixed-point epilogue (every split-K contributor rotates and adds its own
+    // partial, no cross-CTA reduction of partials), then one pass converts the sums
+    if (c->bf) {
+      EpiArgs e = epi_base(c, EPI_QKV_FX, R, qkv_out);
+      e.in_split = split;
+      e.q_fx = c->mk_qfx;
+      e.kv_fx = c->mk_kvfx;
+      e.row_pos = c->row_pos;
+      GEMM(PEAGLE_STAGE_QKV, c, c->qkv[l], a_in, din, qkv_out, din, R, e, s);
+      TIMED(PEAGLE_STAGE_QKV,
+            launch_qkv_finalize(R, K, nq, nkv, hd, kv->capacity, c->mk_qfx, c->mk_kvfx, c->Qf,
+                                (char*)kv->k + l * layer_stride, (char*)kv->v + l * layer_stride,
+                                c->row_pos, c->err, c->num_sms, s));
+    } else {
       EpiArgs e = epi_base(c, EPI_QKV_ROPE, R, qkv_out);
       e.in_split = split;
       e.q_out = c->Qf;
