@@ -214,9 +214,10 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
     case EPI_QKV_FX: {
       // RoPE is a rotation and the row scale a constant, so each split-K partial can be
       // rotated, scaled and added on its own: the fixed-point sums are exact and the same
-      // for any order of arrival.  One output feature per thread; the positions of sixteen
-      // rows are fetched together, then their RoPE factors together, so a chunk of rows
-      // waits for two dependent loads rather than two per row.
+      // for any order of arrival.  One output feature per thread, its rotation partner
+      // (i +- hd/2, same head, same tile) read from the tile: every thread adds one value
+      // per row.  The positions of sixteen rows are fetched together, then their RoPE
+      // factors together, so a batch of rows waits for two dependent loads.
       const int hd = a.hd, half = hd >> 1;
       const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd, kvw = a.nkv * hd;
       constexpr int U = 16;
@@ -224,7 +225,13 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
         const int m = m0 + ml;
         const int i = m % hd;
         const int sec = (m < qend) ? 0 : (m < kend ? 1 : 2);
-        if (sec != 2 && i >= half) continue;  // handled together with its pair partner
+        const bool first = i < half;  // i < hd/2: out = x_i c - x_{i+h} s, else x_i c + x_{i-h} s
+        const int ip = first ? i : i - half;
+        const int mlp = first ? ml + half : ml - half;
+        fx_t* dst = sec == 0 ? a.q_fx + m
+                    : sec == 1 ? a.kv_fx + (m - qend)
+                               : a.kv_fx + kvw + (m - kend);
+        const size_t ld = sec == 0 ? (size_t)qend : (size_t)2 * kvw;
         for (int t0 = 0; t0 < rcount; t0 += U) {
           int pos[U];
           float2 cs[U];
@@ -236,7 +243,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
           }
 #pragma unroll
           for (int u = 0; u < U; ++u)
-            cs[u] = (pos[u] >= 0 && pos[u] < a.max_pos) ? __ldg(a.rope + (size_t)pos[u] * half + i)
+            cs[u] = (pos[u] >= 0 && pos[u] < a.max_pos) ? __ldg(a.rope + (size_t)pos[u] * half + ip)
                                                         : make_float2(1.f, 0.f);
 #pragma unroll
           for (int u = 0; u < U; ++u) {
@@ -244,18 +251,13 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
             if (ti >= rcount) break;
             const int r = r0 + ti;
             const float sc = rsc(ti);
-            const float v0 = val(ti, ml) * sc;
-            if (sec == 2) {
-              red_add_fx(a.kv_fx + ((size_t)r * 2 + 1) * kvw + (m - kend), to_fx(v0));
-              continue;
+            const float x = val(ti, ml) * sc;
+            float out = x;
+            if (sec != 2) {
+              const float xp = val(ti, mlp) * sc;
+              out = first ? x * cs[u].x - xp * cs[u].y : x * cs[u].x + xp * cs[u].y;
             }
-            const float v1 = val(ti, ml + half) * sc;
-            const float out0 = v0 * cs[u].x - v1 * cs[u].y;
-            const float out1 = v1 * cs[u].x + v0 * cs[u].y;
-            fx_t* dst = sec == 0 ? a.q_fx + (size_t)r * qend + m
-                                 : a.kv_fx + (size_t)r * 2 * kvw + (m - qend);
-            red_add_fx(dst, to_fx(out0));
-            red_add_fx(dst + half, to_fx(out1));
+            red_add_fx(dst + (size_t)r * ld, to_fx(out));
           }
         }
       }

@@ -326,41 +326,59 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
       const int nch = (lrows + step - 1) / step;
       if (cf == cl || p.additive) {
         // ---- sole owner, or an additive epilogue (each contributor adds its own partial):
-        //      TMEM -> staging -> epilogue
+        //      TMEM -> staging -> epilogue.  The fixed-point adds (residual, fc output) are
+        //      elementwise: each thread adds its own feature's rows straight from the
+        //      registers it loaded, with no staging and no group barrier.
+        const bool direct = epi.kind == EPI_RESID || epi.kind == EPI_STORE;
+        constexpr int HALF = 16 / NEG;  // TMEM columns per load
         for (int ch = eg; ch < nch; ch += NEG) {
           const int i0 = ch * step;
-          if (NEG == 1) {
-            float v[16], w[16];
+          float v[HALF], w[HALF];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = 0.f;
+          for (int j = 0; j < HALF; ++j) w[j] = 0.f;
+          if (NEG == 1) {
             tc::tmem_ld16(tb + i0, v);
             if (p.split) {
               tc::tmem_ld16(tb + p.lo_col + i0, w);
             } else if (i0 + 16 < p.BN) {
               tc::tmem_ld16(tb + i0 + 16, w);
             }
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              gstg[j * 128 + ml] = v[j];
-              gstg[(16 + j) * 128 + ml] = w[j];
-            }
           } else {
-            float v[8], w[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = 0.f;
             tc::tmem_ld8(tb + i0, v);
             if (p.split) {
               tc::tmem_ld8(tb + p.lo_col + i0, w);
             } else if (i0 + 8 < p.BN) {
               tc::tmem_ld8(tb + i0 + 8, w);
             }
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              gstg[j * 128 + ml] = v[j];
-              gstg[(8 + j) * 128 + ml] = w[j];
+          }
+          tc::tmem_ld_wait();
+          if (direct) {
+            if (ch + NEG >= nch) {  // this group's last TMEM read of the segment
+              tc::fence_before_sync();
+              tc::mbar_arrive(&acce[buf]);
             }
+            const int m = m0 + ml;
+            const int rc = min(step, lrows - i0);
+            fx_t* dst = epi.kind == EPI_STORE ? epi.out_fx : epi.resid;
+            const int ldd = epi.kind == EPI_STORE ? epi.out_ld : epi.ld_res;
+            if (m < epi.Nout) {
+              fx_t* col = dst + (size_t)(row0 + i0) * ldd + m;
+#pragma unroll
+              for (int j = 0; j < HALF; ++j) {
+                if (p.split) {
+                  if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j] + w[j]));
+                } else {
+                  if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j]));
+                  if (HALF + j < rc) red_add_fx(col + (size_t)(HALF + j) * ldd, to_fx(w[j]));
+                }
+              }
+            }
+            continue;
+          }
+#pragma unroll
+          for (int j = 0; j < HALF; ++j) {
+            gstg[j * 128 + ml] = v[j];
+            gstg[(HALF + j) * 128 + ml] = w[j];
           }
           if (ch + NEG >= nch) {  // this group's last TMEM read of the segment
             tc::fence_before_sync();
@@ -913,8 +931,10 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, mw, mx, q, epi);
     return e == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
   }
-  // large-M projections are tensor-bound: two epilogue groups keep up with the MMA
-  const int neg = p.n_tiles > 1 ? 2 : 1;
+  // large-M projections are tensor-bound: two epilogue groups keep up with the MMA; a
+  // single tile of 64+ rows (hi + lo operand rows >= 128) also drains faster with two
+  // (ragged batch of 16 x K=5, 80 rows: 1285 -> 1214 us per pass)
+  const int neg = (p.n_tiles > 1 || p.BN >= 128) ? 2 : 1;
   const int m_tiles = (Nout + 127) / 128;
   const long long tiles = (long long)m_tiles * p.n_tiles;
   p.m_tiles = m_tiles;
@@ -928,7 +948,10 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   }
   if (tiles > pl->max_tiles || Kd % 64) return PEAGLE_ERR_CAPACITY;
   p.G = (int)(tiles * p.KB < pl->num_sms ? tiles * p.KB : pl->num_sms);
-  p.dp_waves = p.n_tiles > 1 ? (int)(tiles / p.G) : 0;
+  // whole-tile waves first: large-M GEMMs (L2 reuse), and single-tile GEMMs of 64+ rows
+  // whose epilogue needs whole tiles (a shared tile costs a partial of BN x 128 fp32 per
+  // contributor, 80 KB at 80 rows)
+  p.dp_waves = (p.n_tiles > 1 || (!p.additive && p.BN >= 128)) ? (int)(tiles / p.G) : 0;
   p.total = (tiles - (long long)p.dp_waves * p.G) * p.KB;
   // shared memory ring: decode-sized tiles keep ~110 KB so a second CTA (the next
   // kernel's, under programmatic dependent launch) fits on the SM; large tiles take more

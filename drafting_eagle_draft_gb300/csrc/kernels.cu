@@ -333,46 +333,45 @@ __global__ void __launch_bounds__(128) rmsnorm_v8_kernel(int H, const fx_t* __re
 // Fixed-point q / k / v of one layer (the additive QKV epilogue's sums) -> fp32 queries
 // [R][nq hd] and the bf16 KV cache slot row_pos[r] of request r / K; the accumulators are
 // cleared for the next layer.  A row without a cache slot raises KV_OVERFLOW and keeps
-// its query.
-__global__ void __launch_bounds__(256) qkv_finalize_kernel(int R, int K, int nq, int nkv, int hd,
-                                                           int cap, fx_t* q_fx, fx_t* kv_fx,
-                                                           float* Qf, bf16* kc, bf16* vc,
+// its query.  Thread = two neighbouring features of row blockIdx.y (16-byte loads; a pair
+// never straddles q / k / v or a head, all widths being even).
+__global__ void __launch_bounds__(256) qkv_finalize_kernel(int K, int nq, int nkv, int hd, int cap,
+                                                           fx_t* q_fx, fx_t* kv_fx, float* Qf,
+                                                           bf16* kc, bf16* vc,
                                                            const int* row_pos, unsigned* err) {
   pdl_enter();
+  const int r = blockIdx.y;
   const int qw = nq * hd, kvw = nkv * hd;
-  const long long nQ = (long long)R * qw, nKV = (long long)R * 2 * kvw;
-  const long long nthr = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nQ + nKV; i += nthr) {
-    if (i < nQ) {
-      Qf[i] = from_fx(q_fx[i]);
-      q_fx[i] = 0;
-      continue;
-    }
-    const long long j = i - nQ;
-    const int r = (int)(j / (2 * kvw)), rem = (int)(j - (long long)r * 2 * kvw);
-    const int sec = rem / kvw, gk = rem - sec * kvw;
-    const int g = gk / hd, e = gk - g * hd;
-    const int pos = row_pos[r];
-    const float v = from_fx(kv_fx[j]);
-    kv_fx[j] = 0;
-    if (pos < 0 || pos >= cap) {
-      if (rem == 0) raise_error(err, PEAGLE_DEV_KV_OVERFLOW);
-      continue;
-    }
-    bf16* dst = sec == 0 ? kc : vc;
-    dst[(((size_t)(r / K) * nkv + g) * cap + pos) * hd + e] = __float2bfloat16_rn(v);
+  const int e = 2 * (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  if (e >= qw + 2 * kvw) return;
+  if (e < qw) {
+    longlong2* src = (longlong2*)(q_fx + (size_t)r * qw + e);
+    const longlong2 v = *src;
+    *src = make_longlong2(0, 0);
+    *(float2*)(Qf + (size_t)r * qw + e) = make_float2(from_fx(v.x), from_fx(v.y));
+    return;
   }
+  const int rem = e - qw;  // keys [0, kvw), values [kvw, 2 kvw)
+  longlong2* src = (longlong2*)(kv_fx + (size_t)r * 2 * kvw + rem);
+  const longlong2 v = *src;
+  *src = make_longlong2(0, 0);
+  const int pos = row_pos[r];
+  if (pos < 0 || pos >= cap) {
+    if (rem == 0) raise_error(err, PEAGLE_DEV_KV_OVERFLOW);
+    return;
+  }
+  const int sec = rem >= kvw ? 1 : 0, gk = rem - sec * kvw;
+  const int g = gk / hd, i = gk - g * hd;
+  bf16* dst = (sec ? vc : kc) + (((size_t)(r / K) * nkv + g) * cap + pos) * hd + i;
+  *(__nv_bfloat162*)dst = __floats2bfloat162_rn(from_fx(v.x), from_fx(v.y));
 }
 
 void launch_qkv_finalize(int R, int K, int nq, int nkv, int hd, int cap, fx_t* q_fx, fx_t* kv_fx,
                          float* Qf, void* kc, void* vc, const int* row_pos, unsigned* err,
-                         int num_sms, cudaStream_t s) {
-  const long long n = (long long)R * (nq + 2 * nkv) * hd;
-  long long blocks = (n + 255) / 256;
-  if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
-  if (blocks < 1) blocks = 1;
-  launch_pdl(qkv_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, s, R, K, nq, nkv, hd, cap,
-             q_fx, kv_fx, Qf, (bf16*)kc, (bf16*)vc, row_pos, err);
+                         cudaStream_t s) {
+  const int pairs = (nq + 2 * nkv) * hd / 2;
+  launch_pdl(qkv_finalize_kernel, dim3((unsigned)cdiv(pairs, 256), (unsigned)R), dim3(256), 0, s, K,
+             nq, nkv, hd, cap, q_fx, kv_fx, Qf, (bf16*)kc, (bf16*)vc, row_pos, err);
 }
 
 void launch_rmsnorm(bool bf16m, int R, int H, const fx_t* res, const void* gamma, float eps,

@@ -59,7 +59,7 @@ void launch_rmsnorm(bool bf16, int R, int H, const fx_t* res, const void* gamma,
 // slots row_pos[r]; clears the sums
 void launch_qkv_finalize(int R, int K, int nq, int nkv, int hd, int cap, fx_t* q_fx, fx_t* kv_fx,
                          float* Qf, void* kc, void* vc, const int* row_pos, unsigned* err,
-                         int num_sms, cudaStream_t s);
+                         cudaStream_t s);
 
 void launch_attention_decode(bool bf16, const AttnArgs& a, cudaStream_t s);
 

@@ -818,7 +818,7 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
       TIMED(PEAGLE_STAGE_QKV,
             launch_qkv_finalize(R, K, nq, nkv, hd, kv->capacity, c->mk_qfx, c->mk_kvfx, c->Qf,
                                 (char*)kv->k + l * layer_stride, (char*)kv->v + l * layer_stride,
-                                c->row_pos, c->err, c->num_sms, s));
+                                c->row_pos, c->err, s));
     } else {
       EpiArgs e = epi_base(c, EPI_QKV_ROPE, R, qkv_out);
       e.in_split = split;

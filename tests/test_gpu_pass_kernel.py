@@ -71,13 +71,17 @@ def test_pass_kernel_decode_b1_repeat_deterministic():
     compare(dims, ref, t1, l1, "pass kernel decode_b1")
 
 
-def test_pass_kernel_device_checks():
+@pytest.mark.parametrize("use_pass", [True, False])
+def test_bf16_device_checks(use_pass):
+    """Bad token and KV overflow are latched by the pass kernel and by the bf16 multi-kernel
+    path (whose fixed-point q / k,v sums are cleared even for rows without a cache slot);
+    a valid pass afterwards matches the oracle."""
     m = pk()
     dims = SMALL_BF16
     wl = synth.Workload("s", dims, 1, 4, (10,))
     w = synth.make_weights(dims, 5)
     inp = synth.make_decode_inputs(wl, 6, capacity=16)
-    ctx = make_ctx(dims, w, 1, 8, 64, pass_kernel=True)
+    ctx = make_ctx(dims, w, 1, 8, 64, pass_kernel=use_pass)
     d = to_dev(inp)
     kv = m.kv_struct(d["ck"], d["cv"], 16, 1)
     toks = torch.empty(1, 4, dtype=torch.int32, device="cuda")
@@ -91,5 +95,5 @@ def test_pass_kernel_device_checks():
     assert m.peagle_device_error_bits(ctx) & m.PEAGLE_DEV_KV_OVERFLOW
     toks2, lg, _ = run_draft(ctx, dims, inp, 4)
     ref = oracle_draft(dims, w, inp, 4)
-    compare(dims, ref, toks2, lg, "pass kernel after errors")
+    compare(dims, ref, toks2, lg, f"after errors (pass kernel {use_pass})")
     ctx.close()
