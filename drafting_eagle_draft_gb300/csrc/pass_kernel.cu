@@ -658,6 +658,29 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                   tc::tmem_ld16(tb + i0 + 16, w);
                 }
                 tc::tmem_ld_wait();
+                if (epi.kind == EPI_RESID || epi.kind == EPI_STORE) {
+                  // elementwise fixed-point adds: straight from the registers, no staging
+                  if (ch == nch - 1) {
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(&acce[buf]);
+                  }
+                  const int rc = min(step, lrows - i0);
+                  fx_t* dst = epi.kind == EPI_STORE ? epi.out_fx : epi.resid;
+                  const int ldd = epi.kind == EPI_STORE ? epi.out_ld : epi.ld_res;
+                  if (m0 + ml < epi.Nout) {
+                    fx_t* col = dst + (size_t)(row0 + i0) * ldd + m0 + ml;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                      if (split) {
+                        if (q < rc) red_add_fx(col + (size_t)q * ldd, to_fx(v[q] + w[q]));
+                      } else {
+                        if (q < rc) red_add_fx(col + (size_t)q * ldd, to_fx(v[q]));
+                        if (16 + q < rc) red_add_fx(col + (size_t)(16 + q) * ldd, to_fx(w[q]));
+                      }
+                    }
+                  }
+                  continue;
+                }
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                   stg[q * 128 + ml] = v[q];
