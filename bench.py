@@ -146,7 +146,7 @@ class ClockSampler:
 
 # DRAM bytes (read + write) of one pass-kernel launch on decode_b1, from the ncu capture
 # summarised in profiles/pass_kernel_decode_b1.md (dram__bytes_read.sum + _write.sum)
-PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_054_971_728
+PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_054_574_336
 
 
 def gemm_weight_bytes(dims) -> int:
