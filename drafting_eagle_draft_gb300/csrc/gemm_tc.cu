@@ -49,6 +49,10 @@ struct TcParams {
   int rpt;      // logical rows per tile
   int lo_col;   // split: TMEM column of the lo part of tile row 0
   int two_box;  // split with several tiles: hi and lo rows come from two 128-row boxes
+  int b_rows;   // operand rows per stage (one box): BN, or 2R when folded
+  int mt;       // 128-row weight sub-tiles per tile (1 or 2), all against the same operand
+  int fold;     // split single tile: the MMA adds the hi and the lo products into the same
+                // R accumulator columns (two MMAs per k-step), so BN = R
   int n_tiles;  // row tiles
   int m_tiles;  // 128-feature weight tiles
   int m_inner;  // tile order: weight tiles vary fastest (the weights are re-read per row
@@ -139,7 +143,7 @@ __device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* m, int k
     tc::tma_load_2d(dst, m, kb * 64, nt * 128, bar, pol);
     tc::tma_load_2d(dst + 128 * 128, m, kb * 64, p.R + nt * 128, bar, pol);
   } else {
-    tc::tma_load_2d(dst, m, kb * 64, nt * p.BN, bar, pol);
+    tc::tma_load_2d(dst, m, kb * 64, nt * p.b_rows, bar, pol);
   }
 }
 
@@ -154,9 +158,10 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
-  const int B_BYTES = p.BN * 128;
+  const int B_BYTES = p.b_rows * 128;
+  const int AS_BYTES = p.mt * A_BYTES;  // weight bytes per stage
   uint8_t* sA = smem;
-  uint8_t* sB = sA + (size_t)S * A_BYTES;
+  uint8_t* sB = sA + (size_t)S * AS_BYTES;
   float* stg = (float*)(sB + (size_t)S * B_BYTES);  // [32][128] fp32 epilogue staging
   uint64_t* full = (uint64_t*)((uint8_t*)stg + STAGE_F_BYTES);
   uint64_t* empty = full + S;
@@ -203,15 +208,16 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
       // weight tiles vary fastest
       const uint64_t pol_w = p.m_inner ? tc::policy_evict_last() : tc::policy_evict_first();
       const uint64_t pol_x = p.m_inner ? tc::policy_evict_first() : tc::policy_evict_last();
-      const uint32_t bytes = A_BYTES + B_BYTES;
+      const uint32_t bytes = AS_BYTES + B_BYTES;
       const long long n_it = wk.n;
       const int npre = (int)(n_it < S ? n_it : S);
       for (int i = 0; i < npre; ++i) {
         int kb;
         const int tile = work_tile(p, wk, c, i, &kb, nullptr);
         tc::mbar_expect_tx(&full[i], bytes);
-        tc::tma_load_2d(sA + (size_t)i * A_BYTES, &tmW, kb * 64, tile_m(tile, p) * 128, &full[i],
-                        pol_w);
+        for (int h = 0; h < p.mt; ++h)
+          tc::tma_load_2d(sA + (size_t)i * AS_BYTES + h * A_BYTES, &tmW, kb * 64,
+                          (tile_m(tile, p) * p.mt + h) * 128, &full[i], pol_w);
       }
       tc::pdl_wait();
       for (int i = 0; i < npre; ++i) {
@@ -230,8 +236,9 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
         int kb;
         const int tile = work_tile(p, wk, c, it, &kb, nullptr);
         tc::mbar_expect_tx(&full[stage], bytes);
-        tc::tma_load_2d(sA + (size_t)stage * A_BYTES, &tmW, kb * 64, tile_m(tile, p) * 128,
-                        &full[stage], pol_w);
+        for (int h = 0; h < p.mt; ++h)
+          tc::tma_load_2d(sA + (size_t)stage * AS_BYTES + h * A_BYTES, &tmW, kb * 64,
+                          (tile_m(tile, p) * p.mt + h) * 128, &full[stage], pol_w);
         load_b(sB + (size_t)stage * B_BYTES, &tmX, kb, tile_n(tile, p), &full[stage], pol_x, p);
         if (++stage == S) {
           stage = 0;
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
           break;
         }
         tc::fence_after_sync();
-        const uint32_t d = tmem + (uint32_t)(buf * p.BN);
+        const uint32_t d = tmem + (uint32_t)(buf * p.mt * p.BN);
         const long long seg_beg = it;
         for (; it < seg_end; ++it) {
           if (!tc::mbar_wait(&full[stage], ph, s_abort)) {
@@ -269,11 +276,20 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
             break;
           }
           tc::fence_after_sync();
-          const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)stage * A_BYTES));
           const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)stage * B_BYTES));
+          // folded: the lo rows start R rows (R * 128 bytes, whole swizzle atoms) later
+          const uint64_t bl = tc::smem_desc_sw128(
+              tc::smem_u32(sB + (size_t)stage * B_BYTES + (size_t)p.R * 128));
+          for (int h = 0; h < p.mt; ++h) {
+            const uint32_t dh = d + (uint32_t)(h * p.BN);
+            const uint64_t ah = tc::smem_desc_sw128(
+                tc::smem_u32(sA + (size_t)stage * AS_BYTES + (size_t)h * A_BYTES));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (it != seg_beg || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              tc::mma_bf16(dh, ah + 2 * k, bd + 2 * k, idesc, (it != seg_beg || k > 0) ? 1u : 0u);
+              if (p.fold) tc::mma_bf16(dh, ah + 2 * k, bl + 2 * k, idesc, 1u);
+            }
+          }
           tc::mma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
@@ -313,17 +329,22 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
       if (*s_abort) break;
       tc::fence_after_sync();
       const int mt = tile_m(tile, p), nt = tile_n(tile, p);
-      const int m0 = mt * 128;
       const int row0 = nt * p.rpt;               // first logical row of this tile
       const int lrows = min(p.rpt, R - row0);    // logical rows in this tile
       const long long t_beg = (long long)(tile - p.dp_waves * p.G) * KB;  // stream-K space
       const int cf = whole ? c : owner_of(t_beg, p);
       const int cl = whole ? c : owner_of(t_beg + KB - 1, p);
-      const uint32_t tb = tmem + (uint32_t)(buf * p.BN) + ((uint32_t)(quarter * 32) << 16);
+      // hi and lo products in separate TMEM columns (split), or summed by the MMA (fold)
+      const int sp = (p.split && !p.fold) ? 1 : 0;
+      // sub-tile h (128 weight rows) of this tile: TMEM columns [h BN, (h+1) BN) of the buffer
+      const uint32_t tb0 =
+          tmem + (uint32_t)(buf * p.mt * p.BN) + ((uint32_t)(quarter * 32) << 16);
       // chunking: split tiles take 16 / NEG logical rows per chunk (hi + lo columns), others
       // 32 / NEG; chunk ch belongs to group ch % NEG
-      const int step = (p.split ? 16 : 32) / NEG;
+      const int step = (sp ? 16 : 32) / NEG;
       const int nch = (lrows + step - 1) / step;
+      // sub-tiles holding output features (a last tile may have one past Nout)
+      const int nh = min(p.mt, (epi.Nout - mt * p.mt * 128 + 127) / 128);
       if (cf == cl || p.additive) {
         // ---- sole owner, or an additive epilogue (each contributor adds its own partial):
         //      TMEM -> staging -> epilogue.  The fixed-point adds (residual, fc output) are
@@ -331,63 +352,69 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
         //      registers it loaded, with no staging and no group barrier.
         const bool direct = epi.kind == EPI_RESID || epi.kind == EPI_STORE;
         constexpr int HALF = 16 / NEG;  // TMEM columns per load
-        for (int ch = eg; ch < nch; ch += NEG) {
-          const int i0 = ch * step;
-          float v[HALF], w[HALF];
+        for (int h = 0; h < nh; ++h) {
+          const int m0 = (mt * p.mt + h) * 128;
+          const uint32_t tb = tb0 + (uint32_t)(h * p.BN);
+          const bool last_h = h == nh - 1;
+          for (int ch = eg; ch < nch; ch += NEG) {
+            const int i0 = ch * step;
+            float v[HALF], w[HALF];
 #pragma unroll
-          for (int j = 0; j < HALF; ++j) w[j] = 0.f;
-          if (NEG == 1) {
-            tc::tmem_ld16(tb + i0, v);
-            if (p.split) {
-              tc::tmem_ld16(tb + p.lo_col + i0, w);
-            } else if (i0 + 16 < p.BN) {
-              tc::tmem_ld16(tb + i0 + 16, w);
+            for (int j = 0; j < HALF; ++j) w[j] = 0.f;
+            if (NEG == 1) {
+              tc::tmem_ld16(tb + i0, v);
+              if (sp) {
+                tc::tmem_ld16(tb + p.lo_col + i0, w);
+              } else if (i0 + 16 < p.BN) {
+                tc::tmem_ld16(tb + i0 + 16, w);
+              }
+            } else {
+              tc::tmem_ld8(tb + i0, v);
+              if (sp) {
+                tc::tmem_ld8(tb + p.lo_col + i0, w);
+              } else if (i0 + 8 < p.BN) {
+                tc::tmem_ld8(tb + i0 + 8, w);
+              }
             }
-          } else {
-            tc::tmem_ld8(tb + i0, v);
-            if (p.split) {
-              tc::tmem_ld8(tb + p.lo_col + i0, w);
-            } else if (i0 + 8 < p.BN) {
-              tc::tmem_ld8(tb + i0 + 8, w);
+            tc::tmem_ld_wait();
+            const bool release = last_h && ch + NEG >= nch;  // group's last TMEM read
+            if (direct) {
+              if (release) {
+                tc::fence_before_sync();
+                tc::mbar_arrive(&acce[buf]);
+              }
+              const int m = m0 + ml;
+              const int rc = min(step, lrows - i0);
+              fx_t* dst = epi.kind == EPI_STORE ? epi.out_fx : epi.resid;
+              const int ldd = epi.kind == EPI_STORE ? epi.out_ld : epi.ld_res;
+              if (m < epi.Nout) {
+                fx_t* col = dst + (size_t)(row0 + i0) * ldd + m;
+#pragma unroll
+                for (int j = 0; j < HALF; ++j) {
+                  if (sp) {
+                    if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j] + w[j]));
+                  } else {
+                    if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j]));
+                    if (HALF + j < rc) red_add_fx(col + (size_t)(HALF + j) * ldd, to_fx(w[j]));
+                  }
+                }
+              }
+              continue;
             }
-          }
-          tc::tmem_ld_wait();
-          if (direct) {
-            if (ch + NEG >= nch) {  // this group's last TMEM read of the segment
+#pragma unroll
+            for (int j = 0; j < HALF; ++j) {
+              gstg[j * 128 + ml] = v[j];
+              gstg[(HALF + j) * 128 + ml] = w[j];
+            }
+            if (release) {
               tc::fence_before_sync();
               tc::mbar_arrive(&acce[buf]);
             }
-            const int m = m0 + ml;
-            const int rc = min(step, lrows - i0);
-            fx_t* dst = epi.kind == EPI_STORE ? epi.out_fx : epi.resid;
-            const int ldd = epi.kind == EPI_STORE ? epi.out_ld : epi.ld_res;
-            if (m < epi.Nout) {
-              fx_t* col = dst + (size_t)(row0 + i0) * ldd + m;
-#pragma unroll
-              for (int j = 0; j < HALF; ++j) {
-                if (p.split) {
-                  if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j] + w[j]));
-                } else {
-                  if (j < rc) red_add_fx(col + (size_t)j * ldd, to_fx(v[j]));
-                  if (HALF + j < rc) red_add_fx(col + (size_t)(HALF + j) * ldd, to_fx(w[j]));
-                }
-              }
-            }
-            continue;
+            epi_bar(eg);
+            epilogue_tile<bf16>(epi, gstg, 128, sp ? 16 / NEG : -1, m0, row0 + i0,
+                                min(step, lrows - i0), et, 128);
+            epi_bar(eg);
           }
-#pragma unroll
-          for (int j = 0; j < HALF; ++j) {
-            gstg[j * 128 + ml] = v[j];
-            gstg[(HALF + j) * 128 + ml] = w[j];
-          }
-          if (ch + NEG >= nch) {  // this group's last TMEM read of the segment
-            tc::fence_before_sync();
-            tc::mbar_arrive(&acce[buf]);
-          }
-          epi_bar(eg);
-          epilogue_tile<bf16>(epi, gstg, 128, p.split ? 16 / NEG : -1, m0, row0 + i0,
-                              min(step, lrows - i0), et, 128);
-          epi_bar(eg);
         }
         if (eg >= nch) {  // a group without a chunk still releases the accumulator
           tc::fence_before_sync();
@@ -395,11 +422,12 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
         }
       } else {
         // ---- shared tile: write this CTA's partial, the last contributor reduces
+        const int SW = p.mt * p.BN;  // partial columns: every sub-tile's accumulator
         const int slot = (range_begin(c, p) >= t_beg) ? 2 * c : 2 * c + 1;
-        float* wsl = p.ws + (size_t)slot * p.BN * 128;
-        for (int c0 = eg * 16; c0 < p.BN; c0 += 16 * NEG) {
+        float* wsl = p.ws + (size_t)slot * SW * 128;
+        for (int c0 = eg * 16; c0 < SW; c0 += 16 * NEG) {
           float v[16];
-          tc::tmem_ld16(tb + c0, v);
+          tc::tmem_ld16(tb0 + c0, v);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) wsl[(size_t)(c0 + j) * 128 + ml] = v[j];
@@ -417,33 +445,36 @@ __global__ void __launch_bounds__(NEG == 1 ? TC_THREADS : TC_THREADS2, NEG == 1 
           // exactly at the tile; every later contributor's share is its first segment
           const int slot_f = (range_begin(cf, p) == t_beg) ? 2 * cf : 2 * cf + 1;
           constexpr int SR = 32 / NEG;  // staging rows per chunk
-          const int half = p.split ? SR / 2 : SR;
-          for (int ch = eg; ch < nch; ch += NEG) {
-            const int i0 = ch * step;
-            // staging rows [0,half) / [half,2 half): hi / lo parts (split) or rows i0..
-            int col[SR];
-            float acc[SR];
+          const int half = sp ? SR / 2 : SR;
+          for (int h = 0; h < nh; ++h) {
+            const int m0 = (mt * p.mt + h) * 128;
+            for (int ch = eg; ch < nch; ch += NEG) {
+              const int i0 = ch * step;
+              // staging rows [0,half) / [half,2 half): hi / lo parts (split) or rows i0..
+              int col[SR];
+              float acc[SR];
 #pragma unroll
-            for (int j = 0; j < SR; ++j) {
-              if (p.split) {
-                const int ii = i0 + (j % half);
-                col[j] = min((j < half) ? ii : p.lo_col + ii, p.BN - 1);
-              } else {
-                col[j] = min(i0 + j, p.BN - 1);
+              for (int j = 0; j < SR; ++j) {
+                if (sp) {
+                  const int ii = i0 + (j % half);
+                  col[j] = h * p.BN + min((j < half) ? ii : p.lo_col + ii, p.BN - 1);
+                } else {
+                  col[j] = h * p.BN + min(i0 + j, p.BN - 1);
+                }
+                acc[j] = 0.f;
               }
-              acc[j] = 0.f;
-            }
-            for (int cc = cf; cc <= cl; ++cc) {
-              const float* src = p.ws + (size_t)(cc == cf ? slot_f : 2 * cc) * p.BN * 128 + ml;
+              for (int cc = cf; cc <= cl; ++cc) {
+                const float* src = p.ws + (size_t)(cc == cf ? slot_f : 2 * cc) * SW * 128 + ml;
 #pragma unroll
-              for (int j = 0; j < SR; ++j) acc[j] += __ldcg(src + (size_t)col[j] * 128);
-            }
+                for (int j = 0; j < SR; ++j) acc[j] += __ldcg(src + (size_t)col[j] * 128);
+              }
 #pragma unroll
-            for (int j = 0; j < SR; ++j) gstg[j * 128 + ml] = acc[j];
-            epi_bar(eg);
-            epilogue_tile<bf16>(epi, gstg, 128, p.split ? half : -1, m0, row0 + i0,
-                                min(step, lrows - i0), et, 128);
-            epi_bar(eg);
+              for (int j = 0; j < SR; ++j) gstg[j * 128 + ml] = acc[j];
+              epi_bar(eg);
+              epilogue_tile<bf16>(epi, gstg, 128, sp ? half : -1, m0, row0 + i0,
+                                  min(step, lrows - i0), et, 128);
+              epi_bar(eg);
+            }
           }
           epi_bar_all<NEG>();
           if (eg == 0 && et == 0) p.counters[tile] = 0u;
@@ -720,6 +751,8 @@ struct TcGemmPlan {
   int num_sms;
   bool pair;  // large-M GEMMs on CTA pairs (PEAGLE_GEMM_PAIR=0 turns it off)
   int pair_clusters;  // CTA pairs that fit on the GPU at once (a cluster stays in one GPC)
+  int fold_mode;      // folded wide tiles: 0 where they pay, 1 wherever the shapes allow,
+                      // -1 never (PEAGLE_GEMM_FOLD=1 / 0)
   int max_bn;
   float* ws;
   unsigned* counters;
@@ -767,8 +800,8 @@ static size_t smem_bytes_pair(int stages) {
 // dynamic shared memory of the pair kernel: the 227 KB per-block limit less its 1 KB of
 // static RoPE position tables
 constexpr size_t PAIR_SMEM_BUDGET = 226 * 1024;
-static size_t smem_bytes(int stages, int bn) {
-  return 1024 /*align slack*/ + (size_t)stages * (A_BYTES + bn * 128) + STAGE_F_BYTES +
+static size_t smem_bytes(int stages, int b_rows, int mt) {
+  return 1024 /*align slack*/ + (size_t)stages * (mt * A_BYTES + b_rows * 128) + STAGE_F_BYTES +
          (size_t)(2 * stages + 4) * 8 + 16;
 }
 
@@ -824,6 +857,8 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
     // two fit (each GPC holds an even number of the CTAs), not num_sms / 2
     const char* env = getenv("PEAGLE_GEMM_PAIR");
     p->pair = !(env && env[0] == '0');
+    const char* fenv = getenv("PEAGLE_GEMM_FOLD");
+    p->fold_mode = fenv ? (fenv[0] == '1' ? 1 : fenv[0] == '0' ? -1 : 0) : 0;
     p->pair_clusters = 0;
     int stages = 2;
     while (stages < 8 && smem_bytes_pair(stages + 1) <= PAIR_SMEM_BUDGET) ++stages;
@@ -888,6 +923,9 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     p.n_tiles = (R + p.BN - 1) / p.BN;
   }
   p.KB = Kd / 64;
+  p.b_rows = p.BN;
+  p.mt = 1;
+  p.fold = 0;
   if (pl->pair && p.n_tiles > 1 && Kd % 64 == 0 && pl->pair_clusters > 0) {
     // CTA pairs: pair-tiles of 256 weight rows x (128 logical rows, hi + lo, or 256 rows)
     TcParams q = p;
@@ -931,11 +969,32 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, mw, mx, q, epi);
     return e == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
   }
+  // A split single tile of 64+ rows (R a multiple of 16, whole 256-row weight blocks):
+  // every stage carries 2R operand rows, more bytes than a 128-row weight tile, and the
+  // tile traffic through L2 and the TMA units (about 7-8 TB/s in all) bounds the GEMM.
+  // Two 128-row weight sub-tiles per tile share each operand stage (32 + 2R/8 KB per
+  // stage instead of 16 + 2R/8), and the MMA adds the hi and the lo products into the
+  // same R accumulator columns (two MMAs per k-step) so both sub-tiles' accumulators fit
+  // in tensor memory twice.  It pays where every CTA streams 20+ k-blocks between
+  // epilogues of the residual or SwiGLU form (80 rows: gate/up 79 -> 71 us, down 40 -> 38
+  // us per launch); with fewer, or the heavier QKV / LM-head epilogues, the doubled tile
+  // gives each epilogue twice the work for the same streaming and loses (QKV 57 -> 73 us).
+  const long long fold_iters = (long long)(Nout / 256) * (Kd / 64);
+  const bool fold_pays =
+      fold_iters >= 20LL * pl->num_sms && (epi.kind == EPI_RESID || epi.kind == EPI_SWIGLU);
+  if (p.split && !p.two_box && R >= 64 && R % 16 == 0 && Nout % 256 == 0 &&
+      2 * R <= pl->max_bn && pl->fold_mode >= 0 && (fold_pays || pl->fold_mode == 1)) {
+    p.fold = 1;
+    p.mt = 2;
+    p.BN = R;
+    p.b_rows = 2 * R;
+    p.lo_col = 0;
+  }
   // large-M projections are tensor-bound: two epilogue groups keep up with the MMA; a
-  // single tile of 64+ rows (hi + lo operand rows >= 128) also drains faster with two
-  // (ragged batch of 16 x K=5, 80 rows: 1285 -> 1214 us per pass)
-  const int neg = (p.n_tiles > 1 || p.BN >= 128) ? 2 : 1;
-  const int m_tiles = (Nout + 127) / 128;
+  // single tile of 128+ operand rows also drains faster with two (ragged batch of 16 x
+  // K=5, 80 rows: 1285 -> 1214 us per pass)
+  const int neg = (p.n_tiles > 1 || p.b_rows >= 128) ? 2 : 1;
+  const int m_tiles = (Nout + 128 * p.mt - 1) / (128 * p.mt);
   const long long tiles = (long long)m_tiles * p.n_tiles;
   p.m_tiles = m_tiles;
   // Concurrent CTAs work on neighbouring tiles: with weight tiles innermost all of W is
@@ -951,29 +1010,30 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
   // whole-tile waves first: large-M GEMMs (L2 reuse), and single-tile GEMMs of 64+ rows
   // whose epilogue needs whole tiles (a shared tile costs a partial of BN x 128 fp32 per
   // contributor, 80 KB at 80 rows)
-  p.dp_waves = (p.n_tiles > 1 || (!p.additive && p.BN >= 128)) ? (int)(tiles / p.G) : 0;
+  p.dp_waves = (p.n_tiles > 1 || (!p.additive && p.b_rows >= 128)) ? (int)(tiles / p.G) : 0;
   p.total = (tiles - (long long)p.dp_waves * p.G) * p.KB;
   // shared memory ring: decode-sized tiles keep ~110 KB so a second CTA (the next
   // kernel's, under programmatic dependent launch) fits on the SM; large tiles take more
-  const size_t budget = p.BN <= 64 ? 112 * 1024 : 220 * 1024;
+  const size_t budget = p.fold ? 227 * 1024 : p.b_rows <= 64 ? 112 * 1024 : 220 * 1024;
   int stages = 2;
-  while (stages < 12 && smem_bytes(stages + 1, p.BN) <= budget) ++stages;
+  while (stages < 12 && smem_bytes(stages + 1, p.b_rows, p.mt) <= budget) ++stages;
   p.stages = stages;
 
   // single-tile split reads 16-column groups starting at column R + i0, which may run
   // up to 15 columns past the second accumulator: keep that slack allocated
-  p.tmem_cols = pow2_at_least((uint32_t)(2 * p.BN + ((p.split && !p.two_box) ? 16 : 0)));
+  p.tmem_cols = pow2_at_least(
+      (uint32_t)(2 * p.mt * p.BN + ((p.split && !p.two_box && !p.fold) ? 16 : 0)));
   if (p.tmem_cols > 512) return PEAGLE_ERR_CAPACITY;
   p.ws = pl->ws;
   p.counters = pl->counters;
   p.err = pl->err;
   CUtensorMap mw, mx;
   if (!encode_map(pl, &mw, W, Nout, Kd, Kd, 128)) return PEAGLE_ERR_CUDA;
-  if (!encode_map(pl, &mx, X, xrows, Kd, ldx, p.two_box ? 128 : p.BN)) return PEAGLE_ERR_CUDA;
+  if (!encode_map(pl, &mx, X, xrows, Kd, ldx, p.two_box ? 128 : p.b_rows)) return PEAGLE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(neg == 1 ? TC_THREADS : TC_THREADS2);
-  cfg.dynamicSmemBytes = smem_bytes(stages, p.BN);
+  cfg.dynamicSmemBytes = smem_bytes(stages, p.b_rows, p.mt);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
