@@ -24,6 +24,17 @@ namespace peagle {
 namespace {
 
 constexpr int FA_LD = 72;  // padded row stride (floats) of the shared-memory tiles
+// Column swizzle of the tiles: rows with bit 2 set hold their 8-float column groups in
+// swapped pairs (column c stored at c ^ 8).  Fragments read the tiles two ways: float2
+// along a row (rows gq, columns 2tq + 8s), conflict-free with the 72-float stride alone,
+// and single floats down rows (rows 2tq, 2tq + 1, columns gq + 8n), where rows 0 and 4
+// (and 2 and 6) would share banks; the swizzle moves one of each pair by eight banks.
+__device__ __forceinline__ int fa_sw(int row) { return (row >> 2) & 1; }
+// Column group g of a row with swizzle bit b lives at group g ^ b: from a pointer p to the
+// row's group-0 position, group g is at (g even ? p + 8b : p - 8b) + 8g, so unrolled loops
+// keep two base pointers and constant offsets.
+__device__ __forceinline__ const float* fa_even(const float* p, int b) { return p + 8 * b; }
+__device__ __forceinline__ const float* fa_odd(const float* p, int b) { return p - 8 * b; }
 
 __device__ __forceinline__ uint32_t tf32(float x) {
   uint32_t r;
@@ -73,7 +84,8 @@ __device__ __forceinline__ void stage64(float* dst, const float* src, int row0, 
   for (int c = tid; c < 64 * 16; c += nthr) {
     const int r = c >> 4, q = c & 15;
     const bool v = row0 + r < nrows;
-    cp16(dst + r * FA_LD + q * 4, src + (size_t)(v ? row0 + r : 0) * 64 + q * 4, v);
+    cp16(dst + r * FA_LD + 4 * (q ^ (fa_sw(r) << 1)), src + (size_t)(v ? row0 + r : 0) * 64 + q * 4,
+         v);
   }
 }
 
@@ -153,10 +165,13 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(TrainAttn a, const flo
         float sc[2][4] = {}, dp[2][4] = {};
         const float* kr = Ks + (kk * 8 + gq) * FA_LD + 2 * tq;
         const float* vr = Vs + (kk * 8 + gq) * FA_LD + 2 * tq;
+        const int bg = fa_sw(gq);
+        const float *kre = fa_even(kr, bg), *kro = fa_odd(kr, bg);
+        const float *vre = fa_even(vr, bg), *vro = fa_odd(vr, bg);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const float2 kb = *reinterpret_cast<const float2*>(kr + 8 * s);
-          const float2 vb = *reinterpret_cast<const float2*>(vr + 8 * s);
+          const float2 kb = *reinterpret_cast<const float2*>(((s & 1) ? kro : kre) + 8 * s);
+          const float2 vb = *reinterpret_cast<const float2*>(((s & 1) ? vro : vre) + 8 * s);
           mma_tf32(sc[s & 1], qa[s][0], qa[s][1], qa[s][2], qa[s][3], bits(kb.x), bits(kb.y));
           mma_tf32(dp[s & 1], oa[s][0], oa[s][1], oa[s][2], oa[s][3], bits(vb.x), bits(vb.y));
         }
@@ -177,9 +192,13 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(TrainAttn a, const flo
         const uint32_t d3 = tf32(p3 * (dp[0][3] - D1) * a.scale);
         // dQ += dS K1: A = dS (keys 2tq, 2tq + 1 as k positions tq, tq + 4), B = K1
         const float* kc0 = Ks + (kk * 8 + 2 * tq) * FA_LD + gq;
+        const int bt = fa_sw(2 * tq);
+        const float *kce = fa_even(kc0, bt), *kco = fa_odd(kc0, bt);
 #pragma unroll
-        for (int nn = 0; nn < 8; ++nn)
-          mma_tf32(dq[nn], d0, d2, d1, d3, bits(kc0[8 * nn]), bits(kc0[FA_LD + 8 * nn]));
+        for (int nn = 0; nn < 8; ++nn) {
+          const float* kc = (nn & 1) ? kco : kce;
+          mma_tf32(dq[nn], d0, d2, d1, d3, bits(kc[8 * nn]), bits(kc[FA_LD + 8 * nn]));
+        }
       }
     }
     __syncthreads();  // the stage is refilled next
@@ -256,7 +275,7 @@ __global__ void __launch_bounds__(128, 3) attn_bwd_dkv_kernel(TrainAttn a, const
       const int i = i0 + r;
       const bool v = i < re;
       const float* src = (which ? dOh : Qh) + ((size_t)h * a.M + (v ? i : 0)) * 64 + q * 4;
-      cp16((which ? st[b].o : st[b].q) + r * FA_LD + q * 4, src, v);
+      cp16((which ? st[b].o : st[b].q) + r * FA_LD + 4 * (q ^ (fa_sw(r) << 1)), src, v);
     }
     if (threadIdx.x < 16) {
       const int i = i0 + threadIdx.x;
@@ -286,10 +305,13 @@ __global__ void __launch_bounds__(128, 3) attn_bwd_dkv_kernel(TrainAttn a, const
       for (int e = 0; e < 4; ++e) sT[j][e] = dpT[j][e] = sT2[j][e] = dpT2[j][e] = 0.f;
       const float* qr = S.q + (8 * j + gq) * FA_LD + 2 * tq;
       const float* orow = S.o + (8 * j + gq) * FA_LD + 2 * tq;
+      const int bg = fa_sw(gq);
+      const float *qre = fa_even(qr, bg), *qro = fa_odd(qr, bg);
+      const float *ore = fa_even(orow, bg), *oro = fa_odd(orow, bg);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const float2 qb = *reinterpret_cast<const float2*>(qr + 8 * s);
-        const float2 ob = *reinterpret_cast<const float2*>(orow + 8 * s);
+        const float2 qb = *reinterpret_cast<const float2*>(((s & 1) ? qro : qre) + 8 * s);
+        const float2 ob = *reinterpret_cast<const float2*>(((s & 1) ? oro : ore) + 8 * s);
         mma_tf32((s & 1) ? sT2[j] : sT[j], ka[s][0], ka[s][1], ka[s][2], ka[s][3], bits(qb.x),
                  bits(qb.y));
         mma_tf32((s & 1) ? dpT2[j] : dpT[j], va[s][0], va[s][1], va[s][2], va[s][3], bits(ob.x),
@@ -319,10 +341,15 @@ __global__ void __launch_bounds__(128, 3) attn_bwd_dkv_kernel(TrainAttn a, const
       // A = P^T / dS^T over the rows ra, rb2 of this k step (k positions tq, tq + 4)
       const float* o0 = S.o + ra * FA_LD + gq;
       const float* q0 = S.q + ra * FA_LD + gq;
+      const int bt = fa_sw(ra);
+      const float *o0e = fa_even(o0, bt), *o0o = fa_odd(o0, bt);
+      const float *q0e = fa_even(q0, bt), *q0o = fa_odd(q0, bt);
 #pragma unroll
       for (int nn = 0; nn < 8; ++nn) {
-        mma_tf32(dv[nn], P0, P2, P1, P3, bits(o0[8 * nn]), bits(o0[FA_LD + 8 * nn]));
-        mma_tf32(dk[nn], d0, d2, d1, d3, bits(q0[8 * nn]), bits(q0[FA_LD + 8 * nn]));
+        const float* ob = (nn & 1) ? o0o : o0e;
+        const float* qb = (nn & 1) ? q0o : q0e;
+        mma_tf32(dv[nn], P0, P2, P1, P3, bits(ob[8 * nn]), bits(ob[FA_LD + 8 * nn]));
+        mma_tf32(dk[nn], d0, d2, d1, d3, bits(qb[8 * nn]), bits(qb[FA_LD + 8 * nn]));
       }
     }
     __syncthreads();  // the buffer is refilled next
@@ -414,9 +441,11 @@ __global__ void __launch_bounds__(256) attn_fwd_prefix_kernel(TrainAttn a, const
       for (int kk = 0; kk < 8; ++kk) {
         float e[2][4] = {};
         const float* kr = Ks + (kk * 8 + gq) * FA_LD + 2 * tq;
+        const int bg = fa_sw(gq);
+        const float *kre = fa_even(kr, bg), *kro = fa_odd(kr, bg);
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) {
-          const float2 kb = *reinterpret_cast<const float2*>(kr + 8 * s2);
+          const float2 kb = *reinterpret_cast<const float2*>(((s2 & 1) ? kro : kre) + 8 * s2);
           mma_tf32(e[s2 & 1], qa[s2][0], qa[s2][1], qa[s2][2], qa[s2][3], bits(kb.x), bits(kb.y));
         }
         const int k0 = kt * 64 + kk * 8 + 2 * tq, k1 = k0 + 1;
@@ -459,10 +488,14 @@ __global__ void __launch_bounds__(256) attn_fwd_prefix_kernel(TrainAttn a, const
         s1 += p2 + p3;
         // O += P V over these 8 keys: A = P (keys 2tq, 2tq + 1 as k positions tq, tq + 4)
         const float* vc = Vs + (kk * 8 + 2 * tq) * FA_LD + gq;
+        const int bt = fa_sw(2 * tq);
+        const float *vce = fa_even(vc, bt), *vco = fa_odd(vc, bt);
         const uint32_t P0 = tf32(p0), P1 = tf32(p1), P2 = tf32(p2), P3 = tf32(p3);
 #pragma unroll
-        for (int nn = 0; nn < 8; ++nn)
-          mma_tf32(o[nn], P0, P2, P1, P3, bits(vc[8 * nn]), bits(vc[FA_LD + 8 * nn]));
+        for (int nn = 0; nn < 8; ++nn) {
+          const float* vb = (nn & 1) ? vco : vce;
+          mma_tf32(o[nn], P0, P2, P1, P3, bits(vb[8 * nn]), bits(vb[FA_LD + 8 * nn]));
+        }
       }
       s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
       s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
