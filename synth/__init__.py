@@ -147,9 +147,14 @@ def make_d2t(dims: Dims, seed) -> np.ndarray:
     return (ids - np.arange(dims.draft_vocab)).astype(np.int32)
 
 
-def make_weights(dims: Dims, seed: int = 1234) -> dict:
+def make_weights(dims: Dims, seed: int = 1234, gains: bool = False) -> dict:
     """Random-init drafter weights: linear and embedding weights N(0, 0.02^2),
     emb(mask) and h_shared N(0, 1), RMSNorm gains 1 (the Llama initialisation).
+
+    ``gains=True`` draws every RMSNorm gain as 1 + 0.3 N(0, 1) instead (rounded to the
+    storage dtype), each gain vector from its own seed, so that a kernel that drops a
+    gain or applies one norm's gain to another shows in its outputs.  The other weights
+    are drawn exactly as with unit gains.
 
     Layout (row-major, PyTorch nn.Linear convention [out, in]):
       embed [Vt, H]; emb_mask [H]; h_shared [3H]; fc [H, 3H];
@@ -197,6 +202,17 @@ def make_weights(dims: Dims, seed: int = 1234) -> dict:
             "attn_norm": torch.ones(H, dtype=dt),
             "post_norm": torch.ones(H, dtype=dt),
         })
+    if gains:
+        g = iter(np.random.SeedSequence(seed + 104729).spawn(3 + 2 * dims.n_layers))
+
+        def gain():
+            return (1.0 + normal((H,), next(g), 0.3, torch.float32)).to(dt)
+
+        for name in ("input_norm", "hidden_norm", "final_norm"):
+            w[name] = gain()
+        for L in w["layers"]:
+            L["attn_norm"] = gain()
+            L["post_norm"] = gain()
     return w
 
 

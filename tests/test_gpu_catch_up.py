@@ -17,7 +17,7 @@ SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_
 
 
 def _case(dims, lens, T, seed):
-    w = synth.make_weights(dims, seed)
+    w = synth.make_weights(dims, seed, gains=True)
     wl = synth.Workload("s", dims, len(lens), T, tuple(lens))
     inp = synth.make_decode_inputs(wl, seed + 1, capacity=max(lens) + T + 8)
     hid = synth.normal((len(lens), T, 3 * dims.hidden), seed + 2, 1.0, dims.torch_dtype)

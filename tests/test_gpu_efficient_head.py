@@ -25,7 +25,7 @@ SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_
 
 def _case(dims, lens, K, seed):
     wl = synth.Workload("e", dims, len(lens), K, tuple(lens))
-    w = synth.make_weights(dims, seed)
+    w = synth.make_weights(dims, seed, gains=True)
     inp = synth.make_decode_inputs(wl, seed + 1)
     return w, inp
 
@@ -131,7 +131,7 @@ def test_forward_parallel_rejects_the_efficient_head():
     import drafting_eagle_draft_gb300 as m
 
     dims = SMALL_BF16
-    w = synth.make_weights(dims, 3)
+    w = synth.make_weights(dims, 3, gains=True)
     ctx = make_ctx(dims, w, 1, 4, 64, max_rows=64, max_seq=16)
     n, K = 8, 2
     rp, rd = m.peagle_cod_rows(n, K, 1.0, np.zeros((n, K)))
@@ -180,7 +180,7 @@ def test_catch_up_with_the_efficient_head(pass_kernel):
     m = pk()
     lens, T = [0, 37, 100], 5
     dims = synth.shrink(SMALL_BF16, lm_rank=128, lm_topk=48)
-    w = synth.make_weights(dims, 29)
+    w = synth.make_weights(dims, 29, gains=True)
     wl = synth.Workload("c", dims, len(lens), T, tuple(lens))
     inp = synth.make_decode_inputs(wl, 30, capacity=max(lens) + T + 8)
     hid = synth.normal((len(lens), T, 3 * dims.hidden), 31, 1.0, dims.torch_dtype)
@@ -211,7 +211,7 @@ def test_efficient_head_at_full_size(vocab):
     dims = synth.shrink(wl.dims, lm_rank=128, lm_topk=128)
     if vocab:
         dims = synth.shrink(dims, draft_vocab=vocab, d2t="identity")
-    w = synth.make_weights(dims, 1234)
+    w = synth.make_weights(dims, 1234, gains=True)
     inp = synth.make_decode_inputs(wl, 99)
     ctx = make_ctx(dims, w, wl.batch, wl.K, inp["capacity"])
     toks, lg, _ = run_draft(ctx, dims, inp, wl.K)

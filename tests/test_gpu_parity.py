@@ -29,7 +29,7 @@ SMALL_FOLD = synth.Dims(hidden=256, n_layers=2, n_q_heads=4, n_kv_heads=2, head_
 
 def _small_case(dims, lens, K, seed, cap=None):
     wl = synth.Workload("s", dims, len(lens), K, tuple(lens))
-    w = synth.make_weights(dims, seed)
+    w = synth.make_weights(dims, seed, gains=True)
     inp = synth.make_decode_inputs(wl, seed + 1, capacity=cap)
     return w, inp
 
@@ -40,7 +40,7 @@ def _small_case(dims, lens, K, seed, cap=None):
 @pytest.fixture(scope="module")
 def tiny():
     wl = synth.WORKLOADS["tiny_f32"]
-    w = synth.make_weights(wl.dims, 1234)
+    w = synth.make_weights(wl.dims, 1234, gains=True)
     inp = synth.make_decode_inputs(wl, 99, capacity=int(wl.seq_lens[0]) + 16)
     ctx = make_ctx(wl.dims, w, wl.batch, 16, inp["capacity"])
     yield wl, w, inp, ctx
@@ -130,7 +130,7 @@ def test_logits_optional():
 @pytest.fixture(scope="module")
 def c1_drafter():
     dims = synth.DIMS_C1
-    w = synth.make_weights(dims, 1234)
+    w = synth.make_weights(dims, 1234, gains=True)
     ctx = make_ctx(dims, w, 2, 8, 10240 + 8)
     yield dims, w, ctx
     ctx.close()
@@ -169,7 +169,7 @@ def test_decode_b2_full_and_verify(c1_drafter):
 def test_ragged_b16_full_sampled():
     wl = synth.WORKLOADS["ragged_b16"]
     dims = wl.dims
-    w = synth.make_weights(dims, 4321)
+    w = synth.make_weights(dims, 4321, gains=True)
     inp = synth.make_decode_inputs(wl, 97)
     ctx = make_ctx(dims, w, wl.batch, wl.K, inp["capacity"])
     toks, lg, _ = run_draft(ctx, dims, inp, wl.K)

@@ -39,7 +39,7 @@ def _both(dims, w, inp, K, cap):
 ])
 def test_pass_kernel_matches_multi_kernel_and_oracle(dims, lens, K):
     wl = synth.Workload("s", dims, len(lens), K, tuple(lens))
-    w = synth.make_weights(dims, 11 + K)
+    w = synth.make_weights(dims, 11 + K, gains=True)
     inp = synth.make_decode_inputs(wl, 12 + K)
     (t1, l1, d1), (t2, l2, d2) = _both(dims, w, inp, K, inp["capacity"] + 1)
     assert float(np.max(np.abs(l1 - l2))) <= LOGIT_TOL["bf16"] / 4
@@ -58,7 +58,7 @@ def test_pass_kernel_decode_b1_repeat_deterministic():
     fixed point and every fix-up adds its partials in a fixed order."""
     wl = synth.WORKLOADS["decode_b1"]
     dims = wl.dims
-    w = synth.make_weights(dims, 1234)
+    w = synth.make_weights(dims, 1234, gains=True)
     inp = synth.make_decode_inputs(wl, 99)
     ctx = make_ctx(dims, w, 1, wl.K, inp["capacity"], pass_kernel=True)
     d = to_dev(inp)
@@ -79,7 +79,7 @@ def test_bf16_device_checks(use_pass):
     m = pk()
     dims = SMALL_BF16
     wl = synth.Workload("s", dims, 1, 4, (10,))
-    w = synth.make_weights(dims, 5)
+    w = synth.make_weights(dims, 5, gains=True)
     inp = synth.make_decode_inputs(wl, 6, capacity=16)
     ctx = make_ctx(dims, w, 1, 8, 64, pass_kernel=use_pass)
     d = to_dev(inp)

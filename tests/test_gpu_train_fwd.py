@@ -53,7 +53,7 @@ def _compare(dims, ref_logits, ref_am, ref_margin, am, lg, what):
 ])
 def test_forward_parallel_small(dims, n, K, r):
     m = pk()
-    w = synth.make_weights(dims, 17 + n)
+    w = synth.make_weights(dims, 17 + n, gains=True)
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
     hidden = synth.normal((n, 3 * dims.hidden), 4, 1.0, dims.torch_dtype)
     u = synth.cod_uniforms(n, K, seed=5)
@@ -72,7 +72,7 @@ def test_forward_parallel_small(dims, n, K, r):
 def test_forward_parallel_rejects_bad_rows():
     m = pk()
     dims = synth.DIMS_TINY
-    w = synth.make_weights(dims, 2)
+    w = synth.make_weights(dims, 2, gains=True)
     n, K = 8, 4
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
     hidden = synth.normal((n, 3 * dims.hidden), 4)
@@ -94,7 +94,7 @@ def test_forward_parallel_dependency_closure():
     positions have no depth-1 row at all."""
     dims = SMALL_BF16
     n, K = 160, 8
-    w = synth.make_weights(dims, 31)
+    w = synth.make_weights(dims, 31, gains=True)
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 7)
     hidden = synth.normal((n, 3 * dims.hidden), 8, 1.0, dims.torch_dtype)
     full = np.array([(p, d) for p in range(n) for d in range(1, K + 1) if p - d + 1 >= 0],
@@ -118,7 +118,7 @@ def test_sequence_partitioned_forward_matches_full():
     m = pk()
     dims = SMALL_BF16
     n, K, r = 180, 8, 0.8
-    w = synth.make_weights(dims, 41)
+    w = synth.make_weights(dims, 41, gains=True)
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 9)
     hidden = synth.normal((n, 3 * dims.hidden), 10, 1.0, dims.torch_dtype)
     rp, rd = m.peagle_cod_rows(n, K, r, synth.cod_uniforms(n, K, seed=12))
@@ -142,7 +142,7 @@ def test_sequence_partitioned_forward_matches_full():
 def test_forward_parallel_rejects_missing_depth1_row():
     m = pk()
     dims = SMALL_BF16
-    w = synth.make_weights(dims, 3)
+    w = synth.make_weights(dims, 3, gains=True)
     n, K = 8, 4
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 3)
     hidden = synth.normal((n, 3 * dims.hidden), 4, 1.0, dims.torch_dtype)
@@ -165,7 +165,7 @@ def test_train_fwd_full_prefix_and_tail():
     m = pk()
     wl = synth.WORKLOADS["train_fwd"]
     dims = wl.dims
-    w = synth.make_weights(dims, 1234)
+    w = synth.make_weights(dims, 1234, gains=True)
     ti = synth.make_train_inputs(wl, 21)
     n, K = wl.n_seq, wl.K
     rp, rd = m.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])

@@ -17,7 +17,7 @@ SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_
 
 def _case(dims, lens, K, seed, cap=None):
     wl = synth.Workload("w", dims, len(lens), K, tuple(lens))
-    w = synth.make_weights(dims, seed)
+    w = synth.make_weights(dims, seed, gains=True)
     inp = synth.make_decode_inputs(wl, seed + 1, capacity=cap)
     return w, inp
 
@@ -70,7 +70,7 @@ def test_forward_parallel_rejects_a_window():
     import torch
 
     dims = synth.shrink(SMALL_BF16, attn_window=16)
-    w = synth.make_weights(dims, 3)
+    w = synth.make_weights(dims, 3, gains=True)
     ctx = make_ctx(dims, w, 1, 4, 64, max_rows=64, max_seq=16)
     n, K = 8, 2
     rp, rd = m.peagle_cod_rows(n, K, 1.0, np.zeros((n, K)))

@@ -277,6 +277,28 @@ def test_sequence_partition_keeps_dependencies():
     assert sizes.min() > 0
 
 
+def test_sequence_partition_depth2_goes_by_index():
+    """3.2: depths 1 and 2 (the paper's depths 0 and 1) are assigned by position index.
+    A depth-2 row at a chunk's first position has its parent (p-1, 1) in the previous
+    chunk, yet lands in its own position's chunk; the depth-3 row below it follows it
+    there, while a depth-3 row at the boundary follows its depth-2 parent back into the
+    previous chunk."""
+    n, K = 12, 4
+    rows = np.array([(p, d) for p in range(n) for d in range(1, K + 1) if p - d + 1 >= 0])
+    b = 6
+    chunk, ctx = O.sequence_partition(rows, [0, b])
+    idx = {(int(p), int(d)): i for i, (p, d) in enumerate(rows)}
+    assert chunk[idx[(b - 1, 1)]] == 0 and chunk[idx[(b, 1)]] == 1
+    assert chunk[idx[(b, 2)]] == 1          # parent (b-1, 1) is in chunk 0
+    assert chunk[idx[(b + 1, 3)]] == 1      # follows its parent (b, 2)
+    assert chunk[idx[(b, 3)]] == 0          # follows its parent (b-1, 2)
+    assert chunk[idx[(b + 1, 4)]] == 0      # chain (b-1, 2) -> (b, 3) -> (b+1, 4)
+    assert chunk[idx[(b - 1, 2)]] == 0
+    # chunk 1's context: every depth-1 position below its end
+    assert ctx[1].tolist() == list(range(n))
+    assert ctx[0].tolist() == list(range(b))
+
+
 # ---------------------------------------------------------------- the draft pass
 
 
@@ -428,6 +450,78 @@ def test_swiglu_mlp_closed_form():
     assert np.allclose(r.logits[0, 0], exp, atol=1e-10)
 
 
+def _gains(w):
+    g = {k: w[k].double().numpy() for k in ("input_norm", "hidden_norm", "final_norm")}
+    g["attn"] = [L["attn_norm"].double().numpy() for L in w["layers"]]
+    g["post"] = [L["post_norm"].double().numpy() for L in w["layers"]]
+    return g
+
+
+def test_norm_gains_route_through_attention_path():
+    """Distinct random gains, two layers, single visible key (no cache, K=1) and down-proj
+    zeroed: layer 1 takes x0 = [rms(e) g_in || rms(f) g_hid], layer 2 takes
+    rms(res1) g_attn[2], the head takes rms(res2) g_final; layer 1's attn_norm and every
+    post_norm play no part."""
+    dims = _tiny_dims(n_layers=2, rms_eps=0.0)
+    w = synth.make_weights(dims, 5, gains=True)
+    for L in w["layers"]:
+        L["down"] = _zero(L["down"])
+    inp = _tiny_inputs(dims, 1, 1, 0)
+    r = _run(dims, w, inp, 1)
+    nq, nkv, hd = dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    g = _gains(w)
+    for a, b in (("input_norm", "hidden_norm"), ("hidden_norm", "final_norm")):
+        assert not np.allclose(g[a], g[b])
+    assert not np.allclose(g["attn"][1], g["post"][1])
+    e = w["embed"][int(inp["new_token"][0])].double().numpy()
+    f = w["fc"].double().numpy() @ inp["target_hidden"][0].double().numpy()
+    x = np.concatenate([_rms(e) * g["input_norm"], _rms(f) * g["hidden_norm"]])
+    res = f
+    for li, L in enumerate(w["layers"]):
+        if li > 0:
+            x = _rms(res) * g["attn"][li]
+        wv = L["qkv"].double().numpy()[(nq + nkv) * hd:]
+        v = (wv @ x).reshape(nkv, hd)
+        o = np.concatenate([v[h // (nq // nkv)] for h in range(nq)])
+        res = res + L["o"].double().numpy() @ o
+    exp = w["lm_head"].double().numpy() @ (_rms(res) * g["final_norm"])
+    assert np.allclose(r.logits[0, 0], exp, atol=1e-10)
+    w2 = dict(w)
+    w2["layers"] = [dict(L) for L in w["layers"]]
+    w2["layers"][0]["attn_norm"] = w["layers"][0]["attn_norm"] * 3.0
+    for L in w2["layers"]:
+        L["post_norm"] = -L["post_norm"]
+    assert np.allclose(_run(dims, w2, inp, 1).logits, r.logits, atol=1e-12)
+
+
+def test_norm_gains_route_through_mlp_path():
+    """Distinct random gains, two layers, o-proj zeroed (attention adds nothing): layer l
+    adds down(silu(gate u) * up u) with u = rms(res) g_post[l]; the head takes
+    rms(res) g_final; the NTP row's input gains and every attn_norm play no part."""
+    dims = _tiny_dims(n_layers=2, rms_eps=0.0)
+    w = synth.make_weights(dims, 6, gains=True)
+    for L in w["layers"]:
+        L["o"] = _zero(L["o"])
+    inp = _tiny_inputs(dims, 1, 2, 3)
+    r = _run(dims, w, inp, 2)
+    g = _gains(w)
+    assert not np.allclose(g["post"][0], g["post"][1])
+    f = w["fc"].double().numpy() @ inp["target_hidden"][0].double().numpy()
+    res = f
+    for li, L in enumerate(w["layers"]):
+        Ld = {k: v.double().numpy() for k, v in L.items()}
+        u = _rms(res) * g["post"][li]
+        gt = Ld["gate"] @ u
+        res = res + Ld["down"] @ (gt * scipy.special.expit(gt) * (Ld["up"] @ u))
+    exp = w["lm_head"].double().numpy() @ (_rms(res) * g["final_norm"])
+    assert np.allclose(r.logits[0, 0], exp, atol=1e-10)
+    w2 = dict(w)
+    w2["input_norm"] = -w["input_norm"]
+    w2["hidden_norm"] = w["hidden_norm"] * 2.0
+    w2["layers"] = [dict(L, attn_norm=L["attn_norm"] * 5.0) for L in w["layers"]]
+    assert np.allclose(_run(dims, w2, inp, 2).logits, r.logits, atol=1e-12)
+
+
 def test_draft_rows_are_causal_in_K():
     """Row j never sees rows > j: outputs of rows 0..j do not depend on K (K=1 is the
     single NTP step of EAGLE-3); and row 0 ignores emb(mask) and h_shared."""
@@ -465,7 +559,7 @@ def test_training_mask_reproduces_the_draft_block():
     target hidden taken at a: the mask's base-context + chain rule is the inference
     draft block."""
     dims = _tiny_dims(n_layers=2, rms_eps=1e-6)
-    w = _tiny_weights(dims)
+    w = synth.make_weights(dims, 3, gains=True)
     n, K, a = 10, 4, 6
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 5)
     hidden = synth.normal((n, 3 * dims.hidden), 6)
@@ -512,7 +606,7 @@ def test_training_forward_prefix_closure():
     """Rows with p < P0 only depend on rows with p < P0 (position invariance, 3.1): the
     forward over the prefix equals the full forward on those rows."""
     dims = _tiny_dims(n_layers=2)
-    w = _tiny_weights(dims)
+    w = synth.make_weights(dims, 3, gains=True)
     n, K = 24, 4
     tokens = synth.uniform_ints(n, 0, dims.target_vocab, 7)
     hidden = synth.normal((n, 3 * dims.hidden), 8)
