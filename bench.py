@@ -12,13 +12,15 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode_b1|decode_b2|ragged_b16]
 
-Four extra objects on the line: train_fwd (the training-style masked forward, n=2048, K=8,
-COD 0.8), train_step (the same rows: forward, mean cross-entropy and every parameter
+Five extra objects on the line: decode_configs (the draft pass on the concurrency-2 and
+the ragged batch-16 workloads, each with its HBM roofline), train_fwd (the training-style
+masked forward, n=2048, K=8, COD 0.8), train_step (the same rows: forward, mean cross-entropy and every parameter
 gradient), sliding_window (the concurrency-2 workload with and without a 4096-position
 drafter attention window) and efficient_head (the headline workload with the rank-128 /
 top-128 LM head and with the full head, on the 32000-entry draft vocabulary and on the
-whole 201088-entry vocabulary); --no-train-fwd / --no-train-step / --no-window / --no-head
-skip them, and --only NAME runs one of them alone (a short driver for profilers).
+whole 201088-entry vocabulary); --no-configs / --no-train-fwd / --no-train-step /
+--no-window / --no-head skip them, and --only NAME runs one of them alone (a short driver
+for profilers).
 
 --impl reference times the fp64 oracle on the host cores instead (a deliberately slow
 plain program; see the cpu_baseline object).  Under torchrun each rank runs an
@@ -54,6 +56,8 @@ def parse():
                     choices=["decode_b1", "decode_b2", "ragged_b16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other decode workloads (decode_b2, ragged_b16)")
     ap.add_argument("--no-train-fwd", action="store_true",
                     help="skip the training-style masked forward measurement")
     ap.add_argument("--no-window", action="store_true",
@@ -63,7 +67,7 @@ def parse():
     ap.add_argument("--no-train-step", action="store_true",
                     help="skip the training step measurement")
     ap.add_argument("--only", choices=["train_fwd", "train_step", "window", "head_draft_vocab",
-                                       "head_full_vocab"],
+                                       "head_full_vocab", "decode_b2", "ragged_b16"],
                     help="run one of the extra measurements alone and print its object "
                          "(a short driver for profilers)")
     return ap.parse_args()
@@ -144,8 +148,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# DRAM bytes (read + write) of one pass-kernel launch on decode_b1, from the ncu capture
-# summarised in profiles/pass_kernel_decode_b1.md (dram__bytes_read.sum + _write.sum)
+# DRAM bytes (read + write) of one pass-kernel launch on decode_b1: dram__bytes_read.sum +
+# dram__bytes_write.sum of one ncu capture of the current pass kernel (None when the kernel
+# has changed since the counters were taken)
 PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_054_574_336
 
 
@@ -164,6 +169,33 @@ def kv_bytes(dims, lens, K) -> int:
     """KV-cache bytes the attention reads per pass (committed context + draft block)."""
     per_pos = dims.n_layers * dims.n_kv_heads * dims.head_dim * 2 * 2
     return int(sum(int(L) + K for L in lens)) * per_pos
+
+
+def masked_pairs(rp, rd) -> int:
+    """Allowed (query, key) pairs of the training mask over retained rows (p, d): every
+    row sees the depth-1 keys at positions 0 .. p-d+1 and the d-1 deeper rows of its own
+    chain, plus itself."""
+    import numpy as np
+
+    p, d = np.asarray(rp, np.int64), np.asarray(rd, np.int64)
+    return int(((p - d + 1) + 1).sum() + (d - 1).sum())
+
+
+def forward_flops(dims, rp, rd) -> float:
+    """Algorithmic FLOPs of the training-style forward over the retained rows: 2 per
+    multiply-add of every projection for every row that needs it (fc only for the depth-1
+    rows -- the deeper rows share the constant fc(h_shared); every layer and the LM head
+    for all rows) plus 4 * nq * hd per allowed (query, key) pair in each of the N layers
+    (the score and the value products)."""
+    import numpy as np
+
+    M = len(rp)
+    n1 = int((np.asarray(rd) == 1).sum())
+    params = gemm_weight_bytes(dims) // 2
+    fc = dims.hidden * 3 * dims.hidden
+    gemm = 2.0 * (M * (params - fc) + n1 * fc)
+    attn = 4.0 * dims.n_layers * dims.n_q_heads * dims.head_dim * masked_pairs(rp, rd)
+    return gemm, attn
 
 
 def whole_job(dist, ms_step, units_per_rank, world, device):
@@ -404,6 +436,9 @@ def run_ours(args, rank, world, dist):
         if cpu:
             out["cpu_baseline"] = cpu
     ctx.close()
+    if rank == 0 and world == 1 and not args.no_configs:
+        out["decode_configs"] = {nm: decode_config_measure(dev, nm)
+                                 for nm in ("decode_b2", "ragged_b16") if nm != wl.name}
     if rank == 0 and world == 1 and not args.no_train_fwd:
         out["train_fwd"] = train_fwd_measure(dev)
     if rank == 0 and world == 1 and not args.no_window:
@@ -452,6 +487,34 @@ def _pass_us(dev, wl, dims, w, inp, reps=20):
     out = toks.cpu().numpy()
     ctx.close()
     return us, out
+
+
+def decode_config_measure(dev, name):
+    """Draft-pass time of another decode workload (decode_b2: concurrency 2, contexts 8192 /
+    10240, K=8; ragged_b16: the H=4096 drafter, 16 requests with contexts U[1024, 8192],
+    K=5) as a CUDA graph, with its HBM roofline: algorithmic bytes (every weight once, the
+    committed KV context and the draft block) over the pass time, against the measured
+    copy bandwidth."""
+    wl = synth.WORKLOADS[name]
+    dims = wl.dims
+    w = synth.make_weights(dims, 1234)
+    inp = synth.make_decode_inputs(wl, 99)
+    us, _ = _pass_us(dev, wl, dims, w, inp)
+    del w
+    lens = [int(x) for x in inp["seq_lens"]]
+    nbytes = gemm_weight_bytes(dims) + kv_bytes(dims, lens, wl.K)
+    pk_ = peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    R = wl.batch * wl.K
+    return {"workload": name, "batch": wl.batch, "K": wl.K,
+            "kv_len": lens if len(lens) <= 2 else {"min": min(lens), "max": max(lens),
+                                                  "mean": round(sum(lens) / len(lens), 1)},
+            "us_per_pass": round(us, 2), "draft_tok_s": round(R / (us * 1e-6), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk_["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk_["hbm_gbs"], 4),
+                         "bytes_per_pass": nbytes,
+                         "pass_roofline_us": round(nbytes / (pk_["hbm_gbs"] * 1e3), 2),
+                         "peak_source": pk_["source"] + " (burst copy)"}}
 
 
 def window_measure(dev, window=4096):
@@ -508,8 +571,7 @@ def head_measure(dev, rank=128, topk=128, vocabs=("draft_vocab", "full_vocab")):
 def train_fwd_measure(dev, reps=3):
     """Training-style masked forward of the decode drafter (n=2048, K=8, COD 0.8): time per
     forward with CUDA events, and the tensor-core roofline of its algorithmic FLOPs
-    (projections 2*M*params + masked attention 4*nq*hd*(allowed pairs)).  The projections
-    execute twice the algorithmic MMA work (bf16 hi + lo activation operands)."""
+    (forward_flops) against the measured bf16 burst peak."""
     import torch
 
     import drafting_eagle_draft_gb300 as pk
@@ -551,18 +613,18 @@ def train_fwd_measure(dev, reps=3):
         fwd()
     st = pk.peagle_read_timing(ctx)
     ctx.close()
-    params = gemm_weight_bytes(dims) // 2
-    p_np, d_np = rp.astype("int64"), rd.astype("int64")
-    # allowed (query, key) pairs of the mask: depth-1 keys up to the anchor + own chain
-    pairs = int(((p_np - d_np + 1) + 1).sum() + (d_np - 1).sum())
-    gemm_flops = 2.0 * M * params
-    attn_flops = 4.0 * dims.n_q_heads * dims.head_dim * pairs
+    gemm_flops, attn_flops = forward_flops(dims, rp, rd)
     pk_ = peaks()
     tflops = (gemm_flops + attn_flops) / (ms * 1e-3) / 1e12
     return {"workload": wl.name, "rows": M, "ms": round(ms, 3),
-            "tflops": round(tflops, 1), "peak_tflops": pk_["bf16_tflops_sustained"],
-            "frac": round(tflops / pk_["bf16_tflops_sustained"], 4),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                         "peak": pk_["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tflops / pk_["bf16_tflops"], 4),
+                         "peak_source": pk_["source"] + " bf16 burst (a forward of ~15 ms)",
+                         "flops": "projections 2 x rows x params (fc for depth-1 rows only) "
+                                  "+ attention 4 x N x nq x hd x allowed pairs"},
             "algorithmic_tflop": round((gemm_flops + attn_flops) / 1e12, 3),
+            "gemm_tflop": round(gemm_flops / 1e12, 3), "attn_tflop": round(attn_flops / 1e12, 3),
             "stages_ms": {k: round(v[0], 3) for k, v in st.items()}}
 
 
@@ -570,8 +632,8 @@ def train_step_measure(dev, reps=3):
     """Training step without optimizer on the training workload (decode drafter, n=2048,
     K=8, COD 0.8): ms per step (forward with kept activations, mean cross-entropy, every
     parameter gradient) with CUDA events, and its algorithmic FLOPs against the TF32 peak
-    (the GEMMs run on TF32 tensor cores): projections 6*M*params (forward, dX, dW) plus
-    attention 12*nq*hd*(allowed pairs) (forward 2 products, backward 4)."""
+    (the GEMMs run on TF32 tensor cores): three times the forward's (forward_flops: every
+    projection forward, dX and dW; attention forward 2 products, backward 4)."""
     import numpy as np
     import torch
 
@@ -625,17 +687,16 @@ def train_step_measure(dev, reps=3):
     e1.synchronize()
     ms = e0.elapsed_time(e1) / reps
     ctx.close()
-    params = gemm_weight_bytes(dims) // 2
-    p_np, d_np = rp.astype("int64"), rd.astype("int64")
-    pairs = int(((p_np - d_np + 1) + 1).sum() + (d_np - 1).sum())
-    flops = 6.0 * M * params + 12.0 * nq * hd * pairs
+    gemm_f, attn_f = forward_flops(dims, rp, rd)
+    flops = 3.0 * gemm_f + 3.0 * attn_f  # forward, then two products per forward product
     pk_ = peaks()
-    # TF32 peak: the measured sustained bf16 peak times the nominal dense ratio 1.1 / 2.25
-    peak = pk_["bf16_tflops_sustained"] * 1.1 / 2.25
+    # TF32 peak: the measured bf16 burst peak times GB300's nominal dense TF32 / bf16 ratio
+    peak = pk_["bf16_tflops"] * 1.1 / 2.25
     tflops = flops / (ms * 1e-3) / 1e12
     return {"workload": wl.name, "rows": M, "ms": round(ms, 3), "loss": round(loss.item(), 5),
             "tflops": round(tflops, 1), "peak_tflops": round(peak, 1),
-            "peak_source": "measured bf16 sustained x nominal TF32/bf16 ratio (1.1/2.25)",
+            "peak_source": "measured bf16 burst x GB300 nominal dense TF32/bf16 ratio "
+                           "(1.1 / 2.25 PFLOP/s)",
             "frac": round(tflops / peak, 4), "algorithmic_tflop": round(flops / 1e12, 3)}
 
 
@@ -729,6 +790,8 @@ def main():
             out = {"train_step": train_step_measure(dev)}
         elif args.only == "window":
             out = {"sliding_window": window_measure(dev)}
+        elif args.only in ("decode_b2", "ragged_b16"):
+            out = {"decode_configs": {args.only: decode_config_measure(dev, args.only)}}
         else:
             out = {"efficient_head": head_measure(dev, vocabs=(args.only[5:],))}
     else:

@@ -36,6 +36,7 @@ EXPORTS = ("peagle_create", "peagle_draft", "peagle_catch_up", "peagle_verify_gr
            "peagle_sequence_partition",
            "peagle_status",
            "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
+           "peagle_set_wait_limit",
            "peagle_decode_attention_static",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
 STAGES = ("fc", "qkv", "attn", "oproj", "gate_up", "down", "lm_head", "norm", "small")
@@ -111,6 +112,7 @@ def lib():
         L.peagle_sequence_partition.argtypes = [_i32, _vp, _vp, _i32, _vp, _vp]
         L.peagle_status.argtypes = [_vp]
         L.peagle_set_timing.argtypes = [_vp, _i32]
+        L.peagle_set_wait_limit.argtypes = [_vp, ctypes.c_uint64, _i32]
         L.peagle_decode_attention_static.argtypes = [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                                      _i32, _vp, _vp, _vp]
         L.peagle_read_timing.argtypes = [_vp, _vp, _vp]
@@ -329,6 +331,13 @@ def peagle_sequence_partition(row_p, row_d, boundaries):
 def peagle_status(ctx: Context) -> int:
     """Synchronises; returns PEAGLE_OK or PEAGLE_ERR_DEVICE (device error bits cleared)."""
     return lib().peagle_status(ctx.handle)
+
+
+def peagle_set_wait_limit(ctx: Context, limit_ns: int, unreachable_step: int = -1):
+    """Bounded-wait drill (see include/peagle.h): wait limit in ns (0 = default 2 s) and a
+    step of the pass whose waits cannot end (-1 none)."""
+    _check(lib().peagle_set_wait_limit(ctx.handle, int(limit_ns), int(unreachable_step)),
+           "peagle_set_wait_limit")
 
 
 def peagle_set_timing(ctx: Context, enable: bool):

@@ -562,12 +562,7 @@ static void attn_mma_launch(const AttnArgs& a, cudaStream_t s) {
   const int rows = a.K * (a.nq / a.nkv);
   const int warps = (rows + 15) / 16;
   const size_t sm = (size_t)4 * MMA_KT * HD * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         100 * 1024);
-    attr_set = true;
-  }
+  smem_optin((const void*)attn_mma_kernel<HD>, 100 * 1024);
   dim3 grid(a.nchunk, a.nkv, a.B);
   launch_pdl(attn_mma_kernel<HD>, grid, dim3(32 * warps), sm, s, a);
   launch_pdl(attn_merge_kernel<bf16, HD>, dim3(cdiv(rows, 4), a.nkv, a.B), dim3(128), 0, s, a);
@@ -577,12 +572,7 @@ template <typename T, int HD>
 static void attn_launch(const AttnArgs& a, cudaStream_t s) {
   const int rows = a.K * (a.nq / a.nkv);
   size_t sm = (size_t)(rows * HD + 32 * (HD + 1) + 32 * HD) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(attn_decode_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
-    attr_set = true;
-  }
+  smem_optin((const void*)attn_decode_kernel<T, HD>, 200 * 1024);
   dim3 grid(a.nchunk, a.nkv, a.B);
   launch_pdl(attn_decode_kernel<T, HD>, grid, dim3(256), sm, s, a);
 }
@@ -971,12 +961,7 @@ static void masked_mma_launch(const MaskedAttnArgs& a, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const int QR = MASK_MMA_ROWS / G;
   const size_t sm = (size_t)4 * MMA_KT * HD * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(masked_attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sm);
-    attr_set = true;
-  }
+  smem_optin((const void*)masked_attn_mma_kernel<HD>, (int)sm);
   dim3 grid((unsigned)cdiv(a.M, QR), (unsigned)a.nkv);
   launch_pdl(masked_attn_mma_kernel<HD>, grid, dim3(128), sm, s, a);
 }
@@ -1339,12 +1324,7 @@ static void head_score_mma_launch(int blocks, cudaStream_t s, int R, int Vd, con
                                   const bf16* score, float* approx, unsigned* hist,
                                   unsigned* err) {
   const size_t smem = (size_t)HS_STAGES * HS_STAGE_BYTES;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(head_score_mma_kernel<RANK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    attr_set = true;
-  }
+  smem_optin((const void*)head_score_mma_kernel<RANK>, (int)smem);
   launch_pdl(head_score_mma_kernel<RANK>, dim3(blocks), dim3(HS_THREADS), smem, s, R, Vd, zfx,
              score, approx, hist, err);
 }
@@ -1780,7 +1760,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 float* g_static_ptr[kMaxDevices] = {};   // device address of the array, per device
-bool g_static_attr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (looked up once per device:
 // in host code the array's name is only a host-side stand-in).
@@ -1798,14 +1777,9 @@ int static_scratch(float** out) {
     }
     g_static_ptr[dev] = (float*)p;
   }
-  if (!g_static_attr[dev]) {
-    if (cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             100 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             100 * 1024) != cudaSuccess)
-      return PEAGLE_ERR_CUDA;
-    g_static_attr[dev] = true;
-  }
+  if (smem_optin((const void*)attn_mma_kernel<64>, 100 * 1024) != cudaSuccess ||
+      smem_optin((const void*)attn_mma_kernel<128>, 100 * 1024) != cudaSuccess)
+    return PEAGLE_ERR_CUDA;
   *out = g_static_ptr[dev];
   return PEAGLE_OK;
 }
@@ -1853,17 +1827,16 @@ extern "C" int peagle_decode_attention_static(int32_t batch, int32_t K, int32_t 
             batch, n_kv_heads, rows, per_chunk, (unsigned)PEAGLE_STATIC_ATTN_SCRATCH_BYTES);
     return PEAGLE_ERR_CAPACITY;
   }
-  int want = (2 * num_sms + batch * n_kv_heads - 1) / (batch * n_kv_heads);
+  const long long units = (long long)batch * n_kv_heads;
+  long long want = (2LL * num_sms + units - 1) / units;
   if (want < 1) want = 1;
   if (want > 64) want = 64;
-  if ((size_t)want > max_chunks) want = (int)max_chunks;
-  int chunk = (capacity + want - 1) / want;
-  chunk = (chunk + 63) / 64 * 64;
-  int nchunk = (capacity + chunk - 1) / chunk;
-  while ((size_t)nchunk > max_chunks || nchunk > 64) {
-    chunk += 64;
-    nchunk = (capacity + chunk - 1) / chunk;
-  }
+  if ((unsigned long long)want > max_chunks) want = (long long)max_chunks;
+  // whole 64-key tiles per chunk; chunk >= capacity / want, so at most `want` chunks
+  const long long chunk64 = ((capacity + want - 1) / want + 63) / 64 * 64;
+  if (chunk64 > 0x7fffffffLL) return PEAGLE_ERR_UNSUPPORTED;
+  const int chunk = (int)chunk64;
+  const int nchunk = (int)((capacity + chunk64 - 1) / chunk64);
   float* scratch = nullptr;
   int r = static_scratch(&scratch);
   if (r != PEAGLE_OK) return r;

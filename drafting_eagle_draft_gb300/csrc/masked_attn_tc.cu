@@ -325,13 +325,8 @@ int masked_attn_tc_launch(TcGemmPlan* pl, const MaskedAttnArgs& a, cudaStream_t 
       !tc_tensor_map(pl, &mv1, a.v1, a.n, w, w, 64) ||
       !tc_tensor_map(pl, &mk, a.k, a.M, w, w, 64) || !tc_tensor_map(pl, &mv, a.v, a.M, w, w, 64))
     return PEAGLE_ERR_UNSUPPORTED;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(masked_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             MT_SMEM) != cudaSuccess)
-      return PEAGLE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (smem_optin((const void*)masked_attn_tc_kernel, MT_SMEM) != cudaSuccess)
+    return PEAGLE_ERR_CUDA;
   const int QR = 128 / (a.nq / a.nkv);
   dim3 grid((unsigned)((a.M + QR - 1) / QR), (unsigned)a.nkv);
   cudaError_t e = launch_pdl(masked_attn_tc_kernel, grid, dim3(MT_THREADS), (size_t)MT_SMEM, s,

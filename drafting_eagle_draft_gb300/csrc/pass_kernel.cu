@@ -36,7 +36,6 @@ namespace {
 constexpr int PK_THREADS = 224;
 constexpr int PK_BWARP = 6;  // activation producer (warps 2-5 are the workers)
 constexpr int PK_A_BYTES = 128 * 128;       // one 128 x 64 bf16 weight tile
-constexpr uint64_t PK_WAIT_NS = 2000000000ull;
 
 __device__ __forceinline__ void wk_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -130,16 +129,17 @@ __device__ bool wk_wait_phase(const PassParams& P, int ph, int et, volatile int*
                               volatile int* s_flag) {
   if (et == 0) {
     int ok = 1;
-    if (ph >= 0 && ld_relaxed(P.phase_cnt + ph) < gridDim.x) {
+    const unsigned need = gridDim.x + (ph == P.stall_phase ? 1u : 0u);
+    if (ph >= 0 && ld_relaxed(P.phase_cnt + ph) < need) {
       const uint64_t t0 = tc::globaltimer();
       unsigned spins = 0;
-      while (ld_relaxed(P.phase_cnt + ph) < gridDim.x) {
+      while (ld_relaxed(P.phase_cnt + ph) < need) {
         if ((++spins & 63u) != 0) continue;
         if (aborted(P, s_abort)) {
           ok = 0;
           break;
         }
-        if (tc::globaltimer() - t0 > PK_WAIT_NS) {
+        if (tc::globaltimer() - t0 > P.wait_ns) {
           set_abort(P, s_abort);
           ok = 0;
           break;
@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 2;
-  uint32_t* s_tmem = (uint32_t*)(acce + 2);
+  uint64_t* drain = acce + 2;  // the MMA issuer's last MMAs after an abort
+  uint32_t* s_tmem = (uint32_t*)(drain + 1);
   volatile int* s_flag = (volatile int*)(s_tmem + 1);
   volatile int* s_abort = s_flag + 1;
   volatile int* s_adone = s_flag + 2;
@@ -379,6 +380,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       tc::mbar_init(&accf[i], 1);
       tc::mbar_init(&acce[i], 128);
     }
+    tc::mbar_init(drain, 1);
     *s_abort = 0;
     *s_adone = 0;
     for (int i = 0; i < 2 * PASS_MAX_ROWS; ++i) s_rs[i] = 0ull;
@@ -394,6 +396,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  const uint64_t wns = P.wait_ns;
   if (P.trace && c == 0 && threadIdx.x == 0) P.trace[0] = tc::globaltimer();
 
   if (warp == 0) {
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       int st = 0;
       uint32_t par = 0;  // parity of the empty-barrier phase the next reuse waits for
       while (ca.g < n_gemm) {
-        if (nA >= S && !tc::mbar_wait(&empty[st], par, s_abort)) {
+        if (nA >= S && !tc::mbar_wait(&empty[st], par, s_abort, wns)) {
           if (!*s_abort) set_abort(P, s_abort);
           break;
         }
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               ok = false;  // the weight producer stopped (abort)
               break;
             }
-            if ((++spins & 255u) == 0 && tc::globaltimer() - t0 > PK_WAIT_NS) {
+            if ((++spins & 255u) == 0 && tc::globaltimer() - t0 > wns) {
               if (!*s_abort) set_abort(P, s_abort);
               ok = false;
               break;
@@ -478,13 +481,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         if (ok && dep > ready) {
           const uint64_t t0 = tc::globaltimer();
           unsigned spins = 0;
-          while (ld_relaxed(phase_cnt + dep) < (unsigned)G) {
+          const unsigned need = (unsigned)G + (dep == P.stall_phase ? 1u : 0u);
+          while (ld_relaxed(phase_cnt + dep) < need) {
             if ((++spins & 63u) == 0) {
               if (aborted(P, s_abort)) {
                 ok = false;
                 break;
               }
-              if (tc::globaltimer() - t0 > PK_WAIT_NS) {
+              if (tc::globaltimer() - t0 > wns) {
                 set_abort(P, s_abort);
                 ok = false;
                 break;
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           if (seg_end > end) seg_end = end;
           const int buf = seg & 1;
           const uint32_t use = (uint32_t)(seg >> 1);
-          if (!tc::mbar_wait(&acce[buf], (use & 1u) ^ 1u, s_abort)) {
+          if (!tc::mbar_wait(&acce[buf], (use & 1u) ^ 1u, s_abort, wns)) {
             if (!*s_abort) set_abort(P, s_abort);
             ok = false;
             break;
@@ -549,7 +553,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           const uint32_t d = tmem + (uint32_t)(buf * acc_stride);
           const long long seg_beg = it;
           for (; it < seg_end; ++it) {
-            if (!tc::mbar_wait(&full[st], ph, s_abort)) {
+            if (!tc::mbar_wait(&full[st], ph, s_abort, wns)) {
               if (!*s_abort) set_abort(P, s_abort);
               ok = false;
               break;
@@ -572,6 +576,13 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           if (it >= end) trace_ev(P, gph, 2);
           ++seg;
         }
+      }
+      if (!ok) {
+        // aborted: the MMAs already issued still write tensor memory, which is freed when
+        // the CTA leaves; wait (bounded) until they have completed
+        int never = 0;
+        tc::mma_commit(drain);
+        tc::mbar_wait(drain, 0u, &never, 10000000ull);
       }
     }
   } else if (warp >= 2 && warp < 6) {
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             const uint32_t use = (uint32_t)(seg >> 1);
             ++seg;
             if (et == 0) {
-              *s_flag = tc::mbar_wait(&accf[buf], use & 1u, s_abort) ? 1 : 0;
+              *s_flag = tc::mbar_wait(&accf[buf], use & 1u, s_abort, wns) ? 1 : 0;
               if (!*s_flag && !*s_abort) set_abort(P, s_abort);
             }
             wk_bar();
@@ -818,23 +829,17 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
 
 size_t pass_smem_bytes(int stages, int b_stage_bytes, int uni_bytes) {
   return 1024 /*align slack*/ + (size_t)stages * (PK_A_BYTES + b_stage_bytes) + uni_bytes +
-         (size_t)(2 * stages + 4) * 8 + 64 + 16;
+         (size_t)(2 * stages + 5) * 8 + 64 + 16;
 }
 
 int pass_launch(const PassParams& P, int head_dim, int grid, cudaStream_t s) {
   const size_t smem = pass_smem_bytes(P.stages, P.b_stage_bytes, P.uni_bytes);
   void (*kern)(const PassParams) = head_dim == 64 ? pass_kernel<64> : pass_kernel<128>;
-  static size_t attr_set[2] = {0, 0};
-  const int ki = head_dim == 64 ? 0 : 1;
-  if (attr_set[ki] < smem) {
-    cudaError_t ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)smem);
-    if (ae != cudaSuccess) {
-      fprintf(stderr, "peagle: pass kernel shared memory (%zu bytes): %s\n", smem,
-              cudaGetErrorString(ae));
-      return PEAGLE_ERR_CUDA;
-    }
-    attr_set[ki] = smem;
+  cudaError_t ae = smem_optin((const void*)kern, smem);
+  if (ae != cudaSuccess) {
+    fprintf(stderr, "peagle: pass kernel shared memory (%zu bytes): %s\n", smem,
+            cudaGetErrorString(ae));
+    return PEAGLE_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -13,6 +13,7 @@ namespace peagle {
 constexpr int PASS_MAX_LAYERS = 8;
 constexpr int PASS_MAX_GEMM = 3 + 4 * PASS_MAX_LAYERS;
 constexpr int PASS_MAX_PHASE = 5 + 9 * PASS_MAX_LAYERS;
+constexpr unsigned long long PASS_DEFAULT_WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 constexpr int PASS_MAX_ROWS = 120;                    // R = B*K (hi + lo rows <= 240)
 constexpr int PASS_SS_SLOTS = 2 + 2 * PASS_MAX_LAYERS;  // per-row sums of squares
 // K/V tile buffers of an attention item (64 keys each).  Deeper pipelines (all four tiles
@@ -62,6 +63,12 @@ struct PassParams {
   int nq, nkv, hd, cap;
   float eps;
   size_t layer_stride;
+  // bounded waits: every wait of the kernel gives up after wait_ns nanoseconds (then the
+  // device error word gets TIMEOUT and the CTAs leave); stall_phase >= 0 names a step whose
+  // waits require one signal more than the grid gives, so that they run out (a test of
+  // that path), -1 none
+  unsigned long long wait_ns;
+  int stall_phase;
   // library-owned buffers
   const void* embed;
   const void* emb_mask;

@@ -119,6 +119,10 @@ struct peagle_ctx {
   std::vector<std::vector<int>> trace_stages;
   unsigned long long* pass_trace_cta;  // per-CTA signal times of the latest traced pass
   int trace_cta_phases;
+  // bounded waits of the pass kernel (peagle_set_wait_limit)
+  unsigned long long wait_ns;
+  int stall_phase;
+  size_t F_bytes;
   std::vector<void*> allocs;
   TrainWs* tw = nullptr;
   cublasHandle_t blas = nullptr;
@@ -285,6 +289,8 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   c->timing = false;
   c->ev_used = 0;
   c->pending_stage = -1;
+  c->wait_ns = PASS_DEFAULT_WAIT_NS;
+  c->stall_phase = -1;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     delete c;
@@ -356,7 +362,8 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
   const int R = c->rows_max;
   // fc outputs: one per request (draft pass), per row (catch-up) or per position (forward)
   const int fr = d.max_batch * d.max_K > d.max_seq ? d.max_batch * d.max_K : d.max_seq;
-  TRY(dalloc(c, (void**)&c->F, (size_t)(fr > 1 ? fr : 1) * H * 8));
+  c->F_bytes = (size_t)(fr > 1 ? fr : 1) * H * 8;
+  TRY(dalloc(c, (void**)&c->F, c->F_bytes));
   TRY(dalloc(c, (void**)&c->f_shared, (size_t)H * 8));
   TRY(dalloc(c, &c->X0, (size_t)R * 2 * H * es));
   TRY(dalloc(c, (void**)&c->res, (size_t)R * H * 8));
@@ -500,6 +507,8 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   key.new_token = new_token;
   key.out_tokens = out_tokens;
   key.out_logits = out_logits;
+  P.wait_ns = c->wait_ns;
+  P.stall_phase = c->stall_phase;
   if (!c->timing && c->pp_valid && memcmp(&key, &c->pp_key, sizeof(key)) == 0) {
     cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, (size_t)(P.n_phase + 1) * 4, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "pass counters");
@@ -1522,6 +1531,31 @@ extern "C" int peagle_sequence_partition(int32_t M, const int32_t* row_p, const 
   return PEAGLE_OK;
 }
 
+// After a pass that gave up on a bounded wait, the accumulators that the kernels clear as
+// they consume them (fixed-point fc rows, q / k / v sums, GEMM tile counters, split-KV merge
+// counters, the efficient head's counters) may hold a partial pass: zero them so the next
+// call starts clean.
+static int reset_after_timeout(peagle_ctx* c) {
+  const peagle_dims& d = c->d;
+  const size_t nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim;
+  struct Z { void* p; size_t n; } z[] = {
+      {c->F, c->F_bytes},
+      {c->pass_qfx, (size_t)PASS_MAX_ROWS * nq * hd * 8},
+      {c->pass_kvfx, (size_t)PASS_MAX_ROWS * 2 * nkv * hd * 8},
+      {c->mk_qfx, (size_t)d.max_batch * d.max_K * nq * hd * 8},
+      {c->mk_kvfx, (size_t)d.max_batch * d.max_K * 2 * nkv * hd * 8},
+      {c->att_cnt, (size_t)d.max_batch * nkv * 4},
+      {c->tc ? tc_tile_counters(c->tc) : nullptr, c->tc ? (size_t)tc_max_tiles(c->tc) * 4 : 0},
+      {c->lm_done, 4},
+      {c->lm_gcount, (size_t)d.max_batch * d.max_K * 4},
+      {c->lm_gdone, (size_t)d.max_batch * d.max_K * 4},
+      {c->lm_hist, (size_t)d.max_batch * d.max_K * 2048 * 4},
+  };
+  for (const Z& e : z)
+    if (e.p && e.n && cudaMemset(e.p, 0, e.n) != cudaSuccess) return PEAGLE_ERR_CUDA;
+  return cudaDeviceSynchronize() == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+}
+
 extern "C" int peagle_status(peagle_ctx* c) {
   if (!c) return PEAGLE_ERR_INVALID;
   cudaError_t e = cudaDeviceSynchronize();
@@ -1531,8 +1565,16 @@ extern "C" int peagle_status(peagle_ctx* c) {
   c->last_err_bits = bits;
   if (bits) {
     cudaMemset(c->err, 0, 4);
+    if ((bits & PEAGLE_DEV_TIMEOUT) && reset_after_timeout(c) != PEAGLE_OK) return PEAGLE_ERR_CUDA;
     return PEAGLE_ERR_DEVICE;
   }
+  return PEAGLE_OK;
+}
+
+extern "C" int peagle_set_wait_limit(peagle_ctx* c, uint64_t limit_ns, int32_t unreachable_step) {
+  if (!c || unreachable_step < -1 || unreachable_step >= PASS_MAX_PHASE) return PEAGLE_ERR_INVALID;
+  c->wait_ns = limit_ns ? (unsigned long long)limit_ns : PASS_DEFAULT_WAIT_NS;
+  c->stall_phase = unreachable_step;
   return PEAGLE_OK;
 }
 

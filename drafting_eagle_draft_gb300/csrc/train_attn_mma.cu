@@ -583,12 +583,7 @@ void launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const
   round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, Qh);
   for (float* p : {K1, V1}) round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
   const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(attn_fwd_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    attr_set = true;
-  }
+  smem_optin((const void*)attn_fwd_prefix_kernel, (int)smem);
   attn_fwd_prefix_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, K1, V1, Op,
                                                                            mrow, lrow);
   attn_fwd_combine_kernel<<<(a.nq * a.M + 7) / 8, 256, 0, s>>>(a, Qh, Kr, Vr, Op, mrow, lrow, Pc,
@@ -601,12 +596,7 @@ void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, c
                            float* dV1, bool qkv_rounded, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    attr_set = true;
-  }
+  smem_optin((const void*)attn_bwd_dq_kernel, (int)smem);
   // the stored operands are rounded to TF32 once, not per use in the products (Q, K1 and
   // V1 already are when the forward ran fused)
   round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)dOh);

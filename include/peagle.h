@@ -135,10 +135,15 @@ typedef struct peagle_kv {
   int32_t batch;    /* request slots in the buffers (>= the call's batch)           */
 } peagle_kv;
 
-/* Create a drafter context: validates dims, allocates all device memory the other
- * calls need (weights, workspaces sized for max_batch x max_K rows and max_rows),
- * copies and repacks the weights, precomputes fc(h_shared) and the RoPE table,
- * and synchronises.  The only allocating call.  *out is NULL on failure. */
+/* Create a drafter context ("P-EAGLE: A Technical Deep Dive into Parallel Speculative
+ * Decoding", section "2. The P-EAGLE Parallel Drafter": the drafter's weights, including
+ * the learnable emb(mask) and h_shared that every MTP position shares, are fixed for the
+ * whole deployment; "Speeding LLM inference with P-EAGLE in vLLM/Speculators", section
+ * "A learnable mask parameter": h_shared is 3H wide).  Validates dims, allocates all
+ * device memory the other calls need (weights, workspaces sized for max_batch x max_K
+ * rows and max_rows), copies and repacks the weights, precomputes fc(h_shared) (a
+ * constant of the weights) and the RoPE table, and synchronises.  The only allocating
+ * call.  *out is NULL on failure. */
 int peagle_create(const peagle_weights* w, const peagle_dims* dims, peagle_ctx** out);
 
 /* One parallel draft pass ("2. The P-EAGLE Parallel Drafter").
@@ -188,7 +193,11 @@ int peagle_verify_greedy(int32_t batch, int32_t K, const int32_t* draft_tokens,
                          const int32_t* target_argmax, int32_t* out_accept_len,
                          int32_t* out_bonus, void* stream);
 
-/* Commit accepted rows to the KV cache and advance seq_lens (device, in place):
+/* Commit accepted rows to the drafter's KV cache ("P-EAGLE: A Technical Deep Dive into
+ * Parallel Speculative Decoding", section "Technical Architecture": each speculative round
+ * ends with the accepted tokens' keys and values entering the drafter's cache, so the next
+ * draft pass attends to them; "EAGLE-4", "EAGLE-4 overview": the accepted prefix plus
+ * the bonus token are what a round emits) and advance seq_lens (device, in place):
  *   n_commit device int32 [batch]; request b commits n = n_commit[b] + n_extra rows
  *     (e.g. out_accept_len of peagle_verify_greedy with n_extra = 1: the NTP row and
  *     the accepted drafts, without a round trip to the host).
@@ -286,8 +295,9 @@ int peagle_sequence_partition(int32_t M, const int32_t* row_p, const int32_t* ro
                               int32_t n_chunks, const int32_t* boundaries, int32_t* out_chunk);
 
 /* Synchronise the context's device work and return PEAGLE_OK, PEAGLE_ERR_DEVICE if
- * the device error word is non-zero (the word is then cleared), or PEAGLE_ERR_CUDA
- * if a sticky CUDA error is pending. */
+ * the device error word is non-zero (the word is then cleared; after a TIMEOUT the
+ * context's accumulators are also reset), or PEAGLE_ERR_CUDA if a sticky CUDA error is
+ * pending. */
 int peagle_status(peagle_ctx* ctx);
 
 /* Per-stage timing (diagnostics).  Stages of the pass: */
@@ -327,6 +337,21 @@ int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches
 int32_t peagle_read_pass_trace(peagle_ctx* ctx, uint64_t* out, int32_t max_entries,
                                int32_t* out_phases, int32_t* out_ctas);
 
+/* Failure-path drill of the bounded waits (diagnostics; the pages have no counterpart:
+ * this tests how the library leaves a wait that cannot end).  Every wait of the persistent
+ * pass kernel (step completions, ring stages, accumulators) gives up after limit_ns
+ * nanoseconds (0 restores the default of 2 s); on expiry the kernel latches
+ * PEAGLE_DEV_TIMEOUT, raises its abort flag so every CTA leaves its waits, lets the loads
+ * and tensor-core operations it issued complete, frees its tensor memory and returns.
+ * unreachable_step >= 0 names a step of the pass (its index in pass order: 0 the fc
+ * projection, 1 the input rows, then per layer the QKV projection(s), q/k/v finalise,
+ * attention, merge, o-projection, norm, gate/up, down, ...) whose waits require one
+ * completion signal more than the grid gives, so that they run out; -1 none.  Applies to
+ * the following draft and catch-up passes of this context.  peagle_status reports the
+ * TIMEOUT bit and resets the context's accumulators, so the next pass starts clean.
+ * Returns PEAGLE_ERR_INVALID for a step index outside the kernel's range. */
+int peagle_set_wait_limit(peagle_ctx* ctx, uint64_t limit_ns, int32_t unreachable_step);
+
 /* Size of the library's static scratch array used by peagle_decode_attention_static. */
 #define PEAGLE_STATIC_ATTN_SCRATCH_BYTES (8u << 20)
 
@@ -340,9 +365,14 @@ int32_t peagle_read_pass_trace(peagle_ctx* ctx, uint64_t* out, int32_t max_entri
  * (rows b*K + j) and query head h, softmax(q . k / sqrt(head_dim)) . v over the cached
  * keys/values of kv head h / (n_q_heads / n_kv_heads) at slots 0 .. seq_lens[b] + j.
  *   q        device fp32 [batch*K][n_q_heads][head_dim] (keys are not rotated here: q and
- *            the cache are taken as already RoPE-rotated)
+ *            the cache are taken as already RoPE-rotated).  The kernel rounds each query
+ *            element to bf16 (round to nearest even) before the score products, as the
+ *            draft pass does; softmax and accumulation stay fp32.
  *   k_cache, v_cache  device bf16 [batch][n_kv_heads][capacity][head_dim] (one layer)
  *   seq_lens device int32 [batch]; keys at slots >= min(seq_lens[b] + K, capacity) unused
+ *            (a row whose slot seq_lens[b] + j is at or beyond capacity sees the keys
+ *            below capacity only); a request with seq_lens[b] < 0 is skipped and its
+ *            output rows are left unwritten
  *   out      device fp32 [batch*K][n_q_heads][head_dim]
  * Limits: head_dim 64 or 128; K * n_q_heads / n_kv_heads <= 128; the split-KV partials,
  * batch * n_kv_heads * chunks * K * (n_q_heads/n_kv_heads) * (head_dim + 2) floats, must fit
