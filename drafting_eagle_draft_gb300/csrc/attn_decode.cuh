@@ -95,7 +95,9 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
 }
 
 // NBUF K/V tile buffers (<= 4): the loads of up to NBUF tiles are in flight at once.
-template <int HD, int NBUF, typename Bar>
+// QFX: a.q holds the queries as 64-bit fixed point (the persistent pass kernel's sums)
+// instead of fp32.
+template <int HD, int NBUF, typename Bar, bool QFX = false>
 __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, int c, int tid,
                                               int nthr, uint8_t* sm_raw, Bar bar) {
   static_assert(NBUF >= 2 && NBUF <= 4, "1 < NBUF <= 4");
@@ -139,22 +141,25 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
   const int r0 = warp * 16 + gq, r1 = r0 + 8;
   const bool v0 = r0 < rows, v1 = r1 < rows;
   const int j0 = v0 ? r0 / G : 0, j1 = v1 ? r1 / G : 0;
-  const float* qg = (const float*)a.q;
-  const float* q0 = qg + ((size_t)(b * a.K + j0) * a.nq + g * G + (r0 - j0 * G)) * HD;
-  const float* q1 = qg + ((size_t)(b * a.K + j1) * a.nq + g * G + (r1 - j1 * G)) * HD;
+  const size_t qo0 = ((size_t)(b * a.K + j0) * a.nq + g * G + (r0 - j0 * G)) * HD;
+  const size_t qo1 = ((size_t)(b * a.K + j1) * a.nq + g * G + (r1 - j1 * G)) * HD;
+  auto qv = [&](size_t off) -> float {
+    if constexpr (QFX) return from_fx(__ldcg((const fx_t*)a.q + off));
+    else return ((const float*)a.q)[off];
+  };
   uint32_t qa[KS][4];  // bf16 queries (the scale is applied to the scores)
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     const int d0 = ks * 16 + 2 * tq, d1 = d0 + 8;
     float x[8];
-    x[0] = v0 ? q0[d0] : 0.f;
-    x[1] = v0 ? q0[d0 + 1] : 0.f;
-    x[2] = v1 ? q1[d0] : 0.f;
-    x[3] = v1 ? q1[d0 + 1] : 0.f;
-    x[4] = v0 ? q0[d1] : 0.f;
-    x[5] = v0 ? q0[d1 + 1] : 0.f;
-    x[6] = v1 ? q1[d1] : 0.f;
-    x[7] = v1 ? q1[d1 + 1] : 0.f;
+    x[0] = v0 ? qv(qo0 + d0) : 0.f;
+    x[1] = v0 ? qv(qo0 + d0 + 1) : 0.f;
+    x[2] = v1 ? qv(qo1 + d0) : 0.f;
+    x[3] = v1 ? qv(qo1 + d0 + 1) : 0.f;
+    x[4] = v0 ? qv(qo0 + d1) : 0.f;
+    x[5] = v0 ? qv(qo0 + d1 + 1) : 0.f;
+    x[6] = v1 ? qv(qo1 + d1) : 0.f;
+    x[7] = v1 ? qv(qo1 + d1 + 1) : 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) qa[ks][u] = pack_bf16(x[2 * u], x[2 * u + 1]);
   }

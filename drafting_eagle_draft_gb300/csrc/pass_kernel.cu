@@ -156,6 +156,37 @@ __device__ bool wk_wait_phase(const PassParams& P, int ph, int et, volatile int*
   return ok;
 }
 
+// Worker thread 0 waits until *ctr >= need (bounded); the result is broadcast to the 128
+// workers.  False on abort or timeout.
+__device__ bool wk_wait_count(const PassParams& P, const unsigned* ctr, unsigned need, int et,
+                              volatile int* s_abort, volatile int* s_flag) {
+  if (et == 0) {
+    int ok = 1;
+    if (ld_relaxed(ctr) < need) {
+      const uint64_t t0 = tc::globaltimer();
+      unsigned spins = 0;
+      while (ld_relaxed(ctr) < need) {
+        if ((++spins & 63u) != 0) continue;
+        if (aborted(P, s_abort)) {
+          ok = 0;
+          break;
+        }
+        if (tc::globaltimer() - t0 > P.wait_ns) {
+          set_abort(P, s_abort);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    fence_acquire_gpu();
+    *s_flag = ok;
+  }
+  wk_bar();
+  const bool ok = *s_flag != 0;
+  wk_bar();
+  return ok;
+}
+
 // Timing: event k of (phase, this CTA) -- 0: activations of a projection ready (seen by
 // the activation producer), 1: first MMA issued, 2: last accumulator committed, 3: done.
 __device__ __forceinline__ void trace_ev(const PassParams& P, int ph, int k) {
@@ -307,36 +338,6 @@ __device__ void step_norm(const PassParams& P, int c, int G, int slot, const bf1
     }
   }
   ss_flush(P, P.ss + (size_t)slot * R, s_rs, et);
-}
-
-// Fixed-point q / k / v of one layer -> fp32 queries and the bf16 KV cache slots of the
-// draft rows (seq_lens[b] + j); the accumulators are cleared for the next layer.
-__device__ void step_qkv_fin(const PassParams& P, int layer, int c, int G, int et) {
-  const int R = P.R, K = P.K, hd = P.hd;
-  const int qw = P.nq * hd, kvw = P.nkv * hd;
-  const int nQ = R * qw, nKV = R * 2 * kvw;
-  const int tid = c * 128 + et, nthr = G * 128;
-  for (int i = tid; i < nQ; i += nthr) {
-    P.Qf[i] = from_fx(P.q_fx[i]);
-    P.q_fx[i] = 0;
-  }
-  bf16* kc = (bf16*)((char*)P.att.kc + (size_t)layer * P.layer_stride);
-  bf16* vc = (bf16*)((char*)P.att.vc + (size_t)layer * P.layer_stride);
-  for (int i = tid; i < nKV; i += nthr) {
-    const int r = i / (2 * kvw), rem = i - r * 2 * kvw;
-    const int sec = rem / kvw, gk = rem - sec * kvw;
-    const int g = gk / hd, e = gk - g * hd;
-    const int b = r / K;
-    const int pos = P.row_pos[r];
-    const float v = from_fx(P.kv_fx[i]);
-    P.kv_fx[i] = 0;
-    if (pos < 0 || pos >= P.cap) {
-      if (rem == 0) raise_error(P.err, PEAGLE_DEV_KV_OVERFLOW);
-      continue;  // no cache slot for this row
-    }
-    bf16* dst = sec == 0 ? kc : vc;
-    dst[(((size_t)b * P.nkv + g) * P.cap + pos) * hd + e] = __float2bfloat16_rn(v);
-  }
 }
 
 template <int HD>
@@ -776,36 +777,86 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           step_input(P, c, G, et, s_rs, s_tok);
         } else if (ph.kind == PP_NORM) {
           step_norm(P, c, G, ph.slot, (const bf16*)ph.gamma, et, s_rs);
-        } else if (ph.kind == PP_QKVFIN) {
-          step_qkv_fin(P, ph.layer, c, G, et);
-        } else if (ph.kind == PP_ATTN || ph.kind == PP_MERGE) {
+        } else if (ph.kind == PP_ATTN) {
+          // One split-KV item (request b, kv head g, key chunk cc) per CTA.  The item reads
+          // its queries straight from the QKV projection's fixed-point sums and first moves
+          // the draft block's keys / values in its key range from the sums into their cache
+          // slots.  Once every item of (b, g) has written its partials (a count per layer,
+          // request and kv head), item cc merges the query rows
+          // [cc * rows / nv, (cc + 1) * rows / nv) and clears their q / k / v sums for the
+          // next layer; for a request without keys item 0 writes zero rows.
           AttnArgs a = P.att;
-          a.kc = (const char*)a.kc + (size_t)ph.layer * P.layer_stride;
-          a.vc = (const char*)a.vc + (size_t)ph.layer * P.layer_stride;
-          const int rows = a.K * (a.nq / a.nkv);
-          if (ph.kind == PP_ATTN) {
-            const int n_items = a.nchunk * a.nkv * a.B;
-            for (int i = c; i < n_items; i += G) {
-              const int cc = i % a.nchunk;
-              const int g = (i / a.nchunk) % a.nkv;
-              const int b = i / (a.nchunk * a.nkv);
-              attn_mma_item<HD, pass_att_nbuf(HD)>(a, b, g, cc, et, 128, uni,
-                                                   []() { wk_bar(); });
+          const int layer = ph.layer;
+          a.kc = (const char*)a.kc + (size_t)layer * P.layer_stride;
+          a.vc = (const char*)a.vc + (size_t)layer * P.layer_stride;
+          a.q = P.q_fx;
+          const int Gq = a.nq / a.nkv;
+          const int rows = a.K * Gq;
+          const int hd = a.hd, kvw = a.nkv * hd;
+          fx_t* const qx = P.q_fx;
+          fx_t* const kvx = P.kv_fx;
+          const int n_items = a.nchunk * a.nkv * a.B;
+          for (int i = c; i < n_items; i += G) {
+            const int cc = i % a.nchunk;
+            const int g = (i / a.nchunk) % a.nkv;
+            const int b = i / (a.nchunk * a.nkv);
+            const int L = a.seq_lens[b];
+            int first = 0, total = 0;
+            attn_span(a, L, &first, &total);
+            const int nv = L < 0 ? 0 : attn_nvalid(a, first, total);
+            if (cc < nv) {
+              const int kbeg = first + cc * a.chunk, kend = min(total, kbeg + a.chunk);
+              const int p0 = max(kbeg, L), p1 = min(kend, L + a.K);
+              bf16* kc = (bf16*)a.kc + ((size_t)b * a.nkv + g) * a.cap * hd;
+              bf16* vc = (bf16*)a.vc + ((size_t)b * a.nkv + g) * a.cap * hd;
+              const int nd = p1 > p0 ? (p1 - p0) * hd : 0;
+              for (int e = et; e < nd; e += 128) {
+                const int p = p0 + e / hd, d = e % hd;
+                const size_t r = (size_t)b * a.K + (p - L);
+                const fx_t* src = kvx + r * 2 * kvw + g * hd + d;
+                kc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(__ldcg(src)));
+                vc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(__ldcg(src + kvw)));
+              }
+              if (et == 0 && g == 0 && cc == nv - 1 && L + a.K > a.cap)
+                raise_error(P.err, PEAGLE_DEV_KV_OVERFLOW);
+              wk_bar();
+              auto bar = []() { wk_bar(); };
+              attn_mma_item<HD, pass_att_nbuf(HD), decltype(bar), true>(a, b, g, cc, et, 128, uni,
+                                                                         bar);
             }
-          } else {
-            const int n_items = rows * a.nkv * a.B;
-            for (int i = c * 4 + wid; i < n_items; i += G * 4) {
-              const int rr = i % rows;
-              const int g = (i / rows) % a.nkv;
-              const int b = i / (rows * a.nkv);
-              const int L = a.seq_lens[b];
-              int first, total;
-              attn_span(a, L, &first, &total);
-              if (L < 0 || total <= first) continue;
-              attn_merge_rows<bf16, HD>(a, b, g, rows, attn_nvalid(a, first, total), rr, rr + 1,
-                                        lane);
+            const int share = nv > 0 ? nv : 1;
+            if (cc >= share) continue;
+            unsigned* acnt = P.phase_cnt + P.n_phase + 1 + ((size_t)layer * a.B + b) * a.nkv + g;
+            wk_bar();
+            if (et == 0) red_release_add(acnt, 1u);
+            if (!wk_wait_count(P, acnt, (unsigned)share, et, s_abort, s_flag)) {
+              alive = false;
+              break;
+            }
+            const int r0 = cc * rows / share, r1 = (cc + 1) * rows / share;
+            if (nv > 0) {
+              for (int rr = r0 + wid; rr < r1; rr += 4)
+                attn_merge_rows<bf16, HD>(a, b, g, rows, nv, rr, rr + 1, lane);
+            } else {
+              for (int e = et; e < (r1 - r0) * hd; e += 128) {
+                const int rr = r0 + e / hd, d = e % hd;
+                const int jr = rr / Gq, h = g * Gq + (rr - jr * Gq);
+                store_act<bf16>((bf16*)a.o, (size_t)a.nq * hd, b * a.K + jr, a.B * a.K, a.split,
+                                h * hd + d, 0.f);
+              }
+            }
+            for (int e = et; e < (r1 - r0) * hd; e += 128) {
+              const int rr = r0 + e / hd, d = e % hd;
+              const int jr = rr / Gq, h = g * Gq + (rr - jr * Gq);
+              const size_t r = (size_t)b * a.K + jr;
+              qx[r * a.nq * hd + h * hd + d] = 0;
+              if (rr - jr * Gq == 0) {  // one merged row per draft row clears its k / v
+                kvx[r * 2 * kvw + g * hd + d] = 0;
+                kvx[r * 2 * kvw + kvw + g * hd + d] = 0;
+              }
             }
           }
+          if (!alive) break;
         } else if (ph.kind == PP_ARGMAX) {
           if (P.out_tokens)
             for (int r = c * 128 + et; r < P.R; r += G * 128) {

@@ -12,7 +12,7 @@ namespace peagle {
 
 constexpr int PASS_MAX_LAYERS = 8;
 constexpr int PASS_MAX_GEMM = 3 + 4 * PASS_MAX_LAYERS;
-constexpr int PASS_MAX_PHASE = 5 + 9 * PASS_MAX_LAYERS;
+constexpr int PASS_MAX_PHASE = 5 + 7 * PASS_MAX_LAYERS;
 constexpr unsigned long long PASS_DEFAULT_WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 constexpr int PASS_MAX_ROWS = 120;                    // R = B*K (hi + lo rows <= 240)
 constexpr int PASS_SS_SLOTS = 2 + 2 * PASS_MAX_LAYERS;  // per-row sums of squares
@@ -27,11 +27,11 @@ constexpr int pass_att_nbuf(int) { return 2; }
 enum PassPhaseKind : int {
   PP_GEMM = 0,    // a projection on the tensor cores (its epilogue writes the next input)
   PP_INPUT = 1,   // NTP / MTP inputs: e * g_in, f * g_hid (+ sums of squares), residual = f
-  PP_ATTN = 2,    // split-KV attention items (request, kv head, key chunk) -> partials
-  PP_MERGE = 3,   // chunk partials -> O (one warp per query row)
+  PP_ATTN = 2,    // split-KV attention items (request, kv head, key chunk): the draft
+                  // block's k / v into the cache, partials, then each item's share of the
+                  // merge of its (request, kv head) -> O
   PP_NORM = 4,    // residual -> x * gamma (+ sums of squares)
-  PP_ARGMAX = 5,  // LM-head argmax keys -> draft tokens (d2t applied)
-  PP_QKVFIN = 6   // fixed-point q -> fp32 queries, k / v -> bf16 KV cache slots
+  PP_ARGMAX = 5   // LM-head argmax keys -> draft tokens (d2t applied)
 };
 
 // One projection: stream-K over (128-feature tile, 64-wide k-block) iterations, single
@@ -48,7 +48,7 @@ struct PassPhase {
   int kind;
   int stage;           // PEAGLE_STAGE_* the step is reported under (timing)
   int gemm;            // PP_GEMM: index into PassParams::gemm
-  int layer;           // PP_ATTN / PP_MERGE / PP_QKVFIN: decoder layer
+  int layer;           // PP_ATTN: decoder layer
   int slot;            // PP_NORM: sum-of-squares slot
   const void* gamma;   // PP_NORM: norm gain
 };
@@ -82,13 +82,13 @@ struct PassParams {
   fx_t* ss;              // [PASS_SS_SLOTS][R] row sums of squares (0: e, 1: f, 2..: norms)
   fx_t* q_fx;            // [R, nq*hd] fixed-point queries of the current layer
   fx_t* kv_fx;           // [R][2][nkv*hd] fixed-point keys / values of the current layer
-  float* Qf;             // [R, nq*hd] fp32 queries read by attention
   unsigned long long* keys;
   int* row_pos;
   const int* d2t;
   float* ws;             // stream-K partial slots
   unsigned* tile_cnt;    // per-tile contributor counters (zero between projections)
-  unsigned* phase_cnt;   // [n_phase + 1]: phase completion counts, then the abort flag
+  unsigned* phase_cnt;   // [n_phase + 1]: phase completion counts, then the abort flag, then
+                         // [layer][B][nkv] attention items that wrote their partials
   unsigned* err;
   unsigned long long* trace;  // timing: [0] start, [j+1] completion of phase j (ns), or null
   unsigned long long* trace_cta;  // timing: [phase][CTA][4] event times, or null

@@ -440,7 +440,10 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
     c->pass_force = env && env[0] == '1';
     if (coop && !(env && env[0] == '0')) {
-      TRY(dalloc(c, (void**)&c->pass_cnt, (size_t)(PASS_MAX_PHASE + 1) * 4));
+      // phase counters, the abort flag, then the attention items' counts per layer,
+      // request and kv head
+      TRY(dalloc(c, (void**)&c->pass_cnt,
+                 ((size_t)PASS_MAX_PHASE + 1 + (size_t)PASS_MAX_LAYERS * d.max_batch * nkv) * 4));
       TRY(dalloc(c, (void**)&c->pass_trace,
                  (size_t)PASS_TRACE_SLOTS * (PASS_MAX_PHASE + 1) * 8));
       TRY(dalloc(c, (void**)&c->pass_trace_cta, (size_t)PASS_MAX_PHASE * c->num_sms * 4 * 8));
@@ -480,6 +483,12 @@ static void attention_plan(peagle_ctx* c, int B, int cap, int* chunk, int* nchun
 }
 
 // ---- the draft pass as one persistent kernel (bf16) --------------------------------------
+// Bytes of the pass kernel's counters a launch starts from zero: the phase counts, the abort
+// flag and the attention items' counts per layer, request and kv head.
+static size_t pass_cnt_bytes(const peagle_ctx* c, const PassParams& P) {
+  return ((size_t)P.n_phase + 1 + (size_t)c->d.n_layers * P.B * c->d.n_kv_heads) * 4;
+}
+
 // Fills the kernel's parameter block with the same steps, epilogues and buffers as the
 // multi-kernel path below.  Returns PEAGLE_ERR_UNSUPPORTED for shapes it does not cover
 // (the caller then runs the multi-kernel path).
@@ -510,7 +519,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   P.wait_ns = c->wait_ns;
   P.stall_phase = c->stall_phase;
   if (!c->timing && c->pp_valid && memcmp(&key, &c->pp_key, sizeof(key)) == 0) {
-    cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, (size_t)(P.n_phase + 1) * 4, s);
+    cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, pass_cnt_bytes(c, P), s);
     if (ce != cudaSuccess) return cuda_fail(ce, "pass counters");
     return pass_launch(P, hd, grid, s);
   }
@@ -528,7 +537,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     PassPhase& ph = P.ph[P.n_phase++];
     ph.kind = kind;
     ph.stage = kind == PP_GEMM ? cur_stage
-               : (kind == PP_ATTN || kind == PP_MERGE) ? PEAGLE_STAGE_ATTN
+               : kind == PP_ATTN ? PEAGLE_STAGE_ATTN
                : kind == PP_ARGMAX ? PEAGLE_STAGE_SMALL : PEAGLE_STAGE_NORM;
     ph.gemm = -1;
     ph.layer = layer;
@@ -616,9 +625,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
       scaled(e, slot++);
       add_gemm(c->qkv[l], H, c->Xn, H, qkv_out, H, R, split, e, -2);
     }
-    add_phase(PP_QKVFIN, l, nullptr);
     add_phase(PP_ATTN, l, nullptr);
-    add_phase(PP_MERGE, l, nullptr);
     {
       EpiArgs eo = epi_base(c, EPI_RESID, R, H);
       eo.in_split = split;
@@ -691,7 +698,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   P.chunk = chunk;
   P.nchunk = nchunk;
   AttnArgs& a = P.att;
-  a.q = c->Qf;
+  a.q = c->pass_qfx;
   a.split = split;
   a.kc = kv->k;
   a.vc = kv->v;
@@ -723,7 +730,6 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   P.ss = c->pass_ss;
   P.q_fx = c->pass_qfx;
   P.kv_fx = c->pass_kvfx;
-  P.Qf = c->Qf;
   P.nq = nq;
   P.nkv = nkv;
   P.hd = hd;
@@ -753,7 +759,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     cudaError_t te = cudaMemsetAsync(P.trace, 0, (size_t)(PASS_MAX_PHASE + 1) * 8, s);
     if (te != cudaSuccess) return cuda_fail(te, "pass trace");
   }
-  cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, (size_t)(P.n_phase + 1) * 4, s);
+  cudaError_t ce = cudaMemsetAsync(c->pass_cnt, 0, pass_cnt_bytes(c, P), s);
   if (ce != cudaSuccess) return cuda_fail(ce, "pass counters");
   if (!c->timing) {
     c->pp_key = key;

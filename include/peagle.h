@@ -344,9 +344,11 @@ int32_t peagle_read_pass_trace(peagle_ctx* ctx, uint64_t* out, int32_t max_entri
  * PEAGLE_DEV_TIMEOUT, raises its abort flag so every CTA leaves its waits, lets the loads
  * and tensor-core operations it issued complete, frees its tensor memory and returns.
  * unreachable_step >= 0 names a step of the pass (its index in pass order: 0 the fc
- * projection, 1 the input rows, then per layer the QKV projection(s), q/k/v finalise,
- * attention, merge, o-projection, norm, gate/up, down, ...) whose waits require one
- * completion signal more than the grid gives, so that they run out; -1 none.  Applies to
+ * projection, 1 the input rows, then per layer the norm (from the second layer on), the
+ * QKV projection (two in the first layer, one per half of its input), attention,
+ * o-projection, norm, gate/up, down; then the final norm, the LM head and the argmax)
+ * whose waits require one completion signal more than the grid gives, so that they run
+ * out; -1 none.  Applies to
  * the following draft and catch-up passes of this context.  peagle_status reports the
  * TIMEOUT bit and resets the context's accumulators, so the next pass starts clean.
  * Returns PEAGLE_ERR_INVALID for a step index outside the kernel's range. */

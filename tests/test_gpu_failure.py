@@ -22,9 +22,10 @@ pytestmark = pytest.mark.gpu
 DIMS = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_dim=64,
                   intermediate=320, draft_vocab=1000, target_vocab=1500,
                   rope_theta=10000.0, rms_eps=1e-5, dtype="bf16", d2t="monotone")
-# steps of the two-layer pass: 0 fc, 1 input rows, 2-3 layer-1 QKV halves, 4 finalise,
-# 5 attention, 6 merge, 7 o-projection, ..., 21 LM head, 22 argmax
-STEPS = [1, 6, 21]
+# steps of the two-layer pass: 0 fc, 1 input rows, 2-3 layer-1 QKV halves, 4 attention,
+# 5 o-projection, 6 norm, 7 gate/up, 8 down, 9-15 layer 2, 16 final norm, 17 LM head,
+# 18 argmax
+STEPS = [1, 4, 17]
 
 
 @pytest.fixture(scope="module")

@@ -33,7 +33,8 @@ def _both(dims, w, inp, K, cap):
 
 @pytest.mark.parametrize("dims,lens,K", [
     (SMALL_BF16, [0, 37, 100], 5),
-    (SMALL_BF16, [64, 1, 300, 17, 5, 9, 250, 3], 8),
+    (SMALL_BF16, [300, 64], 8),
+    (SMALL_BF16, [1, 250, 17, 5], 4),
     (SMALL_HD128, [50, 200], 4),
     (SMALL_HD128, [0], 1),
 ])
