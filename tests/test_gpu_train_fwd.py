@@ -113,8 +113,9 @@ def test_forward_parallel_dependency_closure():
 
 def test_sequence_partitioned_forward_matches_full():
     """Sequence partitioning (3.2): each chunk's rows, run with every depth-1 row below the
-    chunk's end as context (one dependency-closed call), give the same outputs as the
-    unpartitioned forward over all rows."""
+    chunk's end as context (one dependency-closed call), match the fp64 oracle's forward on
+    the same rows (bf16 logit tolerance, ids where the margin allows), and give the same
+    outputs as the unpartitioned GPU forward over all rows."""
     m = pk()
     dims = SMALL_BF16
     n, K, r = 180, 8, 0.8
@@ -126,11 +127,16 @@ def test_sequence_partitioned_forward_matches_full():
     chunk = m.peagle_sequence_partition(rp, rd, bnd)
     ctx = make_ctx(dims, w, 1, K, n, max_rows=len(rp), max_seq=n)
     am, lg = _run_fwd(ctx, dims, tokens, hidden, rp, rd, n, K)
+    W = O.Weights64.from_synth(w)
     for c in range(len(bnd)):
         end = bnd[c + 1] if c + 1 < len(bnd) else n
         sel = (chunk == c) | ((rd == 1) & (rp < end))
         own = chunk[sel] == c
         am_c, lg_c = _run_fwd(ctx, dims, tokens, hidden, rp[sel], rd[sel], n, K)
+        rows_c = np.stack([rp[sel], rd[sel]], 1).astype(np.int64)
+        rl, ra, rm = O.forward_parallel(W, dims, tokens, hidden, rows_c,
+                                        bf16=O.FORWARD_BF16_CASTS)
+        _compare(dims, rl[own], ra[own], rm[own], am_c[own], lg_c[own], f"chunk {c} vs oracle")
         err = float(np.max(np.abs(lg_c[own] - lg[sel][own])))
         assert err < 2e-3, f"chunk {c}: {err:.3e}"
         ok = np.sort(lg[sel][own], axis=1)
@@ -187,3 +193,40 @@ def test_train_fwd_full_prefix_and_tail():
     idx = {(int(p), int(d)): i for i, (p, d) in enumerate(clo)}
     sel = [idx[(int(p), int(d))] for p, d in tail]
     _compare(dims, cl[sel], ca[sel], cm[sel], am[-3:], lg[-3:], "train_fwd tail")
+
+
+def test_sequence_partition_workspace_follows_the_chunk():
+    """The memory side of sequence partitioning (3.2): a context sized for one chunk's rows
+    allocates less device memory for the training forward than one sized for the whole
+    sequence, in proportion to the rows (n = 8192, K = 8, COD 0.8: about 34K rows, four
+    chunks).  The dense (nK)^2 mask whose size the pages' memory law counts is never
+    allocated: the mask is evaluated from its closed form per (row, key)."""
+    m = pk()
+    dims = SMALL_BF16
+    n, K = 8192, 8
+    w = synth.make_weights(dims, 5)
+    rp, rd = m.peagle_cod_rows(n, K, 0.8, synth.cod_uniforms(n, K, seed=13))
+    chunk = m.peagle_sequence_partition(rp, rd, [0, 2048, 4096, 6144])
+    rows_chunk = max(int(((chunk == c) | ((rd == 1) & (rp < e))).sum())
+                     for c, e in enumerate([2048, 4096, 6144, n]))
+
+    def alloc(max_rows):
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        ctx = make_ctx(dims, w, 1, K, n, max_rows=max_rows, max_seq=n if max_rows else 0)
+        torch.cuda.synchronize()
+        used = free0 - torch.cuda.mem_get_info()[0]
+        ctx.close()
+        return used
+
+    base = alloc(0)
+    full = alloc(len(rp)) - base
+    part = alloc(rows_chunk) - base
+    RECORD.append({"case": "partition workspace", "rows_full": len(rp), "rows_chunk": rows_chunk,
+                   "bytes_full": full, "bytes_chunk": part,
+                   "dense_mask_bytes_full": O.attention_matrix_bytes(n, K),
+                   "dense_mask_bytes_chunk": O.attention_matrix_bytes(n // 4, K)})
+    assert 0 < part < full
+    # linear in the rows (the per-row buffers dominate), far below the dense mask's bytes
+    assert part / full < 1.5 * rows_chunk / len(rp)
+    assert full < O.attention_matrix_bytes(n, K) / 10

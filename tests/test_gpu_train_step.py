@@ -2,10 +2,16 @@
 Parallel-Drafting EAGLE with Scalable Training", A2 section 2 and section 3) on the GPU
 against the fp64 oracle ``peagle_train_step``'s counterpart in oracle/peagle_train_oracle.
 
-Tolerances, from the arithmetic: fp32 drafters run every product in fp32 (relative error
-of a gradient tensor about 1e-6, bound 1e-4); bf16 drafters run the GEMMs on TF32 tensor
-cores (operands rounded to 11 significant bits, 2^-11 = 4.9e-4 per element), bound 1e-2
-on each tensor's relative Frobenius error and 1e-3 on the loss."""
+Every gradient is compared element by element: |got - want| <= atol + rtol * |want|, with
+atol a fraction of the tensor's largest entry (a gradient entry is a sum of many products,
+so its rounding error scales with the tensor's magnitude, not with the entry's own, which
+may sit near zero after cancellation).  From the arithmetic: fp32 drafters run every
+product in fp32 (unit roundoff 2^-24 = 6e-8 per operation; sums over up to a few
+thousand rows): rtol 1e-4, atol 1e-5 of the largest entry.  bf16 drafters' products round
+their operands to at most 11 significant bits (TF32; 2^-11 = 4.9e-4 per operand, chained
+through the backward's few dependent products): rtol 2e-2, atol 2e-3 of the largest entry,
+and 1e-3 on the loss.  A wrong block of entries (one key tile's dK, one chunk's rows)
+exceeds these bounds by orders of magnitude."""
 import numpy as np
 import pytest
 import torch
@@ -89,30 +95,41 @@ def _flat(g, ref, n_layers):
             yield f"layers.{l}.{k}", g[k][l], ref["layers"][l][k]
 
 
-def _compare(dims, out, tol, loss_tol):
+GRAD_RECORD = []  # (case, tensor, worst |got - want| / (atol + rtol |want|))
+
+
+def _compare(dims, out, rtol, atol_frac, loss_tol, case=""):
     loss, g, ref_loss, ref = out
     assert abs(loss - ref_loss) <= loss_tol * abs(ref_loss), (loss, ref_loss)
     for name, got, want in _flat(g, ref, dims.n_layers):
         got = got.cpu().double().numpy()
         assert np.all(np.isfinite(got)), name
-        den = np.linalg.norm(want)
-        err = np.linalg.norm(got - want)
-        if den == 0:
-            assert err == 0, name
-        else:
-            assert err <= tol * den, f"{name}: relative error {err / den:.3e}"
+        scale = float(np.max(np.abs(want))) if want.size else 0.0
+        if scale == 0.0:
+            assert np.all(got == 0), name
+            continue
+        bound = atol_frac * scale + rtol * np.abs(want)
+        ratio = np.abs(got - want) / bound
+        worst = float(ratio.max())
+        GRAD_RECORD.append((case, name, worst))
+        bad = np.argwhere(ratio > 1.0)
+        assert len(bad) == 0, (f"{case} {name}: {len(bad)} of {ratio.size} entries outside "
+                               f"the bound, worst ratio {worst:.2f} at {bad[0].tolist()}")
 
 
 @pytest.mark.parametrize("n,K,cod", [(24, 4, 0.8), (16, 1, None), (12, 8, None)])
 def test_tiny_f32_train_step(n, K, cod):
     dims = synth.DIMS_TINY
-    _compare(dims, _run(dims, 3 + K, n, K, cod), 1e-4, 1e-5)
+    _compare(dims, _run(dims, 3 + K, n, K, cod), 1e-4, 1e-5, 1e-5, f"f32 n={n} K={K}")
 
 
-@pytest.mark.parametrize("n,K,cod", [(40, 8, 0.8), (33, 3, 0.6)])
+# (n=40, K=8) and (33, 3) fit one 64-key tile and one 512-row chunk of the fused attention
+# backward; (220, 8, 0.8) has four tiles of depth-1 keys and about 900 rows (two chunks of
+# the key-major kernel, its double-buffered loop), so every tiling path is compared
+@pytest.mark.parametrize("n,K,cod", [(40, 8, 0.8), (33, 3, 0.6), (220, 8, 0.8)])
 def test_small_bf16_train_step(n, K, cod):
     dims = SMALL_BF16
-    _compare(dims, _run(dims, 7 + K, n, K, cod), 1e-2, 1e-3)
+    _compare(dims, _run(dims, 7 + K, n, K, cod), 2e-2, 2e-3, 1e-3, f"bf16 n={n} K={K}")
 
 
 def test_train_step_rejects_a_window():
