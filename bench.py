@@ -646,7 +646,7 @@ def train_step_measure(dev, reps=3):
     n, K = wl.n_seq, wl.K
     rp, rd = pk.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
     M = len(rp)
-    ctx = pk.peagle_create(w, pk.make_dims(dims, 1, K, n, max_rows=M, max_seq=n))
+    ctx = pk.peagle_create(w, pk.make_dims(dims, 1, K, n, max_rows=M, max_seq=n, train=True))
     del w
     H, I, nq, nkv, hd, L = (dims.hidden, dims.intermediate, dims.n_q_heads, dims.n_kv_heads,
                             dims.head_dim, dims.n_layers)

@@ -51,7 +51,7 @@ class PeagleDims(ctypes.Structure):
         "draft_vocab", "target_vocab", "max_batch", "max_K", "max_rows", "max_seq",
         "max_positions", "dtype")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
                                       ("attn_window", _i32), ("lm_rank", _i32),
-                                      ("lm_topk", _i32)]
+                                      ("lm_topk", _i32), ("train", _i32)]
 
 
 class PeagleWeights(ctypes.Structure):
@@ -152,8 +152,10 @@ def _stream_ptr(stream):
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
-def make_dims(dims, max_batch, max_K, max_positions, max_rows=0, max_seq=0) -> PeagleDims:
-    """C struct from a ``synth.Dims``-like object plus the context's capacity limits."""
+def make_dims(dims, max_batch, max_K, max_positions, max_rows=0, max_seq=0,
+              train=False) -> PeagleDims:
+    """C struct from a ``synth.Dims``-like object plus the context's capacity limits
+    (``train``: the context also holds the training step's workspaces)."""
     return PeagleDims(hidden=dims.hidden, n_layers=dims.n_layers, n_q_heads=dims.n_q_heads,
                       n_kv_heads=dims.n_kv_heads, head_dim=dims.head_dim,
                       intermediate=dims.intermediate, draft_vocab=dims.draft_vocab,
@@ -163,7 +165,7 @@ def make_dims(dims, max_batch, max_K, max_positions, max_rows=0, max_seq=0) -> P
                       rope_theta=dims.rope_theta, rms_eps=dims.rms_eps,
                       attn_window=int(getattr(dims, "attn_window", 0) or 0),
                       lm_rank=int(getattr(dims, "lm_rank", 0) or 0),
-                      lm_topk=int(getattr(dims, "lm_topk", 0) or 0))
+                      lm_topk=int(getattr(dims, "lm_topk", 0) or 0), train=int(bool(train)))
 
 
 class Context:

@@ -1,0 +1,329 @@
+// The training step's plain products on the library's own kernels.
+//
+// bf16 drafters: C = alpha A B^T + beta C on tcgen05 tensor cores, kind::tf32 -- fp32
+// operands in memory, rounded to TF32 by the MMA, fp32 accumulation in tensor memory.
+// Both operands K-major ([rows][k], 32 fp32 = one 128-byte row per k-block, loaded by TMA
+// with 128-byte swizzle); an operand stored the other way round (the backward's dX = dY W
+// and dW = dY^T X) is first transposed into a scratch buffer by a tiled transpose kernel,
+// and so is one whose row stride is not a multiple of 16 bytes (TMA's rule).  One
+// 128 x 128 output tile per CTA (two CTAs per SM): warp 0 lane 0 issues the TMA loads
+// into a 3-stage ring, warp 1 lane 0 issues the MMAs (4 of K = 8 per k-block) and owns the
+// tensor memory, warps 2-5 read the accumulator back (one output row per thread) and
+// store alpha * acc + beta * C.
+//
+// fp32 drafters keep fp32 arithmetic: a tiled CUDA-core GEMM with the same transposes.
+#include <cuda.h>
+#include <stdio.h>
+
+#include "gemm_tc.h"
+#include "gemm_tf32.h"
+#include "tc_ptx.cuh"
+
+namespace peagle {
+
+namespace {
+
+constexpr int TF_THREADS = 192;
+constexpr int TF_TILE = 128 * 128;  // bytes of one 128-row x 32-fp32 operand tile
+constexpr int TF_STAGES = 3;
+constexpr uint64_t TF_WAIT_NS = 2000000000ull;
+
+size_t tf_smem_bytes() { return 1024 + (size_t)TF_STAGES * 2 * TF_TILE + (2 * TF_STAGES + 2) * 8 + 16; }
+
+struct TfArgs {
+  int M, N, K, ldc;
+  float alpha, beta;
+  float* C;
+  unsigned* err;
+};
+
+// Instruction descriptor of tcgen05.mma kind::tf32: TF32 A and B (format code 2), fp32 D,
+// both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(TF_THREADS, 2)
+    tf32_gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+                     TfArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + TF_STAGES * TF_TILE;
+  uint64_t* full = (uint64_t*)(sB + TF_STAGES * TF_TILE);
+  uint64_t* empty = full + TF_STAGES;
+  uint64_t* accf = empty + TF_STAGES;
+  uint32_t* s_tmem = (uint32_t*)(accf + 1);
+  volatile int* s_abort = (volatile int*)(s_tmem + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const int KB = (a.K + 31) / 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TF_STAGES; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::mbar_init(accf, 1);
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(s_tmem, 128u);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = tc::policy_evict_last();
+      long long issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int st = kb % TF_STAGES;
+        if (kb >= TF_STAGES &&
+            !tc::mbar_wait(&empty[st], (uint32_t)(((kb / TF_STAGES) - 1) & 1), s_abort,
+                           TF_WAIT_NS)) {
+          if (!*s_abort) raise_error(a.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        tc::mbar_expect_tx(&full[st], 2u * TF_TILE);
+        tc::tma_load_2d(sA + (size_t)st * TF_TILE, &ma, kb * 32, m0, &full[st], pol);
+        tc::tma_load_2d(sB + (size_t)st * TF_TILE, &mb, kb * 32, n0, &full[st], pol);
+        ++issued;
+      }
+      if (*s_abort) {
+        // the loads in flight land (bounded) before the CTA can exit
+        int never = 0;
+        for (long long n = (issued > TF_STAGES ? issued - TF_STAGES : 0); n < issued; ++n)
+          tc::mbar_wait(&full[n % TF_STAGES], (uint32_t)((n / TF_STAGES) & 1), &never,
+                        10000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_tf32(128, 128);
+      for (int kb = 0; kb < KB; ++kb) {
+        const int st = kb % TF_STAGES;
+        if (!tc::mbar_wait(&full[st], (uint32_t)((kb / TF_STAGES) & 1), s_abort, TF_WAIT_NS)) {
+          if (!*s_abort) raise_error(a.err, PEAGLE_DEV_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)st * TF_TILE));
+        const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)st * TF_TILE));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 8 TF32 values (32 bytes) per MMA
+          mma_tf32(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[st]);
+      }
+      // arrives once every MMA issued above has completed (also after an abort, so that
+      // tensor memory is freed only when nothing writes it any more)
+      tc::mma_commit(accf);
+    }
+  } else {
+    // epilogue: thread t holds output row m0 + t (TMEM lane t), 128 columns
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int m = m0 + r;
+    int never = 0;
+    const bool ok = tc::mbar_wait(accf, 0u, &never, TF_WAIT_NS) && !*s_abort;
+    tc::fence_after_sync();
+    if (ok) {
+      const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+      float* crow = a.C + (size_t)m * a.ldc;
+      const bool vec = (a.ldc & 3) == 0 && ((uintptr_t)a.C & 15) == 0;
+      for (int c0 = 0; c0 < 128; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tb + c0, v);
+        tc::tmem_ld_wait();
+        if (m >= a.M) continue;
+        const int n = n0 + c0;
+        if (vec && n + 16 <= a.N) {
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            float4 o = make_float4(a.alpha * v[q], a.alpha * v[q + 1], a.alpha * v[q + 2],
+                                   a.alpha * v[q + 3]);
+            if (a.beta != 0.f) {
+              const float4 c = *(const float4*)(crow + n + q);
+              o.x += a.beta * c.x;
+              o.y += a.beta * c.y;
+              o.z += a.beta * c.z;
+              o.w += a.beta * c.w;
+            }
+            *(float4*)(crow + n + q) = o;
+          }
+        } else {
+          for (int q = 0; q < 16 && n + q < a.N; ++q) {
+            float o = a.alpha * v[q];
+            if (a.beta != 0.f) o += a.beta * crow[n + q];
+            crow[n + q] = o;
+          }
+        }
+      }
+    } else if (threadIdx.x == 64) {
+      raise_error(a.err, PEAGLE_DEV_TIMEOUT);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 128u);
+  }
+}
+
+// out[c][r] = in[r][c] for r < rows, c < cols (32 x 32 tiles through shared memory).
+__global__ void transpose_kernel(const float* __restrict__ in, int rows, int cols, int ld_in,
+                                 float* __restrict__ out, int ld_out) {
+  __shared__ float t[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) t[i][threadIdx.x] = in[(size_t)r * ld_in + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[(size_t)c * ld_out + r] = t[threadIdx.x][i];
+  }
+}
+
+// out[r][c] = in[r][c] into a buffer whose row stride is padded.
+__global__ void pack_kernel(const float* __restrict__ in, int rows, int cols, int ld_in,
+                            float* __restrict__ out, int ld_out) {
+  const size_t total = (size_t)rows * cols;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / cols, c = i - r * cols;
+    out[r * ld_out + c] = in[r * ld_in + c];
+  }
+}
+
+// fp32 drafters: C[m x n] = alpha op(A) op(B) + beta C on the CUDA cores, 64 x 64 tiles,
+// 4 x 4 outputs per thread; op(A) is A [m x k] or A^T of A [k x m], op(B) is B [k x n] or
+// B^T of B [n x k].
+__global__ void __launch_bounds__(256) simt_gemm_kernel(bool ta, bool tb, int m, int n, int k,
+                                                       float alpha, const float* __restrict__ A,
+                                                       int lda, const float* __restrict__ B,
+                                                       int ldb, float beta, float* C, int ldc) {
+  __shared__ float sa[16][65];
+  __shared__ float sb[16][65];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int l0 = 0; l0 < k; l0 += 16) {
+    for (int e = threadIdx.x; e < 16 * 64; e += 256) {
+      const int l = e / 64, q = e % 64;
+      const int gi = i0 + q, gj = j0 + q, gl = l0 + l;
+      float av = 0.f, bv = 0.f;
+      if (gi < m && gl < k) av = ta ? A[(size_t)gl * lda + gi] : A[(size_t)gi * lda + gl];
+      if (gj < n && gl < k) bv = tb ? B[(size_t)gj * ldb + gl] : B[(size_t)gl * ldb + gj];
+      sa[l][q] = av;
+      sb[l][q] = bv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+      float x[4], y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[u] = sa[l][ty * 4 + u];
+        y[u] = sb[l][tx * 4 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(x[u], y[v], acc[u][v]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = i0 + ty * 4 + u;
+    if (i >= m) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int j = j0 + tx * 4 + v;
+      if (j >= n) continue;
+      float o = alpha * acc[u][v];
+      if (beta != 0.f) o += beta * C[(size_t)i * ldc + j];
+      C[(size_t)i * ldc + j] = o;
+    }
+  }
+}
+
+int cdiv_i(long long a, int b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+size_t tf32_scratch_floats(int rows, int cols) {
+  return (size_t)rows * (size_t)((cols + 3) / 4 * 4);
+}
+
+int train_gemm(const TrainGemmCtx& g, bool ta, bool tb, int m, int n, int k, float alpha,
+               const float* A, int lda, const float* B, int ldb, float beta, float* C, int ldc,
+               cudaStream_t s) {
+  if (m <= 0 || n <= 0) return PEAGLE_OK;
+  if (!g.tc) {
+    dim3 grid(cdiv_i(n, 64), cdiv_i(m, 64));
+    simt_gemm_kernel<<<grid, 256, 0, s>>>(ta, tb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc);
+    return cudaGetLastError() == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+  }
+  // K-major operands A' [m][k] and B' [n][k] with 16-byte row strides
+  auto k_major = [&](const float* X, int ldx, bool stored_k_major, int rows, float* scratch,
+                     size_t cap, int* ld_out) -> const float* {
+    const bool aligned = (ldx & 3) == 0 && ((uintptr_t)X & 15) == 0;
+    if (stored_k_major && aligned) {
+      *ld_out = ldx;
+      return X;
+    }
+    const int ld = (k + 3) / 4 * 4;
+    if ((size_t)rows * ld > cap) return nullptr;
+    if (stored_k_major) {  // [rows][k] with an unaligned stride: copy
+      pack_kernel<<<1024, 256, 0, s>>>(X, rows, k, ldx, scratch, ld);
+    } else {  // stored [k][rows]: transpose
+      dim3 grid(cdiv_i(rows, 32), cdiv_i(k, 32));
+      transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(X, k, rows, ldx, scratch, ld);
+    }
+    *ld_out = ld;
+    return scratch;
+  };
+  int lda_k = 0, ldb_k = 0;
+  const float* Ak = k_major(A, lda, !ta, m, g.scratch_a, g.scratch_floats, &lda_k);
+  const float* Bk = k_major(B, ldb, tb, n, g.scratch_b, g.scratch_floats, &ldb_k);
+  if (!Ak || !Bk) return PEAGLE_ERR_CAPACITY;
+  CUtensorMap mA, mB;
+  if (!tc_tensor_map_f32(g.tc, &mA, Ak, m, k, lda_k) || !tc_tensor_map_f32(g.tc, &mB, Bk, n, k, ldb_k))
+    return PEAGLE_ERR_UNSUPPORTED;
+  const size_t smem = tf_smem_bytes();
+  if (smem_optin((const void*)tf32_gemm_kernel, smem) != cudaSuccess) return PEAGLE_ERR_CUDA;
+  TfArgs a;
+  a.M = m;
+  a.N = n;
+  a.K = k;
+  a.ldc = ldc;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.C = C;
+  a.err = g.err;
+  dim3 grid(cdiv_i(n, 128), cdiv_i(m, 128));
+  tf32_gemm_kernel<<<grid, TF_THREADS, smem, s>>>(mA, mB, a);
+  return cudaGetLastError() == cudaSuccess ? PEAGLE_OK : PEAGLE_ERR_CUDA;
+}
+
+}  // namespace peagle

@@ -11,12 +11,12 @@
 #include <memory>
 #include <vector>
 
-#include <cublas_v2.h>
 
 #include "gemm_tc.h"
 #include "kernels.h"
 #include "pass_kernel.h"
 #include "tc_ptx.cuh"
+#include "gemm_tf32.h"
 #include "train_kernels.h"
 
 using namespace peagle;
@@ -28,6 +28,8 @@ constexpr int PASS_TRACE_SLOTS = 64;
 // max_seq positions: fp32 copies of the weights (bf16 contexts), the forward's saved
 // activations per layer and the backward's buffers.
 struct TrainWs {
+  float *gscratch_a = nullptr, *gscratch_b = nullptr;  // transposed GEMM operands
+  size_t gscratch_floats = 0;
   int Mmax = 0, nmax = 0;
   // fp32 weights (the context's own buffers on fp32 contexts); gate / up interleaved
   float *fc, *lm, *in_norm, *hid_norm, *fin_norm;
@@ -125,7 +127,6 @@ struct peagle_ctx {
   size_t F_bytes;
   std::vector<void*> allocs;
   TrainWs* tw = nullptr;
-  cublasHandle_t blas = nullptr;
   // optional per-stage timing: CUDA events recorded around each launch on its stream
   bool timing;
   std::vector<cudaEvent_t> ev;
@@ -193,7 +194,6 @@ static void free_ctx(peagle_ctx* c) {
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->tc) tc_destroy(c->tc);
-  if (c->blas) cublasDestroy(c->blas);
   delete c->tw;
   delete c->pp;
   delete c;
@@ -224,6 +224,9 @@ static int validate_dims(const peagle_dims* d) {
     return PEAGLE_ERR_UNSUPPORTED;
   // the masked attention tile holds 64 (row, q head) pairs of one kv head
   if (d->max_rows > 0 && d->n_q_heads / d->n_kv_heads > 64) return PEAGLE_ERR_UNSUPPORTED;
+  if (d->train != 0 && d->train != 1) return PEAGLE_ERR_INVALID;
+  if (d->train && d->max_rows <= 0) return PEAGLE_ERR_INVALID;
+  if (d->train && (d->attn_window > 0 || d->lm_rank > 0)) return PEAGLE_ERR_UNSUPPORTED;
   return PEAGLE_OK;
 }
 
@@ -263,6 +266,8 @@ static EpiArgs epi_base(peagle_ctx* c, int kind, int R, int Nout) {
   e.ld_res = c->d.hidden;
   return e;
 }
+
+static int train_ws(peagle_ctx* c);
 
 extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, peagle_ctx** out) {
   if (!out) return PEAGLE_ERR_INVALID;
@@ -453,6 +458,15 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
       TRY(dalloc(c, (void**)&c->pass_kvfx, pr * 2 * nkv * hd * 8));
       c->pp = new PassParams();
       c->pass_on = true;
+    }
+  }
+  // the training step's workspaces (fp32 weight copies, every layer's kept activations,
+  // the GEMMs' scratch operands): made here, so that no other call allocates
+  if (d.train) {
+    const int tr = train_ws(c);
+    if (tr != PEAGLE_OK) {
+      free_ctx(c);
+      return tr;
     }
   }
 #undef TRY
@@ -1140,21 +1154,14 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
 // 2 and section 3): the training-style forward with its activations kept, the mean
 // cross-entropy over the retained rows, and the gradient of every parameter.  fp32
 // activations; the plain GEMMs (projections, the attention's depth-1 prefix products) run
-// on cuBLAS, TF32 tensor cores for bf16 drafters and fp32 for fp32 drafters.
+// on this library's own kernels: TF32 tcgen05 MMAs for bf16 drafters, fp32 FMA tiles for
+// fp32 drafters.  Every workspace is made by peagle_create.
 
-// row-major C[m x n] = alpha op(A) op(B) + beta C, with op(A) m x k and op(B) k x n
 #define TRY_RET(x)  \
   do {              \
     int _r = (x);   \
     if (_r) return _r; \
   } while (0)
-
-static bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int m, int n, int k, float alpha,
-                    const float* A, int lda, const float* B, int ldb, float beta, float* C,
-                    int ldc) {
-  return cublasSgemm(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, n, m, k,
-                     &alpha, B, ldb, A, lda, &beta, C, ldc) == CUBLAS_STATUS_SUCCESS;
-}
 
 static int train_ws(peagle_ctx* c) {
   if (c->tw) return PEAGLE_OK;
@@ -1239,7 +1246,19 @@ static int train_ws(peagle_ctx* c) {
   w->res_in[0] = w->f;
   w->a[0] = w->x0;
   TRY_RET(fl(&w->qkvb, (size_t)M * qkv_out));
-  w->S1 = w->dP1 = nullptr;  // the dense prefix score matrices: allocated when first used
+  // the dense prefix score matrices [G M][n]: only where the fused attention does not apply
+  TrainAttn probe;
+  memset(&probe, 0, sizeof(probe));
+  probe.nq = nq;
+  probe.nkv = nkv;
+  probe.hd = hd;
+  const bool dense_attn = !(c->bf && attn_bwd_fused_ok(probe));
+  w->S1 = w->dP1 = nullptr;
+  if (dense_attn) {
+    const size_t count = (size_t)(nq / nkv) * M * n;
+    TRY_RET(dalloc(c, (void**)&w->S1, count * 4));
+    TRY_RET(dalloc(c, (void**)&w->dP1, count * 4));
+  }
   TRY_RET(fl(&w->Oh, (size_t)nq * M * hd));
   TRY_RET(fl(&w->lrow, (size_t)nq * M));
   // backward
@@ -1263,8 +1282,24 @@ static int train_ws(peagle_ctx* c) {
   TRY_RET(fl(&w->df, (size_t)M * H));
   TRY_RET(fl(&w->dHin, (size_t)M * 3 * H));
   TRY_RET(fl(&w->dy, (size_t)M * H));
-  if (!c->blas && cublasCreate(&c->blas) != CUBLAS_STATUS_SUCCESS) return PEAGLE_ERR_CUDA;
-  cublasSetMathMode(c->blas, c->bf ? CUBLAS_TF32_TENSOR_OP_MATH : CUBLAS_DEFAULT_MATH);
+  // the tensor-core GEMMs' scratch operands (bf16 drafters): the largest operand that a
+  // product reads transposed -- an activation [M][widest] or a weight [rows][cols]
+  if (c->bf) {
+    const int widest = std::max({3 * H, 2 * I, Vd, qkv_out, nq * hd, 2 * H});
+    size_t cap = std::max(tf32_scratch_floats(M, widest), tf32_scratch_floats(widest, M));
+    cap = std::max(cap, tf32_scratch_floats(widest, 3 * H));
+    cap = std::max(cap, tf32_scratch_floats(widest, I));
+    cap = std::max(cap, tf32_scratch_floats(widest, nq * hd));
+    if (dense_attn) {
+      // the dense prefix-attention path's operands: [G M][n] scores
+      const int G = nq / nkv;
+      cap = std::max(cap, tf32_scratch_floats(G * M, n));
+      cap = std::max(cap, tf32_scratch_floats(n, G * M));
+    }
+    TRY_RET(fl(&w->gscratch_a, cap));
+    TRY_RET(fl(&w->gscratch_b, cap));
+    w->gscratch_floats = cap;
+  }
   c->tw = hold.release();
   return PEAGLE_OK;
 }
@@ -1292,20 +1327,25 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     if (!gr->qkv[l] || !gr->o[l] || !gr->post_norm[l] || !gr->gate[l] || !gr->up[l] ||
         !gr->down[l])
       return PEAGLE_ERR_INVALID;
-  TRY_RET(train_ws(c));
+  if (!c->tw) return PEAGLE_ERR_CAPACITY;  // workspaces are made by peagle_create
   TrainWs* w = c->tw;
   cudaStream_t s = (cudaStream_t)stream;
-  cublasHandle_t hb = c->blas;
-  if (cublasSetStream(hb, s) != CUBLAS_STATUS_SUCCESS) return PEAGLE_ERR_CUDA;
+  TrainGemmCtx tg;
+  tg.tc = c->bf ? c->tc : nullptr;
+  tg.scratch_a = w->gscratch_a;
+  tg.scratch_b = w->gscratch_b;
+  tg.scratch_floats = w->gscratch_floats;
+  tg.err = c->err;
   const int H = d.hidden, I = d.intermediate, Vd = d.draft_vocab, Vt = d.target_vocab;
   const int nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, G = nq / nkv;
   const int qkv_out = (nq + 2 * nkv) * hd, N = d.n_layers, nqhd = nq * hd;
   const float eps = d.rms_eps, scale = 1.f / sqrtf((float)hd);
   const int Kmax = 16;
-  bool ok = true;
+  int gerr = PEAGLE_OK;
   auto GM = [&](bool ta, bool tb, int m, int nn, int k, float alpha, const float* A, int lda,
                 const float* B, int ldb, float beta, float* C, int ldc) {
-    ok = ok && gemm_rm(hb, ta, tb, m, nn, k, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (gerr == PEAGLE_OK)
+      gerr = train_gemm(tg, ta, tb, m, nn, k, alpha, A, lda, B, ldb, beta, C, ldc, s);
   };
   launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s);
   launch_chain(M, n, K, Kmax, row_p, row_d, c->row_index, w->chain, s);
@@ -1320,15 +1360,10 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   ta.row_p = row_p;
   ta.row_d = row_d;
   ta.chain = w->chain;
-  // bf16 drafters take the fused TF32 attention backward (fp32 drafters keep fp32 GEMMs);
-  // PEAGLE_TRAIN_FUSED_ATTN=0 selects the dense score matrices for them too
-  const char* fa_env = getenv("PEAGLE_TRAIN_FUSED_ATTN");
-  const bool fused_attn = c->bf && attn_bwd_fused_ok(ta) && !(fa_env && fa_env[0] == '0');
-  if (!fused_attn && !w->S1) {
-    const size_t count = (size_t)G * w->Mmax * w->nmax;
-    TRY_RET(dalloc(c, (void**)&w->S1, count * 4));
-    TRY_RET(dalloc(c, (void**)&w->dP1, count * 4));
-  }
+  // bf16 drafters take the fused TF32 attention (fp32 drafters keep fp32 GEMMs over the
+  // dense prefix score matrices, made by peagle_create)
+  const bool fused_attn = c->bf && attn_bwd_fused_ok(ta);
+  if (!fused_attn && !w->S1) return PEAGLE_ERR_UNSUPPORTED;
 
   // ---- forward
   launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
@@ -1463,7 +1498,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     TRY_RET(zero(gr->embed, (size_t)Vt * H, s));
     launch_embed_grad(M, n, K, H, Vt, row_p, row_d, tokens, w->dE, gr->embed, s);
   }
-  if (!ok) return PEAGLE_ERR_CUDA;
+  if (gerr != PEAGLE_OK) return gerr;
   cudaError_t ce = cudaGetLastError();
   return ce == cudaSuccess ? PEAGLE_OK : cuda_fail(ce, "training step launch");
 }

@@ -1,7 +1,7 @@
 // Training step of the parallel-prediction forward ("P-EAGLE: Parallel-Drafting EAGLE with
 // Scalable Training", A2 section 2 and section 3): the non-GEMM kernels of the forward
 // with saved activations and of the backward, all on fp32 rows.  The projections and the
-// prefix part of the attention are plain GEMMs issued by the host (cuBLAS).
+// prefix part of the attention are plain GEMMs (gemm_tf32.cu) issued by the host.
 //
 // Attention structure used throughout ("Speeding LLM inference with P-EAGLE in
 // vLLM/Speculators", "Flex-attention mask"): row i = (p, d) sees the depth-1 rows at

@@ -95,6 +95,10 @@ typedef struct peagle_dims {
                             the draft vocabulary means all of it).  With the
                             efficient head, out_logits holds the exact logits of
                             the candidates and -inf elsewhere.                   */
+  int32_t train;         /* 1: peagle_create also makes the training step's
+                            workspaces for max_rows rows and max_seq positions
+                            (needs max_rows > 0, neither attn_window nor lm_rank);
+                            0: peagle_train_step returns PEAGLE_ERR_CAPACITY.    */
 } peagle_dims;
 
 /* Drafter weights (host or device pointers; dtype = dims.dtype for every float
@@ -141,9 +145,11 @@ typedef struct peagle_kv {
  * whole deployment; "Speeding LLM inference with P-EAGLE in vLLM/Speculators", section
  * "A learnable mask parameter": h_shared is 3H wide).  Validates dims, allocates all
  * device memory the other calls need (weights, workspaces sized for max_batch x max_K
- * rows and max_rows), copies and repacks the weights, precomputes fc(h_shared) (a
- * constant of the weights) and the RoPE table, and synchronises.  The only allocating
- * call.  *out is NULL on failure. */
+ * rows and max_rows; with dims.train, also the training step's fp32 weight copies,
+ * kept activations and gradient scratch), copies
+ * and repacks the weights, precomputes fc(h_shared) (a constant of the weights) and the
+ * RoPE table, and synchronises.  The only allocating call of a drafter context.  *out is
+ * NULL on failure (PEAGLE_ERR_CUDA when device memory runs out). */
 int peagle_create(const peagle_weights* w, const peagle_dims* dims, peagle_ctx** out);
 
 /* One parallel draft pass ("2. The P-EAGLE Parallel Drafter").
@@ -261,14 +267,16 @@ typedef struct peagle_grads {
  * draft-vocabulary logits against labels[i] (device int32 [M], in [0, Vd)), and the
  * gradient of the loss with respect to every parameter into `grads`.
  *   out_loss  device fp32 scalar.
- * Arithmetic: fp32 activations; projections and the attention's depth-1 products on
- * cuBLAS (TF32 tensor cores for bf16 drafters, fp32 for fp32 drafters); for bf16
- * drafters with head_dim 64 the attention backward's depth-1 part runs on the library's
- * own TF32 tensor-core kernels.  Needs
- * dims.max_rows > 0; the first call allocates the step's workspaces (fp32 weight copies
- * for bf16 drafters and every layer's kept activations), so it is not capturable in a
- * CUDA graph.  UNSUPPORTED with attn_window or lm_rank set.  Device checks: BAD_ROW for
- * rows outside the contract, BAD_TOKEN for tokens or labels out of range. */
+ * Arithmetic: fp32 activations; the projections and the attention's depth-1 products
+ * run on the library's own GEMM kernels: TF32 tcgen05 tensor-core MMAs with fp32
+ * accumulation for bf16 drafters, fp32 FMA tiles for fp32 drafters; for bf16 drafters
+ * with head_dim 64 the whole depth-1 attention (forward and backward) is one fused TF32
+ * tensor-core kernel per step, otherwise the dense [G M][n] prefix scores are formed.
+ * Needs a context made with dims.train = 1: peagle_create then makes every workspace of
+ * the step (fp32 weight copies for bf16 drafters, every layer's kept activations, the
+ * GEMMs' scratch operands), so the call allocates nothing.  UNSUPPORTED with attn_window or lm_rank set.
+ * Device checks: BAD_ROW for rows outside the contract, BAD_TOKEN for tokens or labels
+ * out of range, TIMEOUT if a GEMM's bounded pipeline wait ran out. */
 int peagle_train_step(peagle_ctx* ctx, int32_t n, int32_t K, const int32_t* tokens,
                       const void* hidden, const int32_t* row_p, const int32_t* row_d, int32_t M,
                       const int32_t* labels, float* out_loss, const peagle_grads* grads,

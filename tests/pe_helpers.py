@@ -23,7 +23,7 @@ def pk():
 
 
 def make_ctx(dims, w, max_batch, max_K, max_positions, max_rows=0, max_seq=0,
-             pass_kernel=None):
+             pass_kernel=None, train=False):
     """A context; pass_kernel True / False forces the persistent pass kernel on / off for
     the bf16 draft pass (None: the library default)."""
     m = pk()
@@ -32,7 +32,7 @@ def make_ctx(dims, w, max_batch, max_K, max_positions, max_rows=0, max_seq=0,
         os.environ["PEAGLE_PASS_KERNEL"] = "1" if pass_kernel else "0"
     try:
         return m.peagle_create(w, m.make_dims(dims, max_batch, max_K, max_positions, max_rows,
-                                              max_seq))
+                                              max_seq, train))
     finally:
         if old is None:
             os.environ.pop("PEAGLE_PASS_KERNEL", None)

@@ -45,11 +45,12 @@ def test_exports_every_declared_symbol(pk):
 
 
 def test_struct_layout_matches_header(pk):
-    # peagle_dims: 14 int32 + 2 float + attn_window, lm_rank, lm_topk;
+    # peagle_dims: 14 int32 + 2 float + attn_window, lm_rank, lm_topk, train;
     # peagle_weights: 18 pointers; peagle_kv: 2 ptr + 2 int
-    assert ctypes.sizeof(pk.PeagleDims) == 76
+    assert ctypes.sizeof(pk.PeagleDims) == 80
     assert pk.PeagleDims.attn_window.offset == 64
     assert pk.PeagleDims.lm_topk.offset == 72
+    assert pk.PeagleDims.train.offset == 76
     assert ctypes.sizeof(pk.PeagleWeights) == 18 * 8
     assert ctypes.sizeof(pk.PeagleKV) == 24
     assert ctypes.sizeof(pk.PeagleGrads) == 15 * 8
@@ -94,9 +95,35 @@ def test_create_rejects_unsupported_dims(pk):
     d = pk.make_dims(synth.shrink(base, dtype="f32"), 1, 4, 256)
     d.dtype = 7
     assert L.peagle_create(ctypes.byref(w), ctypes.byref(d), ctypes.byref(h)) == pk.PEAGLE_ERR_UNSUPPORTED
+    # training workspaces need parallel-forward rows and no window / efficient head
+    d = pk.make_dims(base, 1, 4, 256, train=True)
+    assert L.peagle_create(ctypes.byref(w), ctypes.byref(d), ctypes.byref(h)) == pk.PEAGLE_ERR_INVALID
+    d = pk.make_dims(synth.shrink(base, attn_window=8), 1, 4, 256, 64, 16, train=True)
+    assert L.peagle_create(ctypes.byref(w), ctypes.byref(d), ctypes.byref(h)) == pk.PEAGLE_ERR_UNSUPPORTED
+    d = pk.make_dims(base, 1, 4, 256, 64, 16)
+    d.train = 2
+    assert L.peagle_create(ctypes.byref(w), ctypes.byref(d), ctypes.byref(h)) == pk.PEAGLE_ERR_INVALID
     # valid dims but missing weight pointers
     d = pk.make_dims(base, 1, 4, 256)
     assert L.peagle_create(ctypes.byref(w), ctypes.byref(d), ctypes.byref(h)) == pk.PEAGLE_ERR_INVALID
+
+
+def test_library_needs_no_vendor_blas():
+    """Every GEMM of the library (draft pass, training forward, training step) runs on its
+    own kernels: the shared object lists no cuBLAS / cuBLASLt dependency."""
+    import shutil
+    import subprocess
+
+    from drafting_eagle_draft_gb300 import build
+
+    path = build.build()
+    tool = shutil.which("readelf")
+    if tool is None:
+        pytest.skip("readelf not available")
+    out = subprocess.run([tool, "-d", path], capture_output=True, text=True, check=True).stdout
+    needed = re.findall(r"\(NEEDED\).*\[(.+?)\]", out)
+    assert needed, out
+    assert not [n for n in needed if "cublas" in n.lower()], needed
 
 
 @pytest.mark.parametrize("n,K,r", [(1, 4, 0.8), (37, 8, 0.8), (500, 8, 0.7), (64, 16, 0.9)])

@@ -70,7 +70,7 @@ def _run(dims, seed, n, K, cod):
     M = len(rp)
     labels = rng.integers(0, dims.draft_vocab, M).astype(np.int32)
     m = pk()
-    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=M, max_seq=n)
+    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=M, max_seq=n, train=True)
     g = _grad_buffers(dims)
     loss = torch.full((1,), float("nan"), device="cuda")
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
@@ -132,9 +132,16 @@ def test_small_bf16_train_step(n, K, cod):
     _compare(dims, _run(dims, 7 + K, n, K, cod), 2e-2, 2e-3, 1e-3, f"bf16 n={n} K={K}")
 
 
-def test_train_step_rejects_a_window():
+def test_train_step_needs_training_workspaces():
+    """A windowed drafter cannot hold the training workspaces (UNSUPPORTED at create), and
+    a context made without them refuses the step (CAPACITY) instead of allocating."""
     m = pk()
     dims = synth.shrink(SMALL_BF16, attn_window=8)
+    w = synth.make_weights(dims, 1)
+    with pytest.raises(m.PeagleError) as e:
+        make_ctx(dims, w, 1, 2, 32, max_rows=16, max_seq=8, train=True)
+    assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
+    dims = SMALL_BF16
     w = synth.make_weights(dims, 1)
     ctx = make_ctx(dims, w, 1, 2, 32, max_rows=16, max_seq=8)
     z = torch.zeros(16, dtype=torch.int32, device="cuda")
@@ -144,7 +151,7 @@ def test_train_step_rejects_a_window():
         m.peagle_train_step(ctx, 8, 2, z, torch.zeros(8, 3 * dims.hidden, device="cuda",
                                                       dtype=torch.bfloat16),
                             z, z, 8, z, loss, g)
-    assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
+    assert e.value.code == m.PEAGLE_ERR_CAPACITY
     ctx.close()
 
 
@@ -162,7 +169,7 @@ def test_train_step_loss_at_full_size_is_the_forward_cross_entropy():
     rp, rd = m.peagle_cod_rows(n, K, wl.cod_ratio, ti["cod_u"])
     M = len(rp)
     labels = np.random.default_rng(5).integers(0, dims.draft_vocab, M).astype(np.int32)
-    ctx = make_ctx(dims, w, 1, K, n, max_rows=M, max_seq=n)
+    ctx = make_ctx(dims, w, 1, K, n, max_rows=M, max_seq=n, train=True)
     del w
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     tok, hid, rpd, rdd, lab = dev(ti["tokens"]), ti["hidden"].cuda(), dev(rp), dev(rd), dev(labels)
@@ -193,7 +200,7 @@ def test_train_step_flags_rows_outside_the_contract():
     w = synth.make_weights(dims, 2)
     n, K = 8, 3
     rp, rd = m.peagle_cod_rows(n, K, 1.0, np.zeros((n, K)))
-    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=len(rp), max_seq=n)
+    ctx = make_ctx(dims, w, 1, K, n + 8, max_rows=len(rp), max_seq=n, train=True)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     tok = dev(np.arange(n, dtype=np.int32))
     hid = torch.randn(n, 3 * dims.hidden, device="cuda")
