@@ -810,10 +810,10 @@ bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, 
   return encode_map(p, out, base, rows, cols, ld, box_rows);
 }
 bool tc_tensor_map_f32(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
-                       int ld) {
+                       int ld, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-  cuuint32_t box[2] = {32, 128};
+  cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = p->encode(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -827,6 +827,7 @@ bool tc_tensor_map_f32(TcGemmPlan* p, CUtensorMap* out, const void* base, int ro
   return true;
 }
 float* tc_partials(TcGemmPlan* p) { return p->ws; }
+int tc_num_sms(TcGemmPlan* p) { return p->num_sms; }
 unsigned* tc_tile_counters(TcGemmPlan* p) { return p->counters; }
 int tc_max_tiles(TcGemmPlan* p) { return p->max_tiles; }
 

@@ -27,11 +27,12 @@ void tc_destroy(TcGemmPlan* p);
 // [2 * num_sms][256][128] fp32 and the per-tile counters (zero between projections).
 bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
                    int ld, int box_rows);
-// [rows][cols] fp32 (row stride ld, a multiple of 4), boxes of 32 columns x 128 rows,
-// 128-byte swizzle: the TF32 GEMM's K-major operands.
+// [rows][cols] fp32 (row stride ld, a multiple of 4), boxes of 32 columns x box_rows rows
+// (<= 256), 128-byte swizzle: the TF32 GEMM's K-major operands.
 bool tc_tensor_map_f32(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
-                       int ld);
+                       int ld, int box_rows);
 float* tc_partials(TcGemmPlan* p);
+int tc_num_sms(TcGemmPlan* p);
 unsigned* tc_tile_counters(TcGemmPlan* p);
 int tc_max_tiles(TcGemmPlan* p);
 

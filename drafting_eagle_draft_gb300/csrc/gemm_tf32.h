@@ -19,6 +19,10 @@ struct TrainGemmCtx {
   unsigned* err;           // device error word (timeouts of the bounded waits)
 };
 
+// out[c][r] = in[r][c] (in: rows x cols, row stride ld_in; out row stride ld_out).
+void launch_transpose_f32(const float* in, int rows, int cols, int ld_in, float* out, int ld_out,
+                          cudaStream_t s);
+
 // Floats of a scratch buffer that holds a [rows][cols] operand with a padded row stride.
 size_t tf32_scratch_floats(int rows, int cols);
 

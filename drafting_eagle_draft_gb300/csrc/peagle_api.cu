@@ -34,6 +34,10 @@ struct TrainWs {
   // fp32 weights (the context's own buffers on fp32 contexts); gate / up interleaved
   float *fc, *lm, *in_norm, *hid_norm, *fin_norm;
   std::vector<float*> qkv, o, gu, down, attn_norm, post_norm;
+  // bf16 contexts: the projection weights transposed ([in][out]), the K-major B operand
+  // of the backward's dX = dY W on the tensor cores (null on fp32 contexts)
+  float *fcT = nullptr, *lmT = nullptr;
+  std::vector<float*> qkvT, oT, guT, downT;
   // forward (saved)
   int* chain;
   float *E, *Hin, *f, *r1, *r2, *x0, *y, *ry, *logits, *row_loss, *resL;
@@ -1206,6 +1210,26 @@ static int train_ws(peagle_ctx* c) {
     if (l > 0) TRY_RET(wcopy(&w->attn_norm[l], c->attn_norm[l], H));
     TRY_RET(wcopy(&w->post_norm[l], c->post_norm[l], H));
   }
+  w->qkvT.assign(N, nullptr);
+  w->oT.assign(N, nullptr);
+  w->guT.assign(N, nullptr);
+  w->downT.assign(N, nullptr);
+  if (c->bf) {
+    // W [out][in] -> W^T [in][out] (every out dimension is a multiple of 4 floats)
+    auto wT = [&](float** dst, const float* src, int out_dim, int in_dim) -> int {
+      TRY_RET(fl(dst, (size_t)out_dim * in_dim));
+      launch_transpose_f32(src, out_dim, in_dim, in_dim, *dst, out_dim, 0);
+      return PEAGLE_OK;
+    };
+    TRY_RET(wT(&w->fcT, w->fc, H, 3 * H));
+    TRY_RET(wT(&w->lmT, w->lm, Vd, H));
+    for (int l = 0; l < N; ++l) {
+      TRY_RET(wT(&w->qkvT[l], w->qkv[l], qkv_out, l == 0 ? 2 * H : H));
+      TRY_RET(wT(&w->oT[l], w->o[l], H, nq * hd));
+      TRY_RET(wT(&w->guT[l], w->gu[l], 2 * I, H));
+      TRY_RET(wT(&w->downT[l], w->down[l], H, I));
+    }
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return PEAGLE_ERR_CUDA;
   // forward, kept for the backward
   TRY_RET(dalloc(c, (void**)&w->chain, (size_t)M * 15 * 4));
@@ -1347,6 +1371,15 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     if (gerr == PEAGLE_OK)
       gerr = train_gemm(tg, ta, tb, m, nn, k, alpha, A, lda, B, ldb, beta, C, ldc, s);
   };
+  // C [m x nn] = A W for a weight W stored [k][nn] (nn.Linear [out][in], k = out): from its
+  // transposed copy WT [nn][k] where the context holds one
+  auto GMW = [&](int m, int nn, int k, const float* A, int lda, const float* W,
+                 const float* WT, float* C, int ldc) {
+    if (WT)
+      GM(false, true, m, nn, k, 1.f, A, lda, WT, k, 0.f, C, ldc);
+    else
+      GM(false, false, m, nn, k, 1.f, A, lda, W, nn, 0.f, C, ldc);
+  };
   launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s);
   launch_chain(M, n, K, Kmax, row_p, row_d, c->row_index, w->chain, s);
   TrainAttn ta;
@@ -1413,7 +1446,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
 
   // ---- backward
   GM(true, false, Vd, H, M, 1.f, w->logits, Vd, w->y, H, 0.f, gr->lm_head, H);
-  GM(false, false, M, H, Vd, 1.f, w->logits, Vd, w->lm, H, 0.f, w->dy, H);
+  GMW(M, H, Vd, w->logits, Vd, w->lm, w->lmT, w->dy, H);
   float* dres = w->bufA;
   float* dmid = w->bufB;
   launch_rms_bwd(M, H, w->resL, H, w->ry, w->fin_norm, w->dy, H, dres, H, false, s);
@@ -1423,11 +1456,11 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     const int din = l == 0 ? 2 * H : H;
     // MLP
     GM(true, false, H, I, M, 1.f, dres, H, w->act[l], I, 0.f, gr->down[l], I);
-    GM(false, false, M, I, H, 1.f, dres, H, w->down[l], I, 0.f, w->dact, I);
+    GMW(M, I, H, dres, H, w->down[l], w->downT[l], w->dact, I);
     launch_swiglu_bwd(M, I, w->GU[l], w->dact, w->dGU, s);
     GM(true, false, 2 * I, H, M, 1.f, w->dGU, 2 * I, w->u[l], H, 0.f, w->dgu_w, H);
     launch_gu_split(I, H, w->dgu_w, gr->gate[l], gr->up[l], s);
-    GM(false, false, M, H, 2 * I, 1.f, w->dGU, 2 * I, w->gu[l], H, 0.f, w->du, H);
+    GMW(M, H, 2 * I, w->dGU, 2 * I, w->gu[l], w->guT[l], w->du, H);
     if (cudaMemcpyAsync(dmid, dres, (size_t)M * H * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return PEAGLE_ERR_CUDA;
     launch_rms_bwd(M, H, w->res_mid[l], H, w->ru[l], w->post_norm[l], w->du, H, dmid, H, true, s);
@@ -1435,7 +1468,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     launch_colsum(M, H, w->du, H, w->res_mid[l], H, w->ru[l], nullptr, gr->post_norm[l], s);
     // attention
     GM(true, false, H, nqhd, M, 1.f, dmid, H, w->O[l], nqhd, 0.f, gr->o[l], nqhd);
-    GM(false, false, M, nqhd, H, 1.f, dmid, H, w->o[l], nqhd, 0.f, w->dO, nqhd);
+    GMW(M, nqhd, H, dmid, H, w->o[l], w->oT[l], w->dO, nqhd);
     launch_attn_bwd_prep(ta, w->dO, w->O[l], w->dOh, w->Dv, s);
     TRY_RET(zero(w->dKr, (size_t)M * nkv * hd, s));
     TRY_RET(zero(w->dVr, (size_t)M * nkv * hd, s));
@@ -1468,7 +1501,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     launch_train_rope_bwd(M, n, K, nq, nkv, hd, w->dQh, w->dKr, w->dVr, row_p, row_d, c->rope,
                           w->dqkv, s);
     GM(true, false, qkv_out, din, M, 1.f, w->dqkv, qkv_out, w->a[l], din, 0.f, gr->qkv[l], din);
-    GM(false, false, M, din, qkv_out, 1.f, w->dqkv, qkv_out, w->qkv[l], din, 0.f, w->da, din);
+    GMW(M, din, qkv_out, w->dqkv, qkv_out, w->qkv[l], w->qkvT[l], w->da, din);
     if (l > 0) {
       launch_rms_bwd(M, H, w->res_in[l], H, w->ra[l], w->attn_norm[l], w->da, H, dmid, H, true, s);
       if (gr->attn_norm && gr->attn_norm[l]) {
@@ -1489,7 +1522,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   launch_colsum(M, H, w->da + H, 2 * H, w->f, H, w->r2, nullptr, gr->hidden_norm, s);
   launch_add((size_t)M * H, dres, w->df, s);
   GM(true, false, H, 3 * H, M, 1.f, w->df, H, w->Hin, 3 * H, 0.f, gr->fc, 3 * H);
-  GM(false, false, M, 3 * H, H, 1.f, w->df, H, w->fc, 3 * H, 0.f, w->dHin, 3 * H);
+  GMW(M, 3 * H, H, w->df, H, w->fc, w->fcT, w->dHin, 3 * H);
   TRY_RET(zero(gr->emb_mask, H, s));
   launch_colsum(M, H, w->dE, H, nullptr, 0, nullptr, row_d, gr->emb_mask, s);
   TRY_RET(zero(gr->h_shared, (size_t)3 * H, s));
