@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpeagle.so")
 SOURCES = ["peagle_api.cu", "kernels.cu", "gemm_tc.cu", "pass_kernel.cu", "masked_attn_tc.cu",
-           "train_kernels.cu", "train_attn_mma.cu", "gemm_tf32.cu"]
+           "train_kernels.cu", "train_attn_mma.cu", "train_attn_tc.cu", "gemm_tf32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

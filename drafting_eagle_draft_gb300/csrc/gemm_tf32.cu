@@ -47,23 +47,6 @@ struct TfArgs {
   unsigned* err;
 };
 
-// Instruction descriptor of tcgen05.mma kind::tf32: TF32 A and B (format code 2), fp32 D,
-// both K-major.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Tile t of the grouped order: groups of TF_GROUP_M row tiles, row tile fastest inside a
 // group, so consecutive tiles share their B tile and a group's tiles share A tiles.
 __device__ __forceinline__ void tf_tile(const TfArgs& a, int t, int& mi, int& ni) {
@@ -146,7 +129,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_tf32(TF_BM, TF_BN);
+      const uint32_t idesc = tc::idesc_tf32(TF_BM, TF_BN);
       long long it = 0;
       int j = 0;  // tiles of this CTA
       for (int t = blockIdx.x; t < tiles && !*s_abort; t += gridDim.x, ++j) {
@@ -174,7 +157,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
           const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)st * TF_B_TILE));
 #pragma unroll
           for (int k = 0; k < 4; ++k)  // K = 8 TF32 values (32 bytes) per MMA
-            mma_tf32(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            tc::mma_tf32(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           tc::mma_commit(&empty[st]);
         }
         if (!ok) break;
@@ -254,9 +237,12 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
 // keeps the column reads free of bank conflicts).
 __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ in, int rows,
                                                         int cols, int ld_in,
-                                                        float* __restrict__ out, int ld_out) {
+                                                        float* __restrict__ out, int ld_out,
+                                                        size_t stride_in, size_t stride_out) {
   __shared__ float t[64][65];
   const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  in += blockIdx.z * stride_in;  // batch z
+  out += blockIdx.z * stride_out;
   const int tx = threadIdx.x, ty = threadIdx.y;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -348,10 +334,11 @@ int cdiv_i(long long a, int b) { return (int)((a + b - 1) / b); }
 }  // namespace
 
 void launch_transpose_f32(const float* in, int rows, int cols, int ld_in, float* out, int ld_out,
-                          cudaStream_t s) {
-  if (rows <= 0 || cols <= 0) return;
-  dim3 grid(cdiv_i(cols, 64), cdiv_i(rows, 64));
-  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, rows, cols, ld_in, out, ld_out);
+                          cudaStream_t s, int batch, size_t stride_in, size_t stride_out) {
+  if (rows <= 0 || cols <= 0 || batch <= 0) return;
+  dim3 grid(cdiv_i(cols, 64), cdiv_i(rows, 64), batch);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, rows, cols, ld_in, out, ld_out, stride_in,
+                                                stride_out);
 }
 
 size_t tf32_scratch_floats(int rows, int cols) {

@@ -19,9 +19,11 @@ struct TrainGemmCtx {
   unsigned* err;           // device error word (timeouts of the bounded waits)
 };
 
-// out[c][r] = in[r][c] (in: rows x cols, row stride ld_in; out row stride ld_out).
+// out[c][r] = in[r][c] (in: rows x cols, row stride ld_in; out row stride ld_out), for
+// `batch` matrices stride_in / stride_out floats apart.
 void launch_transpose_f32(const float* in, int rows, int cols, int ld_in, float* out, int ld_out,
-                          cudaStream_t s);
+                          cudaStream_t s, int batch = 1, size_t stride_in = 0,
+                          size_t stride_out = 0);
 
 // Floats of a scratch buffer that holds a [rows][cols] operand with a padded row stride.
 size_t tf32_scratch_floats(int rows, int cols);

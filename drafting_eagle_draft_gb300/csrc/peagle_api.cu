@@ -38,6 +38,9 @@ struct TrainWs {
   // of the backward's dX = dY W on the tensor cores (null on fp32 contexts)
   float *fcT = nullptr, *lmT = nullptr;
   std::vector<float*> qkvT, oT, guT, downT;
+  // the tcgen05 prefix attention: one layer's keys or values transposed [nkv][64][ldn]
+  float* kvT = nullptr;
+  int ldn = 0;
   // forward (saved)
   int* chain;
   float *E, *Hin, *f, *r1, *r2, *x0, *y, *ry, *logits, *row_loss, *resL;
@@ -1283,6 +1286,10 @@ static int train_ws(peagle_ctx* c) {
     TRY_RET(dalloc(c, (void**)&w->S1, count * 4));
     TRY_RET(dalloc(c, (void**)&w->dP1, count * 4));
   }
+  if (!dense_attn && attn_tc_ok(probe)) {
+    w->ldn = (n + 3) / 4 * 4;
+    TRY_RET(fl(&w->kvT, (size_t)nkv * 64 * w->ldn));
+  }
   TRY_RET(fl(&w->Oh, (size_t)nq * M * hd));
   TRY_RET(fl(&w->lrow, (size_t)nq * M));
   // backward
@@ -1397,6 +1404,11 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   // dense prefix score matrices, made by peagle_create)
   const bool fused_attn = c->bf && attn_bwd_fused_ok(ta);
   if (!fused_attn && !w->S1) return PEAGLE_ERR_UNSUPPORTED;
+  TrainAttnTc atc;
+  atc.tc = c->tc;
+  atc.err = c->err;
+  atc.kvT = w->kvT;
+  atc.ldn = w->ldn;
 
   // ---- forward
   launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
@@ -1414,8 +1426,9 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     launch_train_rope(M, n, K, nq, nkv, hd, w->qkvb, row_p, row_d, c->rope, w->Qh[l], w->Kr[l],
                       w->Vr[l], w->K1[l], w->V1[l], s);
     if (fused_attn)  // online softmax over the prefix, then the chain keys per row
-      launch_attn_fwd_fused(ta, w->Qh[l], w->Kr[l], w->Vr[l], w->K1[l], w->V1[l], w->Oh, w->Dv,
-                            w->lrow, w->Pc[l], w->lse[l], w->O[l], s);
+      TRY_RET(launch_attn_fwd_fused(ta, w->Qh[l], w->Kr[l], w->Vr[l], w->K1[l], w->V1[l], w->Oh,
+                                    w->Dv, w->lrow, w->Pc[l], w->lse[l], w->O[l],
+                                    w->kvT ? &atc : nullptr, s));
     for (int g = 0; g < nkv && !fused_attn; ++g) {
       const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;
       const float* K1g = w->K1[l] + (size_t)g * n * hd;

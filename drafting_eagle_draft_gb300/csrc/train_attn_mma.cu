@@ -576,18 +576,25 @@ bool attn_bwd_fused_ok(const TrainAttn& a) {
   return a.hd == 64 && G >= 1 && G <= 8;
 }
 
-void launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
-                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
-                           float* lse, float* O, cudaStream_t s) {
+int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
+                          float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
+                          float* lse, float* O, const TrainAttnTc* tcx, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, Qh);
   for (float* p : {K1, V1}) round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
-  const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
-  smem_optin((const void*)attn_fwd_prefix_kernel, (int)smem);
-  attn_fwd_prefix_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, K1, V1, Op,
-                                                                           mrow, lrow);
+  if (tcx && attn_tc_ok(a)) {
+    const int r = launch_attn_fwd_prefix_tc(a, *tcx, Qh, K1, V1, Op, mrow, lrow, s);
+    if (r != PEAGLE_OK) return r;
+  } else {
+    const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
+    if (smem_optin((const void*)attn_fwd_prefix_kernel, (int)smem) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    attn_fwd_prefix_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, K1, V1, Op,
+                                                                             mrow, lrow);
+  }
   attn_fwd_combine_kernel<<<(a.nq * a.M + 7) / 8, 256, 0, s>>>(a, Qh, Kr, Vr, Op, mrow, lrow, Pc,
                                                               lse, O);
+  return PEAGLE_OK;
 }
 
 void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,

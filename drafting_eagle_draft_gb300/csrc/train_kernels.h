@@ -18,6 +18,16 @@ struct TrainAttn {
   const int* chain;
 };
 
+// tcgen05 forms of the fused prefix attention (train_attn_tc.cu): head_dim 64 and
+// G = nq / nkv in {1, 2, 4, 8}.
+struct TcGemmPlan;
+struct TrainAttnTc {
+  TcGemmPlan* tc;  // tensor-map encoder
+  unsigned* err;   // device error word (bounded waits latch TIMEOUT)
+  float* kvT;      // [nkv][64][ldn]: one layer's keys or values transposed
+  int ldn;         // >= n, a multiple of 4
+};
+
 void launch_train_inputs(bool bf16, int M, int n, int K, int H, const int* row_p,
                          const int* row_d, const int* tokens, const void* hidden,
                          const void* embed, int Vt, const void* emb_mask, const void* h_shared,
@@ -62,13 +72,20 @@ bool attn_bwd_fused_ok(const TrainAttn& a);
 // The forward the same way (Q, K1, V1 rounded to TF32 in place first): the prefix's unnormalised
 // output Op (per-head rows [nq][M][64]) with its row max / sum, then the chain keys joined
 // per row: lse, Pc and O [M][nq hd].
-void launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
-                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
-                           float* lse, float* O, cudaStream_t s);
+// With tcx (and attn_tc_ok), the prefix part runs on the tcgen05 kernel.
+int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
+                          float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
+                          float* lse, float* O, const TrainAttnTc* tcx, cudaStream_t s);
 void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
                            const float* dOh, const float* K1, const float* V1,
                            const float* lse, const float* Dv, float* dQh, float* dK1,
                            float* dV1, bool qkv_rounded, cudaStream_t s);
+bool attn_tc_ok(const TrainAttn& a);
+// The prefix part of the forward (Q, K1, V1 already rounded to TF32): Op, mrow, lrow as
+// launch_attn_fwd_fused's prefix kernel writes them.  V1 is transposed into kvT first.
+int launch_attn_fwd_prefix_tc(const TrainAttn& a, const TrainAttnTc& x, const float* Qh,
+                              const float* K1, const float* V1, float* Op, float* mrow,
+                              float* lrow, cudaStream_t s);
 void launch_ce(int M, int V, float* logits, const int* labels, float* row_loss, float* loss,
                unsigned* err, cudaStream_t s);
 void launch_embed_grad(int M, int n, int K, int H, int Vt, const int* row_p, const int* row_d,
