@@ -41,6 +41,8 @@ struct TrainWs {
   // the tcgen05 prefix attention: one layer's keys or values transposed [nkv][64][ldn]
   float* kvT = nullptr;
   int ldn = 0;
+  float *qT = nullptr, *doT = nullptr;  // [nq][64][ldm]: queries / dO transposed
+  int ldm = 0;
   // forward (saved)
   int* chain;
   float *E, *Hin, *f, *r1, *r2, *x0, *y, *ry, *logits, *row_loss, *resL;
@@ -1289,6 +1291,9 @@ static int train_ws(peagle_ctx* c) {
   if (!dense_attn && attn_tc_ok(probe)) {
     w->ldn = (n + 3) / 4 * 4;
     TRY_RET(fl(&w->kvT, (size_t)nkv * 64 * w->ldn));
+    w->ldm = (M + 3) / 4 * 4;
+    TRY_RET(fl(&w->qT, (size_t)nq * 64 * w->ldm));
+    TRY_RET(fl(&w->doT, (size_t)nq * 64 * w->ldm));
   }
   TRY_RET(fl(&w->Oh, (size_t)nq * M * hd));
   TRY_RET(fl(&w->lrow, (size_t)nq * M));
@@ -1409,6 +1414,9 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
   atc.err = c->err;
   atc.kvT = w->kvT;
   atc.ldn = w->ldn;
+  atc.qT = w->qT;
+  atc.doT = w->doT;
+  atc.ldm = w->ldm;
 
   // ---- forward
   launch_train_inputs(c->bf, M, n, K, H, row_p, row_d, tokens, hidden, c->embed, Vt, c->emb_mask,
@@ -1493,8 +1501,9 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
                            w->Vr[l], w->dOh, w->dQh, w->dKr, w->dVr, s);
       TRY_RET(zero(w->dK1, (size_t)nkv * n * hd, s));
       TRY_RET(zero(w->dV1, (size_t)nkv * n * hd, s));
-      launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l], w->V1[l],
-                            w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, true, s);
+      TRY_RET(launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l],
+                                    w->V1[l], w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, true,
+                                    w->kvT ? &atc : nullptr, s));
     }
     for (int g = 0; g < nkv && !fused_attn; ++g) {
       const float* Qg = w->Qh[l] + (size_t)g * G * M * hd;

@@ -597,13 +597,13 @@ int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const 
   return PEAGLE_OK;
 }
 
-void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
-                           const float* dOh, const float* K1, const float* V1,
-                           const float* lse, const float* Dv, float* dQh, float* dK1,
-                           float* dV1, bool qkv_rounded, cudaStream_t s) {
+int launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
+                          const float* dOh, const float* K1, const float* V1,
+                          const float* lse, const float* Dv, float* dQh, float* dK1,
+                          float* dV1, bool qkv_rounded, const TrainAttnTc* tcx,
+                          cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
-  smem_optin((const void*)attn_bwd_dq_kernel, (int)smem);
   // the stored operands are rounded to TF32 once, not per use in the products (Q, K1 and
   // V1 already are when the forward ran fused)
   round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)dOh);
@@ -612,10 +612,24 @@ void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, c
     for (float* p : {(float*)K1, (float*)V1})
       round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
   }
-  attn_bwd_dq_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, dOh, K1, V1, lse,
-                                                                       Dv, dQh);
-  attn_bwd_dkv_kernel<<<dim3((a.n + 63) / 64, a.nkv, (a.M + DKV_CHUNK - 1) / DKV_CHUNK), 128, 0,
-                        s>>>(a, row_index, Kmax, Qh, dOh, K1, V1, lse, Dv, dK1, dV1);
+  if (tcx && attn_tc_ok(a)) {
+    const int r = launch_attn_bwd_dq_tc(a, *tcx, Qh, dOh, K1, V1, lse, Dv, dQh, s);
+    if (r != PEAGLE_OK) return r;
+  } else {
+    if (smem_optin((const void*)attn_bwd_dq_kernel, (int)smem) != cudaSuccess)
+      return PEAGLE_ERR_CUDA;
+    attn_bwd_dq_kernel<<<dim3((a.M + 15) / 16, a.nkv), 32 * G, smem, s>>>(a, Qh, dOh, K1, V1,
+                                                                         lse, Dv, dQh);
+  }
+  if (tcx && attn_tc_ok(a) && tcx->qT) {
+    const int r = launch_attn_bwd_dkv_tc(a, *tcx, row_index, Kmax, Qh, dOh, K1, V1, lse, Dv,
+                                         dK1, dV1, s);
+    if (r != PEAGLE_OK) return r;
+  } else {
+    attn_bwd_dkv_kernel<<<dim3((a.n + 63) / 64, a.nkv, (a.M + DKV_CHUNK - 1) / DKV_CHUNK), 128,
+                          0, s>>>(a, row_index, Kmax, Qh, dOh, K1, V1, lse, Dv, dK1, dV1);
+  }
+  return PEAGLE_OK;
 }
 
 }  // namespace peagle

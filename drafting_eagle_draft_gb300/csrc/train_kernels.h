@@ -26,6 +26,9 @@ struct TrainAttnTc {
   unsigned* err;   // device error word (bounded waits latch TIMEOUT)
   float* kvT;      // [nkv][64][ldn]: one layer's keys or values transposed
   int ldn;         // >= n, a multiple of 4
+  float* qT;       // [nq][64][ldm]: queries transposed (backward)
+  float* doT;      // [nq][64][ldm]: dO transposed (backward)
+  int ldm;         // >= M, a multiple of 4
 };
 
 void launch_train_inputs(bool bf16, int M, int n, int K, int H, const int* row_p,
@@ -76,16 +79,29 @@ bool attn_bwd_fused_ok(const TrainAttn& a);
 int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const float* Vr,
                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
                           float* lse, float* O, const TrainAttnTc* tcx, cudaStream_t s);
-void launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
-                           const float* dOh, const float* K1, const float* V1,
-                           const float* lse, const float* Dv, float* dQh, float* dK1,
-                           float* dV1, bool qkv_rounded, cudaStream_t s);
+// With tcx (and attn_tc_ok), the dQ part runs on the tcgen05 kernel.
+int launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
+                          const float* dOh, const float* K1, const float* V1,
+                          const float* lse, const float* Dv, float* dQh, float* dK1,
+                          float* dV1, bool qkv_rounded, const TrainAttnTc* tcx,
+                          cudaStream_t s);
 bool attn_tc_ok(const TrainAttn& a);
 // The prefix part of the forward (Q, K1, V1 already rounded to TF32): Op, mrow, lrow as
 // launch_attn_fwd_fused's prefix kernel writes them.  V1 is transposed into kvT first.
 int launch_attn_fwd_prefix_tc(const TrainAttn& a, const TrainAttnTc& x, const float* Qh,
                               const float* K1, const float* V1, float* Op, float* mrow,
                               float* lrow, cudaStream_t s);
+// dQh += dS K1 over the prefix (Q, dO, K1, V1 already rounded to TF32); K1 is
+// transposed into kvT first.
+int launch_attn_bwd_dq_tc(const TrainAttn& a, const TrainAttnTc& x, const float* Qh,
+                          const float* dOh, const float* K1, const float* V1, const float* lse,
+                          const float* Dv, float* dQh, cudaStream_t s);
+// dK1 += dS^T Q, dV1 += P^T dO over the prefix (operands already rounded to TF32); Q and
+// dO are transposed into qT / doT first.
+int launch_attn_bwd_dkv_tc(const TrainAttn& a, const TrainAttnTc& x, const int* row_index,
+                           int Kmax, const float* Qh, const float* dOh, const float* K1,
+                           const float* V1, const float* lse, const float* Dv, float* dK1,
+                           float* dV1, cudaStream_t s);
 void launch_ce(int M, int V, float* logits, const int* labels, float* row_loss, float* loss,
                unsigned* err, cudaStream_t s);
 void launch_embed_grad(int M, int n, int K, int H, int Vt, const int* row_p, const int* row_d,
