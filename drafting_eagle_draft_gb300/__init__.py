@@ -36,7 +36,7 @@ EXPORTS = ("peagle_create", "peagle_draft", "peagle_catch_up", "peagle_verify_gr
            "peagle_sequence_partition",
            "peagle_status",
            "peagle_set_timing", "peagle_read_timing", "peagle_read_pass_trace",
-           "peagle_set_wait_limit",
+           "peagle_set_wait_limit", "peagle_set_pass_kernel",
            "peagle_decode_attention_static",
            "peagle_device_error_bits", "peagle_strerror", "peagle_destroy")
 STAGES = ("fc", "qkv", "attn", "oproj", "gate_up", "down", "lm_head", "norm", "small")
@@ -113,6 +113,7 @@ def lib():
         L.peagle_status.argtypes = [_vp]
         L.peagle_set_timing.argtypes = [_vp, _i32]
         L.peagle_set_wait_limit.argtypes = [_vp, ctypes.c_uint64, _i32]
+        L.peagle_set_pass_kernel.argtypes = [_vp, _i32]
         L.peagle_decode_attention_static.argtypes = [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                                      _i32, _vp, _vp, _vp]
         L.peagle_read_timing.argtypes = [_vp, _vp, _vp]
@@ -333,6 +334,11 @@ def peagle_sequence_partition(row_p, row_d, boundaries):
 def peagle_status(ctx: Context) -> int:
     """Synchronises; returns PEAGLE_OK or PEAGLE_ERR_DEVICE (device error bits cleared)."""
     return lib().peagle_status(ctx.handle)
+
+
+def peagle_set_pass_kernel(ctx: Context, mode: int):
+    """-1: the persistent pass kernel up to 16 draft rows (default); 0: never; 1: always."""
+    _check(lib().peagle_set_pass_kernel(ctx.handle, int(mode)), "peagle_set_pass_kernel")
 
 
 def peagle_set_wait_limit(ctx: Context, limit_ns: int, unreachable_step: int = -1):

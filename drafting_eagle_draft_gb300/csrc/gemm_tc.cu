@@ -749,10 +749,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 struct TcGemmPlan {
   int num_sms;
-  bool pair;  // large-M GEMMs on CTA pairs (PEAGLE_GEMM_PAIR=0 turns it off)
+  bool pair;  // large-M GEMMs on CTA pairs
   int pair_clusters;  // CTA pairs that fit on the GPU at once (a cluster stays in one GPC)
-  int fold_mode;      // folded wide tiles: 0 where they pay, 1 wherever the shapes allow,
-                      // -1 never (PEAGLE_GEMM_FOLD=1 / 0)
+  int fold_mode;      // folded wide tiles: 0 where they pay (the only mode in use)
   int max_bn;
   float* ws;
   unsigned* counters;
@@ -873,10 +872,8 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
   {
     // a persistent grid of pairs must be resident at once: as many pairs as clusters of
     // two fit (each GPC holds an even number of the CTAs), not num_sms / 2
-    const char* env = getenv("PEAGLE_GEMM_PAIR");
-    p->pair = !(env && env[0] == '0');
-    const char* fenv = getenv("PEAGLE_GEMM_FOLD");
-    p->fold_mode = fenv ? (fenv[0] == '1' ? 1 : fenv[0] == '0' ? -1 : 0) : 0;
+    p->pair = true;
+    p->fold_mode = 0;
     p->pair_clusters = 0;
     int stages = 2;
     while (stages < 8 && smem_bytes_pair(stages + 1) <= PAIR_SMEM_BUDGET) ++stages;
@@ -897,9 +894,6 @@ int tc_create(TcGemmPlan** out, int num_sms, int rows_max, int max_dim, unsigned
       nc = 0;
     }
     p->pair_clusters = nc < num_sms / 2 ? nc : num_sms / 2;
-    if (getenv("PEAGLE_GEMM_PAIR_INFO"))
-      fprintf(stderr, "peagle: %d CTA pairs resident at once (%d SMs)\n", p->pair_clusters,
-              num_sms);
   }
   *out = p;
   return PEAGLE_OK;

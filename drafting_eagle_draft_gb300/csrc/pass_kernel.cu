@@ -187,8 +187,10 @@ __device__ bool wk_wait_count(const PassParams& P, const unsigned* ctr, unsigned
   return ok;
 }
 
-// Timing: event k of (phase, this CTA) -- 0: activations of a projection ready (seen by
-// the activation producer), 1: first MMA issued, 2: last accumulator committed, 3: done.
+// Timing: event k of (phase, this CTA) -- projections: 0 activations ready (seen by the
+// activation producer), 1 first MMA issued, 2 last accumulator committed; other steps: 0
+// the previous step seen complete; attention: 1 the item's partials written, 2 every
+// item of its (request, kv head) in; 3: done.
 __device__ __forceinline__ void trace_ev(const PassParams& P, int ph, int k) {
   if (P.trace_cta)
     P.trace_cta[((size_t)ph * gridDim.x + blockIdx.x) * 4 + k] = tc::globaltimer();
@@ -773,6 +775,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           alive = false;
           break;
         }
+        if (et == 0) trace_ev(P, j, 0);
         if (ph.kind == PP_INPUT) {
           step_input(P, c, G, et, s_rs, s_tok);
         } else if (ph.kind == PP_NORM) {
@@ -823,6 +826,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               auto bar = []() { wk_bar(); };
               attn_mma_item<HD, pass_att_nbuf(HD), decltype(bar), true>(a, b, g, cc, et, 128, uni,
                                                                          bar);
+              if (et == 0) trace_ev(P, j, 1);
             }
             const int share = nv > 0 ? nv : 1;
             if (cc >= share) continue;
@@ -833,6 +837,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               alive = false;
               break;
             }
+            if (et == 0) trace_ev(P, j, 2);
             const int r0 = cc * rows / share, r1 = (cc + 1) * rows / share;
             if (nv > 0) {
               for (int rr = r0 + wid; rr < r1; rr += 4)

@@ -112,11 +112,10 @@ struct peagle_ctx {
   unsigned last_err_bits;
   TcGemmPlan* tc;   // tensor-core GEMM state (bf16 only)
   // persistent pass kernel (bf16): phase counters + abort flag, host-side parameter block
-  bool pass_on;     // available (bf16, cooperative launch, not disabled)
-  bool pass_force;  // PEAGLE_PASS_KERNEL=1: use it for every shape it supports
+  bool pass_on;     // available (bf16, cooperative launch, at most PASS_MAX_LAYERS layers)
+  int pass_mode;    // peagle_set_pass_kernel: -1 up to 16 draft rows, 0 never, 1 always
   bool pp_valid;    // *pp holds a complete block built for pp_key (not in timing mode)
   PassKey pp_key;
-  bool masked_tc;   // training forward: tcgen05 masked attention (PEAGLE_MASKED_TC=0: off)
   unsigned* pass_cnt;
   PassParams* pp;
   // timing of the pass kernel: per-call phase completion times (device slots) and the
@@ -439,21 +438,16 @@ extern "C" int peagle_create(const peagle_weights* w, const peagle_dims* dims, p
       return PEAGLE_ERR_CUDA;
     }
   }
-  {
-    const char* env = getenv("PEAGLE_MASKED_TC");
-    c->masked_tc = !(env && env[0] == '0');
-  }
-  // the whole bf16 pass as one persistent kernel, unless disabled (PEAGLE_PASS_KERNEL=0)
+  // the whole bf16 pass as one persistent kernel (peagle_set_pass_kernel chooses when)
   c->pass_on = false;
+  c->pass_mode = -1;
   c->pp = nullptr;
   c->pp_valid = false;
   c->pass_cnt = nullptr;
   if (c->bf && d.n_layers <= PASS_MAX_LAYERS) {
-    const char* env = getenv("PEAGLE_PASS_KERNEL");
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
-    c->pass_force = env && env[0] == '1';
-    if (coop && !(env && env[0] == '0')) {
+    if (coop) {
       // phase counters, the abort flag, then the attention items' counts per layer,
       // request and kv head
       TRY(dalloc(c, (void**)&c->pass_cnt,
@@ -844,7 +838,7 @@ static int draft_impl(peagle_ctx* c, int32_t batch, const peagle_kv* kv,
   // attention runs several CTAs per SM, is faster: decode_b1 (8 rows) 431 vs 448 us,
   // decode_b2 (16 rows) 613 vs 609 us, ragged_b16 (80 rows) 1927 vs 1465 us.
   const bool eff_head = d.lm_rank > 0 && (out_draft_tokens || out_logits);
-  if (c->pass_on && (c->pass_force || R <= 16)) {
+  if (c->pass_on && c->pass_mode != 0 && (c->pass_mode == 1 || R <= 16)) {
     // with the efficient LM head the pass kernel stops at the last layer's residual
     const int r = pass_draft(c, batch, kv, seq_lens, target_hidden, new_token, K, all_ntp,
                              eff_head ? nullptr : out_draft_tokens,
@@ -1115,7 +1109,7 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       // tcgen05 kernel for bf16 and head_dim 64, else the mma.sync / fp32 kernels
       TIMED(PEAGLE_STAGE_ATTN, {
         int ar = PEAGLE_ERR_UNSUPPORTED;
-        if (c->bf && c->masked_tc) ar = masked_attn_tc_launch(c->tc, a, s);
+        if (c->bf) ar = masked_attn_tc_launch(c->tc, a, s);
         if (ar == PEAGLE_ERR_UNSUPPORTED) launch_masked_attention(c->bf, a, s);
       });
     }
@@ -1664,6 +1658,13 @@ extern "C" int peagle_status(peagle_ctx* c) {
     if ((bits & PEAGLE_DEV_TIMEOUT) && reset_after_timeout(c) != PEAGLE_OK) return PEAGLE_ERR_CUDA;
     return PEAGLE_ERR_DEVICE;
   }
+  return PEAGLE_OK;
+}
+
+extern "C" int peagle_set_pass_kernel(peagle_ctx* c, int32_t mode) {
+  if (!c || mode < -1 || mode > 1) return PEAGLE_ERR_INVALID;
+  if (mode == 1 && !c->pass_on) return PEAGLE_ERR_UNSUPPORTED;
+  c->pass_mode = mode;
   return PEAGLE_OK;
 }
 

@@ -362,6 +362,16 @@ int32_t peagle_read_pass_trace(peagle_ctx* ctx, uint64_t* out, int32_t max_entri
  * Returns PEAGLE_ERR_INVALID for a step index outside the kernel's range. */
 int peagle_set_wait_limit(peagle_ctx* ctx, uint64_t limit_ns, int32_t unreachable_step);
 
+/* Which implementation runs the bf16 draft and catch-up passes.  Both compute the same
+ * pass ("2. The P-EAGLE Parallel Drafter"); they differ in speed with the number of draft
+ * rows R = batch x K.  mode -1 (the default): the persistent pass kernel (one launch per
+ * pass, one CTA per SM) up to R = 16, separate kernel launches above; 0: always the
+ * separate launches; 1: always the persistent kernel (up to its limits, R <= 120).
+ * Returns PEAGLE_ERR_INVALID for another mode, PEAGLE_ERR_UNSUPPORTED for mode 1 on a
+ * context without the persistent kernel (fp32 drafters, more than 8 layers, no
+ * cooperative launch). */
+int peagle_set_pass_kernel(peagle_ctx* ctx, int32_t mode);
+
 /* Size of the library's static scratch array used by peagle_decode_attention_static. */
 #define PEAGLE_STATIC_ATTN_SCRATCH_BYTES (8u << 20)
 

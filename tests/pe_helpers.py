@@ -1,6 +1,5 @@
 """Shared helpers of the GPU parity tests: build contexts, run the draft pass through the
 C ABI, and compare with the fp64 oracle."""
-import os
 
 import numpy as np
 import torch
@@ -27,17 +26,12 @@ def make_ctx(dims, w, max_batch, max_K, max_positions, max_rows=0, max_seq=0,
     """A context; pass_kernel True / False forces the persistent pass kernel on / off for
     the bf16 draft pass (None: the library default)."""
     m = pk()
-    old = os.environ.get("PEAGLE_PASS_KERNEL")
-    if pass_kernel is not None:
-        os.environ["PEAGLE_PASS_KERNEL"] = "1" if pass_kernel else "0"
-    try:
-        return m.peagle_create(w, m.make_dims(dims, max_batch, max_K, max_positions, max_rows,
-                                              max_seq, train))
-    finally:
-        if old is None:
-            os.environ.pop("PEAGLE_PASS_KERNEL", None)
-        else:
-            os.environ["PEAGLE_PASS_KERNEL"] = old
+    ctx = m.peagle_create(w, m.make_dims(dims, max_batch, max_K, max_positions, max_rows,
+                                         max_seq, train))
+    if pass_kernel is not None and (dims.dtype == "bf16" or not pass_kernel):
+        # fp32 drafters have no persistent pass kernel: they always take separate launches
+        m.peagle_set_pass_kernel(ctx, 1 if pass_kernel else 0)
+    return ctx
 
 
 def to_dev(inp, dev="cuda"):

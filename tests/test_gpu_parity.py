@@ -20,8 +20,8 @@ SMALL_BF16 = synth.Dims(hidden=192, n_layers=2, n_q_heads=6, n_kv_heads=2, head_
 SMALL_HD128 = synth.Dims(hidden=256, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=128,
                          intermediate=384, draft_vocab=777, target_vocab=777,
                          rope_theta=500000.0, rms_eps=1e-5, dtype="bf16", d2t="identity")
-# every projection width a multiple of 256: with 64+ draft rows (a multiple of 16) the
-# GEMMs fold the hi / lo operand rows into one accumulator and pair 128-row weight tiles
+# every projection width a multiple of 256 and 80 draft rows: the shapes the folded GEMM
+# form accepts (it is chosen where it pays: the full-size ragged_b16 pass below runs it)
 SMALL_FOLD = synth.Dims(hidden=256, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         intermediate=384, draft_vocab=1024, target_vocab=1536,
                         rope_theta=10000.0, rms_eps=1e-5, dtype="bf16", d2t="monotone")
@@ -97,11 +97,8 @@ def test_tiny_f32_empty_cache():
     (SMALL_HD128, [5, 40, 0, 77, 120, 9, 300, 64], 8),
     (SMALL_FOLD, [3, 50, 0, 17, 90, 200, 8, 64, 33, 1, 120, 77, 9, 45, 150, 260], 5),
 ])
-def test_small_bf16_parity(dims, lens, K, monkeypatch):
+def test_small_bf16_parity(dims, lens, K):
     w, inp = _small_case(dims, lens, K, 7 + K + len(lens))
-    if dims is SMALL_FOLD or len(lens) * K >= 64:
-        # the folded wide-tile GEMMs only pay at full size: force them on these shapes
-        monkeypatch.setenv("PEAGLE_GEMM_FOLD", "1")
     ctx = make_ctx(dims, w, len(lens), K, inp["capacity"] + 1)
     toks, lg, d = run_draft(ctx, dims, inp, K)
     ref = oracle_draft(dims, w, inp, K)

@@ -82,3 +82,18 @@ def test_forward_parallel_rejects_a_window():
                                   torch.from_numpy(rd).cuda(), len(rp), am, None)
     assert e.value.code == m.PEAGLE_ERR_UNSUPPORTED
     ctx.close()
+
+
+def test_decode_b2_full_size_window_4096():
+    """The full-size drafter of the decode workloads with a 4096-position window on the
+    concurrency-2 contexts (8192 and 10240 cached positions, K = 8): the pass kernel's
+    logits and ids against the fp64 oracle's windowed attention."""
+    wl = synth.WORKLOADS["decode_b2"]
+    dims = synth.shrink(wl.dims, attn_window=4096)
+    w = synth.make_weights(dims, 1234, gains=True)
+    inp = synth.make_decode_inputs(wl, 98)
+    ctx = make_ctx(dims, w, wl.batch, wl.K, inp["capacity"] + 1)
+    toks, lg, _ = run_draft(ctx, dims, inp, wl.K)
+    ctx.close()
+    ref = oracle_draft(dims, w, inp, wl.K)
+    compare(dims, ref, toks, lg, "decode_b2 window 4096")
