@@ -29,6 +29,7 @@ independent replica on its own GPU (the pass shards by request: no collective).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -66,6 +67,11 @@ def parse():
                     help="skip the efficient LM head measurement")
     ap.add_argument("--no-train-step", action="store_true",
                     help="skip the training step measurement")
+    ap.add_argument("--train-seq", type=int, default=0,
+                    help="with --only train_step: a shorter sequence than the workload's "
+                         "(a small case for profiler captures)")
+    ap.add_argument("--train-layers", type=int, default=0,
+                    help="with --only train_step: fewer decoder layers (profiler captures)")
     ap.add_argument("--only", choices=["train_fwd", "train_step", "window", "head_draft_vocab",
                                        "head_full_vocab", "decode_b2", "ragged_b16"],
                     help="run one of the extra measurements alone and print its object "
@@ -628,7 +634,7 @@ def train_fwd_measure(dev, reps=3):
             "stages_ms": {k: round(v[0], 3) for k, v in st.items()}}
 
 
-def train_step_measure(dev, reps=3):
+def train_step_measure(dev, reps=3, n_seq=0, n_layers=0):
     """Training step without optimizer on the training workload (decode drafter, n=2048,
     K=8, COD 0.8): ms per step (forward with kept activations, mean cross-entropy, every
     parameter gradient) with CUDA events, and its algorithmic FLOPs against the TF32 peak
@@ -640,6 +646,9 @@ def train_step_measure(dev, reps=3):
     import drafting_eagle_draft_gb300 as pk
 
     wl = synth.WORKLOADS["train_fwd"]
+    if n_seq or n_layers:  # a reduced case (profiler captures), never a bench line
+        wl = dataclasses.replace(wl, n_seq=n_seq or wl.n_seq,
+                                 dims=synth.shrink(wl.dims, n_layers=n_layers or wl.dims.n_layers))
     dims = wl.dims
     w = synth.make_weights(dims, 1234)
     ti = synth.make_train_inputs(wl, 21)
@@ -693,7 +702,8 @@ def train_step_measure(dev, reps=3):
     # TF32 peak: the measured bf16 burst peak times GB300's nominal dense TF32 / bf16 ratio
     peak = pk_["bf16_tflops"] * 1.1 / 2.25
     tflops = flops / (ms * 1e-3) / 1e12
-    return {"workload": wl.name, "rows": M, "ms": round(ms, 3), "loss": round(loss.item(), 5),
+    return {"workload": wl.name, "n_seq": n, "layers": dims.n_layers, "rows": M,
+            "ms": round(ms, 3), "loss": round(loss.item(), 5),
             "tflops": round(tflops, 1), "peak_tflops": round(peak, 1),
             "peak_source": "measured bf16 burst x GB300 nominal dense TF32/bf16 ratio "
                            "(1.1 / 2.25 PFLOP/s)",
@@ -787,7 +797,8 @@ def main():
         if args.only == "train_fwd":
             out = {"train_fwd": train_fwd_measure(dev)}
         elif args.only == "train_step":
-            out = {"train_step": train_step_measure(dev)}
+            out = {"train_step": train_step_measure(dev, n_seq=args.train_seq,
+                                                    n_layers=args.train_layers)}
         elif args.only == "window":
             out = {"sliding_window": window_measure(dev)}
         elif args.only in ("decode_b2", "ragged_b16"):
