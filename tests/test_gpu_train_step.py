@@ -123,13 +123,35 @@ def test_tiny_f32_train_step(n, K, cod):
     _compare(dims, _run(dims, 3 + K, n, K, cod), 1e-4, 1e-5, 1e-5, f"f32 n={n} K={K}")
 
 
-# (n=40, K=8) and (33, 3) fit one 64-key tile and one 512-row chunk of the fused attention
-# backward; (220, 8, 0.8) has four tiles of depth-1 keys and about 900 rows (two chunks of
-# the key-major kernel, its double-buffered loop), so every tiling path is compared
+# SMALL_BF16 has three q heads per kv head: the TF32 mma.sync prefix-attention kernels.
+# (n=40, K=8) and (33, 3) fit one 64-key tile and one 512-row chunk of them; (220, 8, 0.8)
+# has four tiles of depth-1 keys and about 900 rows (two chunks of the key-major kernel,
+# its double-buffered loop), so every tiling path is compared
 @pytest.mark.parametrize("n,K,cod", [(40, 8, 0.8), (33, 3, 0.6), (220, 8, 0.8)])
 def test_small_bf16_train_step(n, K, cod):
     dims = SMALL_BF16
     _compare(dims, _run(dims, 7 + K, n, K, cod), 2e-2, 2e-3, 1e-3, f"bf16 n={n} K={K}")
+
+
+# bf16 drafters whose q heads per kv head (G) take the tcgen05 prefix-attention kernels
+# (head_dim 64, G in {1, 2, 4, 8}): 128 MMA rows per CTA = 128 / G query rows x G heads
+TC_DIMS = {
+    g: synth.Dims(hidden=256, n_layers=2, n_q_heads=2 * g, n_kv_heads=2, head_dim=64,
+                  intermediate=384, draft_vocab=1000, target_vocab=1500, rope_theta=10000.0,
+                  rms_eps=1e-5, dtype="bf16", d2t="monotone")
+    for g in (1, 2, 4, 8)
+}
+
+
+# (220, 8, 0.8): about 900 rows, seven 32-key tiles of depth-1 keys (the last one ragged),
+# two 128-key blocks and two 512-row chunks of the key-major backward, row blocks of
+# 128 / G rows with a ragged last one; (40, 4, 0.8) fits one key tile
+@pytest.mark.parametrize("G,n,K,cod", [(8, 220, 8, 0.8), (4, 220, 8, 0.8), (2, 220, 8, 0.8),
+                                       (1, 220, 8, 0.8), (8, 40, 4, 0.8)])
+def test_bf16_train_step_tcgen05_attention(G, n, K, cod):
+    dims = TC_DIMS[G]
+    _compare(dims, _run(dims, 31 + G + K, n, K, cod), 2e-2, 2e-3, 1e-3,
+             f"bf16 tcgen05 attention G={G} n={n} K={K}")
 
 
 def test_train_step_needs_training_workspaces():
