@@ -808,6 +808,26 @@ bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, 
                    int ld, int box_rows) {
   return encode_map(p, out, base, rows, cols, ld, box_rows);
 }
+bool tc_tensor_map_ku(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
+                      int ld, int box_rows, int ku) {
+  // (element within a 64-wide k-block, row, k-block): one box = ku consecutive k-blocks
+  // of box_rows rows, each a 128-byte-swizzled [box_rows][64] tile
+  if (cols % 64 || ku < 1) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)ku};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = p->encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "peagle: cuTensorMapEncodeTiled (3D) failed (%d) rows=%d cols=%d ld=%d\n",
+            (int)r, rows, cols, ld);
+    return false;
+  }
+  return true;
+}
 bool tc_tensor_map_f32(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
                        int ld, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};

@@ -27,6 +27,11 @@ void tc_destroy(TcGemmPlan* p);
 // [2 * num_sms][256][128] fp32 and the per-tile counters (zero between projections).
 bool tc_tensor_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
                    int ld, int box_rows);
+// [rows][cols] bf16 (row stride ld, cols a multiple of 64) as ku-k-block boxes: one load
+// brings ku consecutive 64-wide k-blocks of box_rows rows, each a 128-byte-swizzled tile
+// (k-blocks past cols read as zero).
+bool tc_tensor_map_ku(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,
+                      int ld, int box_rows, int ku);
 // [rows][cols] fp32 (row stride ld, a multiple of 4), boxes of 32 columns x box_rows rows
 // (<= 256), 128-byte swizzle: the TF32 GEMM's K-major operands.
 bool tc_tensor_map_f32(TcGemmPlan* p, CUtensorMap* out, const void* base, int rows, int cols,

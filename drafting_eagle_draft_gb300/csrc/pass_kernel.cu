@@ -35,7 +35,7 @@ namespace {
 
 constexpr int PK_THREADS = 224;
 constexpr int PK_BWARP = 6;  // activation producer (warps 2-5 are the workers)
-constexpr int PK_A_BYTES = 128 * 128;       // one 128 x 64 bf16 weight tile
+constexpr int PK_A_BYTES = 128 * 128 * PASS_KU;  // PASS_KU 128 x 64 bf16 weight tiles
 
 __device__ __forceinline__ void wk_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -421,8 +421,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           if (!*s_abort) set_abort(P, s_abort);
           break;
         }
-        tc::mbar_expect_tx(&full[st], (uint32_t)(PK_A_BYTES + ca.BN * 128));
-        tc::tma_load_2d(sA + (size_t)st * PK_A_BYTES, ca.tw, ca.kb * 64, ca.tile * 128,
+        tc::mbar_expect_tx(&full[st], (uint32_t)(PK_A_BYTES + ca.BN * 128 * PASS_KU));
+        tc::tma_load_3d(sA + (size_t)st * PK_A_BYTES, ca.tw, 0, ca.tile * 128, ca.kb * PASS_KU,
                         &full[st], pol_w);
         cur_next(P, c, ca);
         ++nA;
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
           trace_ev(P, P.gemm[cb.g].phase, 0);
           last_traced = cb.g;
         }
-        tc::tma_load_2d(sB + (size_t)st * BS, cb.tx, cb.kb * 64, 0, &full[st], pol_x);
+        tc::tma_load_3d(sB + (size_t)st * BS, cb.tx, 0, 0, cb.kb * PASS_KU, &full[st], pol_x);
         cur_next(P, c, cb);
         ++nB;
         if (++st == S) st = 0;
@@ -536,6 +536,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
       for (int g = 0; g < n_gemm && ok; ++g) {
         // the projection's parameters in registers (see Cur)
         const int Gm = P.gemm[g].Gm, KB = P.gemm[g].KB;
+        const int kstep = P.gemm[g].BN * 128;  // bytes between a stage's activation k-blocks
         const long long total = P.gemm[g].total;
         const uint32_t idesc = P.gemm[g].idesc;
         if (c >= Gm) continue;
@@ -563,11 +564,19 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             }
             tc::fence_after_sync();
             if (it == beg) trace_ev(P, gph, 1);
-            const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)st * PK_A_BYTES));
-            const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)st * BS));
+            // the stage's PASS_KU k-blocks: weight tiles 16 KB apart, activation tiles
+            // BN x 128 bytes apart (the projection's own box height)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (it != seg_beg || k > 0) ? 1u : 0u);
+            for (int j = 0; j < PASS_KU; ++j) {
+              const uint64_t ad = tc::smem_desc_sw128(
+                  tc::smem_u32(sA + (size_t)st * PK_A_BYTES + (size_t)j * (PK_A_BYTES / PASS_KU)));
+              const uint64_t bd = tc::smem_desc_sw128(
+                  tc::smem_u32(sB + (size_t)st * BS + (size_t)j * kstep));
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc,
+                             (it != seg_beg || j > 0 || k > 0) ? 1u : 0u);
+            }
             tc::mma_commit(&empty[st]);
             if (++st == S) {
               st = 0;

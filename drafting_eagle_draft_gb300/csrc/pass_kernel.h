@@ -15,6 +15,10 @@ constexpr int PASS_MAX_GEMM = 3 + 4 * PASS_MAX_LAYERS;
 constexpr int PASS_MAX_PHASE = 5 + 7 * PASS_MAX_LAYERS;
 constexpr unsigned long long PASS_DEFAULT_WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 constexpr int PASS_MAX_ROWS = 120;                    // R = B*K (hi + lo rows <= 240)
+// 64-wide k-blocks per ring stage: one tensor load brings PASS_KU k-blocks of a 128-row
+// weight tile (32 KB).  A cold stream of 16 KB loads reached 3.9 TB/s over 152 SMs with 160
+// KB in flight per SM; 32 KB loads with the same bytes in flight, 4.9 TB/s.
+constexpr int PASS_KU = 2;
 constexpr int PASS_SS_SLOTS = 2 + 2 * PASS_MAX_LAYERS;  // per-row sums of squares
 // K/V tile buffers of an attention item (64 keys each).  Deeper pipelines (all four tiles
 // of a 256-key chunk in flight) measured no faster: an item is bound by its compute and
@@ -34,10 +38,10 @@ enum PassPhaseKind : int {
   PP_ARGMAX = 5   // LM-head argmax keys -> draft tokens (d2t applied)
 };
 
-// One projection: stream-K over (128-feature tile, 64-wide k-block) iterations, single
-// activation box of BN rows (hi rows [0,R), lo rows [R,2R) when split).
+// One projection: stream-K over (128-feature tile, k-unit of PASS_KU 64-wide k-blocks)
+// iterations, activation boxes of BN rows (hi rows [0,R), lo rows [R,2R) when split).
 struct PassGemm {
-  int Nout, Kd, R, split, additive, BN, lo_col, n_tiles, KB, Gm, phase;
+  int Nout, Kd, R, split, additive, BN, lo_col, n_tiles, KB, Gm, phase;  // KB: k-units
   int dep;  // phase whose completion the activation operand waits for (-1: none)
   uint32_t idesc;
   long long total;
@@ -100,7 +104,8 @@ struct PassParams {
   AttnArgs att;        // per layer: kc / vc advanced by layer_stride bytes
   PassPhase ph[PASS_MAX_PHASE];
   PassGemm gemm[PASS_MAX_GEMM];
-  CUtensorMap tm[2 * PASS_MAX_GEMM];  // per projection: weights, activations
+  CUtensorMap tm[2 * PASS_MAX_GEMM];  // per projection: weights, activations (PASS_KU-k-block
+                                      // boxes, tc_tensor_map_ku)
 };
 
 // Bytes of dynamic shared memory the kernel needs for `stages` ring stages.

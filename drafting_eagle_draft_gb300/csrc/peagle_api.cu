@@ -579,7 +579,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     m.BN = ((split ? 2 * rows : rows) + 15) / 16 * 16;
     m.lo_col = split ? rows : 0;
     m.n_tiles = 1;
-    m.KB = Kd / 64;
+    m.KB = (Kd / 64 + PASS_KU - 1) / PASS_KU;  // k-units (the last may run past Kd: zeros)
     const long long tiles = (long long)((Nout + 127) / 128) * m.n_tiles;
     m.total = tiles * m.KB;
     m.Gm = (int)(m.total < grid ? m.total : grid);
@@ -590,9 +590,9 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
     m.idesc = tc::idesc_bf16(128, m.BN);
     m.epi = e;
     if (tiles > tc_max_tiles(c->tc) || Kd % 64 || m.BN > 240) fail = true;
-    if (!tc_tensor_map(c->tc, &P.tm[2 * P.n_gemm], W, Nout, Kd, ldw, 128) ||
-        !tc_tensor_map(c->tc, &P.tm[2 * P.n_gemm + 1], X, split ? 2 * rows : rows, Kd, ldx,
-                       m.BN))
+    if (!tc_tensor_map_ku(c->tc, &P.tm[2 * P.n_gemm], W, Nout, Kd, ldw, 128, PASS_KU) ||
+        !tc_tensor_map_ku(c->tc, &P.tm[2 * P.n_gemm + 1], X, split ? 2 * rows : rows, Kd, ldx,
+                          m.BN, PASS_KU))
       fail = true;
     if (m.BN > bn_max) bn_max = m.BN;
     m.phase = P.n_phase;
@@ -686,7 +686,7 @@ static int pass_draft(peagle_ctx* c, int B, const peagle_kv* kv, const int32_t* 
   if (slot > PASS_SS_SLOTS) fail = true;
   if (fail) return PEAGLE_ERR_UNSUPPORTED;
 
-  P.b_stage_bytes = bn_max * 128;
+  P.b_stage_bytes = bn_max * 128 * PASS_KU;
   P.acc_stride = bn_max + 16;
   uint32_t tc_cols = 32;
   while (tc_cols < (uint32_t)(2 * P.acc_stride)) tc_cols <<= 1;

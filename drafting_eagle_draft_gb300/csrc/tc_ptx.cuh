@@ -82,6 +82,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
       "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// 3D tiled load of box {x.., y.., z..} into shared memory, completion on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 // Prefetch the box at {x, y} of a tensor map into L2 (no shared memory, no completion).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
