@@ -38,6 +38,9 @@ namespace peagle {
 constexpr int TC_THREADS = 192;  // one epilogue group (decode-sized GEMMs)
 constexpr int TC_THREADS2 = 320; // two epilogue groups (large-M GEMMs)
 constexpr int A_BYTES = 128 * 128;  // one 128 x 64 bf16 weight tile
+// 64-wide k-blocks per stage of the CTA-pair kernel: one tensor load brings two k-blocks of
+// a 128-row tile (32 KB), which the TMA units stream faster than twice as many 16 KB loads
+constexpr int PAIR_KU = 2;
 constexpr int STAGE_F_BYTES = 32 * 128 * 4;
 
 struct TcParams {
@@ -520,9 +523,9 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int S = p.stages;
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + (size_t)S * A_BYTES;
-  float* stg = (float*)(sB + (size_t)S * HB);  // [NEG][32][128] fp32 epilogue staging
+  uint8_t* sA = smem;                                       // [S][PAIR_KU] weight tiles
+  uint8_t* sB = sA + (size_t)S * PAIR_KU * A_BYTES;          // [S][PAIR_KU] activation halves
+  float* stg = (float*)(sB + (size_t)S * PAIR_KU * HB);  // [NEG][32][128] fp32 epilogue staging
   uint64_t* full = (uint64_t*)((uint8_t*)stg + NEG * STAGE_F_BYTES);
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
@@ -573,15 +576,17 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
     if (lane == 0) {
       const uint64_t pol_w = p.m_inner ? tc::policy_evict_last() : tc::policy_evict_first();
       const uint64_t pol_x = p.m_inner ? tc::policy_evict_first() : tc::policy_evict_last();
-      const uint32_t bytes = 2 * (A_BYTES + HB);  // both CTAs' loads count on the even one
+      // both CTAs' loads count on the even one
+      const uint32_t bytes = 2 * PAIR_KU * (A_BYTES + HB);
       const uint32_t lead_full = tc::mapa_shared(full, 0);
-      // A and B halves into this CTA's stage, completing on the even CTA's barrier
+      // A and B halves of PAIR_KU k-blocks into this CTA's stage, completing on the even
+      // CTA's barrier
       auto load = [&](int st, int kb, int wr, int xr, bool a, bool b) {
         if (a)
-          tc::tma_load_2d_pair(sA + (size_t)st * A_BYTES, &tmW, kb * 64, wr,
+          tc::tma_load_3d_pair(sA + (size_t)st * PAIR_KU * A_BYTES, &tmW, 0, wr, kb * PAIR_KU,
                                lead_full + (uint32_t)(st * 8), pol_w);
         if (b)
-          tc::tma_load_2d_pair(sB + (size_t)st * HB, &tmX, kb * 64, xr,
+          tc::tma_load_3d_pair(sB + (size_t)st * PAIR_KU * HB, &tmX, 0, xr, kb * PAIR_KU,
                                lead_full + (uint32_t)(st * 8), pol_x);
       };
       auto coords = [&](long long it, int* kb, int* wrow, int* xrow) {
@@ -649,11 +654,17 @@ __global__ void __launch_bounds__(TC_THREADS2, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(sA + (size_t)stage * A_BYTES));
-          const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(sB + (size_t)stage * HB));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int j = 0; j < PAIR_KU; ++j) {
+            const uint64_t ad = tc::smem_desc_sw128(
+                tc::smem_u32(sA + ((size_t)stage * PAIR_KU + j) * A_BYTES));
+            const uint64_t bd =
+                tc::smem_desc_sw128(tc::smem_u32(sB + ((size_t)stage * PAIR_KU + j) * HB));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc,
+                                (kb > 0 || j > 0 || k > 0) ? 1u : 0u);
+          }
           issued = true;
           tc::mma_commit_pair(&empty[stage], (uint16_t)3);
           if (++stage == S) {
@@ -793,7 +804,7 @@ static bool encode_map(TcGemmPlan* p, CUtensorMap* out, const void* base, int ro
 }
 
 static size_t smem_bytes_pair(int stages) {
-  return 1024 + (size_t)stages * (A_BYTES + 128 * 128) + 2 * STAGE_F_BYTES +
+  return 1024 + (size_t)stages * PAIR_KU * (A_BYTES + 128 * 128) + 2 * STAGE_F_BYTES +
          (size_t)(2 * stages + 5) * 8 + 16;
 }
 // dynamic shared memory of the pair kernel: the 227 KB per-block limit less its 1 KB of
@@ -981,9 +992,10 @@ int tc_gemm(TcGemmPlan* pl, const void* W, const void* X, int ldx, int Nout, int
     q.ws = pl->ws;
     q.counters = pl->counters;
     q.err = pl->err;
+    q.KB = (Kd / 64 + PAIR_KU - 1) / PAIR_KU;  // k-units (the last may read zeros past Kd)
     CUtensorMap mw, mx;
-    if (!encode_map(pl, &mw, W, Nout, Kd, Kd, 128)) return PEAGLE_ERR_CUDA;
-    if (!encode_map(pl, &mx, X, xrows, Kd, ldx, 128)) return PEAGLE_ERR_CUDA;
+    if (!tc_tensor_map_ku(pl, &mw, W, Nout, Kd, Kd, 128, PAIR_KU)) return PEAGLE_ERR_CUDA;
+    if (!tc_tensor_map_ku(pl, &mx, X, xrows, Kd, ldx, 128, PAIR_KU)) return PEAGLE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * npairs);
     cfg.blockDim = dim3(TC_THREADS2);
