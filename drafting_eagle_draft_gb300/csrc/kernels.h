@@ -25,7 +25,7 @@ struct AttnArgs {
 };
 
 struct MaskedAttnArgs {
-  const void* q;          // [M, nq*hd] fp32 (post-RoPE)
+  const void* q;          // [M, nq*hd] post-RoPE: fp32, or bf16 when q_bf16
   const void* k;          // [M, nkv, hd]   all rows
   const void* v;
   const void* k1;         // [n, nkv, hd]   depth-1 rows by position
@@ -35,6 +35,7 @@ struct MaskedAttnArgs {
   const int* row_index;   // [n * (Kmax + 1)] row of (p, d), -1 if absent
   void* o;                // [M, nq*hd] (hi rows, then lo rows when split)
   int split;
+  int q_bf16;             // queries stored as bf16 (the tensor-core kernel only)
   int M, n, Kmax, nq, nkv, hd;
   float scale;
   unsigned* err;          // device error word (timeouts of the tensor-core kernel)

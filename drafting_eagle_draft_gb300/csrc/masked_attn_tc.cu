@@ -146,7 +146,16 @@ __global__ void __launch_bounds__(MT_THREADS) masked_attn_tc_kernel(
       dd = d;
     }
   }
-  {
+  if (a.q_bf16) {
+    // queries stored as bf16 by the QKV epilogue: the row's 128 bytes as they are
+    const uint4* q =
+        (const uint4*)((const bf16*)a.q + ((size_t)(in ? qi : 0) * a.nq + h) * HD);
+    uint4 x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = in ? q[c] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *(uint4*)(sQ + sw128(tid, c)) = x[c];
+  } else {
     // queries (bf16, the scale is applied to the scores) into the A tile of S = Q K^T
     const float4* q = (const float4*)((const float*)a.q + ((size_t)(in ? qi : 0) * a.nq + h) * HD);
     float4 x[16];

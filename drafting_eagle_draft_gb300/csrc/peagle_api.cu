@@ -1045,6 +1045,10 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
   const int qkv_out = (nq + 2 * nkv) * hd;
   const int Kmax = 16;
   const int split = use_split(c);
+  // bf16 drafters with head_dim 64 take the tensor-core masked attention, which reads the
+  // queries as bf16 (its operand precision; the QKV epilogue rounds them once, RN, as the
+  // kernel would); the mma.sync kernels read fp32 queries
+  const bool tc_attn = c->bf && hd == 64 && 128 % (nq / nkv) == 0;
   TIMED(PEAGLE_STAGE_SMALL,
         launch_rows_prepare(M, n, K, Kmax, row_p, row_d, c->row_index, c->err, s));
   // the fc projection accumulates into F; clear every row of this sequence first (a row
@@ -1075,7 +1079,7 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       EpiArgs e = epi_base(c, EPI_QKV_ROPE, M, qkv_out);
       e.in_split = split;
       e.q_out = c->Qf;
-      e.q_f32 = 1;
+      e.q_f32 = tc_attn ? 0 : 1;
       e.k_dst = c->Kr;
       e.v_dst = c->Vr;
       e.k1_dst = c->K1;
@@ -1089,6 +1093,7 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
     {
       MaskedAttnArgs a;
       a.q = c->Qf;
+      a.q_bf16 = tc_attn ? 1 : 0;
       a.split = split;
       a.k = c->Kr;
       a.v = c->Vr;
@@ -1107,11 +1112,14 @@ extern "C" int peagle_forward_parallel(peagle_ctx* c, int32_t n, int32_t K, cons
       a.scale = 1.f / sqrtf((float)hd);
       a.err = c->err;
       // tcgen05 kernel for bf16 and head_dim 64, else the mma.sync / fp32 kernels
+      int ar = PEAGLE_OK;
       TIMED(PEAGLE_STAGE_ATTN, {
-        int ar = PEAGLE_ERR_UNSUPPORTED;
-        if (c->bf) ar = masked_attn_tc_launch(c->tc, a, s);
-        if (ar == PEAGLE_ERR_UNSUPPORTED) launch_masked_attention(c->bf, a, s);
+        if (tc_attn)
+          ar = masked_attn_tc_launch(c->tc, a, s);
+        else
+          launch_masked_attention(c->bf, a, s);
       });
+      if (ar != PEAGLE_OK) return ar;
     }
     {
       EpiArgs e = epi_base(c, EPI_RESID, M, H);
