@@ -1498,9 +1498,11 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     if (fused_attn) {
       // chain part per row, then the prefix part on TF32 tensor cores without the dense
       // score matrices
-      for (int g = 0; g < nkv; ++g)
-        launch_attn_bwd_ds(ta, g, nullptr, nullptr, w->lse[l], w->Dv, w->Qh[l], w->Kr[l],
-                           w->Vr[l], w->dOh, w->dQh, w->dKr, w->dVr, s);
+      if (!launch_attn_bwd_chain(ta, w->lse[l], w->Dv, w->Qh[l], w->Kr[l], w->Vr[l], w->dOh,
+                                 w->dQh, w->dKr, w->dVr, s))
+        for (int g = 0; g < nkv; ++g)
+          launch_attn_bwd_ds(ta, g, nullptr, nullptr, w->lse[l], w->Dv, w->Qh[l], w->Kr[l],
+                             w->Vr[l], w->dOh, w->dQh, w->dKr, w->dVr, s);
       TRY_RET(zero(w->dK1, (size_t)nkv * n * hd, s));
       TRY_RET(zero(w->dV1, (size_t)nkv * n * hd, s));
       TRY_RET(launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l],

@@ -357,6 +357,82 @@ __global__ void attn_bwd_ds_kernel(TrainAttn a, int g, float* S1, float* dP1, co
   for (int c = lane, u = 0; c < a.hd; c += 32, ++u) dq[c] = acc[u];
 }
 
+// The chain part of the backward when the prefix part runs on the fused kernels: one
+// warp per (kv head g, row i) walks the G q heads of the group; per head the chain keys'
+// scores are recomputed, dQ's chain part is stored (the prefix part is added later), and
+// each chain key's dK / dV is summed over the G heads in registers before one atomic add
+// per element (G times fewer atomics than one warp per head).
+template <int HD>
+__global__ void __launch_bounds__(256) attn_bwd_chain_kernel(TrainAttn a, const float* lse,
+                                                             const float* Dv, const float* Qh,
+                                                             const float* Kr, const float* Vr,
+                                                             const float* dOh, float* dQh,
+                                                             float* dKr, float* dVr) {
+  constexpr int U = HD / 32;
+  constexpr int CMAX = 15;  // K <= 16: at most 15 chain keys per row
+  const int G = a.nq / a.nkv, lane = threadIdx.x & 31, K1n = a.K - 1;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= a.nkv * a.M) return;
+  const int g = w / a.M, i = w - g * a.M;
+  int rr[CMAX];
+  float dk[CMAX][U], dv[CMAX][U];
+#pragma unroll
+  for (int t = 0; t < CMAX; ++t) {
+    rr[t] = t < K1n ? a.chain[(size_t)i * K1n + t] : -1;
+#pragma unroll
+    for (int u = 0; u < U; ++u) dk[t][u] = dv[t][u] = 0.f;
+  }
+  for (int hl = 0; hl < G; ++hl) {
+    const int h = g * G + hl;
+    const float L = lse[(size_t)h * a.M + i], D = Dv[(size_t)h * a.M + i];
+    const float* qrow = Qh + ((size_t)h * a.M + i) * HD;
+    const float* orow = dOh + ((size_t)h * a.M + i) * HD;
+    float q[U], o[U], dq[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      q[u] = qrow[lane + 32 * u];
+      o[u] = orow[lane + 32 * u];
+      dq[u] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) {
+      if (rr[t] < 0) continue;  // warp-uniform
+      const float* kr = Kr + ((size_t)rr[t] * a.nkv + g) * HD;
+      const float* vr = Vr + ((size_t)rr[t] * a.nkv + g) * HD;
+      float k[U], v[U], sd = 0.f, dd = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        k[u] = kr[lane + 32 * u];
+        v[u] = vr[lane + 32 * u];
+        sd += q[u] * k[u];
+        dd += o[u] * v[u];
+      }
+      const float pr = expf(warp_sum(sd) * a.scale - L);
+      const float ds = pr * (warp_sum(dd) - D) * a.scale;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        dq[u] += ds * k[u];
+        dk[t][u] += ds * q[u];
+        dv[t][u] += pr * o[u];
+      }
+    }
+    float* dqrow = dQh + ((size_t)h * a.M + i) * HD;
+#pragma unroll
+    for (int u = 0; u < U; ++u) dqrow[lane + 32 * u] = dq[u];
+  }
+#pragma unroll
+  for (int t = 0; t < CMAX; ++t) {
+    if (rr[t] < 0) continue;
+    float* gk = dKr + ((size_t)rr[t] * a.nkv + g) * HD;
+    float* gv = dVr + ((size_t)rr[t] * a.nkv + g) * HD;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      atomicAdd(gk + lane + 32 * u, dk[t][u]);
+      atomicAdd(gv + lane + 32 * u, dv[t][u]);
+    }
+  }
+}
+
 // dK1 / dV1 [nkv][n][hd] (by position) added into the depth-1 rows' dKr / dVr
 __global__ void kv1_scatter_kernel(int M, int n, int K, int nkv, int hd, const int* row_p,
                                    const int* row_d, const float* dK1, const float* dV1,
@@ -525,6 +601,18 @@ void launch_attn_bwd_ds(const TrainAttn& a, int g, float* S1, float* dP1, const 
   const int G = a.nq / a.nkv;
   attn_bwd_ds_kernel<<<cdiv(G * a.M, 8), 256, 0, s>>>(a, g, S1, dP1, lse, Dv, Qh, Kr, Vr, dOh,
                                                       dQh, dKr, dVr);
+}
+
+bool launch_attn_bwd_chain(const TrainAttn& a, const float* lse, const float* Dv,
+                           const float* Qh, const float* Kr, const float* Vr, const float* dOh,
+                           float* dQh, float* dKr, float* dVr, cudaStream_t s) {
+  if (a.K > 16 || (a.hd != 64 && a.hd != 128)) return false;
+  const int blocks = cdiv(a.nkv * a.M, 8);
+  if (a.hd == 64)
+    attn_bwd_chain_kernel<64><<<blocks, 256, 0, s>>>(a, lse, Dv, Qh, Kr, Vr, dOh, dQh, dKr, dVr);
+  else
+    attn_bwd_chain_kernel<128><<<blocks, 256, 0, s>>>(a, lse, Dv, Qh, Kr, Vr, dOh, dQh, dKr, dVr);
+  return true;
 }
 
 void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, const int* row_d,

@@ -64,6 +64,12 @@ void launch_attn_bwd_prep(const TrainAttn& a, const float* dO, const float* O, f
 void launch_attn_bwd_ds(const TrainAttn& a, int g, float* S1, float* dP1, const float* lse,
                         const float* Dv, const float* Qh, const float* Kr, const float* Vr,
                         const float* dOh, float* dQh, float* dKr, float* dVr, cudaStream_t s);
+// The chain part of the backward (the prefix part on the fused kernels): dQh's chain part
+// stored, the chain keys' dKr / dVr added; one launch for every kv head.  False (nothing
+// launched) for K > 16 or head_dim other than 64 / 128.
+bool launch_attn_bwd_chain(const TrainAttn& a, const float* lse, const float* Dv,
+                           const float* Qh, const float* Kr, const float* Vr, const float* dOh,
+                           float* dQh, float* dKr, float* dVr, cudaStream_t s);
 void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, const int* row_d,
                         const float* dK1, const float* dV1, float* dKr, float* dVr,
                         cudaStream_t s);
