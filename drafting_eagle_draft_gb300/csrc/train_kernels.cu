@@ -481,6 +481,62 @@ __global__ void ce_kernel(int M, int V, float* logits, const int* labels, float*
   if (threadIdx.x == 0) row_loss[i] = L - xl;
 }
 
+// The same with the row held in registers (V <= 32 * 1024, V % 4 == 0): one pass over the
+// logits from memory and one over the result, 1024 threads per row, 8 float4 per thread.
+__global__ void __launch_bounds__(1024, 1) ce_reg_kernel(int M, int V, float* logits,
+                                                         const int* labels, float* row_loss,
+                                                         unsigned* err) {
+  constexpr int PER = 8;
+  __shared__ float red[32];
+  const int i = blockIdx.x;
+  float4* x = reinterpret_cast<float4*>(logits + (size_t)i * V);
+  const int V4 = V / 4;
+  float4 v[PER];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int j = threadIdx.x + k * 1024;
+    v[k] = j < V4 ? x[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    m = fmaxf(m, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
+  }
+  {
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = warp_max(red[threadIdx.x & 31]);
+    __syncthreads();  // red is reused by block_sum
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    sum += (expf(v[k].x - m) + expf(v[k].y - m)) + (expf(v[k].z - m) + expf(v[k].w - m));
+  sum = block_sum(sum, red);
+  const float L = m + logf(sum);
+  int lab = labels[i];
+  if (lab < 0 || lab >= V) {
+    if (threadIdx.x == 0) raise_error(err, PEAGLE_DEV_BAD_TOKEN);
+    lab = -1;
+  }
+  const float inv = 1.f / M;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int j = threadIdx.x + k * 1024;
+    if (j >= V4) continue;
+    const int e = 4 * j;
+    float4 o;
+    o.x = (expf(v[k].x - L) - (e == lab ? 1.f : 0.f)) * inv;
+    o.y = (expf(v[k].y - L) - (e + 1 == lab ? 1.f : 0.f)) * inv;
+    o.z = (expf(v[k].z - L) - (e + 2 == lab ? 1.f : 0.f)) * inv;
+    o.w = (expf(v[k].w - L) - (e + 3 == lab ? 1.f : 0.f)) * inv;
+    if (lab >= e && lab < e + 4) {
+      const float xl = lab == e ? v[k].x : lab == e + 1 ? v[k].y : lab == e + 2 ? v[k].z : v[k].w;
+      row_loss[i] = L - xl;
+    }
+    x[j] = o;
+  }
+  if (lab < 0 && threadIdx.x == 0) row_loss[i] = 0.f;
+}
+
 __global__ void mean_kernel(int M, const float* v, float* out) {
   __shared__ float red[32];
   float s = 0.f;
@@ -623,7 +679,10 @@ void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, 
 
 void launch_ce(int M, int V, float* logits, const int* labels, float* row_loss, float* loss,
                unsigned* err, cudaStream_t s) {
-  ce_kernel<<<M, 256, 0, s>>>(M, V, logits, labels, row_loss, err);
+  if (V % 4 == 0 && V <= 32 * 1024)
+    ce_reg_kernel<<<M, 1024, 0, s>>>(M, V, logits, labels, row_loss, err);
+  else
+    ce_kernel<<<M, 256, 0, s>>>(M, V, logits, labels, row_loss, err);
   mean_kernel<<<1, 1024, 0, s>>>(M, row_loss, loss);
 }
 
