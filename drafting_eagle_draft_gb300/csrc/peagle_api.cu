@@ -1434,7 +1434,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     TRY_RET(zero(w->K1[l], (size_t)nkv * n * hd, s));
     TRY_RET(zero(w->V1[l], (size_t)nkv * n * hd, s));
     launch_train_rope(M, n, K, nq, nkv, hd, w->qkvb, row_p, row_d, c->rope, w->Qh[l], w->Kr[l],
-                      w->Vr[l], w->K1[l], w->V1[l], s);
+                      w->Vr[l], w->K1[l], w->V1[l], fused_attn, s);
     if (fused_attn)  // online softmax over the prefix, then the chain keys per row
       TRY_RET(launch_attn_fwd_fused(ta, w->Qh[l], w->Kr[l], w->Vr[l], w->K1[l], w->V1[l], w->Oh,
                                     w->Dv, w->lrow, w->Pc[l], w->lse[l], w->O[l],
@@ -1492,7 +1492,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
     // attention
     GM(true, false, H, nqhd, M, 1.f, dmid, H, w->O[l], nqhd, 0.f, gr->o[l], nqhd);
     GMW(M, nqhd, H, dmid, H, w->o[l], w->oT[l], w->dO, nqhd);
-    launch_attn_bwd_prep(ta, w->dO, w->O[l], w->dOh, w->Dv, s);
+    launch_attn_bwd_prep(ta, w->dO, w->O[l], w->dOh, w->Dv, fused_attn, s);
     TRY_RET(zero(w->dKr, (size_t)M * nkv * hd, s));
     TRY_RET(zero(w->dVr, (size_t)M * nkv * hd, s));
     if (fused_attn) {
@@ -1506,7 +1506,7 @@ extern "C" int peagle_train_step(peagle_ctx* c, int32_t n, int32_t K, const int3
       TRY_RET(zero(w->dK1, (size_t)nkv * n * hd, s));
       TRY_RET(zero(w->dV1, (size_t)nkv * n * hd, s));
       TRY_RET(launch_attn_bwd_fused(ta, c->row_index, Kmax, w->Qh[l], w->dOh, w->K1[l],
-                                    w->V1[l], w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1, true,
+                                    w->V1[l], w->lse[l], w->Dv, w->dQh, w->dK1, w->dV1,
                                     w->kvT ? &atc : nullptr, s));
     }
     for (int g = 0; g < nkv && !fused_attn; ++g) {

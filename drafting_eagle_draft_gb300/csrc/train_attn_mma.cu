@@ -42,14 +42,9 @@ __device__ __forceinline__ uint32_t tf32(float x) {
   return r;
 }
 
-// operands stored already rounded to TF32 (round_tf32_kernel) enter as their bits
+// operands stored already rounded to TF32 by their producers (the RoPE kernel for Q, K1 and
+// V1, the backward's preparation kernel for dO) enter as their bits
 __device__ __forceinline__ uint32_t bits(float x) { return __float_as_uint(x); }
-
-__global__ void round_tf32_kernel(size_t n, float* p) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x)
-    p[i] = __uint_as_float(tf32(p[i]));
-}
 
 __device__ __forceinline__ void mma_tf32(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -580,8 +575,6 @@ int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const 
                           float* K1, float* V1, float* Op, float* mrow, float* lrow, float* Pc,
                           float* lse, float* O, const TrainAttnTc* tcx, cudaStream_t s) {
   const int G = a.nq / a.nkv;
-  round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, Qh);
-  for (float* p : {K1, V1}) round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
   if (tcx && attn_tc_ok(a)) {
     const int r = launch_attn_fwd_prefix_tc(a, *tcx, Qh, K1, V1, Op, mrow, lrow, s);
     if (r != PEAGLE_OK) return r;
@@ -600,18 +593,9 @@ int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const 
 int launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
                           const float* dOh, const float* K1, const float* V1,
                           const float* lse, const float* Dv, float* dQh, float* dK1,
-                          float* dV1, bool qkv_rounded, const TrainAttnTc* tcx,
-                          cudaStream_t s) {
+                          float* dV1, const TrainAttnTc* tcx, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const size_t smem = (size_t)2 * 2 * 64 * FA_LD * sizeof(float);
-  // the stored operands are rounded to TF32 once, not per use in the products (Q, K1 and
-  // V1 already are when the forward ran fused)
-  round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)dOh);
-  if (!qkv_rounded) {
-    round_tf32_kernel<<<1024, 256, 0, s>>>((size_t)a.nq * a.M * 64, (float*)Qh);
-    for (float* p : {(float*)K1, (float*)V1})
-      round_tf32_kernel<<<256, 256, 0, s>>>((size_t)a.nkv * a.n * 64, p);
-  }
   if (tcx && attn_tc_ok(a)) {
     const int r = launch_attn_bwd_dq_tc(a, *tcx, Qh, dOh, K1, V1, lse, Dv, dQh, s);
     if (r != PEAGLE_OK) return r;

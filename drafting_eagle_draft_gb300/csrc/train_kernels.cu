@@ -155,9 +155,20 @@ __global__ void gu_split_kernel(int I, int H, const float* dw, float* dgate, flo
 // ---- RoPE (rotate-half pairs (c, c + hd/2), the table holds (cos, sin) per position) ----
 // q rows -> head-major Qh [nq][M][hd]; k -> Kr [M][nkv][hd]; v -> Vr; the depth-1 rows'
 // keys and values also to K1 / V1 [nkv][n][hd] by position.
+// x rounded to TF32 (round to nearest, ties away), kept as fp32: the form the fused
+// attention kernels' tensor-core products read their operands in
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// tf32: the queries and the depth-1 keys / values (K1, V1) are stored rounded to TF32
+// (the operands of the fused attention); the all-row keys / values keep fp32
 __global__ void train_rope_kernel(int M, int n, int K, int nq, int nkv, int hd, const float* qkv,
                                   const int* row_p, const int* row_d, const float2* tab,
-                                  float* Qh, float* Kr, float* Vr, float* K1, float* V1) {
+                                  float* Qh, float* Kr, float* Vr, float* K1, float* V1,
+                                  bool tf32) {
   const int i = blockIdx.x;
   const int p = row_p[i], d = row_d[i];
   const bool ok = row_ok(p, d, n, K);
@@ -170,8 +181,8 @@ __global__ void train_rope_kernel(int M, int n, int K, int nq, int nkv, int hd, 
     const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
     if (h < nq) {
       float* o = Qh + ((size_t)h * M + i) * hd;
-      o[c] = y1;
-      o[c + half] = y2;
+      o[c] = tf32 ? round_tf32(y1) : y1;
+      o[c + half] = tf32 ? round_tf32(y2) : y2;
     } else {
       const int g = h - nq;
       float* o = Kr + ((size_t)i * nkv + g) * hd;
@@ -179,15 +190,15 @@ __global__ void train_rope_kernel(int M, int n, int K, int nq, int nkv, int hd, 
       o[c + half] = y2;
       if (ok && d == 1) {
         float* o1 = K1 + ((size_t)g * n + p) * hd;
-        o1[c] = y1;
-        o1[c + half] = y2;
+        o1[c] = tf32 ? round_tf32(y1) : y1;
+        o1[c + half] = tf32 ? round_tf32(y2) : y2;
       }
     }
   }
   for (int t = threadIdx.x; t < nkv * hd; t += blockDim.x) {
     const float v = src[(nq + nkv) * hd + t];
     Vr[(size_t)i * nkv * hd + t] = v;
-    if (ok && d == 1) V1[((size_t)(t / hd) * n + p) * hd + t % hd] = v;
+    if (ok && d == 1) V1[((size_t)(t / hd) * n + p) * hd + t % hd] = tf32 ? round_tf32(v) : v;
   }
 }
 
@@ -290,8 +301,9 @@ __global__ void attn_fwd_out_kernel(TrainAttn a, int g, const float* Oh, const f
 
 // ---- attention backward ------------------------------------------------------------
 // Dv[h][i] = dO . O (the softmax backward's row term), dOh head-major copy of dO
+// tf32: dOh is stored rounded to TF32 (D uses the fp32 values)
 __global__ void attn_bwd_prep_kernel(TrainAttn a, const float* dO, const float* O, float* dOh,
-                                     float* Dv) {
+                                     float* Dv, bool tf32) {
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= a.nq * a.M) return;
@@ -300,7 +312,7 @@ __global__ void attn_bwd_prep_kernel(TrainAttn a, const float* dO, const float* 
   float s = 0.f;
   for (int c = lane; c < a.hd; c += 32) {
     const float x = dO[src + c];
-    dOh[((size_t)h * a.M + i) * a.hd + c] = x;
+    dOh[((size_t)h * a.M + i) * a.hd + c] = tf32 ? round_tf32(x) : x;
     s += x * O[src + c];
   }
   s = warp_sum(s);
@@ -617,9 +629,9 @@ void launch_gu_split(int I, int H, const float* dw, float* dgate, float* dup, cu
 
 void launch_train_rope(int M, int n, int K, int nq, int nkv, int hd, const float* qkv,
                        const int* row_p, const int* row_d, const float2* tab, float* Qh,
-                       float* Kr, float* Vr, float* K1, float* V1, cudaStream_t s) {
+                       float* Kr, float* Vr, float* K1, float* V1, bool tf32, cudaStream_t s) {
   train_rope_kernel<<<M, 128, 0, s>>>(M, n, K, nq, nkv, hd, qkv, row_p, row_d, tab, Qh, Kr, Vr,
-                                      K1, V1);
+                                      K1, V1, tf32);
 }
 
 void launch_train_rope_bwd(int M, int n, int K, int nq, int nkv, int hd, const float* dQh,
@@ -647,8 +659,8 @@ void launch_attn_fwd_out(const TrainAttn& a, int g, const float* Oh, const float
 }
 
 void launch_attn_bwd_prep(const TrainAttn& a, const float* dO, const float* O, float* dOh,
-                          float* Dv, cudaStream_t s) {
-  attn_bwd_prep_kernel<<<cdiv(a.nq * a.M, 8), 256, 0, s>>>(a, dO, O, dOh, Dv);
+                          float* Dv, bool tf32, cudaStream_t s) {
+  attn_bwd_prep_kernel<<<cdiv(a.nq * a.M, 8), 256, 0, s>>>(a, dO, O, dOh, Dv, tf32);
 }
 
 void launch_attn_bwd_ds(const TrainAttn& a, int g, float* S1, float* dP1, const float* lse,

@@ -49,7 +49,7 @@ void launch_swiglu_bwd(int M, int I, const float* gu, const float* dact, float* 
 void launch_gu_split(int I, int H, const float* dw, float* dgate, float* dup, cudaStream_t s);
 void launch_train_rope(int M, int n, int K, int nq, int nkv, int hd, const float* qkv,
                        const int* row_p, const int* row_d, const float2* tab, float* Qh,
-                       float* Kr, float* Vr, float* K1, float* V1, cudaStream_t s);
+                       float* Kr, float* Vr, float* K1, float* V1, bool tf32, cudaStream_t s);
 void launch_train_rope_bwd(int M, int n, int K, int nq, int nkv, int hd, const float* dQh,
                            const float* dKr, const float* dVr, const int* row_p,
                            const int* row_d, const float2* tab, float* dqkv, cudaStream_t s);
@@ -60,7 +60,7 @@ void launch_attn_fwd_softmax(const TrainAttn& a, int g, float* S1, const float* 
 void launch_attn_fwd_out(const TrainAttn& a, int g, const float* Oh, const float* Pc,
                          const float* Vr, float* O, cudaStream_t s);
 void launch_attn_bwd_prep(const TrainAttn& a, const float* dO, const float* O, float* dOh,
-                          float* Dv, cudaStream_t s);
+                          float* Dv, bool tf32, cudaStream_t s);
 void launch_attn_bwd_ds(const TrainAttn& a, int g, float* S1, float* dP1, const float* lse,
                         const float* Dv, const float* Qh, const float* Kr, const float* Vr,
                         const float* dOh, float* dQh, float* dKr, float* dVr, cudaStream_t s);
@@ -75,10 +75,11 @@ void launch_kv1_scatter(int M, int n, int K, int nkv, int hd, const int* row_p, 
                         cudaStream_t s);
 // Fused prefix-attention backward on TF32 tensor cores (train_attn_mma.cu), for head_dim
 // 64 and at most 8 q heads per kv head: dQh += dS K1 (dQh holds the chain part) and
-// dK1 / dV1 (zero beforehand) += dS^T Q / P^T dO; row_index as from rows-prepare.  dOh
-// (and Qh, K1, V1 unless qkv_rounded) are rounded to TF32 in place first.
+// dK1 / dV1 (zero beforehand) += dS^T Q / P^T dO; row_index as from rows-prepare.  Qh, K1,
+// V1 and dOh are stored rounded to TF32 by their producers (launch_train_rope and
+// launch_attn_bwd_prep with tf32 set).
 bool attn_bwd_fused_ok(const TrainAttn& a);
-// The forward the same way (Q, K1, V1 rounded to TF32 in place first): the prefix's unnormalised
+// The forward the same way (Q, K1, V1 stored rounded to TF32): the prefix's unnormalised
 // output Op (per-head rows [nq][M][64]) with its row max / sum, then the chain keys joined
 // per row: lse, Pc and O [M][nq hd].
 // With tcx (and attn_tc_ok), the prefix part runs on the tcgen05 kernel.
@@ -89,8 +90,7 @@ int launch_attn_fwd_fused(const TrainAttn& a, float* Qh, const float* Kr, const 
 int launch_attn_bwd_fused(const TrainAttn& a, const int* row_index, int Kmax, const float* Qh,
                           const float* dOh, const float* K1, const float* V1,
                           const float* lse, const float* Dv, float* dQh, float* dK1,
-                          float* dV1, bool qkv_rounded, const TrainAttnTc* tcx,
-                          cudaStream_t s);
+                          float* dV1, const TrainAttnTc* tcx, cudaStream_t s);
 bool attn_tc_ok(const TrainAttn& a);
 // The prefix part of the forward (Q, K1, V1 already rounded to TF32): Op, mrow, lrow as
 // launch_attn_fwd_fused's prefix kernel writes them.  V1 is transposed into kvT first.
