@@ -20,6 +20,12 @@ namespace peagle {
 // =====================================================================================
 // round to the nearest bf16 value, kept in fp32
 __device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+// 2^x on the SFU (relative error about 2^-22, far below the bf16 rounding that follows)
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -203,20 +209,23 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
       }
       // ---- scale (1/sqrt(hd) and log2 e), mask and online softmax (log2 domain)
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        sc[n][0] *= qscale;
-        sc[n][1] *= qscale;
-        sc[n][2] *= qscale;
-        sc[n][3] *= qscale;
+      // the mask: only tiles that reach a row's last visible key, the window's first or the
+      // chunk's end need it (the raw scores are masked; the scale is applied in the exponent)
+      const bool full = v0 && v1 && t0 + MMA_KT <= kend && t0 + MMA_KT - 1 <= min(lim0, lim1) &&
+                        t0 >= max(lo0, lo1);
+      if (!full) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const int kp = t0 + n * 8 + 2 * tq;
+          sc[n][0] = (kp < kend && kp <= lim0 && kp >= lo0 && v0) ? sc[n][0] : -INFINITY;
+          sc[n][1] = (kp + 1 < kend && kp + 1 <= lim0 && kp + 1 >= lo0 && v0) ? sc[n][1] : -INFINITY;
+          sc[n][2] = (kp < kend && kp <= lim1 && kp >= lo1 && v1) ? sc[n][2] : -INFINITY;
+          sc[n][3] = (kp + 1 < kend && kp + 1 <= lim1 && kp + 1 >= lo1 && v1) ? sc[n][3] : -INFINITY;
+        }
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
-        const int kp = t0 + n * 8 + 2 * tq;
-        sc[n][0] = (kp < kend && kp <= lim0 && kp >= lo0 && v0) ? sc[n][0] : -INFINITY;
-        sc[n][1] = (kp + 1 < kend && kp + 1 <= lim0 && kp + 1 >= lo0 && v0) ? sc[n][1] : -INFINITY;
-        sc[n][2] = (kp < kend && kp <= lim1 && kp >= lo1 && v1) ? sc[n][2] : -INFINITY;
-        sc[n][3] = (kp + 1 < kend && kp + 1 <= lim1 && kp + 1 >= lo1 && v1) ? sc[n][3] : -INFINITY;
         mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
         mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
       }
@@ -224,19 +233,20 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // running max in the log2 domain of the scaled scores (the scale is positive)
+      const float mn0 = fmaxf(m0, mx0 * qscale), mn1 = fmaxf(m1, mx1 * qscale);
       const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
       const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float cr0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - base0);
-      const float cr1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - base1);
+      const float cr0 = (m0 == -INFINITY) ? 0.f : fast_ex2(m0 - base0);
+      const float cr1 = (m1 == -INFINITY) ? 0.f : fast_ex2(m1 - base1);
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
         // probabilities rounded to bf16 once: the PV product and the row sum use the same
-        sc[n][0] = bf16r(exp2f(sc[n][0] - base0));
-        sc[n][1] = bf16r(exp2f(sc[n][1] - base0));
-        sc[n][2] = bf16r(exp2f(sc[n][2] - base1));
-        sc[n][3] = bf16r(exp2f(sc[n][3] - base1));
+        sc[n][0] = bf16r(fast_ex2(fmaf(sc[n][0], qscale, -base0)));
+        sc[n][1] = bf16r(fast_ex2(fmaf(sc[n][1], qscale, -base0)));
+        sc[n][2] = bf16r(fast_ex2(fmaf(sc[n][2], qscale, -base1)));
+        sc[n][3] = bf16r(fast_ex2(fmaf(sc[n][3], qscale, -base1)));
         ps0 += sc[n][0] + sc[n][1];
         ps1 += sc[n][2] + sc[n][3];
       }
