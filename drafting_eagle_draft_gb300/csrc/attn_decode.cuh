@@ -13,10 +13,11 @@ namespace peagle {
 // Split-KV decode attention on the tensor cores (bf16 caches): mma.sync m16n8k16.
 // One warp per 16 query rows (rows = K*G of one kv head, <= 128), CTA = one chunk of
 // keys of one (request, kv head).  K/V tiles of 64 keys are double-buffered in shared
-// memory by cp.async with a 16-byte XOR swizzle and read with ldmatrix.  Queries (fp32)
-// and softmax probabilities are each split into bf16 hi + lo parts, so both products
-// carry about 16 significant bits; keys and values are the cache's bf16.  Online softmax
-// in the log2 domain; partials and the merge are those of the CUDA-core kernel.
+// memory by cp.async with a 16-byte XOR swizzle and read with ldmatrix.  Queries and
+// softmax probabilities are rounded to bf16 (the probabilities once: the PV product and the
+// row sum use the same values); keys and values are the cache's bf16; products accumulate
+// in fp32.  Online softmax in the log2 domain; partials and the merge are those of the
+// CUDA-core kernel.
 // =====================================================================================
 // round to the nearest bf16 value, kept in fp32
 __device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -142,7 +143,7 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
     cp_async_commit();
   };
   load_tile(0, kbeg);  // the first K/V tile is in flight while the queries load
-  // query fragments of this warp's 16 rows, pre-scaled for exp2, split hi / lo
+  // query fragments of this warp's 16 rows (bf16; the scale is applied in the exponent)
   const float qscale = a.scale * 1.4426950408889634f;
   const int r0 = warp * 16 + gq, r1 = r0 + 8;
   const bool v0 = r0 < rows, v1 = r1 < rows;
@@ -208,7 +209,6 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
         }
       }
       // ---- scale (1/sqrt(hd) and log2 e), mask and online softmax (log2 domain)
-#pragma unroll
       // the mask: only tiles that reach a row's last visible key, the window's first or the
       // chunk's end need it (the raw scores are masked; the scale is applied in the exponent)
       const bool full = v0 && v1 && t0 + MMA_KT <= kend && t0 + MMA_KT - 1 <= min(lim0, lim1) &&
@@ -265,7 +265,7 @@ __device__ __forceinline__ void attn_mma_item(const AttnArgs& a, int b, int g, i
         o[n][2] *= cr1;
         o[n][3] *= cr1;
       }
-      // ---- O += P V: 4 k-steps of 16 keys, P split hi / lo
+      // ---- O += P V: 4 k-steps of 16 keys
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t ph[4];
@@ -335,7 +335,17 @@ __device__ __forceinline__ void attn_merge_rows(const AttnArgs& a, int b, int g,
   const int G = a.nq / a.nkv;
   const float* pbase = a.part + ((size_t)b * a.nkv + g) * a.nchunk * rows * (HD + 2);
   T* og = (T*)a.o;
+  // the values of the first CB chunks are loaded together with the statistics (one round
+  // trip to L2 for up to CB chunks)
+  constexpr int CB = 64 / E;
   for (int rr = rbeg; rr < rend; rr += rstep) {
+    float pv[CB][E];
+#pragma unroll
+    for (int cc = 0; cc < CB; ++cc) {
+      const float* pr = pbase + ((size_t)cc * rows + rr) * (HD + 2);
+#pragma unroll
+      for (int e = 0; e < E; ++e) pv[cc][e] = cc < nvalid ? __ldcg(pr + lane + 32 * e) : 0.f;
+    }
     // chunk statistics in parallel: lane c holds chunks c and c + 32 (nchunk <= 64)
     float mc[2], lc[2], wc[2];
 #pragma unroll
@@ -356,8 +366,14 @@ __device__ __forceinline__ void attn_merge_rows(const AttnArgs& a, int b, int g,
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < CB; ++cc) {
+      const float w = __shfl_sync(0xffffffffu, cc < 32 ? wc[0] : wc[1], cc & 31);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(pv[cc][e], w, acc[e]);
+    }
 #pragma unroll 8
-    for (int cc = 0; cc < nvalid; ++cc) {
+    for (int cc = CB; cc < nvalid; ++cc) {
       const float w = __shfl_sync(0xffffffffu, cc < 32 ? wc[0] : wc[1], cc & 31);
       const float* pr = pbase + ((size_t)cc * rows + rr) * (HD + 2);
 #pragma unroll

@@ -342,6 +342,33 @@ __device__ void step_norm(const PassParams& P, int c, int G, int slot, const bf1
   ss_flush(P, P.ss + (size_t)slot * R, s_rs, et);
 }
 
+// The cache rows that this CTA's attention items of `layer` read and that exist before the
+// pass (positions below seq_lens[b]) are fetched into L2 while the QKV projection runs, so
+// that the items' tile loads do not wait on HBM.
+template <int HD>
+__device__ void prefetch_attn_rows(const PassParams& P, int layer, int c, int G) {
+  const AttnArgs& a = P.att;
+  const char* kc = (const char*)a.kc + (size_t)layer * P.layer_stride;
+  const char* vc = (const char*)a.vc + (size_t)layer * P.layer_stride;
+  const int n_items = a.nchunk * a.nkv * a.B;
+  for (int i = c; i < n_items; i += G) {
+    const int cc = i % a.nchunk;
+    const int g = (i / a.nchunk) % a.nkv;
+    const int b = i / (a.nchunk * a.nkv);
+    const int L = a.seq_lens[b];
+    if (L <= 0) continue;
+    int first, total;
+    attn_span(a, L, &first, &total);
+    const int kbeg = first + cc * a.chunk;
+    const int kend = min(min(total, kbeg + a.chunk), L);
+    if (kend <= kbeg) continue;
+    const size_t off = (((size_t)b * a.nkv + g) * a.cap + kbeg) * HD * sizeof(bf16);
+    const uint32_t bytes = (uint32_t)(kend - kbeg) * HD * (uint32_t)sizeof(bf16);
+    tc::bulk_prefetch_l2(kc + off, bytes);
+    tc::bulk_prefetch_l2(vc + off, bytes);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(PK_THREADS, 1)
     pass_kernel(const __grid_constant__ PassParams P) {
@@ -368,6 +395,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
   volatile int* s_flag = (volatile int*)(s_tmem + 1);
   volatile int* s_abort = s_flag + 1;
   volatile int* s_adone = s_flag + 2;
+  volatile int* s_fin = s_flag + 3;  // a tile's last contributor (read between two barriers)
   volatile long long* s_nA = (volatile long long*)(s_tmem + 8);
   volatile long long* s_nB = s_nA + 1;
 
@@ -618,6 +646,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         // the projection's parameters in registers and its epilogue arguments in shared
         // memory (see Cur)
         const PassGemm& m = P.gemm[ph.gemm];
+        if (et == 0 && j + 1 < n_phase && P.ph[j + 1].kind == PP_ATTN)
+          prefetch_attn_rows<HD>(P, P.ph[j + 1].layer, c, G);
         const int Gm = m.Gm, KB = m.KB, BN = m.BN, mR = m.R, split = m.split;
         const int lo_col = m.lo_col, additive = m.additive;
         const long long total = m.total;
@@ -737,10 +767,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               wk_bar();
               if (et == 0) {
                 const unsigned prev = atom_add_acq_rel(tile_cnt + tile, 1u);
-                *s_flag = (prev == (unsigned)(cl - cf)) ? 1 : 0;
+                *s_fin = (prev == (unsigned)(cl - cf)) ? 1 : 0;
               }
               wk_bar();
-              if (*s_flag) {
+              if (*s_fin) {
                 const int slot_f = (rbeg(cf, total, Gm) == t_beg) ? 2 * cf : 2 * cf + 1;
                 for (int ch = 0; ch < nch; ++ch) {
                   const int i0 = ch * step;
@@ -822,12 +852,30 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
               bf16* kc = (bf16*)a.kc + ((size_t)b * a.nkv + g) * a.cap * hd;
               bf16* vc = (bf16*)a.vc + ((size_t)b * a.nkv + g) * a.cap * hd;
               const int nd = p1 > p0 ? (p1 - p0) * hd : 0;
-              for (int e = et; e < nd; e += 128) {
-                const int p = p0 + e / hd, d = e % hd;
-                const size_t r = (size_t)b * a.K + (p - L);
-                const fx_t* src = kvx + r * 2 * kvw + g * hd + d;
-                kc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(__ldcg(src)));
-                vc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(__ldcg(src + kvw)));
+              // every load of a batch is issued before the first store
+              constexpr int UM = 4;
+              for (int e0 = et; e0 < nd; e0 += 128 * UM) {
+                fx_t kq[UM], vq[UM];
+#pragma unroll
+                for (int u = 0; u < UM; ++u) {
+                  const int e = e0 + u * 128;
+                  kq[u] = vq[u] = 0;
+                  if (e < nd) {
+                    const int p = p0 + e / hd, d = e % hd;
+                    const fx_t* src = kvx + ((size_t)b * a.K + (p - L)) * 2 * kvw + g * hd + d;
+                    kq[u] = __ldcg(src);
+                    vq[u] = __ldcg(src + kvw);
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < UM; ++u) {
+                  const int e = e0 + u * 128;
+                  if (e < nd) {
+                    const int p = p0 + e / hd, d = e % hd;
+                    kc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(kq[u]));
+                    vc[(size_t)p * hd + d] = __float2bfloat16_rn(from_fx(vq[u]));
+                  }
+                }
               }
               if (et == 0 && g == 0 && cc == nv - 1 && L + a.K > a.cap)
                 raise_error(P.err, PEAGLE_DEV_KV_OVERFLOW);

@@ -73,6 +73,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Fetch `bytes` (a multiple of 16; the address 16-byte aligned) of global memory into L2
+// without waiting for them.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes)
+               : "memory");
+}
 // 2D tiled load of box {x .. x+bx, y .. y+by} into shared memory, completion on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y,
                                             uint64_t* bar, uint64_t policy) {
