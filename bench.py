@@ -157,7 +157,7 @@ class ClockSampler:
 # DRAM bytes (read + write) of one pass-kernel launch on decode_b1: dram__bytes_read.sum +
 # dram__bytes_write.sum of one ncu capture of the current pass kernel (None when the kernel
 # has changed since the counters were taken)
-PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_052_124_160
+PASS_KERNEL_DECODE_B1_DRAM_BYTES = 1_052_764_160
 
 
 def gemm_weight_bytes(dims) -> int:
