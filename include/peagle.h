@@ -332,13 +332,14 @@ int peagle_set_timing(peagle_ctx* ctx, int32_t enable);
 int peagle_read_timing(peagle_ctx* ctx, float* stage_ms, int32_t* stage_launches);
 
 /* Diagnostics of the persistent pass kernel (the bf16 draft pass as one launch of one CTA
- * per SM, used unless the environment variable PEAGLE_PASS_KERNEL=0 was set when the
- * context was created; with no variable set it runs passes of up to 16 draft rows,
- * PEAGLE_PASS_KERNEL=1 uses it for every shape it supports).  For the latest pass run
- * while timing was enabled, writes four
+ * per SM; by default it runs passes of up to 16 draft rows, peagle_set_pass_kernel(ctx, 1)
+ * uses it for every shape it supports and peagle_set_pass_kernel(ctx, 0) never).  For the
+ * latest pass run while timing was enabled, writes four
  * globaltimer values (ns) per step of the pass and CTA, as out[(phase * ctas + cta) * 4 + k]:
- * k = 0 the step's activations were seen ready, 1 its first MMA was issued, 2 its last
- * accumulator was committed (projections only, else 0), 3 the CTA finished the step; and
+ * projections: k = 0 the step's activations were seen ready, 1 its first MMA was issued,
+ * 2 its last accumulator was committed; other steps: 0 the previous step was seen complete,
+ * and for attention 1 the CTA's item wrote its partials, 2 every item of its (request, kv
+ * head) was in (else 0); 3 the CTA finished the step; and
  * the two sizes.  Returns the number of entries (0 if no pass was traced),
  * PEAGLE_ERR_CAPACITY if max_entries is too small.  The paper has no counterpart: this
  * reports how this library schedules the pass. */
