@@ -132,11 +132,86 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
       }
     } break;
     case EPI_QKV_ROPE: {
+      const int hd = a.hd, half = hd >> 1;
+      const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
+      // the output of row r, section sec (0 q, 1 k, 2 v), feature m (kv head g, index i
+      // within the head): out0 at i, and for q / k the rotated partner out1 at i + half
+      auto put = [&](int r, int sec, int m, int g, int i, int pos, int dep, float out0,
+                     float out1) {
+        if (sec == 0) {
+          if (a.q_f32) {
+            float* q = (float*)a.q_out + (size_t)r * a.nq * hd + m;
+            q[0] = out0;
+            q[half] = out1;
+          } else {
+            T* q = (T*)a.q_out + (size_t)r * a.nq * hd + m;
+            q[0] = from_f32<T>(out0);
+            q[half] = from_f32<T>(out1);
+          }
+          return;
+        }
+        T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
+        size_t off;
+        if (a.decode)
+          off = (((size_t)(r / a.K) * a.nkv + g) * a.cap + pos) * hd + i;
+        else
+          off = ((size_t)r * a.nkv + g) * hd + i;
+        dst[off] = from_f32<T>(out0);
+        if (sec == 1) dst[off + half] = from_f32<T>(out1);
+        if (!a.decode && dep == 1 && pos >= 0 && pos < a.n_seq) {
+          T* d1 = (T*)(sec == 1 ? a.k1_dst : a.v1_dst);
+          if (d1) {
+            const size_t o1 = ((size_t)pos * a.nkv + g) * hd + i;
+            d1[o1] = from_f32<T>(out0);
+            if (sec == 1) d1[o1 + half] = from_f32<T>(out1);
+          }
+        }
+      };
+      if (nthr == 128 && mcount == 128 && 128 % hd == 0 &&
+          (m0 + 128 <= qend || (m0 >= qend && m0 + 128 <= kend))) {
+        // A tile of rotated features only (q or k): thread = (rotation pair, row parity),
+        // so that every thread works; rows' positions, depths and RoPE factors of a batch
+        // are fetched before any of them is used.
+        const int sec = m0 < qend ? 0 : 1;
+        const int pr = tid & 63, rg = tid >> 6;
+        const int i = pr % half;
+        const int ml = (pr / half) * hd + i;
+        const int m = m0 + ml;
+        const int g = sec == 0 ? 0 : (m - qend) / hd;
+        constexpr int U = 8;
+        for (int t0 = rg; t0 < rcount; t0 += 2 * U) {
+          int pos_u[U], dep_u[U];
+          float2 cs_u[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int ti = t0 + 2 * u;
+            pos_u[u] = ti < rcount ? (rpos ? rpos[ti] : __ldg(a.row_pos + r0 + ti)) : -1;
+            dep_u[u] = (ti < rcount && !a.decode && a.row_depth) ? __ldg(a.row_depth + r0 + ti) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const bool need = pos_u[u] >= 0 && pos_u[u] < a.max_pos;
+            cs_u[u] = need ? __ldg(a.rope + (size_t)pos_u[u] * half + i) : make_float2(1.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int ti = t0 + 2 * u;
+            if (ti >= rcount) break;
+            const int pos = pos_u[u];
+            if (a.decode && (pos < 0 || pos >= a.cap)) {
+              if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
+              if (sec != 0) continue;  // no cache slot for this row
+            }
+            const float v0 = val(ti, ml), v1 = val(ti, ml + half);
+            put(r0 + ti, sec, m, g, i, pos, dep_u[u], v0 * cs_u[u].x - v1 * cs_u[u].y,
+                v1 * cs_u[u].x + v0 * cs_u[u].y);
+          }
+        }
+        break;
+      }
       // One output feature per thread (consecutive threads write consecutive features);
       // the rows' positions, depths and RoPE factors of a batch of 16 rows are fetched
       // before any of them is used.
-      const int hd = a.hd, half = hd >> 1;
-      const int qend = a.nq * hd, kend = (a.nq + a.nkv) * hd;
       constexpr int U = 16;
       for (int ml = tid; ml < mcount; ml += nthr) {
         const int m = m0 + ml;
@@ -164,8 +239,6 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
             if (ti >= rcount) break;
             const int r = r0 + ti;
             const int pos = pos_u[u];
-            int b = 0;
-            if (a.decode) b = r / a.K;
             if (a.decode && (pos < 0 || pos >= a.cap)) {
               if (sec == 0 && i == 0 && m == 0) raise_error(a.err, PEAGLE_DEV_KV_OVERFLOW);
               if (sec != 0) continue;  // no cache slot for this row
@@ -179,34 +252,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& a, const float* src
               out0 = v0 * cs_u[u].x - v1 * cs_u[u].y;
               out1 = v1 * cs_u[u].x + v0 * cs_u[u].y;
             }
-            if (sec == 0) {
-              if (a.q_f32) {
-                float* q = (float*)a.q_out + (size_t)r * a.nq * hd + m;
-                q[0] = out0;
-                q[half] = out1;
-              } else {
-                T* q = (T*)a.q_out + (size_t)r * a.nq * hd + m;
-                q[0] = from_f32<T>(out0);
-                q[half] = from_f32<T>(out1);
-              }
-            } else {
-              T* dst = (T*)(sec == 1 ? a.k_dst : a.v_dst);
-              size_t off;
-              if (a.decode)
-                off = (((size_t)b * a.nkv + g) * a.cap + pos) * hd + i;
-              else
-                off = ((size_t)r * a.nkv + g) * hd + i;
-              dst[off] = from_f32<T>(out0);
-              if (sec == 1) dst[off + half] = from_f32<T>(out1);
-              if (!a.decode && dep_u[u] == 1 && pos >= 0 && pos < a.n_seq) {
-                T* d1 = (T*)(sec == 1 ? a.k1_dst : a.v1_dst);
-                if (d1) {
-                  const size_t o1 = ((size_t)pos * a.nkv + g) * hd + i;
-                  d1[o1] = from_f32<T>(out0);
-                  if (sec == 1) d1[o1 + half] = from_f32<T>(out1);
-                }
-              }
-            }
+            put(r, sec, m, g, i, pos, dep_u[u], out0, out1);
           }
         }
       }
