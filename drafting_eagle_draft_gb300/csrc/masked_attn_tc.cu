@@ -14,7 +14,8 @@
 // The output accumulator stays in tensor memory; when a row's max grows, its thread
 // rescales the row there (tcgen05.ld / st) before the next product.  K and V tiles arrive
 // by TMA, two tiles ahead.  Queries and probabilities are rounded to bf16 as in the
-// mma.sync kernel, so both kernels compute the same function.
+// mma.sync kernel, so both kernels compute the same function (exponentials here on the
+// SFU, 2^x to about 2^-22 relative, far below the probabilities' bf16 rounding).
 #include <cuda.h>
 #include <stdio.h>
 
@@ -228,11 +229,11 @@ __global__ void __launch_bounds__(MT_THREADS) masked_attn_tc_kernel(
     }
     const float mn = fmaxf(m, mx);
     const float base = (mn == -INFINITY) ? 0.f : mn;
-    const float cr = (m == -INFINITY) ? 0.f : exp2f(m - base);
+    const float cr = (m == -INFINITY) ? 0.f : fast_ex2(m - base);
     float ps = 0.f;
 #pragma unroll
     for (int j = 0; j < 64; ++j) {
-      s[j] = bf16r(exp2f(s[j] - base));
+      s[j] = bf16r(fast_ex2(s[j] - base));  // SFU 2^x (error far below the bf16 rounding)
       ps += s[j];
     }
     l = l * cr + ps;
