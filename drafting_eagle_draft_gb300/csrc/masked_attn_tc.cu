@@ -11,8 +11,9 @@
 //                updates the running max / sum (log2 domain) and writes its bf16
 //                probabilities to shared memory (the next MMA's A operand)
 //   O += P V     tcgen05.mma M=128, N=64 (head dims), K=64 keys, V read MN-major
-// The output accumulator stays in tensor memory; when a row's max grows, its thread
-// rescales the row there (tcgen05.ld / st) before the next product.  K and V tiles arrive
+// The output accumulator stays in tensor memory; when a row's reference maximum is raised
+// (lazily: only by more than 2^8), its thread rescales the row there (tcgen05.ld / st)
+// before the next product.  K and V tiles arrive
 // by TMA, two tiles ahead.  Queries and probabilities are rounded to bf16 as in the
 // mma.sync kernel, so both kernels compute the same function (exponentials here on the
 // SFU, 2^x to about 2^-22 relative, far below the probabilities' bf16 rounding).
@@ -34,6 +35,7 @@ constexpr int MT_THREADS = 128;     // one thread per MMA row
 constexpr int MT_TILE = 64 * 128;   // 64 rows x 64 bf16 (128 B), 128-byte swizzle
 constexpr int MT_SMEM = 1024 + 2 * 16384 + 4 * MT_TILE;  // Q, P, K[2], V[2]
 constexpr uint64_t MT_WAIT_NS = 2000000000ull;
+constexpr int MT_LAZY_LOG2 = 8;  // rescale O only when a row's maximum grows by more than 2^8
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -227,9 +229,16 @@ __global__ void __launch_bounds__(MT_THREADS) masked_attn_tc_kernel(
         mx = fmaxf(mx, s[j]);
       }
     }
-    const float mn = fmaxf(m, mx);
-    const float base = (mn == -INFINITY) ? 0.f : mn;
-    const float cr = (m == -INFINITY) ? 0.f : fast_ex2(m - base);
+    // the row's reference maximum m is raised the first time and then only when a tile's
+    // maximum exceeds it by more than 2^MT_LAZY_LOG2 (O and l rescaled): probabilities stay
+    // within [0, 2^MT_LAZY_LOG2] with the same bf16 relative precision, and O is rarely
+    // read back
+    float cr = 1.f;
+    if (mx > m + (float)MT_LAZY_LOG2 || (m == -INFINITY && mx > -INFINITY)) {
+      cr = (m == -INFINITY) ? 0.f : fast_ex2(m - mx);
+      m = mx;
+    }
+    const float base = (m == -INFINITY) ? 0.f : m;
     float ps = 0.f;
 #pragma unroll
     for (int j = 0; j < 64; ++j) {
@@ -237,7 +246,6 @@ __global__ void __launch_bounds__(MT_THREADS) masked_attn_tc_kernel(
       ps += s[j];
     }
     l = l * cr + ps;
-    m = mn;
     // ---- the previous product is done with P, O and its K / V buffer
     if (it > 0) {
       wait_bar(&pv_done, (uint32_t)(it - 1) & 1u);
